@@ -1,0 +1,211 @@
+/*
+ * va.h - C ABI of the B300 (sm_103a) block-sparse video attention library.
+ *
+ * Operations (sources named by page and section):
+ *   - static spatiotemporal block masks over a flattened (frame, height, width)
+ *     latent token grid: the radial energy-decay mask (Radial Attention news
+ *     page, hyper.ai) and the LVSA local-window + rotating periodic anchor
+ *     mask (LVSA review, secrett2633 blog, sec. 3 and Fig. 2);
+ *   - block-sparse softmax attention forward under such a mask (LVSA review
+ *     sec. 1 "block-sparse attention"; LinVideo, gist.science 2510.08318,
+ *     technical summary sec. 1 on the O(n^2) attention bottleneck);
+ *   - k-means clustering of query/key tokens and centroid-compensated sparse
+ *     attention with error-aware routing under a density budget (SVG-EAR,
+ *     gist.science 2603.08982, technical summary sec. 2, ideas 1 and 2).
+ *
+ * Conventions shared by every call:
+ *   - Token n of a T x H x W latent is n = t*H*W + h*W + w (t-major).
+ *   - Tensors are DEVICE pointers owned by the caller, contiguous
+ *     [B, heads, N, d] (d fastest), 16-byte aligned. dtype VA_BF16 means
+ *     bfloat16 elements, VA_F32 means float32.
+ *   - Calls are asynchronous on the given stream (a cudaStream_t; NULL is the
+ *     legacy default stream) unless documented otherwise, and run on the
+ *     CUDA device current in the calling thread.
+ *   - Every call returns VA_OK (0) or a negative VA_ERR_* code; on an error
+ *     return nothing was launched unless stated. The library never aborts the
+ *     process and never traps the GPU: a device-side wait that times out, or a
+ *     device-side bounds check that fails, records a code that
+ *     va_device_error() reports.
+ */
+#ifndef VA_H
+#define VA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* va_stream_t; /* identical to cudaStream_t */
+typedef struct va_mask va_mask;          /* opaque, library-owned */
+
+/* status codes */
+#define VA_OK 0
+#define VA_ERR_INVALID (-1)     /* null pointer, bad size, misaligned, shape mismatch */
+#define VA_ERR_UNSUPPORTED (-2) /* dtype / head_dim / block / device not supported */
+#define VA_ERR_CUDA (-3)        /* a CUDA runtime call failed */
+#define VA_ERR_OOM (-4)         /* device allocation failed */
+#define VA_ERR_TIMEOUT (-5)     /* a device-side wait gave up (from va_device_error) */
+#define VA_ERR_DEVICE (-6)      /* a device-side bounds check failed (from va_device_error) */
+
+/* mask kinds */
+#define VA_MASK_DENSE 0  /* every block pair live (dense attention on the same kernel) */
+#define VA_MASK_RADIAL 1 /* radial energy-decay mask */
+#define VA_MASK_LVSA 2   /* local frame window + rotating periodic anchor frames */
+
+/* element types */
+#define VA_F32 0
+#define VA_BF16 1
+
+/*
+ * Mask parameters.
+ *   block      tokens per block (query and key blocks are the same size); the
+ *              last block holds N - (nqb-1)*block tokens. 1..4096.
+ *   w0         radial: base half-width W0 of the in-frame window; token pair
+ *              (i, j) is live iff |s_i - s_j| <= W0 >> octave(|t_i - t_j|)
+ *              with s = in-frame index, octave(0)=0 and octave(dt) = bit
+ *              length of dt. 0 selects W0 = H*W.
+ *   local      LVSA: frames within +-local of the query frame are attended.
+ *   period     LVSA: anchor period P; key frame t is an anchor at denoising
+ *              step s iff (t - anchor0 - rot_stride*s) mod P == 0. P == 0
+ *              means the single anchor frame anchor0 (no rotation).
+ *   anchor0    LVSA: anchor offset.
+ *   rot_stride LVSA: anchor shift per denoising step.
+ * A (query block, key block) pair is live iff some real token pair in it is
+ * live under the token rule; a live pair is computed in full.
+ */
+typedef struct va_mask_params {
+  int32_t block;
+  int32_t w0;
+  int32_t local;
+  int32_t period;
+  int32_t anchor0;
+  int32_t rot_stride;
+} va_mask_params;
+
+/*
+ * Build the block mask of `kind` for a T x H x W grid at denoising `step` and
+ * return it as a library-owned handle holding a device CSR:
+ *   row_ptr[nqb + 1] (int32), col_idx[nnz] (int32, strictly ascending per row),
+ *   nqb = ceil(T*H*W / block).
+ * The mask is identical for every batch element and head. The result is
+ * bit-exact (integer arithmetic only). This call synchronises `stream` once
+ * (to size col_idx); the handle is ready when it returns.
+ * Errors: VA_ERR_INVALID (null out/params, non-positive sizes, N >= 2^31,
+ * block outside 1..4096, negative local/period/w0), VA_ERR_OOM, VA_ERR_CUDA.
+ */
+int va_mask_build(int kind, int T, int H, int W, const va_mask_params* params, int step,
+                  va_mask** out, va_stream_t stream);
+
+/* Device CSR arrays of a mask (owned by the handle) and its sizes. Any output
+ * pointer may be NULL. Errors: VA_ERR_INVALID for a NULL mask. */
+int va_mask_csr(const va_mask* mask, const int32_t** row_ptr_dev, const int32_t** col_idx_dev,
+                int* nqb, int64_t* nnz);
+
+/* Grid and accounting data of a mask: N = T*H*W, block, and live_pairs =
+ * sum over live block pairs of |I|*|J| (real tokens only). Any output may be
+ * NULL. Errors: VA_ERR_INVALID for a NULL mask. */
+int va_mask_info(const va_mask* mask, int* N, int* block, int64_t* live_pairs);
+
+/* Copy the CSR to caller-owned HOST arrays row_ptr[nqb+1] and col_idx[nnz]
+ * (synchronous). Errors: VA_ERR_INVALID, VA_ERR_CUDA. */
+int va_mask_to_host(const va_mask* mask, int32_t* row_ptr, int32_t* col_idx);
+
+/* Release a mask (NULL is accepted). Synchronises the device work that may
+ * still use it only through the caller: do not free a mask that a queued
+ * kernel still reads. */
+int va_mask_free(va_mask* mask);
+
+/*
+ * Block-sparse attention forward. For every batch b, head h and query token i
+ * with block I = i / block:
+ *   l_j   = scale * q_i . k_j   for keys j in live key blocks of row I, j < N
+ *   o_i   = sum_j exp(l_j - m) v_j / sum_j exp(l_j - m),  m = max_j l_j
+ *   lse_i = m + ln sum_j exp(l_j - m)       (natural log; -inf, o_i = 0 if
+ *                                            row I has no live block)
+ * q, k, v, out: [B, heads, N, d] device arrays of `dtype`; lse: NULL or a
+ * [B, heads, N] float32 device array. Softmax and accumulation are float32;
+ * VA_BF16 inputs give a bf16 output, VA_F32 inputs a float32 output.
+ * Supported: VA_BF16 with d = 128 and block 128 (tcgen05 tensor-core kernel);
+ * VA_F32 with d in {64, 128} and block in {64, 128} (float32 FMA kernel).
+ * Errors: VA_ERR_INVALID (null pointers, N != T*H*W of the mask, B or heads
+ * < 1, misaligned pointers), VA_ERR_UNSUPPORTED (other dtype/d/block),
+ * VA_ERR_CUDA (launch failure).
+ */
+int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mask* mask,
+                       void* out, float* lse, int B, int heads, int N, int d, float scale,
+                       int dtype, va_stream_t stream);
+
+/*
+ * Lloyd k-means per (batch, head) on x [B, heads, N, d] (squared Euclidean
+ * distance), SVG-EAR's semantic clustering:
+ *   centroid <- x[init_idx]; repeat iters times: assign each token to the
+ *   nearest centroid (ties: lowest index), then replace each centroid by the
+ *   mean of its members (an empty cluster keeps its centroid).
+ * iters == 0 returns the assignment to the initial centroids.
+ * init_idx: device int32 [B, heads, C], distinct indices in [0, N) (the
+ * seeded random draw, supplied by the caller). Outputs (device, caller-owned):
+ * assign int32 [B, heads, N], centroid float32 [B, heads, C, d] (means of the
+ * returned assignment), count int32 [B, heads, C]. Distances are float32.
+ * Scratch: allocated and released on `stream` (stream-ordered allocator).
+ * Supported: dtype VA_BF16 or VA_F32, d in {64, 128}, 1 <= C <= min(N, 4096).
+ * Errors: VA_ERR_INVALID, VA_ERR_UNSUPPORTED, VA_ERR_OOM, VA_ERR_CUDA.
+ */
+int va_cluster(const void* x, const int32_t* init_idx, int B, int heads, int N, int d, int C,
+               int iters, int dtype, int32_t* assign, float* centroid, int32_t* count,
+               va_stream_t stream);
+
+/*
+ * SVG-EAR compensated sparse attention with error-aware routing.
+ * A block is (query cluster p, key cluster c); n_p, n_c are cluster sizes and
+ * qc_p, kc_c, vc_c member means (float32) of q, k, v.
+ *   probe (proxy qc_p, logits s*qc_p.k_j, m_p their max):
+ *     Z_p = sum_j e^(l_j - m_p), O_p = sum_j e^(l_j - m_p) v_j / Z_p,
+ *     dE = sum_{j in c} e^(l_j - m_p) v_j - n_c e^(s qc_p.kc_c - m_p) vc_c,
+ *     dZ = sum_{j in c} e^(l_j - m_p)     - n_c e^(s qc_p.kc_c - m_p),
+ *     err(p, c) = || dE - O_p dZ ||_2 / Z_p
+ *   routing: ratio = err / n_c (float32); blocks ordered by ratio descending,
+ *     ties by p then c ascending; the longest prefix whose summed cost
+ *     n_p * n_c is <= floor(density * N * N) is computed exactly; blocks with
+ *     an empty cluster are never selected;
+ *   output for query i in cluster p: one softmax over the exact keys of the
+ *     selected clusters and, for every other non-empty key cluster c, a
+ *     virtual key kc_c with logit bias ln n_c and value vc_c.
+ * qassign/kassign: device int32 [B, heads, N] with values in [0, Cq) / [0, Ck).
+ * out: [B, heads, N, d] of dtype (bf16 for VA_BF16, float32 for VA_F32).
+ * err_out: NULL or device float32 [B, heads, Cq, Ck] (the probe errors).
+ * sel_out: NULL or device uint8 [B, heads, Cq, Ck] (1 = computed exactly).
+ * Scratch: allocated and released on `stream` (stream-ordered allocator).
+ * Supported: d in {64, 128}, 1 <= Cq, Ck <= 4096, 0 <= density <= 1.
+ * Errors: VA_ERR_INVALID, VA_ERR_UNSUPPORTED, VA_ERR_OOM, VA_ERR_CUDA;
+ * assignment values out of range are reported by va_device_error() as
+ * VA_ERR_DEVICE.
+ */
+int va_compensate_route(const void* q, const void* k, const void* v, const int32_t* qassign,
+                        int Cq, const int32_t* kassign, int Ck, double density, float scale,
+                        int B, int heads, int N, int d, int dtype, void* out, float* err_out,
+                        uint8_t* sel_out, va_stream_t stream);
+
+/*
+ * Synchronise `stream`, then return and clear the sticky device error word of
+ * the current device: VA_OK, VA_ERR_TIMEOUT or VA_ERR_DEVICE (or VA_ERR_CUDA
+ * if the synchronisation itself failed).
+ */
+int va_device_error(va_stream_t stream);
+
+/* Set the bound of every device-side wait in clock64 cycles (default 4e9,
+ * about 2 s at 2 GHz). Values < 1000 are rejected with VA_ERR_INVALID. */
+int va_set_wait_limit(int64_t cycles);
+
+/* Static text for a status code. */
+const char* va_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int va_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VA_H */

@@ -1,0 +1,226 @@
+"""Block-sparse video attention for NVIDIA B300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/va.h`` (``libva.so``, built
+in-tree by ``build.py``). Every operation runs in the library's CUDA kernels;
+this module only marshals torch tensors (device memory) and the current CUDA
+stream into the C calls. There is no CPU implementation here: if ``libva.so``
+is missing, importing the binding raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libva.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6
+DENSE, RADIAL, LVSA = 0, 1, 2
+F32, BF16 = 0, 1
+
+
+class VAError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s failed: %s (%d)" % (what, status_string(status), status))
+        self.status = status
+
+
+class _MaskParams(ctypes.Structure):
+    _fields_ = [("block", ctypes.c_int32), ("w0", ctypes.c_int32), ("local", ctypes.c_int32),
+                ("period", ctypes.c_int32), ("anchor0", ctypes.c_int32),
+                ("rot_stride", ctypes.c_int32)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libva.so is not built (%s); run __graft_entry__.build() or "
+                          "python linear_attention_video_fwd_b300/build.py" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, f32, f64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                              ctypes.c_double)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    sig = {
+        "va_mask_build": [i32, i32, i32, i32, ctypes.POINTER(_MaskParams), i32,
+                          ctypes.POINTER(vp), vp],
+        "va_mask_csr": [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i32),
+                        ctypes.POINTER(i64)],
+        "va_mask_info": [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i64)],
+        "va_mask_to_host": [vp, i32p, i32p],
+        "va_mask_free": [vp],
+        "va_sparse_attn_fwd": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp],
+        "va_cluster": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp],
+        "va_compensate_route": [vp, vp, vp, vp, i32, vp, i32, f64, f32, i32, i32, i32, i32, i32,
+                                vp, vp, vp, vp],
+        "va_device_error": [vp],
+        "va_set_wait_limit": [i64],
+        "va_status_string": [i32],
+        "va_version": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "va_status_string" else ctypes.c_int
+    return lib
+
+
+_lib = _load()
+
+
+def lib():
+    """The loaded ctypes library (C ABI of include/va.h)."""
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return _lib.va_status_string(status).decode()
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise VAError(status, what)
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise VAError(ERR_UNSUPPORTED, "dtype %s" % t.dtype)
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise VAError(ERR_INVALID, "tensor argument (needs contiguous CUDA tensors)")
+
+
+class Mask:
+    """A library-owned block mask (device CSR). Free with .free() or on GC."""
+
+    def __init__(self, handle, kind, T, H, W, params, step):
+        self._h = handle
+        self.kind, self.T, self.H, self.W, self.step = kind, T, H, W, step
+        self.params = params
+        nqb, nnz = ctypes.c_int(), ctypes.c_int64()
+        _check(_lib.va_mask_csr(self._h, None, None, ctypes.byref(nqb), ctypes.byref(nnz)),
+               "va_mask_csr")
+        N, block, lp = ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+        _check(_lib.va_mask_info(self._h, ctypes.byref(N), ctypes.byref(block), ctypes.byref(lp)),
+               "va_mask_info")
+        self.nqb, self.nnz, self.N, self.block, self.live_pairs = (
+            nqb.value, nnz.value, N.value, block.value, lp.value)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def csr(self):
+        """(row_ptr [nqb+1], col_idx [nnz]) as host int32 arrays."""
+        rp = np.zeros(self.nqb + 1, dtype=np.int32)
+        col = np.zeros(max(self.nnz, 1), dtype=np.int32)
+        _check(_lib.va_mask_to_host(self._h, rp.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                    col.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))),
+               "va_mask_to_host")
+        return rp, col[: self.nnz]
+
+    def free(self):
+        if self._h:
+            _lib.va_mask_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def mask_build(kind: int, T: int, H: int, W: int, block: int = 128, w0: int = 0, local: int = 1,
+               period: int = 0, anchor0: int = 0, rot_stride: int = 1, step: int = 0,
+               stream=None) -> Mask:
+    """va_mask_build: the static block mask of a T x H x W latent grid."""
+    p = _MaskParams(block, w0, local, period, anchor0, rot_stride)
+    h = ctypes.c_void_p()
+    _check(_lib.va_mask_build(kind, T, H, W, ctypes.byref(p), step, ctypes.byref(h),
+                              _stream(stream)), "va_mask_build")
+    return Mask(h, kind, T, H, W, p, step)
+
+
+def sparse_attn_fwd(q, k, v, mask: Mask, scale: float | None = None, out=None, lse=None,
+                    stream=None):
+    """va_sparse_attn_fwd on [B, heads, N, d] CUDA tensors. Returns (out, lse or None)."""
+    import torch
+    _require_cuda(q, k, v, out, lse)
+    B, Hh, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise VAError(ERR_INVALID, "q/k/v shapes or dtypes differ")
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(_lib.va_sparse_attn_fwd(_ptr(q), _ptr(k), _ptr(v), mask.handle, _ptr(out), _ptr(lse),
+                                   B, Hh, N, d, float(scale), _dtype_code(q), _stream(stream)),
+           "va_sparse_attn_fwd")
+    return out, lse
+
+
+def cluster(x, C: int, iters: int, init_idx, assign=None, centroid=None, count=None,
+            stream=None):
+    """va_cluster: Lloyd k-means per (batch, head). Returns (assign, centroid, count)."""
+    import torch
+    _require_cuda(x, init_idx, assign, centroid, count)
+    B, Hh, N, d = x.shape
+    if init_idx.dtype != torch.int32 or tuple(init_idx.shape) != (B, Hh, C):
+        raise VAError(ERR_INVALID, "init_idx must be int32 [B, heads, C]")
+    dev = x.device
+    if assign is None:
+        assign = torch.empty((B, Hh, N), dtype=torch.int32, device=dev)
+    if centroid is None:
+        centroid = torch.empty((B, Hh, C, d), dtype=torch.float32, device=dev)
+    if count is None:
+        count = torch.empty((B, Hh, C), dtype=torch.int32, device=dev)
+    _check(_lib.va_cluster(_ptr(x), _ptr(init_idx), B, Hh, N, d, C, iters, _dtype_code(x),
+                           _ptr(assign), _ptr(centroid), _ptr(count), _stream(stream)),
+           "va_cluster")
+    return assign, centroid, count
+
+
+def compensate_route(q, k, v, qassign, Cq: int, kassign, Ck: int, density: float,
+                     scale: float | None = None, out=None, err=None, sel=None, stream=None):
+    """va_compensate_route. Returns (out, err or None, sel or None)."""
+    import torch
+    _require_cuda(q, k, v, qassign, kassign, out, err, sel)
+    B, Hh, N, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(_lib.va_compensate_route(_ptr(q), _ptr(k), _ptr(v), _ptr(qassign), Cq, _ptr(kassign),
+                                    Ck, float(density), float(scale), B, Hh, N, d,
+                                    _dtype_code(q), _ptr(out), _ptr(err), _ptr(sel),
+                                    _stream(stream)), "va_compensate_route")
+    return out, err, sel
+
+
+def device_error(stream=None) -> int:
+    """va_device_error: sync the stream and return/clear the device error word."""
+    return _lib.va_device_error(_stream(stream))
+
+
+def set_wait_limit(cycles: int):
+    _check(_lib.va_set_wait_limit(int(cycles)), "va_set_wait_limit")

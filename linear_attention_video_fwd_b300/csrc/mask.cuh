@@ -1,0 +1,166 @@
+// Static spatiotemporal block masks as CSR lists (integer arithmetic only).
+//
+// Token rules (readings of the pages; identical for every batch and head):
+//   radial (Radial Attention news page, hyper.ai: the window shrinks
+//     exponentially with temporal distance):
+//       live(i, j) <=> |s_i - s_j| <= W0 >> octave(|t_i - t_j|),
+//       octave(0) = 0, octave(dt) = bit length of dt;
+//   LVSA (LVSA review, secrett2633 blog, sec. 3 and Fig. 2: local frame window
+//     plus periodic global anchor frames that rotate per denoising step):
+//       live(i, j) <=> |t_i - t_j| <= L  or  (t_j - a0 - rho*step) mod P == 0
+//       (P == 0: t_j == a0);
+//   dense: always live.
+// A block pair is live iff some real token pair in it is live. Blocks are
+// split into runs of one frame each; for two runs the smallest in-frame
+// distance is max(0, lo_j - hi_i, lo_i - hi_j), which decides the radial rule.
+#pragma once
+
+#include "common.cuh"
+
+namespace va {
+
+struct MaskDesc {
+  int kind, T, F, N, block, nb;
+  int w0, local, period, anchor0, rot_stride, step;
+};
+
+__device__ __forceinline__ bool run_pair_live(const MaskDesc& m, int ti, int lo_i, int hi_i,
+                                              int tj, int lo_j, int hi_j) {
+  if (m.kind == VA_MASK_DENSE) return true;
+  const int dt = ti > tj ? ti - tj : tj - ti;
+  if (m.kind == VA_MASK_RADIAL) {
+    const int oct = 32 - __clz(dt);  // bit length; __clz(0) == 32
+    const int w = oct >= 31 ? 0 : (m.w0 >> oct);
+    const int gap = max(0, max(lo_j - hi_i, lo_i - hi_j));
+    return gap <= w;
+  }
+  if (dt <= m.local) return true;
+  if (m.period > 0) {
+    long long r = (static_cast<long long>(tj) - m.anchor0 -
+                   static_cast<long long>(m.rot_stride) * m.step) % m.period;
+    if (r < 0) r += m.period;
+    return r == 0;
+  }
+  return tj == m.anchor0;
+}
+
+__device__ bool block_pair_live(const MaskDesc& m, int I, int J) {
+  const int qs = I * m.block, qe = min(m.N, qs + m.block);
+  const int ks = J * m.block, ke = min(m.N, ks + m.block);
+  for (int n = qs; n < qe;) {
+    const int ti = n / m.F;
+    const int qstop = min(qe, (ti + 1) * m.F);
+    const int lo_i = n - ti * m.F, hi_i = qstop - 1 - ti * m.F;
+    for (int j = ks; j < ke;) {
+      const int tj = j / m.F;
+      const int kstop = min(ke, (tj + 1) * m.F);
+      if (run_pair_live(m, ti, lo_i, hi_i, tj, j - tj * m.F, kstop - 1 - tj * m.F)) return true;
+      j = kstop;
+    }
+    n = qstop;
+  }
+  return false;
+}
+
+// One warp per query block: number of live key blocks and the number of key
+// tokens they hold.
+__global__ void mask_count_kernel(MaskDesc m, int* __restrict__ cnt,
+                                  long long* __restrict__ key_tokens) {
+  const int I = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (I >= m.nb) return;
+  int c = 0;
+  long long kt = 0;
+  for (int J0 = 0; J0 < m.nb; J0 += 32) {
+    const int J = J0 + lane;
+    const bool live = J < m.nb && block_pair_live(m, I, J);
+    c += __popc(__ballot_sync(0xffffffffu, live));
+    if (live) kt += min(m.N, (J + 1) * m.block) - J * m.block;
+  }
+  for (int o = 16; o; o >>= 1) kt += __shfl_xor_sync(0xffffffffu, kt, o);
+  if (lane == 0) {
+    cnt[I] = c;
+    key_tokens[I] = kt;
+  }
+}
+
+// Single CTA: exclusive scan of the counts into row_ptr, nnz and live token
+// pairs into summary[0..1], and the rows ordered by descending length
+// (stable), the longest-first order the attention kernel schedules in.
+// hist must hold nb + 1 ints.
+__global__ void mask_scan_kernel(MaskDesc m, const int* __restrict__ cnt,
+                                 const long long* __restrict__ key_tokens,
+                                 int* __restrict__ row_ptr, long long* __restrict__ summary,
+                                 int* __restrict__ order, int* __restrict__ hist) {
+  __shared__ long long part[1024];
+  __shared__ long long part_pairs[1024];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int per = (m.nb + nt - 1) / nt;
+  const int lo = min(m.nb, tid * per), hi = min(m.nb, lo + per);
+  long long s = 0, pairs = 0;
+  for (int i = lo; i < hi; ++i) {
+    s += cnt[i];
+    const long long rows = min(m.N, (i + 1) * m.block) - i * m.block;
+    pairs += rows * key_tokens[i];
+  }
+  part[tid] = s;
+  part_pairs[tid] = pairs;
+  __syncthreads();
+  if (tid == 0) {
+    long long acc = 0, accp = 0;
+    for (int t = 0; t < nt; ++t) {
+      const long long v = part[t];
+      part[t] = acc;
+      acc += v;
+      accp += part_pairs[t];
+    }
+    summary[0] = acc;
+    summary[1] = accp;
+    row_ptr[m.nb] = static_cast<int>(acc);
+  }
+  __syncthreads();
+  long long base = part[tid];
+  for (int i = lo; i < hi; ++i) {
+    row_ptr[i] = static_cast<int>(base);
+    base += cnt[i];
+  }
+  // stable counting sort of rows by descending count (counts are 0..nb)
+  for (int i = tid; i <= m.nb; i += nt) hist[i] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    for (int i = 0; i < m.nb; ++i) hist[m.nb - cnt[i]]++;
+    int acc = 0;
+    for (int b = 0; b <= m.nb; ++b) {
+      const int v = hist[b];
+      hist[b] = acc;
+      acc += v;
+    }
+    for (int i = 0; i < m.nb; ++i) order[hist[m.nb - cnt[i]]++] = i;
+  }
+}
+
+// One warp per query block: write the live key blocks in ascending order.
+__global__ void mask_fill_kernel(MaskDesc m, const int* __restrict__ row_ptr,
+                                 int* __restrict__ col) {
+  const int I = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (I >= m.nb) return;
+  int base = row_ptr[I];
+  const int end = row_ptr[I + 1];
+  for (int J0 = 0; J0 < m.nb; J0 += 32) {
+    const int J = J0 + lane;
+    const bool live = J < m.nb && block_pair_live(m, I, J);
+    const unsigned bal = __ballot_sync(0xffffffffu, live);
+    const int pos = base + __popc(bal & ((1u << lane) - 1u));
+    if (live) {
+      if (pos < end) {
+        col[pos] = J;
+      } else {
+        raise_error(VA_ERR_DEVICE);
+      }
+    }
+    base += __popc(bal);
+  }
+}
+
+}  // namespace va

@@ -1,0 +1,310 @@
+// libva: C ABI of the block-sparse video attention library (see include/va.h).
+// One translation unit: the kernels live in the headers included below.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "va.h"
+#include "common.cuh"
+#include "mask.cuh"
+#include "attn_simt.cuh"
+
+#define VA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+int64_t g_wait_limit = 4000000000LL;
+
+struct Scoped {
+  // Stream-ordered scratch allocations released at scope exit.
+  cudaStream_t s;
+  void* ptrs[16];
+  int n = 0;
+  explicit Scoped(cudaStream_t st) : s(st) {}
+  ~Scoped() {
+    for (int i = 0; i < n; ++i) cudaFreeAsync(ptrs[i], s);
+  }
+  template <typename T>
+  int alloc(T** p, size_t count) {
+    *p = nullptr;
+    if (count == 0) count = 1;
+    if (fault_injected()) return VA_ERR_OOM;
+    void* raw = nullptr;
+    cudaError_t e = cudaMallocAsync(&raw, count * sizeof(T), s);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return e == cudaErrorMemoryAllocation ? VA_ERR_OOM : VA_ERR_CUDA;
+    }
+    ptrs[n++] = raw;
+    *p = static_cast<T*>(raw);
+    return VA_OK;
+  }
+  // VA_FAULT_INJECT=alloc makes every scratch allocation fail (host-side
+  // fault injection for the error paths).
+  static bool fault_injected() {
+    const char* f = std::getenv("VA_FAULT_INJECT");
+    return f != nullptr && std::strstr(f, "alloc") != nullptr;
+  }
+};
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return VA_OK;
+  cudaGetLastError();
+  return e == cudaErrorMemoryAllocation ? VA_ERR_OOM : VA_ERR_CUDA;
+}
+
+int launch_status() { return cuda_status(cudaGetLastError()); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct va_mask {
+  int kind, T, H, W, N, step;
+  va_mask_params p;
+  int nqb;
+  int64_t nnz, live_pairs;
+  int32_t* row_ptr = nullptr;  // device [nqb + 1]
+  int32_t* col = nullptr;      // device [nnz]
+  int32_t* order = nullptr;    // device [nqb]: rows by descending length
+  int device = 0;
+};
+
+VA_EXPORT int va_version(void) { return 100; }
+
+VA_EXPORT const char* va_status_string(int status) {
+  switch (status) {
+    case VA_OK: return "ok";
+    case VA_ERR_INVALID: return "invalid argument";
+    case VA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case VA_ERR_CUDA: return "CUDA runtime error";
+    case VA_ERR_OOM: return "device allocation failed";
+    case VA_ERR_TIMEOUT: return "device-side wait timed out";
+    case VA_ERR_DEVICE: return "device-side bounds check failed";
+    default: return "unknown status";
+  }
+}
+
+VA_EXPORT int va_set_wait_limit(int64_t cycles) {
+  if (cycles < 1000) return VA_ERR_INVALID;
+  g_wait_limit = cycles;
+  return VA_OK;
+}
+
+VA_EXPORT int va_device_error(va_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status(e);
+  int word = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&word, va::g_err_word, sizeof(int));
+  if (e != cudaSuccess) return cuda_status(e);
+  e = cudaMemcpyToSymbol(va::g_err_word, &zero, sizeof(int));
+  if (e != cudaSuccess) return cuda_status(e);
+  return word;
+}
+
+// ------------------------------------------------------------------ masks --
+
+VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params* params,
+                            int step, va_mask** out, va_stream_t stream) {
+  if (out == nullptr || params == nullptr) return VA_ERR_INVALID;
+  *out = nullptr;
+  if (kind != VA_MASK_DENSE && kind != VA_MASK_RADIAL && kind != VA_MASK_LVSA)
+    return VA_ERR_INVALID;
+  if (T < 1 || H < 1 || W < 1) return VA_ERR_INVALID;
+  const int64_t F64 = static_cast<int64_t>(H) * W;
+  const int64_t N64 = F64 * T;
+  if (N64 >= (1LL << 30)) return VA_ERR_INVALID;
+  const va_mask_params p = *params;
+  if (p.block < 1 || p.block > 4096) return VA_ERR_INVALID;
+  if (p.w0 < 0 || p.local < 0 || p.period < 0) return VA_ERR_INVALID;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  va::MaskDesc md;
+  md.kind = kind;
+  md.T = T;
+  md.F = static_cast<int>(F64);
+  md.N = static_cast<int>(N64);
+  md.block = p.block;
+  md.nb = static_cast<int>((N64 + p.block - 1) / p.block);
+  md.w0 = (kind == VA_MASK_RADIAL && p.w0 == 0) ? md.F : p.w0;
+  md.local = p.local;
+  md.period = p.period;
+  md.anchor0 = p.anchor0;
+  md.rot_stride = p.rot_stride;
+  md.step = step;
+
+  va_mask* m = new va_mask();
+  m->kind = kind;
+  m->T = T;
+  m->H = H;
+  m->W = W;
+  m->N = md.N;
+  m->step = step;
+  m->p = p;
+  m->nqb = md.nb;
+  cudaGetDevice(&m->device);
+
+  int st = VA_OK;
+  {
+    Scoped scratch(s);
+    int* cnt = nullptr;
+    long long* keytok = nullptr;
+    long long* summary = nullptr;
+    int* hist = nullptr;
+    if ((st = scratch.alloc(&cnt, md.nb)) || (st = scratch.alloc(&keytok, md.nb)) ||
+        (st = scratch.alloc(&summary, 2)) || (st = scratch.alloc(&hist, md.nb + 1))) {
+      delete m;
+      return st;
+    }
+    if (Scoped::fault_injected()) {
+      delete m;
+      return VA_ERR_OOM;
+    }
+    if ((st = cuda_status(cudaMalloc(&m->row_ptr, sizeof(int32_t) * (md.nb + 1)))) ||
+        (st = cuda_status(cudaMalloc(&m->order, sizeof(int32_t) * md.nb)))) {
+      va_mask_free(m);
+      return st;
+    }
+    const int threads = 256;
+    const int blocks = (md.nb * 32 + threads - 1) / threads;
+    va::mask_count_kernel<<<blocks, threads, 0, s>>>(md, cnt, keytok);
+    va::mask_scan_kernel<<<1, 1024, 0, s>>>(md, cnt, keytok, m->row_ptr, summary, m->order, hist);
+    if ((st = launch_status())) {
+      va_mask_free(m);
+      return st;
+    }
+    long long host_summary[2] = {0, 0};
+    if ((st = cuda_status(cudaMemcpyAsync(host_summary, summary, sizeof(host_summary),
+                                          cudaMemcpyDeviceToHost, s))) ||
+        (st = cuda_status(cudaStreamSynchronize(s)))) {
+      va_mask_free(m);
+      return st;
+    }
+    m->nnz = host_summary[0];
+    m->live_pairs = host_summary[1];
+    if ((st = cuda_status(cudaMalloc(&m->col, sizeof(int32_t) * (m->nnz > 0 ? m->nnz : 1))))) {
+      va_mask_free(m);
+      return st;
+    }
+    va::mask_fill_kernel<<<blocks, threads, 0, s>>>(md, m->row_ptr, m->col);
+    if ((st = launch_status())) {
+      va_mask_free(m);
+      return st;
+    }
+  }
+  if ((st = cuda_status(cudaStreamSynchronize(s)))) {
+    va_mask_free(m);
+    return st;
+  }
+  *out = m;
+  return VA_OK;
+}
+
+VA_EXPORT int va_mask_csr(const va_mask* m, const int32_t** row_ptr_dev,
+                          const int32_t** col_idx_dev, int* nqb, int64_t* nnz) {
+  if (m == nullptr) return VA_ERR_INVALID;
+  if (row_ptr_dev) *row_ptr_dev = m->row_ptr;
+  if (col_idx_dev) *col_idx_dev = m->col;
+  if (nqb) *nqb = m->nqb;
+  if (nnz) *nnz = m->nnz;
+  return VA_OK;
+}
+
+VA_EXPORT int va_mask_info(const va_mask* m, int* N, int* block, int64_t* live_pairs) {
+  if (m == nullptr) return VA_ERR_INVALID;
+  if (N) *N = m->N;
+  if (block) *block = m->p.block;
+  if (live_pairs) *live_pairs = m->live_pairs;
+  return VA_OK;
+}
+
+VA_EXPORT int va_mask_to_host(const va_mask* m, int32_t* row_ptr, int32_t* col_idx) {
+  if (m == nullptr || row_ptr == nullptr || (col_idx == nullptr && m->nnz > 0))
+    return VA_ERR_INVALID;
+  int st = cuda_status(
+      cudaMemcpy(row_ptr, m->row_ptr, sizeof(int32_t) * (m->nqb + 1), cudaMemcpyDeviceToHost));
+  if (st) return st;
+  if (m->nnz > 0)
+    st = cuda_status(
+        cudaMemcpy(col_idx, m->col, sizeof(int32_t) * m->nnz, cudaMemcpyDeviceToHost));
+  return st;
+}
+
+VA_EXPORT int va_mask_free(va_mask* m) {
+  if (m == nullptr) return VA_OK;
+  if (m->row_ptr) cudaFree(m->row_ptr);
+  if (m->col) cudaFree(m->col);
+  if (m->order) cudaFree(m->order);
+  delete m;
+  return VA_OK;
+}
+
+// -------------------------------------------------------------- attention --
+
+namespace {
+
+template <typename T, int D, int BLK>
+int launch_simt(const void* q, const void* k, const void* v, const va_mask* m, void* out,
+                float* lse, int BH, int N, float scale, cudaStream_t s) {
+  dim3 grid(m->nqb, BH);
+  va::attn_simt_kernel<T, D, BLK><<<grid, BLK * 4, 0, s>>>(
+      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), m->row_ptr,
+      m->col, static_cast<T*>(out), lse, N, scale * 1.4426950408889634f);
+  return launch_status();
+}
+
+}  // namespace
+
+VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mask* m,
+                                 void* out, float* lse, int B, int heads, int N, int d,
+                                 float scale, int dtype, va_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || m == nullptr || out == nullptr)
+    return VA_ERR_INVALID;
+  if (B < 1 || heads < 1 || N != m->N) return VA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VA_ERR_INVALID;
+  if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return VA_ERR_INVALID;
+  if (!std::isfinite(scale)) return VA_ERR_INVALID;
+  const int64_t BH64 = static_cast<int64_t>(B) * heads;
+  if (BH64 > 65535) return VA_ERR_UNSUPPORTED;
+  const int BH = static_cast<int>(BH64);
+  const int blk = m->p.block;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == VA_F32) {
+    if (d == 64 && blk == 64) return launch_simt<float, 64, 64>(q, k, v, m, out, lse, BH, N, scale, s);
+    if (d == 64 && blk == 128) return launch_simt<float, 64, 128>(q, k, v, m, out, lse, BH, N, scale, s);
+    if (d == 128 && blk == 64) return launch_simt<float, 128, 64>(q, k, v, m, out, lse, BH, N, scale, s);
+    if (d == 128 && blk == 128) return launch_simt<float, 128, 128>(q, k, v, m, out, lse, BH, N, scale, s);
+    return VA_ERR_UNSUPPORTED;
+  }
+  if (dtype == VA_BF16) {
+    if (d == 128 && blk == 128)
+      return launch_simt<__nv_bfloat16, 128, 128>(q, k, v, m, out, lse, BH, N, scale, s);
+    return VA_ERR_UNSUPPORTED;
+  }
+  return VA_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------------------ clustering --
+
+VA_EXPORT int va_cluster(const void* x, const int32_t* init_idx, int B, int heads, int N, int d,
+                         int C, int iters, int dtype, int32_t* assign, float* centroid,
+                         int32_t* count, va_stream_t stream) {
+  (void)x; (void)init_idx; (void)B; (void)heads; (void)N; (void)d; (void)C; (void)iters;
+  (void)dtype; (void)assign; (void)centroid; (void)count; (void)stream;
+  return VA_ERR_UNSUPPORTED;
+}
+
+VA_EXPORT int va_compensate_route(const void* q, const void* k, const void* v,
+                                  const int32_t* qassign, int Cq, const int32_t* kassign, int Ck,
+                                  double density, float scale, int B, int heads, int N, int d,
+                                  int dtype, void* out, float* err_out, uint8_t* sel_out,
+                                  va_stream_t stream) {
+  (void)q; (void)k; (void)v; (void)qassign; (void)Cq; (void)kassign; (void)Ck; (void)density;
+  (void)scale; (void)B; (void)heads; (void)N; (void)d; (void)dtype; (void)out; (void)err_out;
+  (void)sel_out; (void)stream;
+  return VA_ERR_UNSUPPORTED;
+}

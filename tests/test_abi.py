@@ -1,0 +1,67 @@
+"""The C-ABI library loads and exports every entry point include/va.h declares.
+
+No compute call is made here (no GPU needed); argument validation that
+returns before touching the device is checked.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "va.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(?:int|const char\s*\*)\s+(va_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_attention_video_fwd_b300.build import build
+    build()
+    return ctypes.CDLL(os.path.join(ROOT, "linear_attention_video_fwd_b300", "libva.so"))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("va_mask_build", "va_sparse_attn_fwd", "va_cluster", "va_compensate_route",
+                 "va_device_error", "va_mask_free", "va_mask_csr", "va_mask_to_host"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_only_declared_symbols_are_exported():
+    import subprocess
+    so = os.path.join(ROOT, "linear_attention_video_fwd_b300", "libva.so")
+    out = subprocess.run(["nm", "-D", "--defined-only", so], capture_output=True, text=True).stdout
+    exported = sorted({ln.split()[-1] for ln in out.splitlines() if " T va_" in ln})
+    assert exported == declared_functions()
+
+
+def test_status_strings_and_version(lib):
+    lib.va_status_string.restype = ctypes.c_char_p
+    assert lib.va_status_string(0) == b"ok"
+    assert lib.va_status_string(-5) == b"device-side wait timed out"
+    assert lib.va_version() >= 100
+
+
+def test_validation_before_device_work(lib):
+    # null output handle / params: rejected on the host
+    assert lib.va_mask_build(1, 4, 4, 4, None, 0, None, None) == -1
+    assert lib.va_sparse_attn_fwd(None, None, None, None, None, None, 1, 1, 1, 128,
+                                  ctypes.c_float(1.0), 1, None) == -1
+    assert lib.va_set_wait_limit(ctypes.c_int64(10)) == -1
+    assert lib.va_set_wait_limit(ctypes.c_int64(4000000000)) == 0
+
+
+def test_python_binding_imports():
+    import linear_attention_video_fwd_b300 as va
+    assert va.status_string(va.ERR_OOM) == "device allocation failed"

@@ -1,0 +1,119 @@
+"""GPU block-sparse attention vs the float64 oracle.
+
+bf16 inputs: max-abs <= 2e-2 and mean-abs <= 2e-3; fp32 inputs: max-abs <= 1e-4.
+Small cases are compared on every output; full-size workloads on 512 seeded
+sampled query rows (always including rows 0, N-1 and the first row of the
+ragged last block) of every (batch, head).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from conftest import assert_bf16_close, cached_video_qkv
+from oracle import attention as OA
+from oracle import masks as OM
+
+pytestmark = pytest.mark.gpu
+
+
+def _mask(va, kind, T, H, W, p, step=0):
+    return va.mask_build(kind, T, H, W, block=p.block, w0=p.w0, local=p.local, period=p.period,
+                         anchor0=p.anchor0, rot_stride=p.rot_stride, step=step)
+
+
+def _run(va, dev, q, k, v, kind, T, H, W, p, step, dtype, rows=None, scale=None):
+    B, Hh, N, d = q.shape
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    qt, kt, vt = (torch.from_numpy(x).to(dev, tdt) for x in (q, k, v))
+    m = _mask(va, kind, T, H, W, p, step)
+    lse = torch.empty((B, Hh, N), dtype=torch.float32, device=dev)
+    out, _ = va.sparse_attn_fwd(qt, kt, vt, m, scale=scale, lse=lse)
+    assert va.device_error() == va.OK
+    bm = OM.block_mask(kind, T, H, W, p, step)
+    o_ref, lse_ref = OA.block_sparse_attention(q, k, v, bm, p.block, scale, rows=rows)
+    got = out.float().cpu().numpy()
+    got_lse = lse.cpu().numpy()
+    if rows is not None:
+        got, got_lse = got[:, :, rows], got_lse[:, :, rows]
+    m.free()
+    return got, o_ref, got_lse, lse_ref
+
+
+def test_tiny_lvsa_fp32(va, dev):
+    # B=1, 2 heads, 4 frames of 8x8, d=64, i.i.d. N(0,1) fp32, block 64,
+    # +-1 frame window + anchor frame 0, scale 1/8.
+    q, k, v = synth.iid_qkv(1, 2, 256, 64, seed=1235)
+    got, want, gl, wl = _run(va, dev, q, k, v, OM.LVSA, 4, 8, 8, OM.MaskParams(block=64, local=1),
+                             0, "f32", scale=0.125)
+    assert np.abs(got - want).max() <= 1e-4
+    assert np.abs(gl - wl).max() <= 1e-4
+
+
+@pytest.mark.parametrize("d,block", [(64, 128), (128, 64), (128, 128)])
+def test_fp32_other_shapes(va, dev, d, block):
+    T, H, W = 5, 6, 11                                    # N = 330: ragged last block
+    q, k, v = synth.iid_qkv(2, 2, T * H * W, d, seed=7)
+    got, want, gl, wl = _run(va, dev, q, k, v, OM.RADIAL, T, H, W, OM.MaskParams(block=block, w0=9),
+                             0, "f32")
+    assert np.abs(got - want).max() <= 1e-4
+    assert np.abs(gl - wl).max() <= 1e-4
+
+
+SMALL_BF16 = [
+    (OM.RADIAL, 5, 6, 20, OM.MaskParams(block=128, w0=10), 0),          # N=600, tail 88
+    (OM.RADIAL, 9, 8, 16, OM.MaskParams(block=128), 0),                 # N=1152, no tail
+    (OM.LVSA, 12, 7, 9, OM.MaskParams(block=128, local=1, period=4, anchor0=2, rot_stride=3), 2),
+    (OM.DENSE, 3, 7, 13, OM.MaskParams(block=128), 0),                 # N=273
+    (OM.RADIAL, 1, 3, 5, OM.MaskParams(block=128), 0),                  # N=15 < block
+    (OM.DENSE, 1, 1, 1, OM.MaskParams(block=128), 0),                   # N=1
+]
+
+
+@pytest.mark.parametrize("case", SMALL_BF16)
+def test_bf16_small_all_rows(va, dev, case):
+    kind, T, H, W, p, step = case
+    q, k, v = synth.video_qkv(2, 3, T, H, W, 128, seed=11)
+    got, want, gl, wl = _run(va, dev, q, k, v, kind, T, H, W, p, step, "bf16")
+    assert_bf16_close(got, want)
+    assert np.abs(gl - wl).max() <= 2e-2
+
+
+def test_bf16_single_live_key_block_extremes(va, dev):
+    # Large-magnitude logits (scale 1): the online softmax must stay finite.
+    T, H, W = 4, 8, 16
+    q, k, v = synth.video_qkv(1, 2, T, H, W, 128, seed=12)
+    got, want, gl, wl = _run(va, dev, q * 4, k * 4, v, OM.RADIAL, T, H, W,
+                             OM.MaskParams(block=128, w0=3), 0, "bf16", scale=1.0)
+    assert_bf16_close(got, want)
+
+
+def test_wan_radial_full_size_sampled_rows(va, dev):
+    # The benchmarked workload: B=1, 12 heads, 21x30x52 = 32,760 tokens, d=128,
+    # bf16, radial mask with block 128 (W0 = H*W).
+    T, H, W = 21, 30, 52
+    q, k, v = cached_video_qkv(1, 12, T, H, W, 128, seed=1235)
+    rows = OA.sample_rows(T * H * W, 128, 512, seed=5)
+    got, want, gl, wl = _run(va, dev, q, k, v, OM.RADIAL, T, H, W, OM.MaskParams(block=128),
+                             0, "bf16", rows=rows)
+    assert_bf16_close(got, want)
+    assert np.abs(gl - wl).max() <= 2e-2
+
+
+def test_attention_rejects_bad_arguments(va, dev):
+    q = torch.zeros((1, 1, 240, 128), dtype=torch.bfloat16, device=dev)
+    m = va.mask_build(va.RADIAL, 3, 4, 20)
+    with pytest.raises(va.VAError) as e:                 # N mismatch
+        va.sparse_attn_fwd(q[:, :, :200].contiguous(), q[:, :, :200].contiguous(),
+                           q[:, :, :200].contiguous(), m)
+    assert e.value.status == va.ERR_INVALID
+    q96 = torch.zeros((1, 1, 240, 96), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(va.VAError) as e:                 # head_dim 96
+        va.sparse_attn_fwd(q96, q96, q96, m)
+    assert e.value.status == va.ERR_UNSUPPORTED
+    m64 = va.mask_build(va.RADIAL, 3, 4, 20, block=64)
+    with pytest.raises(va.VAError) as e:                 # bf16 needs block 128
+        va.sparse_attn_fwd(q, q, q, m64)
+    assert e.value.status == va.ERR_UNSUPPORTED
+    assert va.device_error() == va.OK

@@ -1,0 +1,80 @@
+"""GPU mask builder vs the oracle: CSR lists must be bit-exact."""
+import numpy as np
+import pytest
+
+from oracle import masks as OM
+
+pytestmark = pytest.mark.gpu
+
+R, L, D = OM.RADIAL, OM.LVSA, OM.DENSE
+
+SMALL = [
+    # kind, T, H, W, params, step
+    (L, 4, 8, 8, OM.MaskParams(block=64, local=1), 0),                       # tiny LVSA check
+    (R, 4, 1, 8, OM.MaskParams(block=4, w0=2), 0),
+    (R, 5, 3, 7, OM.MaskParams(block=16), 0),
+    (R, 9, 4, 4, OM.MaskParams(block=32, w0=3), 0),
+    (R, 3, 1, 1, OM.MaskParams(block=2), 0),                                 # F = 1
+    (R, 7, 5, 6, OM.MaskParams(block=64, w0=5), 0),
+    (R, 40, 2, 3, OM.MaskParams(block=128, w0=6), 0),                        # block spans frames
+    (L, 11, 2, 3, OM.MaskParams(block=8, local=2, period=3, anchor0=1, rot_stride=2), 1),
+    (L, 10, 5, 5, OM.MaskParams(block=16, local=0, period=4, anchor0=-3, rot_stride=5), 7),
+    (L, 6, 4, 4, OM.MaskParams(block=1, local=1, period=0, anchor0=5), 0),   # block 1
+    (D, 3, 5, 7, OM.MaskParams(block=16), 0),
+    (D, 1, 1, 1, OM.MaskParams(block=128), 0),                               # N = 1
+    (R, 1, 3, 5, OM.MaskParams(block=128), 0),                               # N < block
+]
+
+FULL = [
+    (R, 21, 30, 52, OM.MaskParams(block=128), 0),                            # Wan-shaped
+    (L, 126, 30, 52, OM.MaskParams(block=128, local=2, period=8, rot_stride=1), 0),
+    (L, 126, 30, 52, OM.MaskParams(block=128, local=2, period=8, rot_stride=1), 1),
+    (L, 126, 30, 52, OM.MaskParams(block=128, local=2, period=8, rot_stride=1), 2),
+    (L, 126, 30, 52, OM.MaskParams(block=128, local=2, period=8, rot_stride=1), 3),
+    (R, 33, 45, 80, OM.MaskParams(block=128), 0),                            # HunyuanVideo 720p
+    (D, 33, 45, 80, OM.MaskParams(block=128), 0),
+]
+
+
+def _build(va, kind, T, H, W, p, step):
+    return va.mask_build(kind, T, H, W, block=p.block, w0=p.w0, local=p.local, period=p.period,
+                         anchor0=p.anchor0, rot_stride=p.rot_stride, step=step)
+
+
+@pytest.mark.parametrize("case", SMALL + FULL)
+def test_mask_csr_bit_exact(va, case):
+    kind, T, H, W, p, step = case
+    m = _build(va, kind, T, H, W, p, step)
+    rp, col = m.csr()
+    bm = OM.block_mask(kind, T, H, W, p, step)
+    want_rp, want_col = OM.to_csr(bm)
+    assert m.nqb == bm.shape[0] and m.nnz == len(want_col)
+    assert np.array_equal(rp, want_rp)
+    assert np.array_equal(col, want_col)
+    assert m.live_pairs == OM.live_pair_tokens(bm, p.block, T * H * W)
+    m.free()
+    assert va.device_error() == va.OK
+
+
+def test_mask_rejects_bad_arguments(va):
+    with pytest.raises(va.VAError) as e:
+        va.mask_build(va.RADIAL, 0, 4, 4)
+    assert e.value.status == va.ERR_INVALID
+    with pytest.raises(va.VAError):
+        va.mask_build(va.RADIAL, 4, 4, 4, block=0)
+    with pytest.raises(va.VAError):
+        va.mask_build(va.LVSA, 4, 4, 4, period=-1)
+    with pytest.raises(va.VAError):
+        va.mask_build(7, 4, 4, 4)
+    with pytest.raises(va.VAError):
+        va.mask_build(va.RADIAL, 1 << 12, 1 << 10, 1 << 9)       # N >= 2^30
+
+
+def test_mask_allocation_failure_is_reported(va, monkeypatch):
+    monkeypatch.setenv("VA_FAULT_INJECT", "alloc")
+    with pytest.raises(va.VAError) as e:
+        va.mask_build(va.RADIAL, 4, 4, 4)
+    assert e.value.status == va.ERR_OOM
+    monkeypatch.delenv("VA_FAULT_INJECT")
+    m = va.mask_build(va.RADIAL, 4, 4, 4, block=16)
+    assert m.nnz > 0
