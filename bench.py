@@ -1,0 +1,347 @@
+"""Benchmark: block-sparse video attention forward on B300.
+
+Workload (one "step"): one va_sparse_attn_fwd call of the Wan-2.1-1.3B-shaped
+radial-mask attention: B=1, 12 heads, 21x30x52 = 32,760 tokens, head_dim 128,
+bf16, 128-token blocks, radial mask with W0 = H*W (29,786 of 65,536 block
+pairs live). The static mask is built once before timing (it is shared by
+every step, layer and head). Inputs are synthetic (seeded Fourier-mode Q/K,
+N(0,1) V) and resident in HBM when device timing starts; one call touches
+Q+K+V+O = 403 MB, more than the 126 MB L2, so no flush is needed between
+timed calls.
+
+Metric: effective TFLOP/s over live blocks, i.e. 4 * d * (sum over live block
+pairs of |I| * |J|, real tokens only) * B * heads per call, and ms per call.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own copy of the workload (weak
+scaling, no collective on the data path); rank 0 prints one JSON line.
+--impl reference times the float64 CPU oracle (the only reference there is)
+on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+T, H, W, HEADS, BATCH, D, BLOCK = 21, 30, 52, 12, 1, 128, 128
+N = T * H * W
+METRIC = "block-sparse attn effective TFLOP/s + ms/call at 32,760 tok; % of B300 BF16 peak"
+UNIT = "TFLOP/s"
+SEED = 1235
+CONFIG = {"workload": "Wan-2.1-1.3B-shaped radial block-sparse attention forward",
+          "B": BATCH, "heads": HEADS, "grid_THW": [T, H, W], "tokens": N, "head_dim": D,
+          "block": BLOCK, "mask": "radial, W0=H*W", "live_blocks": "29786/65536",
+          "l2": "inputs larger than L2 (Q+K+V+O = 403 MB per call vs 126 MB L2), no flush"}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_tc_wan_radial_traffic.json")
+KERNEL_SRC = os.path.join(ROOT, "linear_attention_video_fwd_b300", "csrc", "attn_tc.cuh")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6400.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason sampling (every 200 ms) while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.samples = []
+        self._proc = None
+        self._t = None
+
+    def _reader(self):
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def __enter__(self):
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._reader, daemon=True)
+            self._t.start()
+        except OSError:
+            self._proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+            self._t.join(timeout=5)
+
+    def summary(self):
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(s[1]) for s in self.samples) if v is not None]
+        smax = [v for v in (num(s[2]) for s in self.samples) if v is not None]
+        reasons = sorted({self.REASONS[i] for s in self.samples for i in range(4)
+                          if s[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(os.environ.get("VA_BENCH_BACKEND", "nccl"))
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        rec = json.load(f)
+    if rec.get("kernel_sha256_16") != kernel_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def threads_used() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def make_inputs(seed):
+    import synth
+    return synth.video_qkv(BATCH, HEADS, T, H, W, D, seed=seed, dtype="bf16")
+
+
+def oracle_sample(q, k, v, bm, rows):
+    """Run the float64 oracle on `rows` of every head; returns (seconds, live FLOPs done)."""
+    from oracle import attention as OA
+    live_keys_per_block = (bm * np.array([min(N, (b + 1) * BLOCK) - b * BLOCK
+                                          for b in range(bm.shape[0])])[None, :]).sum(1)
+    flops = 4.0 * D * float(live_keys_per_block[rows // BLOCK].sum()) * BATCH * HEADS
+    t0 = time.perf_counter()
+    OA.block_sparse_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(D), rows=rows)
+    return time.perf_counter() - t0, flops
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import linear_attention_video_fwd_b300 as va
+    from oracle import attention as OA
+    from oracle import masks as OM
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v = make_inputs(SEED + rank)
+    qt, kt, vt = (torch.from_numpy(x).to(dev, torch.bfloat16) for x in (q, k, v))
+    out = torch.empty_like(qt)
+    mask = va.mask_build(va.RADIAL, T, H, W, block=BLOCK)
+    flops = 4.0 * D * mask.live_pairs * BATCH * HEADS
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
+    if va.device_error() != va.OK:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- device-timed region: inputs resident in HBM --------------------------
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        time.sleep(0.3)
+        t_begin.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
+            ends[i].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    if va.device_error() != va.OK:
+        raise RuntimeError("device error in the timed region")
+    total_ms = t_begin.elapsed_time(t_end)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(total_ms, world, dev)
+    ms_per_step = total_ms / args.steps
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ------------------
+    qh, kh, vh = (x.to("cpu").pin_memory() for x in (qt, kt, vt))
+    oh = torch.empty(qh.shape, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        qt.copy_(qh, non_blocking=True); kt.copy_(kh, non_blocking=True); vt.copy_(vh, non_blocking=True)
+        va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
+        oh.copy_(out, non_blocking=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        qt.copy_(qh, non_blocking=True); kt.copy_(kh, non_blocking=True); vt.copy_(vh, non_blocking=True)
+        va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
+        oh.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+    tensor_bytes = qt.numel() * qt.element_size()
+
+    pk, src = peaks()
+    achieved = flops / (float(np.mean(launch_ms)) * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Fourier-mode Q/K + N(0,0.5^2), V~N(0,1)); no weights needed",
+        "config": dict(CONFIG, parallelism="replicas: one independent workload per GPU"),
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": 3 * tensor_bytes, "d2h_bytes_per_step": tensor_bytes},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2),
+                     "peak": pk["bf16_tflops"], "unit": UNIT,
+                     "frac": round(achieved / pk["bf16_tflops"], 4),
+                     "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json)" % src
+                     if src == "measured" else "fallback 1800 TFLOP/s",
+                     "frac_of_sustained": round(achieved / pk["bf16_tflops_sustained"], 4),
+                     "flops_per_launch": flops, "launch_ms_mean": round(float(np.mean(launch_ms)), 4),
+                     "launch_ms_min": round(float(np.min(launch_ms)), 4),
+                     "traffic": profiled_traffic(), "kernel": "va::attn_tc_kernel"},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        bm = OM.block_mask(OM.RADIAL, T, H, W, OM.MaskParams(block=BLOCK))
+        rows = OA.sample_rows(N, BLOCK, args.oracle_rows, seed=7)
+        secs, oflops = oracle_sample(q, k, v, bm, rows)
+        line["cpu_baseline"] = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT,
+                                "cores": threads_used(), "kind": "oracle",
+                                "seconds": round(secs, 2),
+                                "sample": "%d seeded query rows x %d heads of the same workload "
+                                          "(float64 numpy oracle, masked dense rows)"
+                                          % (len(rows), HEADS)}
+    mask.free()
+    return line
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: bounded samples of the same workload per step."""
+    if rank != 0:
+        return None
+    from oracle import attention as OA
+    from oracle import masks as OM
+    q, k, v = make_inputs(SEED)
+    bm = OM.block_mask(OM.RADIAL, T, H, W, OM.MaskParams(block=BLOCK))
+    per_step = args.reference_rows
+    for i in range(args.warmup):
+        oracle_sample(q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=1000 + i))
+    secs, fl = 0.0, 0.0
+    for i in range(args.steps):
+        s, f = oracle_sample(q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=2000 + i))
+        secs += s
+        fl += f
+    value = fl / secs / 1e12
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (same seeded inputs as the GPU arm)", "impl": "reference",
+        "config": dict(CONFIG, parallelism="single process, host cores"),
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads_used(),
+                         "kind": "oracle",
+                         "sample": "%d seeded query rows x %d heads per step" % (per_step, HEADS)},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--oracle-rows", type=int, default=512,
+                    help="query rows per head in the CPU-oracle baseline sample")
+    ap.add_argument("--reference-rows", type=int, default=16,
+                    help="query rows per head per step of the reference (oracle) arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if world != args.gpus:
+        print("warning: --gpus %d but WORLD_SIZE %d" % (args.gpus, world), file=sys.stderr)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+    else:
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -12,6 +12,7 @@
 #include "common.cuh"
 #include "mask.cuh"
 #include "attn_simt.cuh"
+#include "attn_tc.cuh"
 
 #define VA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -60,6 +61,42 @@ int cuda_status(cudaError_t e) {
 int launch_status() { return cuda_status(cudaGetLastError()); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  }
+  return fn;
+}
+
+// 3-D map over a [BH, N, D] bf16 tensor: box of 64 dims x 128 rows x 1 head,
+// 128-byte swizzle; rows beyond N read as zeros.
+int encode_bf16_rows(CUtensorMap* map, const void* base, int BH, int N, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return VA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VA_OK : VA_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -257,6 +294,39 @@ int launch_simt(const void* q, const void* k, const void* v, const va_mask* m, v
   return launch_status();
 }
 
+int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, void* out, float* lse,
+              int BH, int N, float scale, cudaStream_t s) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    int st = cuda_status(cudaFuncSetAttribute(
+        va::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, va::TC_SMEM_BYTES));
+    if (st) return st;
+    configured[dev] = true;
+  }
+  CUtensorMap mq, mk, mv;
+  int st;
+  if ((st = encode_bf16_rows(&mq, q, BH, N, 128)) || (st = encode_bf16_rows(&mk, k, BH, N, 128)) ||
+      (st = encode_bf16_rows(&mv, v, BH, N, 128)))
+    return st;
+  va::TcArgs a;
+  a.row_ptr = m->row_ptr;
+  a.col = m->col;
+  a.order = m->order;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.N = N;
+  a.nqb = m->nqb;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit = g_wait_limit;
+  const long long grid = static_cast<long long>(m->nqb) * BH;
+  if (grid > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
+  va::attn_tc_kernel<<<static_cast<unsigned>(grid), va::TC_THREADS, va::TC_SMEM_BYTES, s>>>(
+      mq, mk, mv, a);
+  return launch_status();
+}
+
 }  // namespace
 
 VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mask* m,
@@ -269,7 +339,8 @@ VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, co
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return VA_ERR_INVALID;
   if (!std::isfinite(scale)) return VA_ERR_INVALID;
   const int64_t BH64 = static_cast<int64_t>(B) * heads;
-  if (BH64 > 65535) return VA_ERR_UNSUPPORTED;
+  if (BH64 > 65535 && dtype == VA_F32) return VA_ERR_UNSUPPORTED;
+  if (BH64 * N >= (1LL << 31)) return VA_ERR_UNSUPPORTED;
   const int BH = static_cast<int>(BH64);
   const int blk = m->p.block;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -281,8 +352,7 @@ VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, co
     return VA_ERR_UNSUPPORTED;
   }
   if (dtype == VA_BF16) {
-    if (d == 128 && blk == 128)
-      return launch_simt<__nv_bfloat16, 128, 128>(q, k, v, m, out, lse, BH, N, scale, s);
+    if (d == 128 && blk == 128) return launch_tc(q, k, v, m, out, lse, BH, N, scale, s);
     return VA_ERR_UNSUPPORTED;
   }
   return VA_ERR_UNSUPPORTED;
