@@ -21,8 +21,8 @@ def declared_functions():
 
 @pytest.fixture(scope="module")
 def lib():
-    from linear_attention_video_fwd_b300.build import build
-    build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     return ctypes.CDLL(os.path.join(ROOT, "linear_attention_video_fwd_b300", "libva.so"))
 
 
