@@ -1,27 +1,34 @@
 // Block-sparse flash-attention forward on the 5th-generation tensor cores
 // (tcgen05 + TMEM + TMA), bf16 inputs, head_dim 128, 128-token blocks.
 //
-// One CTA per (batch*head, query block I); CTAs are ordered head-major and,
-// within a head, by descending CSR row length (longest first), so the K/V
-// working set of the CTAs in flight stays within L2 and the grid tail holds
-// the shortest rows. 192 threads:
-//   warp 0      TMA producer: Q tile once, then K_j and V_j of every live key
-//               block j of row I into a ring of NS stages (128B-swizzled);
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//               score buffers, O += P_j V_j with P_j read from TMEM;
-//   warps 2..5  softmax / correction / epilogue; thread r owns query row r
-//               (TMEM lane r), so row max and row sum need no shuffles.
-// Tensor-pipe order: QK(0), QK(1), PV(0), QK(2), PV(1), ... so the softmax of
-// block j overlaps PV(j-1) and QK(j+1).
+// Work unit: one CTA per (batch*head, query-block pair {2P, 2P+1}). The two
+// query tiles share one stream of K/V tiles: the union of the two CSR rows,
+// precomputed at mask build time as entries (J << 2 | live bits), so every
+// key block that either tile needs is fetched once. CTAs run head-major and,
+// within a head, longest pair first (LPT), so the K/V working set in flight
+// stays in L2 and the grid tail holds the shortest pairs.
 //
-// TMEM (512 columns): S buffers at columns [0,128) and [128,256) (fp32; P_j
-// is written back over the first 64 columns of its S buffer as packed bf16
-// pairs), O accumulator at [256,384).
+// 384 threads (12 warps):
+//   warp 0       TMA producer: Q tiles once, then K_u and V_u of every union
+//                entry u into rings of NK and NV stages (128B-swizzled);
+//   warp 1       MMA issuer (one thread): for tile t live at u,
+//                S_t = Q_t K_u^T into TMEM, and O_t += P_t V_u once the
+//                softmax of tile t has written P_t;
+//   warps 2, 3   idle (they only take part in set-up and tear-down);
+//   warps 4..7   softmax / correction / epilogue of tile 0,
+//   warps 8..11  the same for tile 1; thread r of a group owns query row r
+//                (TMEM lane r), so row max and row sum need no shuffles.
+// Tensor-pipe order per union entry: PV_0(prev), QK_0(u), PV_1(prev), QK_1(u):
+// the softmax of tile 0 overlaps the MMAs of tile 1 and the other way round.
+//
+// TMEM (512 columns): tile t uses columns [256t, 256t + 128) for S_t (fp32;
+// P_t is written back over its first 64 columns as packed bf16 pairs) and
+// [256t + 128, 256t + 256) for the O_t accumulator.
 //
 // Online softmax in the log2 domain: the running max used for exponentiation
 // is only raised when a block's max exceeds it by more than TAU (so P <= 2^TAU
-// and fp32 O/l stay exact to rounding); raising it rescales O in TMEM after
-// waiting for the previous PV to complete.
+// and fp32 O and l stay exact to rounding); raising it rescales O_t in TMEM
+// after waiting for the previous PV_t to complete.
 //
 // Every mbarrier wait is bounded (clock64 limit): on a timeout the CTA records
 // VA_ERR_TIMEOUT in the device error word, drains its own copies and MMAs
@@ -34,35 +41,49 @@ namespace va {
 
 constexpr int TC_BLK = 128;
 constexpr int TC_D = 128;
-constexpr int TC_NS = 2;                    // K/V ring stages
-constexpr int TC_THREADS = 192;
+constexpr int TC_NK = 2;                    // K ring stages
+constexpr int TC_NV = 2;                    // V ring stages
+constexpr int TC_THREADS = 384;
 constexpr int TC_TILE_BYTES = TC_BLK * TC_D * 2;  // 32 KB: one 128 x 128 bf16 tile
 constexpr int TC_HALF_BYTES = TC_TILE_BYTES / 2;  // 16 KB: 128 rows x 64 dims
-constexpr int TC_SMEM_BYTES = 1024 + TC_TILE_BYTES * (1 + 2 * TC_NS);
+constexpr int TC_SMEM_BYTES = 1024 + TC_TILE_BYTES * (2 + TC_NK + TC_NV);
 constexpr float TC_TAU = 8.0f;
+// Register split (setmaxnreg): the kernel is compiled to TC_LAUNCH_REGS per
+// thread; warpgroup 0 (producer, MMA, idle warps) gives registers back and the
+// two softmax warpgroups take them. 128 * DEC + 256 * INC must not exceed
+// 384 * TC_LAUNCH_REGS, or the increase would wait forever; the host checks
+// the compiled register count before every first launch.
+constexpr int TC_LAUNCH_REGS = 168;
+constexpr int TC_REGS_DEC = 72;
+constexpr int TC_REGS_INC = 216;
+static_assert(128 * TC_REGS_DEC + 256 * TC_REGS_INC <= TC_THREADS * TC_LAUNCH_REGS,
+              "register split exceeds the launch allocation");
+static_assert(TC_NV >= 2 && TC_NV <= 4, "V stage bookkeeping assumes 2..4 stages");
 
 struct TcArgs {
-  const int* row_ptr;
-  const int* col;
-  const int* order;
+  const int* row_ptr;  // [nqb + 1] CSR rows
+  const int* col;      // [nnz] live key blocks per row (ascending)
+  const int* pcol;     // pair unions: pair P's entries start at row_ptr[2P]
+  const int* plen;     // [npairs] union length per pair
+  const int* porder;   // [npairs] pairs, longest first
   __nv_bfloat16* out;
   float* lse;
-  int N, nqb;
+  int N, nqb, npairs;
   float scale_log2;
   long long wait_limit;
 };
 
 // barrier slots
 enum : int {
-  B_Q_FULL = 0,
-  B_K_FULL = 1,
-  B_K_EMPTY = B_K_FULL + TC_NS,
-  B_V_FULL = B_K_EMPTY + TC_NS,
-  B_V_EMPTY = B_V_FULL + TC_NS,
-  B_S_FULL = B_V_EMPTY + TC_NS,  // 2
-  B_P_FULL = B_S_FULL + 2,       // 2
-  B_O_DONE = B_P_FULL + 2,
-  B_DRAIN = B_O_DONE + 1,
+  B_Q_FULL = 0,                  // 2 (per tile)
+  B_K_FULL = B_Q_FULL + 2,
+  B_K_EMPTY = B_K_FULL + TC_NK,
+  B_V_FULL = B_K_EMPTY + TC_NK,
+  B_V_EMPTY = B_V_FULL + TC_NV,
+  B_S_FULL = B_V_EMPTY + TC_NV,  // 2 (per tile)
+  B_P_FULL = B_S_FULL + 2,       // 2 (per tile), 128 arrivals
+  B_O_DONE = B_P_FULL + 2,       // 2 (per tile)
+  B_DRAIN = B_O_DONE + 2,
   B_COUNT = B_DRAIN + 1
 };
 
@@ -85,6 +106,206 @@ __device__ __forceinline__ void tc_issue_pv(uint32_t o_tmem, uint32_t p_tmem, ui
   }
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (d0, d1) = (a0 * b + c, a1 * b + c) as one packed f32x2 FMA.
+__device__ __forceinline__ void ffma2_bc(float& d0, float& d1, float a0, float a1, float b,
+                                         float c) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %4};\n\t"
+      "mov.b64 rc, {%5, %5};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1) as one packed f32x2 add.
+__device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rs;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rs, {%0, %1};\n\t"
+      "add.rn.f32x2 rs, rs, ra;\n\t"
+      "mov.b64 {%0, %1}, rs;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
+// Softmax of one tile: its CSR row, its TMEM columns and its barriers.
+__device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I, int bh,
+                                                uint32_t tmem, uint64_t* bars,
+                                                volatile int* abort_p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3;               // TMEM lane quarter of this warp
+  const int r = wq * 32 + lane;          // query row within the tile
+  const int row = I * TC_BLK + r;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + tile * 256 + lane_off;
+  const uint32_t tO = tS + 128;
+  const uint32_t bS = smem_u32(&bars[B_S_FULL + tile]);
+  const uint32_t bP = smem_u32(&bars[B_P_FULL + tile]);
+  const uint32_t bO = smem_u32(&bars[B_O_DONE + tile]);
+  const long long lim = a.wait_limit;
+  const float sl2 = a.scale_log2;
+  const int beg = a.row_ptr[I];
+  const int n = a.row_ptr[I + 1] - beg;
+  // Only the last live block of a row can be the ragged tail block.
+  const int tail_valid =
+      (n > 0 && a.col[beg + n - 1] == a.nqb - 1) ? a.N - (a.nqb - 1) * TC_BLK : TC_BLK;
+
+  float m_used = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < n; ++j) {
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bS, j & 1, lim, abort_p));
+    if (!ok) break;
+    tc_fence_after();
+    float s[128];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tS + c * 32, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+    }
+    tmem_wait_ld();
+    const int valid = (j == n - 1) ? tail_valid : TC_BLK;
+    if (valid < TC_BLK) {
+      // Key columns >= valid hold zero-filled rows: give them a real value of
+      // the block for the max, and a zero weight below.
+#pragma unroll
+      for (int i = 1; i < 128; ++i) s[i] = (i < valid) ? s[i] : s[0];
+    }
+    // Largest scaled logit of the block (sl2 may be negative).
+    float mx;
+    if (sl2 >= 0.f) {
+      float m0 = fmax3(s[0], s[1], s[2]), m1 = fmax3(s[3], s[4], s[5]);
+      float m2 = fmax3(s[6], s[7], s[8]), m3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+      for (int i = 12; i < 124; i += 8) {
+        m0 = fmax3(m0, s[i], s[i + 1]);
+        m1 = fmax3(m1, s[i + 2], s[i + 3]);
+        m2 = fmax3(m2, s[i + 4], s[i + 5]);
+        m3 = fmax3(m3, s[i + 6], s[i + 7]);
+      }
+      mx = fmax3(fmax3(m0, m1, s[124]), fmax3(m2, m3, s[125]), fmaxf(s[126], s[127]));
+    } else {
+      float m0 = fmin3(s[0], s[1], s[2]), m1 = fmin3(s[3], s[4], s[5]);
+      float m2 = fmin3(s[6], s[7], s[8]), m3 = fmin3(s[9], s[10], s[11]);
+#pragma unroll
+      for (int i = 12; i < 124; i += 8) {
+        m0 = fmin3(m0, s[i], s[i + 1]);
+        m1 = fmin3(m1, s[i + 2], s[i + 3]);
+        m2 = fmin3(m2, s[i + 4], s[i + 5]);
+        m3 = fmin3(m3, s[i + 6], s[i + 7]);
+      }
+      mx = fmin3(fmin3(m0, m1, s[124]), fmin3(m2, m3, s[125]), fminf(s[126], s[127]));
+    }
+    const float m_cand = mx * sl2;
+    const bool need = m_cand > m_used + TC_TAU;
+    float alpha = 1.f;
+    if (need) {
+      alpha = ex2_approx(m_used - m_cand);
+      m_used = m_cand;
+      l *= alpha;
+    }
+    if (__any_sync(0xffffffffu, need && j > 0)) {
+      // O_t holds the sum up to PV_t(j-1): wait for it, then rescale in TMEM.
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (j - 1) & 1, lim, abort_p));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+        tmem_st32(tO + c * 32, v);
+      }
+    }
+    const float neg_m = -m_used;
+#pragma unroll
+    for (int i = 0; i < 128; i += 2) {
+      ffma2_bc(s[i], s[i + 1], s[i], s[i + 1], sl2, neg_m);
+      s[i] = ex2_approx(s[i]);
+      s[i + 1] = ex2_approx(s[i + 1]);
+    }
+    if (valid < TC_BLK) {
+#pragma unroll
+      for (int i = 1; i < 128; ++i) s[i] = (i < valid) ? s[i] : 0.f;
+    }
+    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+    uint32_t pk[64];
+#pragma unroll
+    for (int i = 0; i < 128; i += 4) {
+      fadd2_acc(r0, r1, s[i], s[i + 1]);
+      fadd2_acc(r2, r3, s[i + 2], s[i + 3]);
+      pk[i / 2] = pack_bf16x2(s[i], s[i + 1]);
+      pk[i / 2 + 1] = pack_bf16x2(s[i + 2], s[i + 3]);
+    }
+    l += (r0 + r1) + (r2 + r3);
+    {
+      uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
+      uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[32]);
+      tmem_st32(tS, lo);
+      tmem_st32(tS + 32, hi);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bP);
+  }
+  // epilogue
+  const long long obase = (static_cast<long long>(bh) * a.N + row) * TC_D;
+  if (n > 0 && ok)
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (n - 1) & 1, lim, abort_p));
+  if (n > 0 && ok) {
+    tc_fence_after();
+    const float inv = 1.f / l;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tO + c * 32, v);
+      tmem_wait_ld();
+      if (row < a.N) {
+        uint4* dst = reinterpret_cast<uint4*>(a.out + obase + c * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv);
+          dst[q4] = w;
+        }
+      }
+    }
+    if (row < a.N && a.lse != nullptr)
+      a.lse[static_cast<long long>(bh) * a.N + row] = (m_used + log2f(l)) * 0.69314718055994530942f;
+  } else if (n == 0 && row < a.N) {
+    uint4* dst = reinterpret_cast<uint4*>(a.out + obase);
+#pragma unroll
+    for (int q4 = 0; q4 < 16; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
+    if (a.lse != nullptr) a.lse[static_cast<long long>(bh) * a.N + row] = -INFINITY;
+  }
+}
+
 __global__ void __launch_bounds__(TC_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
@@ -96,31 +317,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + TC_TILE_BYTES;
-  const uint32_t sV0 = sK0 + TC_NS * TC_TILE_BYTES;
+  const uint32_t sQ0 = smem_u32(smem);
+  const uint32_t sK0 = sQ0 + 2 * TC_TILE_BYTES;
+  const uint32_t sV0 = sK0 + TC_NK * TC_TILE_BYTES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  const int bh = blockIdx.x / a.nqb;
-  const int I = a.order[blockIdx.x % a.nqb];
-  const int beg = a.row_ptr[I];
-  const int n = a.row_ptr[I + 1] - beg;
+  const int bh = blockIdx.x / a.npairs;
+  const int P = a.porder[blockIdx.x % a.npairs];
+  const int I0 = 2 * P, I1 = 2 * P + 1;
+  const bool has1 = I1 < a.nqb;
+  const int pbeg = a.row_ptr[I0];
+  const int nu = a.plen[P];
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (tid == 0) {
     abort_flag = 0;
-    mbar_init(bar(B_Q_FULL), 1);
-    for (int s = 0; s < TC_NS; ++s) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(B_Q_FULL + t), 1);
+      mbar_init(bar(B_S_FULL + t), 1);
+      mbar_init(bar(B_P_FULL + t), 128);
+      mbar_init(bar(B_O_DONE + t), 1);
+    }
+    for (int s = 0; s < TC_NK; ++s) {
       mbar_init(bar(B_K_FULL + s), 1);
       mbar_init(bar(B_K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < TC_NV; ++s) {
       mbar_init(bar(B_V_FULL + s), 1);
       mbar_init(bar(B_V_EMPTY + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(B_S_FULL + b), 1);
-      mbar_init(bar(B_P_FULL + b), 128);
-    }
-    mbar_init(bar(B_O_DONE), 1);
     mbar_init(bar(B_DRAIN), 1);
     fence_barrier_init();
   }
@@ -132,83 +357,116 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t tS0 = tmem, tO = tmem + 256;
   volatile int* abort_p = &abort_flag;
   const long long lim = a.wait_limit;
 
+  if (warp >= 4) {
+    // ------------------------------------------- softmax / correction / out --
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(TC_REGS_INC));
+    const int tile = (warp - 4) >> 2;
+    if (tile == 0 || has1) tc_softmax_tile(a, tile, tile == 0 ? I0 : I1, bh, tmem, bars, abort_p);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(TC_REGS_DEC));
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
-    if (lane == 0 && n > 0) {
+    if (lane == 0 && nu > 0) {
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      mbar_arrive_expect_tx(bar(B_Q_FULL), TC_TILE_BYTES);
-      tma_load_3d(sQ, &map_q, bar(B_Q_FULL), 0, I * TC_BLK, bh);
-      tma_load_3d(sQ + TC_HALF_BYTES, &map_q, bar(B_Q_FULL), 64, I * TC_BLK, bh);
+      mbar_arrive_expect_tx(bar(B_Q_FULL + 0), TC_TILE_BYTES);
+      tma_load_3d(sQ0, &map_q, bar(B_Q_FULL + 0), 0, I0 * TC_BLK, bh);
+      tma_load_3d(sQ0 + TC_HALF_BYTES, &map_q, bar(B_Q_FULL + 0), 64, I0 * TC_BLK, bh);
+      if (has1) {
+        const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
+        mbar_arrive_expect_tx(bar(B_Q_FULL + 1), TC_TILE_BYTES);
+        tma_load_3d(sQ1, &map_q, bar(B_Q_FULL + 1), 0, I1 * TC_BLK, bh);
+        tma_load_3d(sQ1 + TC_HALF_BYTES, &map_q, bar(B_Q_FULL + 1), 64, I1 * TC_BLK, bh);
+      }
       int issued_k = 0, issued_v = 0;
-      for (int j = 0; j < n; ++j) {
-        const int st = j % TC_NS;
-        const uint32_t ph = (j / TC_NS) & 1;
-        const int J = a.col[beg + j];
-        const uint32_t sK = sK0 + st * TC_TILE_BYTES, sV = sV0 + st * TC_TILE_BYTES;
-        if (j >= TC_NS && !mbar_wait_bounded(bar(B_K_EMPTY + st), ph ^ 1, lim, abort_p)) break;
-        mbar_arrive_expect_tx(bar(B_K_FULL + st), TC_TILE_BYTES);
-        tma_load_3d(sK, &map_k, bar(B_K_FULL + st), 0, J * TC_BLK, bh);
-        tma_load_3d(sK + TC_HALF_BYTES, &map_k, bar(B_K_FULL + st), 64, J * TC_BLK, bh);
-        issued_k = j + 1;
-        if (j >= TC_NS && !mbar_wait_bounded(bar(B_V_EMPTY + st), ph ^ 1, lim, abort_p)) break;
-        mbar_arrive_expect_tx(bar(B_V_FULL + st), TC_TILE_BYTES);
-        tma_load_3d(sV, &map_v, bar(B_V_FULL + st), 0, J * TC_BLK, bh);
-        tma_load_3d(sV + TC_HALF_BYTES, &map_v, bar(B_V_FULL + st), 64, J * TC_BLK, bh);
-        issued_v = j + 1;
+      for (int u = 0; u < nu; ++u) {
+        const int J = a.pcol[pbeg + u] >> 2;
+        const int sk = u % TC_NK, sv = u % TC_NV;
+        const uint32_t sK = sK0 + sk * TC_TILE_BYTES, sV = sV0 + sv * TC_TILE_BYTES;
+        if (u >= TC_NK &&
+            !mbar_wait_bounded(bar(B_K_EMPTY + sk), ((u / TC_NK) & 1) ^ 1, lim, abort_p))
+          break;
+        mbar_arrive_expect_tx(bar(B_K_FULL + sk), TC_TILE_BYTES);
+        tma_load_3d(sK, &map_k, bar(B_K_FULL + sk), 0, J * TC_BLK, bh);
+        tma_load_3d(sK + TC_HALF_BYTES, &map_k, bar(B_K_FULL + sk), 64, J * TC_BLK, bh);
+        issued_k = u + 1;
+        if (u >= TC_NV &&
+            !mbar_wait_bounded(bar(B_V_EMPTY + sv), ((u / TC_NV) & 1) ^ 1, lim, abort_p))
+          break;
+        mbar_arrive_expect_tx(bar(B_V_FULL + sv), TC_TILE_BYTES);
+        tma_load_3d(sV, &map_v, bar(B_V_FULL + sv), 0, J * TC_BLK, bh);
+        tma_load_3d(sV + TC_HALF_BYTES, &map_v, bar(B_V_FULL + sv), 64, J * TC_BLK, bh);
+        issued_v = u + 1;
       }
       if (*abort_p) {
         // Drain: every copy issued must land before this CTA's shared memory
-        // is released. Only the last TC_NS blocks can still be in flight (a
-        // stage is reloaded only after its previous copy was consumed).
+        // is released. Only the last NK (NV) loads of a ring can still be in
+        // flight: a stage is reloaded only after its previous copy was used.
         volatile int no_abort = 0;
-        mbar_wait_bounded(bar(B_Q_FULL), 0, lim, &no_abort);
-        for (int j = issued_k > TC_NS ? issued_k - TC_NS : 0; j < issued_k; ++j) {
-          const int st = j % TC_NS;
-          const uint32_t ph = (j / TC_NS) & 1;
+        mbar_wait_bounded(bar(B_Q_FULL + 0), 0, lim, &no_abort);
+        if (has1) {
           no_abort = 0;
-          mbar_wait_bounded(bar(B_K_FULL + st), ph, lim, &no_abort);
-          if (j < issued_v) {
-            no_abort = 0;
-            mbar_wait_bounded(bar(B_V_FULL + st), ph, lim, &no_abort);
-          }
+          mbar_wait_bounded(bar(B_Q_FULL + 1), 0, lim, &no_abort);
+        }
+        for (int u = issued_k > TC_NK ? issued_k - TC_NK : 0; u < issued_k; ++u) {
+          no_abort = 0;
+          mbar_wait_bounded(bar(B_K_FULL + u % TC_NK), (u / TC_NK) & 1, lim, &no_abort);
+        }
+        for (int u = issued_v > TC_NV ? issued_v - TC_NV : 0; u < issued_v; ++u) {
+          no_abort = 0;
+          mbar_wait_bounded(bar(B_V_FULL + u % TC_NV), (u / TC_NV) & 1, lim, &no_abort);
         }
       }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA --
-    if (lane == 0 && n > 0) {
-      bool ok = mbar_wait_bounded(bar(B_Q_FULL), 0, lim, abort_p);
-      if (ok) ok = mbar_wait_bounded(bar(B_K_FULL + 0), 0, lim, abort_p);
-      if (ok) {
+    if (lane == 0 && nu > 0) {
+      const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
+      bool ok = mbar_wait_bounded(bar(B_Q_FULL + 0), 0, lim, abort_p);
+      if (ok && has1) ok = mbar_wait_bounded(bar(B_Q_FULL + 1), 0, lim, abort_p);
+      int pend[2] = {-1, -1};   // union entry whose PV is still to issue, per tile
+      int cnt[2] = {0, 0};      // QKs issued per tile
+      uint32_t outst = 0;       // per V stage, 2 bits: tiles still to read it
+      // Issue PV_t for the pending entry of tile t (after its softmax wrote P_t).
+      auto issue_pv = [&](int t) -> bool {
+        const int pu = pend[t];
+        const int jj = cnt[t] - 1;
+        if (!mbar_wait_bounded(bar(B_P_FULL + t), jj & 1, lim, abort_p)) return false;
+        const int sv = pu % TC_NV;
+        if (!mbar_wait_bounded(bar(B_V_FULL + sv), (pu / TC_NV) & 1, lim, abort_p)) return false;
         tc_fence_after();
-        tc_issue_qk(tS0, sQ, sK0);
-        umma_commit(bar(B_K_EMPTY + 0));
-        umma_commit(bar(B_S_FULL + 0));
-      }
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) {
-          const int st1 = (j + 1) % TC_NS;
-          if (!(ok = mbar_wait_bounded(bar(B_K_FULL + st1), ((j + 1) / TC_NS) & 1, lim, abort_p)))
-            break;
-          tc_fence_after();
-          tc_issue_qk(tS0 + ((j + 1) & 1) * 128, sQ, sK0 + st1 * TC_TILE_BYTES);
-          umma_commit(bar(B_K_EMPTY + st1));
-          umma_commit(bar(B_S_FULL + ((j + 1) & 1)));
+        tc_issue_pv(tmem + t * 256 + 128, tmem + t * 256, sV0 + sv * TC_TILE_BYTES, jj > 0);
+        umma_commit(bar(B_O_DONE + t));
+        outst &= ~(1u << (2 * sv + t));
+        if (((outst >> (2 * sv)) & 3u) == 0) umma_commit(bar(B_V_EMPTY + sv));
+        pend[t] = -1;
+        return true;
+      };
+      for (int u = 0; ok && u < nu; ++u) {
+        const uint32_t f = static_cast<uint32_t>(a.pcol[pbeg + u]) & 3u;
+        const int sk = u % TC_NK;
+        outst |= f << (2 * (u % TC_NV));
+        if (!(ok = mbar_wait_bounded(bar(B_K_FULL + sk), (u / TC_NK) & 1, lim, abort_p))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (pend[t] >= 0 && !(ok = issue_pv(t))) break;
+          if ((f >> t) & 1u) {
+            tc_issue_qk(tmem + t * 256, t == 0 ? sQ0 : sQ1, sK0 + sk * TC_TILE_BYTES);
+            umma_commit(bar(B_S_FULL + t));
+            pend[t] = u;
+            ++cnt[t];
+          }
         }
-        const int st = j % TC_NS;
-        if (!(ok = mbar_wait_bounded(bar(B_P_FULL + (j & 1)), (j >> 1) & 1, lim, abort_p))) break;
-        if (!(ok = mbar_wait_bounded(bar(B_V_FULL + st), (j / TC_NS) & 1, lim, abort_p))) break;
-        tc_fence_after();
-        tc_issue_pv(tO, tS0 + (j & 1) * 128, sV0 + st * TC_TILE_BYTES, j > 0);
-        umma_commit(bar(B_V_EMPTY + st));
-        umma_commit(bar(B_O_DONE));
+        if (!ok) break;
+        umma_commit(bar(B_K_EMPTY + sk));
       }
+      if (ok && pend[0] >= 0) ok = issue_pv(0);
+      if (ok && pend[1] >= 0) ok = issue_pv(1);
       if (!ok) {
         // Drain this thread's MMAs before TMEM is released.
         umma_commit(bar(B_DRAIN));
@@ -216,119 +474,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         mbar_wait_bounded(bar(B_DRAIN), 0, lim, &no_abort);
       }
     }
-  } else {
-    // ------------------------------------------- softmax / correction / out --
-    const int wq = warp & 3;               // TMEM lane quarter of this warp
-    const int r = wq * 32 + lane;          // query row within the tile
-    const int row = I * TC_BLK + r;
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const float sl2 = a.scale_log2;
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      const int b = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_S_FULL + b), (j >> 1) & 1, lim, abort_p));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tS = tS0 + b * 128 + lane_off;
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
-      }
-      tmem_wait_ld();
-      const int J = a.col[beg + j];
-      const int valid = min(TC_BLK, a.N - J * TC_BLK);
-      // largest scaled logit of the valid columns (valid >= 1 for a live block)
-      float mx = -INFINITY, mn = INFINITY;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        if (i < valid) {
-          mx = fmaxf(mx, s[i]);
-          mn = fminf(mn, s[i]);
-        }
-      }
-      const float m_cand = (sl2 >= 0.f ? mx : mn) * sl2;
-      const bool need = m_cand > m_used + TC_TAU;
-      float alpha = 1.f;
-      if (need) {
-        alpha = exp2f(m_used - m_cand);
-        m_used = m_cand;
-        l *= alpha;
-      }
-      if (__any_sync(0xffffffffu, need && j > 0)) {
-        // O holds the sum up to PV(j-1): wait for it, then rescale in TMEM.
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_O_DONE), (j - 1) & 1, lim, abort_p));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + lane_off + c * 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(tO + lane_off + c * 32, v);
-        }
-      }
-      const float neg_m = -m_used;
-      uint32_t pk[64];
-      float rs = 0.f;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float p0 = (2 * i < valid) ? exp2f(fmaf(s[2 * i], sl2, neg_m)) : 0.f;
-        const float p1 = (2 * i + 1 < valid) ? exp2f(fmaf(s[2 * i + 1], sl2, neg_m)) : 0.f;
-        rs += p0 + p1;
-        pk[i] = pack_bf16x2(p0, p1);
-      }
-      l += rs;
-      {
-        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
-        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[32]);
-        const uint32_t tP = tS0 + b * 128 + lane_off;
-        tmem_st32(tP, lo);
-        tmem_st32(tP + 32, hi);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(B_P_FULL + b));
-    }
-    // epilogue
-    const long long obase = (static_cast<long long>(bh) * a.N + row) * TC_D;
-    if (n > 0 && ok)
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(B_O_DONE), (n - 1) & 1, lim, abort_p));
-    if (n > 0 && ok) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + lane_off + c * 32, v);
-        tmem_wait_ld();
-        if (row < a.N) {
-          uint4* dst = reinterpret_cast<uint4*>(a.out + obase + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv);
-            dst[q4] = w;
-          }
-        }
-      }
-      if (row < a.N && a.lse != nullptr)
-        a.lse[static_cast<long long>(bh) * a.N + row] = (m_used + log2f(l)) * 0.69314718055994530942f;
-    } else if (n == 0 && row < a.N) {
-      uint4* dst = reinterpret_cast<uint4*>(a.out + obase);
-#pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
-      if (a.lse != nullptr) a.lse[static_cast<long long>(bh) * a.N + row] = -INFINITY;
-    }
+  }
   }
 
   tc_fence_before();

@@ -164,3 +164,68 @@ __global__ void mask_fill_kernel(MaskDesc m, const int* __restrict__ row_ptr,
 }
 
 }  // namespace va
+
+namespace va {
+
+// Query-block pairs {2P, 2P+1} for the two-tile attention kernel: the merged
+// (union) key-block list of the two rows, entry = J << 2 | live bits (bit 0:
+// row 2P, bit 1: row 2P+1). Pair P's entries start at row_ptr[2P] (the union
+// is never longer than both rows together). One thread per pair.
+__global__ void pair_merge_kernel(int nb, const int* __restrict__ row_ptr,
+                                  const int* __restrict__ col, int* __restrict__ pcol,
+                                  int* __restrict__ plen) {
+  const int P = blockIdx.x * blockDim.x + threadIdx.x;
+  const int npairs = (nb + 1) / 2;
+  if (P >= npairs) return;
+  int a = row_ptr[2 * P];
+  const int ae = row_ptr[2 * P + 1];
+  int b = ae;
+  const int be = (2 * P + 1 < nb) ? row_ptr[2 * P + 2] : ae;
+  const int out = row_ptr[2 * P];
+  int k = 0;
+  while (a < ae || b < be) {
+    const int ja = a < ae ? col[a] : 0x7fffffff;
+    const int jb = b < be ? col[b] : 0x7fffffff;
+    int e;
+    if (ja < jb) {
+      e = (ja << 2) | 1;
+      ++a;
+    } else if (jb < ja) {
+      e = (jb << 2) | 2;
+      ++b;
+    } else {
+      e = (ja << 2) | 3;
+      ++a;
+      ++b;
+    }
+    pcol[out + k] = e;
+    ++k;
+  }
+  plen[P] = k;
+}
+
+// Single thread: pairs ordered by descending summed row length (stable
+// counting sort; lengths are 0..2*nb). hist must hold 2*nb + 2 ints.
+__global__ void pair_order_kernel(int nb, const int* __restrict__ row_ptr,
+                                  int* __restrict__ porder, int* __restrict__ hist) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  const int npairs = (nb + 1) / 2;
+  const int top = 2 * nb + 1;
+  for (int i = 0; i <= top; ++i) hist[i] = 0;
+  for (int P = 0; P < npairs; ++P) {
+    const int e = min(2 * P + 2, nb);
+    hist[top - (row_ptr[e] - row_ptr[2 * P])]++;
+  }
+  int acc = 0;
+  for (int i = 0; i <= top; ++i) {
+    const int v = hist[i];
+    hist[i] = acc;
+    acc += v;
+  }
+  for (int P = 0; P < npairs; ++P) {
+    const int e = min(2 * P + 2, nb);
+    porder[hist[top - (row_ptr[e] - row_ptr[2 * P])]++] = P;
+  }
+}
+
+}  // namespace va

@@ -108,6 +108,11 @@ struct va_mask {
   int32_t* row_ptr = nullptr;  // device [nqb + 1]
   int32_t* col = nullptr;      // device [nnz]
   int32_t* order = nullptr;    // device [nqb]: rows by descending length
+  // query-block pairs {2P, 2P+1} for the two-tile tensor-core kernel
+  int npairs = 0;
+  int32_t* pcol = nullptr;     // device [nnz]: merged rows, entry J << 2 | live bits
+  int32_t* plen = nullptr;     // device [npairs]: merged length per pair
+  int32_t* porder = nullptr;   // device [npairs]: pairs by descending work
   int device = 0;
 };
 
@@ -232,6 +237,22 @@ VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params*
       va_mask_free(m);
       return st;
     }
+    m->npairs = (md.nb + 1) / 2;
+    int* phist = nullptr;
+    if ((st = scratch.alloc(&phist, 2 * static_cast<size_t>(md.nb) + 2)) ||
+        (st = cuda_status(cudaMalloc(&m->pcol, sizeof(int32_t) * (m->nnz > 0 ? m->nnz : 1)))) ||
+        (st = cuda_status(cudaMalloc(&m->plen, sizeof(int32_t) * m->npairs))) ||
+        (st = cuda_status(cudaMalloc(&m->porder, sizeof(int32_t) * m->npairs)))) {
+      va_mask_free(m);
+      return st;
+    }
+    va::pair_merge_kernel<<<(m->npairs + 127) / 128, 128, 0, s>>>(md.nb, m->row_ptr, m->col,
+                                                                   m->pcol, m->plen);
+    va::pair_order_kernel<<<1, 1, 0, s>>>(md.nb, m->row_ptr, m->porder, phist);
+    if ((st = launch_status())) {
+      va_mask_free(m);
+      return st;
+    }
   }
   if ((st = cuda_status(cudaStreamSynchronize(s)))) {
     va_mask_free(m);
@@ -276,6 +297,9 @@ VA_EXPORT int va_mask_free(va_mask* m) {
   if (m->row_ptr) cudaFree(m->row_ptr);
   if (m->col) cudaFree(m->col);
   if (m->order) cudaFree(m->order);
+  if (m->pcol) cudaFree(m->pcol);
+  if (m->plen) cudaFree(m->plen);
+  if (m->porder) cudaFree(m->porder);
   delete m;
   return VA_OK;
 }
@@ -300,7 +324,13 @@ int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, voi
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !configured[dev]) {
-    int st = cuda_status(cudaFuncSetAttribute(
+    // The kernel's setmaxnreg split assumes this exact per-thread register
+    // count at launch; anything else could leave the increase waiting.
+    cudaFuncAttributes fa;
+    int st = cuda_status(cudaFuncGetAttributes(&fa, va::attn_tc_kernel));
+    if (st) return st;
+    if (fa.numRegs != va::TC_LAUNCH_REGS) return VA_ERR_UNSUPPORTED;
+    st = cuda_status(cudaFuncSetAttribute(
         va::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, va::TC_SMEM_BYTES));
     if (st) return st;
     configured[dev] = true;
@@ -313,14 +343,17 @@ int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, voi
   va::TcArgs a;
   a.row_ptr = m->row_ptr;
   a.col = m->col;
-  a.order = m->order;
+  a.pcol = m->pcol;
+  a.plen = m->plen;
+  a.porder = m->porder;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   a.N = N;
   a.nqb = m->nqb;
+  a.npairs = m->npairs;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit = g_wait_limit;
-  const long long grid = static_cast<long long>(m->nqb) * BH;
+  const long long grid = static_cast<long long>(m->npairs) * BH;
   if (grid > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
   va::attn_tc_kernel<<<static_cast<unsigned>(grid), va::TC_THREADS, va::TC_SMEM_BYTES, s>>>(
       mq, mk, mv, a);
