@@ -208,7 +208,13 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
-        time.sleep(0.3)
+        # Keep the GPU busy with the same call for >= 0.6 s before timing, so the
+        # 200 ms clock samples are all taken under this load.
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < 0.6:
+            for _ in range(20):
+                va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
+            torch.cuda.synchronize()
         t_begin.record(stream)
         for i in range(args.steps):
             starts[i].record(stream)
@@ -216,6 +222,7 @@ def run_ours(args, world, rank, local):
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        time.sleep(0.25)
     barrier(world)
     if va.device_error() != va.OK:
         raise RuntimeError("device error in the timed region")
@@ -318,8 +325,8 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--oracle-rows", type=int, default=512,
                     help="query rows per head in the CPU-oracle baseline sample")
