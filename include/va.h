@@ -118,6 +118,41 @@ int va_mask_to_host(const va_mask* mask, int32_t* row_ptr, int32_t* col_idx);
 int va_mask_free(va_mask* mask);
 
 /*
+ * Allocation-free mask build (the paper has no counterpart: this is an
+ * interface for callers, not part of the method).
+ *
+ * Builds the same CSR as va_mask_build, bit for bit, into caller-owned DEVICE
+ * arrays row_ptr[nqb + 1] and col_idx[col_capacity] (int32), with
+ * nqb = ceil(T*H*W / block), and writes the number of live block pairs to
+ * *nnz (host). It is meant for callers that must not allocate device memory
+ * on this path: code running under a caching or arena allocator that owns the
+ * whole device, real-time loops where a cudaMalloc would stall or synchronise
+ * the device, and embedders whose memory is handed out by the host framework.
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine. Its scratch (per-row counts and a small summary) lives in a
+ * statically sized device array inside the library, which every GPU that
+ * loads the library keeps until the process exits (about 1.3 MB).
+ *
+ * Limit: nqb <= VA_STATIC_MAX_BLOCKS; larger grids return VA_ERR_UNSUPPORTED
+ * before any device work.
+ * The first call on a device looks up that device's address of the scratch
+ * array (cudaGetSymbolAddress); make that first call before any stream
+ * capture. Every call shares the one scratch array, so calls that overlap on
+ * the GPU (different streams, or host threads without ordering) race and must
+ * be serialised by the caller. The call synchronises `stream` once, after the
+ * counting pass, to read nnz; the column fill is queued on `stream` after that.
+ * If nnz > col_capacity, *nnz is still set, col_idx is left untouched and
+ * VA_ERR_INVALID is returned (call again with a larger array).
+ * Errors: VA_ERR_INVALID (as va_mask_build; null row_ptr/nnz; col_idx NULL
+ * with col_capacity > 0; capacity too small), VA_ERR_UNSUPPORTED (grid too
+ * large for the static scratch), VA_ERR_CUDA.
+ */
+#define VA_STATIC_MAX_BLOCKS 65536
+int va_mask_build_static(int kind, int T, int H, int W, const va_mask_params* params, int step,
+                         int32_t* row_ptr, int32_t* col_idx, int64_t col_capacity, int64_t* nnz,
+                         va_stream_t stream);
+
+/*
  * Block-sparse attention forward. For every batch b, head h and query token i
  * with block I = i / block:
  *   l_j   = scale * q_i . k_j   for keys j in live key blocks of row I, j < N

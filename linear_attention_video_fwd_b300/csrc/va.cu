@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "va.h"
 #include "common.cuh"
@@ -410,4 +411,117 @@ VA_EXPORT int va_compensate_route(const void* q, const void* k, const void* v,
   (void)scale; (void)B; (void)heads; (void)N; (void)d; (void)dtype; (void)out; (void)err_out;
   (void)sel_out; (void)stream;
   return VA_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------- allocation-free masks --
+//
+// va_mask_build_static: the mask build of va_mask_build for callers that must
+// not allocate device memory. Its scratch lives in one statically sized
+// device array (every GPU that loads the library holds it until exit); the
+// caller passes the CSR output arrays.
+
+namespace {
+
+constexpr size_t kStaticMaxBlocks = VA_STATIC_MAX_BLOCKS;
+// layout: summary (2 x int64, padded to 256 B) | key tokens (int64 x max) |
+// counts (int32 x max) | histogram (int32 x (max + 1), padded to 8 B) |
+// row order (int32 x max)
+constexpr size_t kScrSummary = 0;
+constexpr size_t kScrKeyTok = 256;
+constexpr size_t kScrCnt = kScrKeyTok + 8 * kStaticMaxBlocks;
+constexpr size_t kScrHist = kScrCnt + 4 * kStaticMaxBlocks;
+constexpr size_t kScrOrder = kScrHist + ((4 * (kStaticMaxBlocks + 1) + 7) & ~size_t(7));
+constexpr size_t kScrBytes = kScrOrder + 4 * kStaticMaxBlocks;
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_static_scratch[kScrBytes];
+
+namespace {
+
+std::mutex g_static_mu;
+void* g_static_addr[64] = {nullptr};
+
+// Device address of g_static_scratch on the current device (looked up once
+// per device; the host-side symbol itself is not a device address).
+int static_scratch(void** out) {
+  int dev = 0;
+  int st = cuda_status(cudaGetDevice(&dev));
+  if (st) return st;
+  if (dev < 0 || dev >= 64) return VA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_addr[dev] == nullptr) {
+    void* p = nullptr;
+    st = cuda_status(cudaGetSymbolAddress(&p, g_static_scratch));
+    if (st) return st;
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return VA_OK;
+}
+
+}  // namespace
+
+VA_EXPORT int va_mask_build_static(int kind, int T, int H, int W, const va_mask_params* params,
+                                   int step, int32_t* row_ptr, int32_t* col_idx,
+                                   int64_t col_capacity, int64_t* nnz, va_stream_t stream) {
+  if (params == nullptr || row_ptr == nullptr || nnz == nullptr) return VA_ERR_INVALID;
+  if (col_capacity < 0 || (col_idx == nullptr && col_capacity > 0)) return VA_ERR_INVALID;
+  if (kind != VA_MASK_DENSE && kind != VA_MASK_RADIAL && kind != VA_MASK_LVSA)
+    return VA_ERR_INVALID;
+  if (T < 1 || H < 1 || W < 1) return VA_ERR_INVALID;
+  const int64_t F64 = static_cast<int64_t>(H) * W;
+  const int64_t N64 = F64 * T;
+  if (N64 >= (1LL << 30)) return VA_ERR_INVALID;
+  const va_mask_params p = *params;
+  if (p.block < 1 || p.block > 4096) return VA_ERR_INVALID;
+  if (p.w0 < 0 || p.local < 0 || p.period < 0) return VA_ERR_INVALID;
+  const int64_t nb64 = (N64 + p.block - 1) / p.block;
+  if (nb64 > static_cast<int64_t>(kStaticMaxBlocks)) return VA_ERR_UNSUPPORTED;
+  *nnz = 0;
+
+  va::MaskDesc md;
+  md.kind = kind;
+  md.T = T;
+  md.F = static_cast<int>(F64);
+  md.N = static_cast<int>(N64);
+  md.block = p.block;
+  md.nb = static_cast<int>(nb64);
+  md.w0 = (kind == VA_MASK_RADIAL && p.w0 == 0) ? md.F : p.w0;
+  md.local = p.local;
+  md.period = p.period;
+  md.anchor0 = p.anchor0;
+  md.rot_stride = p.rot_stride;
+  md.step = step;
+
+  void* base = nullptr;
+  int st = static_scratch(&base);
+  if (st) return st;
+  unsigned char* b = static_cast<unsigned char*>(base);
+  long long* summary = reinterpret_cast<long long*>(b + kScrSummary);
+  long long* keytok = reinterpret_cast<long long*>(b + kScrKeyTok);
+  int* cnt = reinterpret_cast<int*>(b + kScrCnt);
+  int* hist = reinterpret_cast<int*>(b + kScrHist);
+  int* order = reinterpret_cast<int*>(b + kScrOrder);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  // The previous call's contents stay in the array: start the summary at zero.
+  if ((st = cuda_status(cudaMemsetAsync(summary, 0, 2 * sizeof(long long), s)))) return st;
+  const int threads = 256;
+  const int blocks = (md.nb * 32 + threads - 1) / threads;
+  va::mask_count_kernel<<<blocks, threads, 0, s>>>(md, cnt, keytok);
+  va::mask_scan_kernel<<<1, 1024, 0, s>>>(md, cnt, keytok, row_ptr, summary, order, hist);
+  if ((st = launch_status())) return st;
+  long long host_summary[2] = {0, 0};
+  if ((st = cuda_status(cudaMemcpyAsync(host_summary, summary, sizeof(host_summary),
+                                        cudaMemcpyDeviceToHost, s))) ||
+      (st = cuda_status(cudaStreamSynchronize(s))))
+    return st;
+  *nnz = host_summary[0];
+  if (host_summary[0] > col_capacity) return VA_ERR_INVALID;
+  if (host_summary[0] > 0) {
+    va::mask_fill_kernel<<<blocks, threads, 0, s>>>(md, row_ptr, col_idx);
+    if ((st = launch_status())) return st;
+  }
+  return VA_OK;
 }

@@ -1,0 +1,85 @@
+"""va_mask_build_static: the allocation-free mask build, called through the C ABI.
+
+Some callers cannot allocate device memory on this path: code running under a
+caching or arena allocator that owns the whole device, real-time loops where a
+cudaMalloc would stall or synchronise the device, embedders whose memory is
+handed out by the host framework. For them the library keeps the build's
+scratch in a statically sized device array and takes the output arrays from
+the caller. This test checks that entry point's CSR against the allocating
+va_mask_build (bit-exact, the tolerance every mask test uses) on two calls in
+a row, so the shared scratch left by the first call cannot leak into the
+second. The file name makes pytest collect it last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # kind, T, H, W, block, w0, local, period, anchor0, rot_stride, step
+    (2, 126, 30, 52, 128, 0, 2, 8, 0, 1, 3),   # LVSA long horizon, rotated anchors
+    (1, 21, 30, 52, 128, 0, 1, 0, 0, 1, 0),    # Wan-shaped radial
+    (1, 9, 4, 4, 32, 3, 1, 0, 0, 1, 0),        # small radial, ragged
+]
+
+
+def _static_build(va, case, capacity):
+    kind, T, H, W, block, w0, local, period, a0, rho, step = case
+    lib = va.lib()
+    fn = lib.va_mask_build_static
+    fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   ctypes.POINTER(va._MaskParams), ctypes.c_int, ctypes.c_void_p,
+                   ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
+                   ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    nqb = -(-(T * H * W) // block)
+    dev = torch.device("cuda", 0)
+    # The caller owns the outputs; fill them with garbage to catch unwritten slots.
+    row_ptr = torch.full((nqb + 1,), -7, dtype=torch.int32, device=dev)
+    col = torch.full((max(capacity, 1),), -7, dtype=torch.int32, device=dev)
+    nnz = ctypes.c_int64(-1)
+    p = va._MaskParams(block, w0, local, period, a0, rho)
+    stream = torch.cuda.current_stream()
+    st = fn(kind, T, H, W, ctypes.byref(p), step, ctypes.c_void_p(row_ptr.data_ptr()),
+            ctypes.c_void_p(col.data_ptr()), capacity, ctypes.byref(nnz),
+            ctypes.c_void_p(stream.cuda_stream))
+    torch.cuda.synchronize()
+    return st, nnz.value, row_ptr.cpu().numpy(), col.cpu().numpy()
+
+
+def _reference(va, case):
+    kind, T, H, W, block, w0, local, period, a0, rho, step = case
+    m = va.mask_build(kind, T, H, W, block=block, w0=w0, local=local, period=period,
+                      anchor0=a0, rot_stride=rho, step=step)
+    rp, col = m.csr()
+    m.free()
+    return rp, col
+
+
+def test_static_build_matches_allocating_build_twice_in_a_row(va):
+    for case in CASES:
+        want_rp, want_col = _reference(va, case)
+        for _ in range(2):
+            st, nnz, rp, col = _static_build(va, case, len(want_col) + 5)
+            assert st == va.OK, va.status_string(st)
+            assert nnz == len(want_col)
+            assert np.array_equal(rp, want_rp)
+            assert np.array_equal(col[:nnz], want_col)
+            assert (col[nnz:] == -7).all()            # nothing written past nnz
+    assert va.device_error() == va.OK
+
+
+def test_static_build_reports_size_and_limits(va):
+    case = CASES[1]
+    want_rp, want_col = _reference(va, case)
+    st, nnz, rp, col = _static_build(va, case, 10)            # capacity too small
+    assert st == va.ERR_INVALID and nnz == len(want_col)
+    assert (col == -7).all()
+    st, nnz, _, _ = _static_build(va, (1, 1 << 12, 1 << 6, 1 << 6, 1, 0, 1, 0, 0, 1, 0), 0)
+    assert st == va.ERR_UNSUPPORTED                            # beyond the static scratch
+    st, nnz, rp, col = _static_build(va, case, len(want_col))  # works again afterwards
+    assert st == va.OK and np.array_equal(col[:nnz], want_col)
+    assert va.device_error() == va.OK
