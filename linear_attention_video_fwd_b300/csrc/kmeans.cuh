@@ -1,0 +1,315 @@
+// Lloyd k-means per (batch, head) and per-cluster statistics, the clustering
+// step of SVG-EAR's parameter-free linear compensation (SVG-EAR, gist.science
+// 2603.08982, technical summary sec. 2, idea 1: queries and keys are grouped
+// by semantic similarity; the page names no algorithm, Lloyd iteration on the
+// raw head vectors with squared Euclidean distance is the reading used).
+//
+// One iteration: assign (nearest centroid, ties to the lowest index) ->
+// counts -> offsets -> member lists -> means. The means are summed in float64
+// over the members of each cluster; for bf16 inputs those sums are exact, so
+// the centroids do not depend on the (atomic, unordered) member order.
+#pragma once
+
+#include "common.cuh"
+
+namespace va {
+
+// 16-byte load of CH = 16 / sizeof(T) consecutive elements, as floats.
+template <typename T>
+struct Chunk16 {
+  static constexpr int CH = 16 / static_cast<int>(sizeof(T));
+  __device__ __forceinline__ static void load(const T* src, float (&out)[16 / sizeof(T)]) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(src);
+    if constexpr (sizeof(T) == 4) {
+      out[0] = __uint_as_float(raw.x);
+      out[1] = __uint_as_float(raw.y);
+      out[2] = __uint_as_float(raw.z);
+      out[3] = __uint_as_float(raw.w);
+    } else {
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        out[2 * i] = __uint_as_float(w[i] << 16);
+        out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+  }
+};
+
+// dstT[d * R + r] = row(r)[d] for r < R, d < D (zeros where row(r) is null).
+// Consecutive threads take consecutive rows, so the shared-memory writes are
+// conflict-free; each thread reads 16 bytes of one row.
+template <typename T, int D, int R, int NT, typename RowFn>
+__device__ __forceinline__ void stage_transposed(float* dstT, RowFn row) {
+  constexpr int CH = Chunk16<T>::CH;
+  for (int e = threadIdx.x; e < R * (D / CH); e += NT) {
+    const int r = e % R, ch = e / R;
+    const T* src = row(r);
+    float f[CH];
+    if (src != nullptr) {
+      Chunk16<T>::load(src + ch * CH, f);
+    } else {
+#pragma unroll
+      for (int i = 0; i < CH; ++i) f[i] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < CH; ++i) dstT[(ch * CH + i) * R + r] = f[i];
+  }
+}
+
+// dst[r * D + d] = row(r)[d] (row-major, zeros where row(r) is null).
+template <typename T, int D, int R, int NT, typename RowFn>
+__device__ __forceinline__ void stage_rows(float* dst, RowFn row) {
+  constexpr int CH = Chunk16<T>::CH;
+  for (int e = threadIdx.x; e < R * (D / CH); e += NT) {
+    const int r = e / (D / CH), ch = e % (D / CH);
+    const T* src = row(r);
+    float f[CH];
+    if (src != nullptr) {
+      Chunk16<T>::load(src + ch * CH, f);
+    } else {
+#pragma unroll
+      for (int i = 0; i < CH; ++i) f[i] = 0.f;
+    }
+    float4* d4 = reinterpret_cast<float4*>(dst + r * D + ch * CH);
+#pragma unroll
+    for (int i = 0; i < CH / 4; ++i)
+      d4[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+  }
+}
+
+constexpr int KM_THREADS = 256;
+constexpr int KM_PT = 64;  // points per CTA
+constexpr int KM_CT = 64;  // centroids per inner tile
+
+// assign[i] = argmin_c (|c|^2 - 2 x_i . c) over c < C (|x_i|^2 is common to
+// all c); ties -> lowest c. count[assign[i]] += 1 (count zeroed by the caller).
+// Grid: (ceil(N / KM_PT), BH). x: [BH, N, D], cent: [BH, C, D] fp32,
+// cnorm: [BH, C] fp32 (|c|^2).
+template <typename T, int D>
+__global__ void __launch_bounds__(KM_THREADS)
+    km_assign_kernel(const T* __restrict__ x, const float* __restrict__ cent,
+                     const float* __restrict__ cnorm, int N, int C, int* __restrict__ assign,
+                     int* __restrict__ count) {
+  extern __shared__ float km_smem[];
+  float* xT = km_smem;                 // [D][KM_PT]
+  float* cT = km_smem + D * KM_PT;     // [D][KM_CT]
+  const int bh = blockIdx.y;
+  const int i0 = blockIdx.x * KM_PT;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const T* xb = x + static_cast<long long>(bh) * N * D;
+  const float* cb = cent + static_cast<long long>(bh) * C * D;
+  const float* nb = cnorm + static_cast<long long>(bh) * C;
+
+  // stage the point tile transposed: xT[d][p]
+  stage_transposed<T, D, KM_PT, KM_THREADS>(xT, [&](int p) -> const T* {
+    return i0 + p < N ? xb + static_cast<long long>(i0 + p) * D : nullptr;
+  });
+  float best[4];
+  int besti[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    best[a] = INFINITY;
+    besti[a] = 0x7fffffff;
+  }
+  for (int c0 = 0; c0 < C; c0 += KM_CT) {
+    __syncthreads();
+    stage_transposed<float, D, KM_CT, KM_THREADS>(cT, [&](int c) -> const float* {
+      return c0 + c < C ? cb + static_cast<long long>(c0 + c) * D : nullptr;
+    });
+    __syncthreads();
+    float acc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+#pragma unroll 8
+    for (int dd = 0; dd < D; ++dd) {
+      const float4 xv = *reinterpret_cast<const float4*>(&xT[dd * KM_PT + ty * 4]);
+      const float4 cv = *reinterpret_cast<const float4*>(&cT[dd * KM_CT + tx * 4]);
+      const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+      const float ca[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(xa[a], ca[b], acc[a][b]);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int c = c0 + tx * 4 + b;
+      if (c < C) {
+        const float cn = nb[c];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float dist = fmaf(-2.f, acc[a][b], cn);
+          if (dist < best[a]) {  // clusters visited in ascending order per thread
+            best[a] = dist;
+            besti[a] = c;
+          }
+        }
+      }
+    }
+  }
+  // reduce over the 16 threads (tx) that share these 4 points
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    float bv = best[a];
+    int bi = besti[a];
+#pragma unroll
+    for (int o = 8; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov < bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    const int i = i0 + ty * 4 + a;
+    if (tx == 0 && i < N) {
+      assign[static_cast<long long>(bh) * N + i] = bi;
+      atomicAdd(&count[static_cast<long long>(bh) * C + bi], 1);
+    }
+  }
+}
+
+// Exclusive scan of count[bh][0..C) into off[bh][0..C] (off[C] = N) and a
+// zeroed fill cursor. One CTA per bh, 1024 threads.
+__global__ void km_offsets_kernel(const int* __restrict__ count, int C, int* __restrict__ off,
+                                  int* __restrict__ fill) {
+  __shared__ int part[1024];
+  const int bh = blockIdx.x, tid = threadIdx.x;
+  const int* cnt = count + static_cast<long long>(bh) * C;
+  int* o = off + static_cast<long long>(bh) * (C + 1);
+  const int per = (C + 1023) / 1024;
+  const int lo = min(C, tid * per), hi = min(C, lo + per);
+  int s = 0;
+  for (int c = lo; c < hi; ++c) s += cnt[c];
+  part[tid] = s;
+  __syncthreads();
+  for (int stride = 1; stride < 1024; stride <<= 1) {
+    const int v = tid >= stride ? part[tid - stride] : 0;
+    __syncthreads();
+    part[tid] += v;
+    __syncthreads();
+  }
+  int base = tid > 0 ? part[tid - 1] : 0;
+  for (int c = lo; c < hi; ++c) {
+    o[c] = base;
+    base += cnt[c];
+    fill[static_cast<long long>(bh) * C + c] = 0;
+  }
+  if (tid == 1023) o[C] = part[1023];
+}
+
+// perm[off[a_i] + k] = i (member lists; order within a cluster unspecified).
+// Assignment values outside [0, C) are reported as VA_ERR_DEVICE and skipped.
+__global__ void km_scatter_kernel(const int* __restrict__ assign, int N, int C,
+                                  const int* __restrict__ off, int* __restrict__ fill,
+                                  int* __restrict__ perm) {
+  const int bh = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const int a = assign[static_cast<long long>(bh) * N + i];
+  if (a < 0 || a >= C) {
+    raise_error(VA_ERR_DEVICE);
+    return;
+  }
+  const int pos = off[static_cast<long long>(bh) * (C + 1) + a] +
+                  atomicAdd(&fill[static_cast<long long>(bh) * C + a], 1);
+  perm[static_cast<long long>(bh) * N + pos] = i;
+}
+
+// Histogram of an externally supplied assignment (range-checked).
+__global__ void km_count_kernel(const int* __restrict__ assign, int N, int C,
+                                int* __restrict__ count) {
+  const int bh = blockIdx.y;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N) return;
+  const int a = assign[static_cast<long long>(bh) * N + i];
+  if (a < 0 || a >= C) {
+    raise_error(VA_ERR_DEVICE);
+    return;
+  }
+  atomicAdd(&count[static_cast<long long>(bh) * C + a], 1);
+}
+
+// One warp per cluster: mean of its members (float64 sums), written as fp32
+// to mean[bh][c]; |mean|^2 (fp32) to norm[bh][c] if norm != nullptr. An empty
+// cluster keeps mean[bh][c] when keep_empty, else gets zeros.
+// Grid: (ceil(C / 8), BH), 256 threads.
+template <typename T, int D>
+__global__ void km_means_kernel(const T* __restrict__ x, int N, int C,
+                                const int* __restrict__ off, const int* __restrict__ perm,
+                                float* __restrict__ mean, float* __restrict__ norm,
+                                int keep_empty) {
+  constexpr int PER = D / 32;
+  const int bh = blockIdx.y;
+  const int c = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (c >= C) return;
+  const int* o = off + static_cast<long long>(bh) * (C + 1);
+  const int beg = o[c], end = o[c + 1];
+  const int* pm = perm + static_cast<long long>(bh) * N;
+  const T* xb = x + static_cast<long long>(bh) * N * D;
+  float* m = mean + (static_cast<long long>(bh) * C + c) * D;
+  double acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.0;
+  for (int t = beg; t < end; ++t) {
+    const T* row = xb + static_cast<long long>(pm[t]) * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] += static_cast<double>(to_f32(row[e]));
+  }
+  float nrm = 0.f;
+  if (end > beg) {
+    const double inv_n = static_cast<double>(end - beg);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const float mv = static_cast<float>(acc[e] / inv_n);
+      m[lane * PER + e] = mv;
+      nrm = fmaf(mv, mv, nrm);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      float mv = keep_empty ? m[lane * PER + e] : 0.f;
+      if (!keep_empty) m[lane * PER + e] = 0.f;
+      nrm = fmaf(mv, mv, nrm);
+    }
+  }
+  if (norm != nullptr) {
+#pragma unroll
+    for (int o2 = 16; o2; o2 >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o2);
+    if (lane == 0) norm[static_cast<long long>(bh) * C + c] = nrm;
+  }
+}
+
+// Initial centroids: cent[bh][c] = x[bh][init[bh][c]] (fp32), |c|^2 to cnorm.
+// Indices outside [0, N) are reported as VA_ERR_DEVICE (the row is zeroed).
+// One warp per centroid; grid (ceil(C / 8), BH).
+template <typename T, int D>
+__global__ void km_init_kernel(const T* __restrict__ x, const int* __restrict__ init, int N,
+                               int C, float* __restrict__ cent, float* __restrict__ cnorm) {
+  constexpr int PER = D / 32;
+  const int bh = blockIdx.y;
+  const int c = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (c >= C) return;
+  const int idx = init[static_cast<long long>(bh) * C + c];
+  const bool ok = idx >= 0 && idx < N;
+  if (!ok && lane == 0) raise_error(VA_ERR_DEVICE);
+  float* m = cent + (static_cast<long long>(bh) * C + c) * D;
+  const T* row = x + (static_cast<long long>(bh) * N + (ok ? idx : 0)) * D;
+  float nrm = 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const float v = ok ? to_f32(row[lane * PER + e]) : 0.f;
+    m[lane * PER + e] = v;
+    nrm = fmaf(v, v, nrm);
+  }
+#pragma unroll
+  for (int o2 = 16; o2; o2 >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o2);
+  if (lane == 0) cnorm[static_cast<long long>(bh) * C + c] = nrm;
+}
+
+}  // namespace va

@@ -14,6 +14,7 @@
 #include "mask.cuh"
 #include "attn_simt.cuh"
 #include "attn_tc.cuh"
+#include "svgear.cuh"
 
 #define VA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -24,7 +25,7 @@ int64_t g_wait_limit = 4000000000LL;
 struct Scoped {
   // Stream-ordered scratch allocations released at scope exit.
   cudaStream_t s;
-  void* ptrs[16];
+  void* ptrs[32];
   int n = 0;
   explicit Scoped(cudaStream_t st) : s(st) {}
   ~Scoped() {
@@ -394,22 +395,216 @@ VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, co
 
 // ------------------------------------------------------------ clustering --
 
+namespace {
+
+constexpr int kMaxClusters = 4096;
+
+template <typename T, int D>
+int set_smem_attrs() {
+  static bool done[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && done[dev]) return VA_OK;
+  int st;
+  if ((st = cuda_status(cudaFuncSetAttribute(va::km_assign_kernel<T, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             2 * D * va::KM_PT * 4))) ||
+      (st = cuda_status(cudaFuncSetAttribute(va::probe_kernel<T, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             va::probe_smem_bytes<D>(kMaxClusters)))) ||
+      (st = cuda_status(cudaFuncSetAttribute(va::comp_attn_kernel<T, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             va::comp_smem_bytes<D>(kMaxClusters)))))
+    return st;
+  if (dev >= 0 && dev < 64) done[dev] = true;
+  return VA_OK;
+}
+
+// Member lists of an assignment: count -> offsets -> perm (order within a
+// cluster unspecified). count must be zeroed by the caller.
+int cluster_lists(const int* assign, int BH, int N, int C, int* count, int* off, int* fill,
+                  int* perm, cudaStream_t s) {
+  const dim3 g((N + 255) / 256, BH);
+  va::km_count_kernel<<<g, 256, 0, s>>>(assign, N, C, count);
+  va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
+  va::km_scatter_kernel<<<g, 256, 0, s>>>(assign, N, C, off, fill, perm);
+  return launch_status();
+}
+
+template <typename T, int D>
+int run_cluster(const T* x, const int* init, int BH, int N, int C, int iters, int* assign,
+                float* cent, int* count, cudaStream_t s) {
+  int st = set_smem_attrs<T, D>();
+  if (st) return st;
+  Scoped scratch(s);
+  float* cnorm = nullptr;
+  int *off = nullptr, *fill = nullptr, *perm = nullptr;
+  if ((st = scratch.alloc(&cnorm, static_cast<size_t>(BH) * C)) ||
+      (st = scratch.alloc(&off, static_cast<size_t>(BH) * (C + 1))) ||
+      (st = scratch.alloc(&fill, static_cast<size_t>(BH) * C)) ||
+      (st = scratch.alloc(&perm, static_cast<size_t>(BH) * N)))
+    return st;
+  const dim3 gc((C + 7) / 8, BH);
+  const dim3 ga((N + va::KM_PT - 1) / va::KM_PT, BH);
+  const dim3 gn((N + 255) / 256, BH);
+  va::km_init_kernel<T, D><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
+  const int rounds = iters > 0 ? iters : 1;
+  for (int it = 0; it < rounds; ++it) {
+    if ((st = cuda_status(cudaMemsetAsync(count, 0, sizeof(int) * BH * C, s)))) return st;
+    va::km_assign_kernel<T, D><<<ga, va::KM_THREADS, 2 * D * va::KM_PT * 4, s>>>(
+        x, cent, cnorm, N, C, assign, count);
+    if (iters == 0) break;
+    va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
+    va::km_scatter_kernel<<<gn, 256, 0, s>>>(assign, N, C, off, fill, perm);
+    va::km_means_kernel<T, D><<<gc, 256, 0, s>>>(x, N, C, off, perm, cent, cnorm, 1);
+  }
+  return launch_status();
+}
+
+}  // namespace
+
 VA_EXPORT int va_cluster(const void* x, const int32_t* init_idx, int B, int heads, int N, int d,
                          int C, int iters, int dtype, int32_t* assign, float* centroid,
                          int32_t* count, va_stream_t stream) {
-  (void)x; (void)init_idx; (void)B; (void)heads; (void)N; (void)d; (void)C; (void)iters;
-  (void)dtype; (void)assign; (void)centroid; (void)count; (void)stream;
+  if (x == nullptr || init_idx == nullptr || assign == nullptr || centroid == nullptr ||
+      count == nullptr)
+    return VA_ERR_INVALID;
+  if (B < 1 || heads < 1 || N < 1 || C < 1 || C > N || iters < 0) return VA_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(centroid) || (reinterpret_cast<uintptr_t>(assign) & 3u) ||
+      (reinterpret_cast<uintptr_t>(count) & 3u) || (reinterpret_cast<uintptr_t>(init_idx) & 3u))
+    return VA_ERR_INVALID;
+  if (C > kMaxClusters || (d != 64 && d != 128)) return VA_ERR_UNSUPPORTED;
+  const int64_t BH64 = static_cast<int64_t>(B) * heads;
+  if (BH64 > 65535 || BH64 * N * d >= (1LL << 40)) return VA_ERR_UNSUPPORTED;
+  const int BH = static_cast<int>(BH64);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == VA_BF16) {
+    const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+    return d == 128 ? run_cluster<__nv_bfloat16, 128>(xb, init_idx, BH, N, C, iters, assign,
+                                                      centroid, count, s)
+                    : run_cluster<__nv_bfloat16, 64>(xb, init_idx, BH, N, C, iters, assign,
+                                                     centroid, count, s);
+  }
+  if (dtype == VA_F32) {
+    const float* xf = static_cast<const float*>(x);
+    return d == 128 ? run_cluster<float, 128>(xf, init_idx, BH, N, C, iters, assign, centroid,
+                                              count, s)
+                    : run_cluster<float, 64>(xf, init_idx, BH, N, C, iters, assign, centroid,
+                                             count, s);
+  }
   return VA_ERR_UNSUPPORTED;
 }
+
+// -------------------------------------------- compensation and routing --
+
+namespace {
+
+template <typename T, int D>
+int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int Cq,
+                   const int* kassign, int Ck, long long budget, float scale, int BH, int N,
+                   T* out, float* err_out, uint8_t* sel_out, cudaStream_t s) {
+  int st = set_smem_attrs<T, D>();
+  if (st) return st;
+  Scoped scratch(s);
+  int *nq, *qoff, *qfill, *qperm, *nk, *koff, *kfill, *kperm, *seln, *selc, *nch, *choff, *chfill;
+  float *qc, *kc, *vc, *err;
+  unsigned long long* cut;
+  const size_t bh = static_cast<size_t>(BH);
+  if ((st = scratch.alloc(&nq, bh * Cq)) || (st = scratch.alloc(&qoff, bh * (Cq + 1))) ||
+      (st = scratch.alloc(&qfill, bh * Cq)) || (st = scratch.alloc(&qperm, bh * N)) ||
+      (st = scratch.alloc(&nk, bh * Ck)) || (st = scratch.alloc(&koff, bh * (Ck + 1))) ||
+      (st = scratch.alloc(&kfill, bh * Ck)) || (st = scratch.alloc(&kperm, bh * N)) ||
+      (st = scratch.alloc(&qc, bh * Cq * D)) || (st = scratch.alloc(&kc, bh * Ck * D)) ||
+      (st = scratch.alloc(&vc, bh * Ck * D)) || (st = scratch.alloc(&seln, bh * Cq)) ||
+      (st = scratch.alloc(&selc, bh * Cq * Ck)) || (st = scratch.alloc(&cut, bh)) ||
+      (st = scratch.alloc(&nch, bh * Cq)) || (st = scratch.alloc(&choff, bh * (Cq + 1))) ||
+      (st = scratch.alloc(&chfill, bh * Cq)))
+    return st;
+  err = err_out;
+  if (err == nullptr && (st = scratch.alloc(&err, bh * Cq * Ck))) return st;
+
+  // cluster sizes, member lists and member means of q (per query cluster) and
+  // of k, v (per key cluster); empty clusters get zero means
+  if ((st = cuda_status(cudaMemsetAsync(nq, 0, sizeof(int) * bh * Cq, s))) ||
+      (st = cuda_status(cudaMemsetAsync(nk, 0, sizeof(int) * bh * Ck, s))))
+    return st;
+  if ((st = cluster_lists(qassign, BH, N, Cq, nq, qoff, qfill, qperm, s)) ||
+      (st = cluster_lists(kassign, BH, N, Ck, nk, koff, kfill, kperm, s)))
+    return st;
+  va::km_means_kernel<T, D><<<dim3((Cq + 7) / 8, BH), 256, 0, s>>>(q, N, Cq, qoff, qperm, qc,
+                                                                  nullptr, 0);
+  va::km_means_kernel<T, D><<<dim3((Ck + 7) / 8, BH), 256, 0, s>>>(k, N, Ck, koff, kperm, kc,
+                                                                  nullptr, 0);
+  va::km_means_kernel<T, D><<<dim3((Ck + 7) / 8, BH), 256, 0, s>>>(v, N, Ck, koff, kperm, vc,
+                                                                  nullptr, 0);
+  if ((st = launch_status())) return st;
+
+  // probe: err = NaN where a cluster is empty, else the proxy error
+  if ((st = cuda_status(cudaMemsetAsync(err, 0xFF, sizeof(float) * bh * Cq * Ck, s)))) return st;
+  va::probe_kernel<T, D><<<dim3((Cq + va::PR_PG - 1) / va::PR_PG, BH), va::PR_THREADS,
+                           va::probe_smem_bytes<D>(Ck), s>>>(
+      k, v, N, Cq, Ck, qc, nq, kc, vc, nk, koff, kperm, kassign, scale, err);
+  if ((st = launch_status())) return st;
+
+  // routing
+  va::route_select_kernel<<<BH, 1024, 0, s>>>(err, nq, nk, Cq, Ck, budget, cut);
+  va::route_mark_kernel<<<dim3(Cq, BH), 256, 0, s>>>(err, nq, nk, Cq, Ck, cut, sel_out, seln,
+                                                     selc);
+  if ((st = launch_status())) return st;
+
+  // compensated attention: chunks of up to 64 queries of one query cluster
+  va::comp_chunks_kernel<<<dim3((Cq + 255) / 256, BH), 256, 0, s>>>(nq, Cq, nch);
+  va::km_offsets_kernel<<<BH, 1024, 0, s>>>(nch, Cq, choff, chfill);
+  const int max_chunks = (N + va::CA_QT - 1) / va::CA_QT + Cq;
+  va::comp_attn_kernel<T, D><<<dim3(max_chunks, BH), va::CA_THREADS, va::comp_smem_bytes<D>(Ck),
+                               s>>>(q, k, v, N, Cq, Ck, choff, qoff, qperm, koff, kperm, kc, vc,
+                                    nk, seln, selc, scale * 1.4426950408889634f, out);
+  return launch_status();
+}
+
+}  // namespace
 
 VA_EXPORT int va_compensate_route(const void* q, const void* k, const void* v,
                                   const int32_t* qassign, int Cq, const int32_t* kassign, int Ck,
                                   double density, float scale, int B, int heads, int N, int d,
                                   int dtype, void* out, float* err_out, uint8_t* sel_out,
                                   va_stream_t stream) {
-  (void)q; (void)k; (void)v; (void)qassign; (void)Cq; (void)kassign; (void)Ck; (void)density;
-  (void)scale; (void)B; (void)heads; (void)N; (void)d; (void)dtype; (void)out; (void)err_out;
-  (void)sel_out; (void)stream;
+  if (q == nullptr || k == nullptr || v == nullptr || qassign == nullptr ||
+      kassign == nullptr || out == nullptr)
+    return VA_ERR_INVALID;
+  if (B < 1 || heads < 1 || N < 1 || Cq < 1 || Ck < 1 || Cq > N || Ck > N) return VA_ERR_INVALID;
+  if (!(density >= 0.0 && density <= 1.0) || !std::isfinite(scale)) return VA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(qassign) & 3u) || (reinterpret_cast<uintptr_t>(kassign) & 3u) ||
+      (reinterpret_cast<uintptr_t>(err_out) & 3u))
+    return VA_ERR_INVALID;
+  if (Cq > kMaxClusters || Ck > kMaxClusters || (d != 64 && d != 128)) return VA_ERR_UNSUPPORTED;
+  const int64_t BH64 = static_cast<int64_t>(B) * heads;
+  if (BH64 > 65535 || BH64 * N * d >= (1LL << 40)) return VA_ERR_UNSUPPORTED;
+  const int BH = static_cast<int>(BH64);
+  const long long budget =
+      static_cast<long long>(std::floor(density * static_cast<double>(N) * static_cast<double>(N)));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == VA_BF16) {
+    using T = __nv_bfloat16;
+    const T *qt = static_cast<const T*>(q), *kt = static_cast<const T*>(k),
+            *vt = static_cast<const T*>(v);
+    T* ot = static_cast<T*>(out);
+    return d == 128 ? run_compensate<T, 128>(qt, kt, vt, qassign, Cq, kassign, Ck, budget, scale,
+                                             BH, N, ot, err_out, sel_out, s)
+                    : run_compensate<T, 64>(qt, kt, vt, qassign, Cq, kassign, Ck, budget, scale,
+                                            BH, N, ot, err_out, sel_out, s);
+  }
+  if (dtype == VA_F32) {
+    using T = float;
+    const T *qt = static_cast<const T*>(q), *kt = static_cast<const T*>(k),
+            *vt = static_cast<const T*>(v);
+    T* ot = static_cast<T*>(out);
+    return d == 128 ? run_compensate<T, 128>(qt, kt, vt, qassign, Cq, kassign, Ck, budget, scale,
+                                             BH, N, ot, err_out, sel_out, s)
+                    : run_compensate<T, 64>(qt, kt, vt, qassign, Cq, kassign, Ck, budget, scale,
+                                            BH, N, ot, err_out, sel_out, s);
+  }
   return VA_ERR_UNSUPPORTED;
 }
 

@@ -1,0 +1,242 @@
+"""GPU SVG-EAR path (k-means, probe, routing, compensated attention) vs the oracle.
+
+Bars (readings of SVG-EAR, gist.science 2603.08982, technical summary sec. 2):
+* k-means: given the same centroids, assignments are bit-exact except points
+  whose best and chosen distances are within 1e-4 relative (near-ties, which
+  float32 may order either way; counted and bounded); counts equal the
+  histogram of the assignment; centroids are the member means (float32
+  rounding of the exact mean).
+* probe: err within 1e-3 relative (plus a small absolute floor) of the float64
+  oracle run on the GPU's clusters.
+* routing: bit-exact against the oracle's selection rule applied to the GPU's
+  own float32 err.
+* output: the attention bars (bf16: max-abs 2e-2, mean-abs 2e-3; fp32: 1e-4)
+  against the float64 compensated attention with the GPU's selection.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from conftest import assert_bf16_close, cached_video_qkv
+from oracle import attention as OA
+from oracle import kmeans as KM
+from oracle import svgear as S
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev_tensor(x, dev, dtype):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(dev, dtype)
+
+
+def _assign_ok(x, c, got, rel=1e-4, max_frac=1e-3):
+    """got[i] is the oracle's argmin against c, except near-ties (bounded)."""
+    dist = KM.sq_distances(x, c)
+    want = np.argmin(dist, axis=1)
+    bad = np.nonzero(got != want)[0]
+    if len(bad):
+        i = bad
+        gap = dist[i, got[i]] - dist[i, want[i]]
+        scale = (x[i] ** 2).sum(1) + (c[want[i]] ** 2).sum(1)
+        assert (gap <= rel * scale).all(), ("assignment off beyond a near-tie", int(bad[0]))
+        assert len(bad) <= max(1, max_frac * len(got)), ("too many near-ties", len(bad))
+    return len(bad)
+
+
+def _means_ok(x, a, C, cent, count):
+    n, means = S.cluster_stats(x, a, C)
+    assert np.array_equal(count, n)
+    nz = n > 0
+    err = np.abs(cent[nz] - means[nz])
+    assert (err <= 2e-7 * np.maximum(1.0, np.abs(means[nz]))).all(), float(err.max())
+
+
+KM_CASES = [
+    # B, heads, N, d, C, dtype
+    (1, 2, 517, 64, 7, "bf16"),
+    (2, 1, 300, 128, 33, "f32"),
+    (1, 3, 1000, 128, 100, "bf16"),
+]
+
+
+@pytest.mark.parametrize("case", KM_CASES)
+def test_kmeans_iteration_chain(va, dev, case):
+    B, Hh, N, d, C, dt = case
+    x = synth.iid_qkv(B, Hh, N, d, seed=21, dtype=dt)[0]
+    init = synth.init_indices(B, Hh, N, C, seed=22)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    xt = _dev_tensor(x, dev, tdt)
+    it = _dev_tensor(init, dev, torch.int32)
+    runs = {}
+    for iters in (0, 1, 2, 3):
+        a, c, n = va.cluster(xt, C, iters, it)
+        assert va.device_error() == va.OK
+        runs[iters] = (a.cpu().numpy().astype(np.int64), c.cpu().numpy().astype(np.float64),
+                       n.cpu().numpy().astype(np.int64))
+    for b in range(B):
+        for h in range(Hh):
+            xs = x[b, h].astype(np.float64)
+            # iteration 0: the assignment to the initial centroids x[init]
+            a0 = runs[0][0][b, h]
+            _assign_ok(xs, xs[init[b, h]], a0)
+            assert np.array_equal(runs[0][2][b, h], np.bincount(a0, minlength=C))
+            for j in (1, 2, 3):
+                a, c, n = (r[b, h] for r in runs[j])
+                prev_c = xs[init[b, h]] if j == 1 else runs[j - 1][1][b, h]
+                _assign_ok(xs, prev_c, a)
+                _means_ok(xs, a, C, c, n)
+
+
+def test_kmeans_recovers_planted_blobs(va, dev):
+    rng = np.random.default_rng(5)
+    C, per, d = 16, 40, 64
+    centers = rng.standard_normal((C, d)) * 6.0
+    labels = np.repeat(np.arange(C), per)
+    x = (centers[labels] + rng.standard_normal((C * per, d))).astype(np.float32)
+    init = np.arange(C, dtype=np.int32) * per + 3        # one seed point per blob
+    a, c, n = va.cluster(_dev_tensor(x[None, None], dev, torch.float32), C, 5,
+                         _dev_tensor(init[None, None], dev, torch.int32))
+    assert np.array_equal(a.cpu().numpy()[0, 0], labels)
+    assert (n.cpu().numpy()[0, 0] == per).all()
+    want = np.stack([x[labels == k].astype(np.float64).mean(0) for k in range(C)])
+    assert np.abs(c.cpu().numpy()[0, 0] - want).max() < 1e-5
+
+
+def test_kmeans_rejects_bad_arguments(va, dev):
+    x = torch.zeros((1, 1, 64, 128), dtype=torch.bfloat16, device=dev)
+    init = torch.arange(8, dtype=torch.int32, device=dev).view(1, 1, 8)
+    with pytest.raises(va.VAError) as e:
+        va.cluster(x, 8, -1, init)
+    assert e.value.status == va.ERR_INVALID
+    x96 = torch.zeros((1, 1, 64, 96), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(va.VAError) as e:
+        va.cluster(x96, 8, 1, init)
+    assert e.value.status == va.ERR_UNSUPPORTED
+    bad = torch.full((1, 1, 8), 64, dtype=torch.int32, device=dev)   # index == N
+    va.cluster(x, 8, 1, bad)
+    assert va.device_error() == va.ERR_DEVICE
+    assert va.device_error() == va.OK
+
+
+def _route_case(va, dev, q, k, v, qa, ka, Cq, Ck, density, scale, dt):
+    B, Hh, N, d = q.shape
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    qt, kt, vt = (_dev_tensor(x, dev, tdt) for x in (q, k, v))
+    err = torch.empty((B, Hh, Cq, Ck), dtype=torch.float32, device=dev)
+    sel = torch.empty((B, Hh, Cq, Ck), dtype=torch.uint8, device=dev)
+    out, _, _ = va.compensate_route(qt, kt, vt, _dev_tensor(qa, dev, torch.int32), Cq,
+                                    _dev_tensor(ka, dev, torch.int32), Ck, density,
+                                    scale=scale, err=err, sel=sel)
+    assert va.device_error() == va.OK
+    return out.float().cpu().numpy(), err.cpu().numpy(), sel.cpu().numpy().astype(bool)
+
+
+def _check_err(got, want, rel=1e-3):
+    finite = np.isfinite(want)
+    assert np.array_equal(np.isfinite(got), finite)
+    floor = 1e-6 * max(1e-30, np.abs(want[finite]).max())
+    diff = np.abs(got[finite] - want[finite])
+    assert (diff <= rel * np.abs(want[finite]) + floor).all(), float((diff / (np.abs(want[finite]) + floor)).max())
+
+
+ROUTE_CASES = [
+    # N, d, Cq, Ck, density, dtype, empty clusters
+    (331, 128, 5, 17, 0.2, "bf16", True),
+    (331, 64, 6, 13, 0.0, "f32", False),
+    (400, 128, 4, 11, 1.0, "f32", True),
+    (700, 128, 9, 40, 0.15, "bf16", False),
+]
+
+
+@pytest.mark.parametrize("case", ROUTE_CASES)
+def test_compensate_route_small(va, dev, case):
+    N, d, Cq, Ck, density, dt, empty = case
+    B, Hh = 1, 2
+    T = 1
+    q, k, v = synth.video_qkv(B, Hh, T, 1, N, d, seed=31, dtype=dt)
+    rng = np.random.default_rng(32)
+    qa = rng.integers(0, Cq - (1 if empty else 0), (B, Hh, N)).astype(np.int32)
+    ka = rng.integers(0, Ck - (2 if empty else 0), (B, Hh, N)).astype(np.int32)
+    scale = 1.0 / np.sqrt(d)
+    out, err, sel = _route_case(va, dev, q, k, v, qa, ka, Cq, Ck, density, scale, dt)
+    for b in range(B):
+        for h in range(Hh):
+            pr = S.probe(q[b, h], k[b, h], v[b, h], qa[b, h], Cq, ka[b, h], Ck, scale)
+            _check_err(err[b, h], pr["err"])
+            want_sel = S.route(err[b, h], pr["nq"], pr["nk"], N, density)
+            assert np.array_equal(sel[b, h], want_sel)
+            want = S.compensated_attention(q[b, h], k[b, h], v[b, h], qa[b, h], ka[b, h], Ck,
+                                           sel[b, h], scale)
+            if dt == "bf16":
+                assert_bf16_close(out[b, h], want)
+            else:
+                assert np.abs(out[b, h] - want).max() <= 1e-4
+
+
+def test_compensate_route_extremes_match_closed_forms(va, dev):
+    # density 1: exact dense attention; singleton key clusters: exact for any density.
+    N, d = 256, 64
+    q, k, v = synth.iid_qkv(1, 1, N, d, seed=41)
+    scale = 0.125
+    rng = np.random.default_rng(42)
+    qa = rng.integers(0, 4, (1, 1, N)).astype(np.int32)
+    dense, _ = OA.attention_rows(q[0, 0], k[0, 0], v[0, 0],
+                                 lambda r: np.ones((len(r), N), dtype=bool), scale)
+    ka = rng.integers(0, 8, (1, 1, N)).astype(np.int32)
+    out, _, sel = _route_case(va, dev, q, k, v, qa, ka, 4, 8, 1.0, scale, "f32")
+    assert sel.all()
+    assert np.abs(out[0, 0] - dense).max() <= 1e-4
+    ka1 = rng.permutation(N).astype(np.int32).reshape(1, 1, N)
+    out, err, _ = _route_case(va, dev, q, k, v, qa, ka1, 4, N, 0.05, scale, "f32")
+    assert np.abs(out[0, 0] - dense).max() <= 1e-4
+    assert np.nanmax(err) < 1e-5
+
+
+def test_svgear_full_size(va, dev):
+    # SVG-EAR-style workload: B=1, 12 heads, 21x30x52 = 32,760 tokens, d=128,
+    # bf16; k-means with 256 query and 1,024 key clusters (10 iterations,
+    # seeded init); routing at 15% density with centroid compensation.
+    T, H, W, Hh, d, Cq, Ck, density = 21, 30, 52, 12, 128, 256, 1024, 0.15
+    N = T * H * W
+    q, k, v = cached_video_qkv(1, Hh, T, H, W, d, seed=1238)
+    qt, kt, vt = (_dev_tensor(x, dev, torch.bfloat16) for x in (q, k, v))
+    qinit = _dev_tensor(synth.init_indices(1, Hh, N, Cq, seed=1238, tensor=synth.INIT), dev,
+                        torch.int32)
+    kinit = _dev_tensor(synth.init_indices(1, Hh, N, Ck, seed=1238, tensor=synth.INIT + 1), dev,
+                        torch.int32)
+    qa9, qc9, _ = va.cluster(qt, Cq, 9, qinit)
+    qa, qc, qn = va.cluster(qt, Cq, 10, qinit)
+    ka9, kc9, _ = va.cluster(kt, Ck, 9, kinit)
+    ka, kc, kn = va.cluster(kt, Ck, 10, kinit)
+    assert va.device_error() == va.OK
+    qa, ka = qa.cpu().numpy(), ka.cpu().numpy()
+    for h in (0, 7):                                       # k-means checks on two heads
+        _assign_ok(q[0, h].astype(np.float64), qc9.cpu().numpy()[0, h].astype(np.float64),
+                   qa[0, h].astype(np.int64))
+        _assign_ok(k[0, h].astype(np.float64), kc9.cpu().numpy()[0, h].astype(np.float64),
+                   ka[0, h].astype(np.int64))
+        _means_ok(k[0, h].astype(np.float64), ka[0, h], Ck, kc.cpu().numpy()[0, h].astype(np.float64),
+                  kn.cpu().numpy()[0, h])
+    scale = 1.0 / np.sqrt(d)
+    err = torch.empty((1, Hh, Cq, Ck), dtype=torch.float32, device=dev)
+    sel = torch.empty((1, Hh, Cq, Ck), dtype=torch.uint8, device=dev)
+    out, _, _ = va.compensate_route(qt, kt, vt, _dev_tensor(qa, dev, torch.int32), Cq,
+                                    _dev_tensor(ka, dev, torch.int32), Ck, density, err=err,
+                                    sel=sel)
+    assert va.device_error() == va.OK
+    err, sel, out = err.cpu().numpy(), sel.cpu().numpy().astype(bool), out.float().cpu().numpy()
+    rows = OA.sample_rows(N, 128, 512, seed=9)
+    for h in range(Hh):
+        nq, _ = S.cluster_stats(q[0, h], qa[0, h], Cq)
+        nk, _ = S.cluster_stats(k[0, h], ka[0, h], Ck)
+        want_sel = S.route(err[0, h], nq, nk, N, density)
+        assert np.array_equal(sel[0, h], want_sel)
+        cost = (nq[:, None] * nk[None, :])[sel[0, h]].sum()
+        assert cost <= S.budget(density, N)
+        want = S.compensated_attention(q[0, h], k[0, h], v[0, h], qa[0, h], ka[0, h], Ck,
+                                       sel[0, h], scale, rows=rows)
+        assert_bf16_close(out[0, h][rows], want)
+    h = 3                                                  # probe on one head
+    pr = S.probe(q[0, h], k[0, h], v[0, h], qa[0, h], Cq, ka[0, h], Ck, scale)
+    _check_err(err[0, h], pr["err"])
