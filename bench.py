@@ -1,18 +1,28 @@
 """Benchmark: block-sparse video attention forward on B300.
 
-Workload (one "step"): one va_sparse_attn_fwd call of the Wan-2.1-1.3B-shaped
-radial-mask attention: B=1, 12 heads, 21x30x52 = 32,760 tokens, head_dim 128,
-bf16, 128-token blocks, radial mask with W0 = H*W (29,786 of 65,536 block
-pairs live). The static mask is built once before timing (it is shared by
-every step, layer and head). Inputs are synthetic (seeded Fourier-mode Q/K,
-N(0,1) V) and resident in HBM when device timing starts; one call touches
-Q+K+V+O = 403 MB, more than the 126 MB L2, so no flush is needed between
-timed calls.
+Default workload (one "step"): one va_sparse_attn_fwd call of the
+Wan-2.1-1.3B-shaped radial-mask attention: B=1, 12 heads, 21x30x52 = 32,760
+tokens, head_dim 128, bf16, 128-token blocks, radial mask with W0 = H*W
+(29,786 of 65,536 block pairs live). The static mask is built once before
+timing (it is shared by every step, layer and head). Inputs are synthetic
+(seeded Fourier-mode Q/K, N(0,1) V) and resident in HBM when device timing
+starts; one call touches Q+K+V+O = 403 MB, more than the 126 MB L2, so no
+flush is needed between timed calls.
 
 Metric: effective TFLOP/s over live blocks, i.e. 4 * d * (sum over live block
 pairs of |I| * |J|, real tokens only) * B * heads per call, and ms per call.
 
+--workload selects another measured workload (its own JSON line, same keys):
+  lvsa_long       LVSA long horizon, 12 heads, 126x30x52 = 196,560 tokens,
+                  +-2-frame window, anchor every 8th frame (step 0)
+  hunyuan_radial  HunyuanVideo 720p shape, 24 heads, 33x45x80 = 118,800 tokens
+  hunyuan_dense   the same with the all-ones mask on the same kernel
+  svgear          one SVG-EAR step on the Wan shape: k-means of Q (256
+                  clusters) and K (1,024 clusters), 10 iterations each, then
+                  va_compensate_route at 15% density
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME]
 Under torchrun (N > 1) every rank runs its own copy of the workload (weak
 scaling, no collective on the data path); rank 0 prints one JSON line.
 --impl reference times the float64 CPU oracle (the only reference there is)
@@ -35,17 +45,47 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-T, H, W, HEADS, BATCH, D, BLOCK = 21, 30, 52, 12, 1, 128, 128
-N = T * H * W
-METRIC = "block-sparse attn effective TFLOP/s + ms/call at 32,760 tok; % of B300 BF16 peak"
+D, BLOCK, BATCH = 128, 128, 1
 UNIT = "TFLOP/s"
-SEED = 1235
-CONFIG = {"workload": "Wan-2.1-1.3B-shaped radial block-sparse attention forward",
-          "B": BATCH, "heads": HEADS, "grid_THW": [T, H, W], "tokens": N, "head_dim": D,
-          "block": BLOCK, "mask": "radial, W0=H*W", "live_blocks": "29786/65536",
-          "l2": "inputs larger than L2 (Q+K+V+O = 403 MB per call vs 126 MB L2), no flush"}
+# attention workloads: grid, heads, mask kind and parameters, input seed
+WORKLOADS = {
+    "wan_radial": dict(T=21, H=30, W=52, heads=12, kind="radial", params={}, step=0, seed=1235,
+                       desc="Wan-2.1-1.3B-shaped radial block-sparse attention forward",
+                       mask="radial, W0=H*W"),
+    "lvsa_long": dict(T=126, H=30, W=52, heads=12, kind="lvsa",
+                      params=dict(local=2, period=8, anchor0=0, rot_stride=1), step=0,
+                      seed=1237, desc="LVSA long-horizon (6x Wan frames) block-sparse attention "
+                      "forward", mask="LVSA, +-2 frames + anchor every 8th frame, step 0"),
+    "hunyuan_radial": dict(T=33, H=45, W=80, heads=24, kind="radial", params={}, step=0,
+                           seed=1239, desc="HunyuanVideo-720p-shaped radial block-sparse "
+                           "attention forward", mask="radial, W0=H*W"),
+    "hunyuan_dense": dict(T=33, H=45, W=80, heads=24, kind="dense", params={}, step=0,
+                          seed=1239, desc="HunyuanVideo-720p-shaped attention forward with the "
+                          "all-ones mask on the same block-sparse kernel", mask="dense"),
+}
+METRIC = "block-sparse attn effective TFLOP/s + ms/call at 32,760 tok; % of B300 BF16 peak"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_tc_wan_radial_traffic.json")
 KERNEL_SRC = os.path.join(ROOT, "linear_attention_video_fwd_b300", "csrc", "attn_tc.cuh")
+# fp32 FMA roof of a B300 (148 SMs x 128 FP32 lanes x 2 FLOP at the 2,032 MHz
+# maximum SM clock), the bound of the SIMT SVG-EAR kernels
+FP32_FMA_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def workload_metric(name, wl):
+    if name == "wan_radial":
+        return METRIC
+    N = wl["T"] * wl["H"] * wl["W"]
+    return "block-sparse attn effective TFLOP/s + ms/call at %s tok (%s); %% of B300 BF16 peak" % (
+        format(N, ","), name)
+
+
+def workload_config(name, wl):
+    N = wl["T"] * wl["H"] * wl["W"]
+    return {"workload": wl["desc"], "B": BATCH, "heads": wl["heads"],
+            "grid_THW": [wl["T"], wl["H"], wl["W"]], "tokens": N, "head_dim": D,
+            "block": BLOCK, "mask": wl["mask"],
+            "l2": "inputs larger than L2 (Q+K+V+O = %d MB per call vs 126 MB L2), no flush"
+                  % round(4 * BATCH * wl["heads"] * N * D * 2 / 1e6)}
 
 
 def peaks():
@@ -165,43 +205,39 @@ def threads_used() -> int:
     return os.cpu_count() or 1
 
 
-def make_inputs(seed):
+def make_inputs(wl, seed):
     import synth
-    return synth.video_qkv(BATCH, HEADS, T, H, W, D, seed=seed, dtype="bf16")
+    return synth.video_qkv(BATCH, wl["heads"], wl["T"], wl["H"], wl["W"], D, seed=seed,
+                           dtype="bf16")
 
 
-def oracle_sample(q, k, v, bm, rows):
+def oracle_block_mask(wl):
+    from oracle import masks as OM
+    kind = {"radial": OM.RADIAL, "lvsa": OM.LVSA, "dense": OM.DENSE}[wl["kind"]]
+    return OM.block_mask(kind, wl["T"], wl["H"], wl["W"],
+                         OM.MaskParams(block=BLOCK, **wl["params"]), wl["step"])
+
+
+def oracle_sample(wl, q, k, v, bm, rows):
     """Run the float64 oracle on `rows` of every head; returns (seconds, live FLOPs done)."""
     from oracle import attention as OA
+    N = q.shape[2]
     live_keys_per_block = (bm * np.array([min(N, (b + 1) * BLOCK) - b * BLOCK
                                           for b in range(bm.shape[0])])[None, :]).sum(1)
-    flops = 4.0 * D * float(live_keys_per_block[rows // BLOCK].sum()) * BATCH * HEADS
+    flops = 4.0 * D * float(live_keys_per_block[rows // BLOCK].sum()) * BATCH * wl["heads"]
     t0 = time.perf_counter()
     OA.block_sparse_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(D), rows=rows)
     return time.perf_counter() - t0, flops
 
 
-def run_ours(args, world, rank, local):
+def timed_region(args, world, local, call, stream):
+    """Warm-up, a >= 0.6 s pre-roll under the clock sampler, then K timed calls.
+
+    Returns (total_ms max over ranks, per-call launch ms list, clock summary).
+    """
     import torch
-    import linear_attention_video_fwd_b300 as va
-    from oracle import attention as OA
-    from oracle import masks as OM
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    q, k, v = make_inputs(SEED + rank)
-    qt, kt, vt = (torch.from_numpy(x).to(dev, torch.bfloat16) for x in (q, k, v))
-    out = torch.empty_like(qt)
-    mask = va.mask_build(va.RADIAL, T, H, W, block=BLOCK)
-    flops = 4.0 * D * mask.live_pairs * BATCH * HEADS
-    stream = torch.cuda.current_stream()
-
     for _ in range(args.warmup):
-        va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
-    if va.device_error() != va.OK:
-        raise RuntimeError("device error during warm-up")
-
-    # ---- device-timed region: inputs resident in HBM --------------------------
+        call()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -212,23 +248,48 @@ def run_ours(args, world, rank, local):
         # 200 ms clock samples are all taken under this load.
         t0 = time.perf_counter()
         while time.perf_counter() - t0 < 0.6:
-            for _ in range(20):
-                va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
+            for _ in range(4):
+                call()
             torch.cuda.synchronize()
         t_begin.record(stream)
         for i in range(args.steps):
             starts[i].record(stream)
-            va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
+            call()
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
         time.sleep(0.25)
     barrier(world)
+    total_ms = max_over_ranks(t_begin.elapsed_time(t_end), world, torch.device("cuda", local))
+    return total_ms, [a.elapsed_time(b) for a, b in zip(starts, ends)], clocks.summary()
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import linear_attention_video_fwd_b300 as va
+    from oracle import attention as OA
+
+    name = args.workload
+    wl = WORKLOADS[name]
+    T, H, W, heads = wl["T"], wl["H"], wl["W"], wl["heads"]
+    N = T * H * W
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v = make_inputs(wl, wl["seed"] + rank)
+    qt, kt, vt = (torch.from_numpy(x).to(dev, torch.bfloat16) for x in (q, k, v))
+    out = torch.empty_like(qt)
+    kind = {"radial": va.RADIAL, "lvsa": va.LVSA, "dense": va.DENSE}[wl["kind"]]
+    mask = va.mask_build(kind, T, H, W, block=BLOCK, step=wl["step"], **wl["params"])
+    flops = 4.0 * D * mask.live_pairs * BATCH * heads
+    stream = torch.cuda.current_stream()
+
+    def call():
+        va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
+
+    # ---- device-timed region: inputs resident in HBM --------------------------
+    total_ms, launch_ms, clocks = timed_region(args, world, local, call, stream)
     if va.device_error() != va.OK:
         raise RuntimeError("device error in the timed region")
-    total_ms = t_begin.elapsed_time(t_end)
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
@@ -236,18 +297,22 @@ def run_ours(args, world, rank, local):
     qh, kh, vh = (x.to("cpu").pin_memory() for x in (qt, kt, vt))
     oh = torch.empty(qh.shape, dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        qt.copy_(qh, non_blocking=True); kt.copy_(kh, non_blocking=True); vt.copy_(vh, non_blocking=True)
+
+    def e2e_call():
+        qt.copy_(qh, non_blocking=True)
+        kt.copy_(kh, non_blocking=True)
+        vt.copy_(vh, non_blocking=True)
         va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
         oh.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_call()
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(e2e_steps):
-        qt.copy_(qh, non_blocking=True); kt.copy_(kh, non_blocking=True); vt.copy_(vh, non_blocking=True)
-        va.sparse_attn_fwd(qt, kt, vt, mask, out=out)
-        oh.copy_(out, non_blocking=True)
+        e2e_call()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -257,11 +322,14 @@ def run_ours(args, world, rank, local):
     pk, src = peaks()
     achieved = flops / (float(np.mean(launch_ms)) * 1e-3) / 1e12
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "metric": workload_metric(name, wl), "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Fourier-mode Q/K + N(0,0.5^2), V~N(0,1)); no weights needed",
-        "config": dict(CONFIG, parallelism="replicas: one independent workload per GPU"),
+        "config": dict(workload_config(name, wl),
+                       live_blocks="%d/%d" % (mask.nnz, mask.nqb * mask.nqb),
+                       parallelism="replicas: one independent workload per GPU"),
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": 3 * tensor_bytes, "d2h_bytes_per_step": tensor_bytes},
@@ -273,21 +341,128 @@ def run_ours(args, world, rank, local):
                      "frac_of_sustained": round(achieved / pk["bf16_tflops_sustained"], 4),
                      "flops_per_launch": flops, "launch_ms_mean": round(float(np.mean(launch_ms)), 4),
                      "launch_ms_min": round(float(np.min(launch_ms)), 4),
-                     "traffic": profiled_traffic(), "kernel": "va::attn_tc_kernel"},
+                     "traffic": profiled_traffic() if name == "wan_radial" else None,
+                     "kernel": "va::attn_tc_kernel"},
         "gpu_launches": args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        bm = OM.block_mask(OM.RADIAL, T, H, W, OM.MaskParams(block=BLOCK))
+        bm = oracle_block_mask(wl)
         rows = OA.sample_rows(N, BLOCK, args.oracle_rows, seed=7)
-        secs, oflops = oracle_sample(q, k, v, bm, rows)
+        secs, oflops = oracle_sample(wl, q, k, v, bm, rows)
         line["cpu_baseline"] = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT,
                                 "cores": threads_used(), "kind": "oracle",
                                 "seconds": round(secs, 2),
                                 "sample": "%d seeded query rows x %d heads of the same workload "
                                           "(float64 numpy oracle, masked dense rows)"
-                                          % (len(rows), HEADS)}
+                                          % (len(rows), heads)}
     mask.free()
+    return line
+
+
+SVG = dict(T=21, H=30, W=52, heads=12, Cq=256, Ck=1024, iters=10, density=0.15, seed=1238)
+
+
+def svgear_flops(qa, ka, sel, Cq, Ck, N, iters):
+    """Algorithmic FLOPs of one SVG-EAR step per stage (all heads), from the
+    step's own clusters and selection."""
+    heads = qa.shape[1]
+    out = {"cluster_q": 2.0 * N * Cq * D * iters * heads,
+           "cluster_k": 2.0 * N * Ck * D * iters * heads, "probe": 0.0, "exact": 0.0,
+           "virtual": 0.0}
+    for h in range(heads):
+        nq = np.bincount(qa[0, h], minlength=Cq).astype(np.float64)
+        nk = np.bincount(ka[0, h], minlength=Ck).astype(np.float64)
+        s = sel[0, h]
+        out["probe"] += 8.0 * (nq > 0).sum() * N * D          # 2 passes x (logits + values)
+        out["exact"] += 4.0 * D * float((nq[:, None] * nk[None, :])[s].sum())
+        virt = (~s) & (nk[None, :] > 0)
+        out["virtual"] += 4.0 * D * float((nq[:, None] * virt).sum())
+    return out
+
+
+def run_svgear(args, world, rank, local):
+    import torch
+    import linear_attention_video_fwd_b300 as va
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    T, H, W, heads, Cq, Ck = SVG["T"], SVG["H"], SVG["W"], SVG["heads"], SVG["Cq"], SVG["Ck"]
+    N = T * H * W
+    q, k, v = synth.video_qkv(BATCH, heads, T, H, W, D, seed=SVG["seed"] + rank, dtype="bf16")
+    qt, kt, vt = (torch.from_numpy(x).to(dev, torch.bfloat16) for x in (q, k, v))
+    qinit = torch.from_numpy(synth.init_indices(BATCH, heads, N, Cq, seed=SVG["seed"])).to(dev)
+    kinit = torch.from_numpy(synth.init_indices(BATCH, heads, N, Ck, seed=SVG["seed"],
+                                                tensor=synth.INIT + 1)).to(dev)
+    qa = torch.empty((BATCH, heads, N), dtype=torch.int32, device=dev)
+    ka = torch.empty_like(qa)
+    qc = torch.empty((BATCH, heads, Cq, D), dtype=torch.float32, device=dev)
+    kc = torch.empty((BATCH, heads, Ck, D), dtype=torch.float32, device=dev)
+    qn = torch.empty((BATCH, heads, Cq), dtype=torch.int32, device=dev)
+    kn = torch.empty((BATCH, heads, Ck), dtype=torch.int32, device=dev)
+    out = torch.empty_like(qt)
+    sel = torch.empty((BATCH, heads, Cq, Ck), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    stage_ms = {"cluster_q": [], "cluster_k": [], "compensate_route": []}
+    record = [False]
+
+    def call():
+        ev[0].record(stream)
+        va.cluster(qt, Cq, SVG["iters"], qinit, qa, qc, qn)
+        ev[1].record(stream)
+        va.cluster(kt, Ck, SVG["iters"], kinit, ka, kc, kn)
+        ev[2].record(stream)
+        va.compensate_route(qt, kt, vt, qa, Cq, ka, Ck, SVG["density"], out=out, sel=sel)
+        ev[3].record(stream)
+        if record[0]:
+            torch.cuda.synchronize()
+            stage_ms["cluster_q"].append(ev[0].elapsed_time(ev[1]))
+            stage_ms["cluster_k"].append(ev[1].elapsed_time(ev[2]))
+            stage_ms["compensate_route"].append(ev[2].elapsed_time(ev[3]))
+
+    total_ms, launch_ms, clocks = timed_region(args, world, local, call, stream)
+    if va.device_error() != va.OK:
+        raise RuntimeError("device error in the timed region")
+    record[0] = True
+    for _ in range(3):
+        call()
+    fl = svgear_flops(qa.cpu().numpy(), ka.cpu().numpy(), sel.cpu().numpy().astype(bool), Cq, Ck,
+                      N, SVG["iters"])
+    step_flops = sum(fl.values())
+    ms_per_step = total_ms / args.steps
+    st = {k2: float(np.median(v2)) for k2, v2 in stage_ms.items()}
+    comp_flops = fl["probe"] + fl["exact"] + fl["virtual"]
+    stages = {"cluster_q": (fl["cluster_q"], st["cluster_q"]),
+              "cluster_k": (fl["cluster_k"], st["cluster_k"]),
+              "compensate_route": (comp_flops, st["compensate_route"])}
+    dom = max(stages, key=lambda n: stages[n][1])
+    dom_tf = stages[dom][0] / (stages[dom][1] * 1e-3) / 1e12
+    line = {
+        "metric": "SVG-EAR step (k-means Q/K + probe + routing + compensated attention) "
+                  "effective TFLOP/s + ms/step at 32,760 tok",
+        "value": round(world * step_flops * args.steps / (total_ms * 1e-3) / 1e12, 3),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 inputs, f32 arithmetic",
+        "data": "synthetic (seeded Fourier-mode Q/K + N(0,0.5^2), V~N(0,1))",
+        "config": {"workload": "SVG-EAR-style compensated sparse attention, Wan shape",
+                   "B": BATCH, "heads": heads, "grid_THW": [T, H, W], "tokens": N,
+                   "head_dim": D, "Cq": Cq, "Ck": Ck, "kmeans_iters": SVG["iters"],
+                   "density": SVG["density"],
+                   "parallelism": "replicas: one independent workload per GPU"},
+        "stages_ms": {k2: round(v2, 3) for k2, v2 in st.items()},
+        "stages_tflops": {n: round(f / (t * 1e-3) / 1e12, 2) for n, (f, t) in stages.items()},
+        "flops_per_step": {k2: float(v2) for k2, v2 in fl.items()},
+        "roofline": {"bound": "alu", "achieved": round(dom_tf, 2),
+                     "peak": round(FP32_FMA_PEAK_TFLOPS, 1), "unit": UNIT,
+                     "frac": round(dom_tf / FP32_FMA_PEAK_TFLOPS, 4),
+                     "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 FLOP x 2032 MHz",
+                     "stage": dom, "traffic": None},
+        "gpu_launches": None,
+        "clocks": clocks,
+    }
     return line
 
 
@@ -296,27 +471,30 @@ def run_reference(args, world, rank):
     if rank != 0:
         return None
     from oracle import attention as OA
-    from oracle import masks as OM
-    q, k, v = make_inputs(SEED)
-    bm = OM.block_mask(OM.RADIAL, T, H, W, OM.MaskParams(block=BLOCK))
+    name = args.workload if args.workload in WORKLOADS else "wan_radial"
+    wl = WORKLOADS[name]
+    N = wl["T"] * wl["H"] * wl["W"]
+    q, k, v = make_inputs(wl, wl["seed"])
+    bm = oracle_block_mask(wl)
     per_step = args.reference_rows
     for i in range(args.warmup):
-        oracle_sample(q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=1000 + i))
+        oracle_sample(wl, q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=1000 + i))
     secs, fl = 0.0, 0.0
     for i in range(args.steps):
-        s, f = oracle_sample(q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=2000 + i))
+        s, f = oracle_sample(wl, q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=2000 + i))
         secs += s
         fl += f
     value = fl / secs / 1e12
     return {
-        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
+        "metric": workload_metric(name, wl), "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (same seeded inputs as the GPU arm)", "impl": "reference",
-        "config": dict(CONFIG, parallelism="single process, host cores"),
+        "config": dict(workload_config(name, wl), parallelism="single process, host cores"),
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads_used(),
                          "kind": "oracle",
-                         "sample": "%d seeded query rows x %d heads per step" % (per_step, HEADS)},
+                         "sample": "%d seeded query rows x %d heads per step"
+                                   % (per_step, wl["heads"])},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -328,6 +506,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["svgear"], default="wan_radial")
     ap.add_argument("--oracle-rows", type=int, default=512,
                     help="query rows per head in the CPU-oracle baseline sample")
     ap.add_argument("--reference-rows", type=int, default=16,
@@ -341,6 +520,8 @@ def main():
         print("warning: --gpus %d but WORLD_SIZE %d" % (args.gpus, world), file=sys.stderr)
     if args.impl == "reference":
         line = run_reference(args, world, rank)
+    elif args.workload == "svgear":
+        line = run_svgear(args, world, rank, local)
     else:
         line = run_ours(args, world, rank, local)
     if rank == 0 and line is not None:
