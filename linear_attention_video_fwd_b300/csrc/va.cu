@@ -15,6 +15,7 @@
 #include "attn_simt.cuh"
 #include "attn_tc.cuh"
 #include "svgear.cuh"
+#include "kmeans_tc.cuh"
 
 #define VA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -431,6 +432,56 @@ int cluster_lists(const int* assign, int BH, int N, int C, int* count, int* off,
   return launch_status();
 }
 
+// bf16, d = 128: distances on the tensor cores (split-bf16 centroids).
+int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C, int iters,
+                   int* assign, float* cent, int* count, cudaStream_t s) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int st;
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    if ((st = set_smem_attrs<__nv_bfloat16, 128>()) ||
+        (st = cuda_status(cudaFuncSetAttribute(va::km_assign_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               va::KA_SMEM_BYTES))))
+      return st;
+    configured[dev] = true;
+  }
+  Scoped scratch(s);
+  float* cnorm = nullptr;
+  int *off = nullptr, *fill = nullptr, *perm = nullptr;
+  __nv_bfloat16 *hi = nullptr, *lo = nullptr;
+  const size_t nc = static_cast<size_t>(BH) * C * 128;
+  if ((st = scratch.alloc(&cnorm, static_cast<size_t>(BH) * C)) ||
+      (st = scratch.alloc(&off, static_cast<size_t>(BH) * (C + 1))) ||
+      (st = scratch.alloc(&fill, static_cast<size_t>(BH) * C)) ||
+      (st = scratch.alloc(&perm, static_cast<size_t>(BH) * N)) ||
+      (st = scratch.alloc(&hi, nc)) || (st = scratch.alloc(&lo, nc)))
+    return st;
+  CUtensorMap mx, mh, ml;
+  if ((st = encode_bf16_rows(&mx, x, BH, N, 128)) || (st = encode_bf16_rows(&mh, hi, BH, C, 128)) ||
+      (st = encode_bf16_rows(&ml, lo, BH, C, 128)))
+    return st;
+  const dim3 gc((C + 7) / 8, BH);
+  const dim3 ga((N + 127) / 128, BH);
+  const dim3 gn((N + 255) / 256, BH);
+  const unsigned gs = static_cast<unsigned>((nc + 255) / 256);
+  va::km_init_kernel<__nv_bfloat16, 128><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
+  va::km_split_kernel<<<gs, 256, 0, s>>>(cent, static_cast<long long>(nc), hi, lo);
+  const int rounds = iters > 0 ? iters : 1;
+  for (int it = 0; it < rounds; ++it) {
+    if ((st = cuda_status(cudaMemsetAsync(count, 0, sizeof(int) * BH * C, s)))) return st;
+    va::km_assign_tc_kernel<<<ga, va::KA_THREADS, va::KA_SMEM_BYTES, s>>>(
+        mx, mh, ml, cnorm, N, C, assign, count, g_wait_limit);
+    if (iters == 0) break;
+    va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
+    va::km_scatter_kernel<<<gn, 256, 0, s>>>(assign, N, C, off, fill, perm);
+    va::km_means_kernel<__nv_bfloat16, 128><<<gc, 256, 0, s>>>(x, N, C, off, perm, cent, cnorm, 1);
+    va::km_split_kernel<<<gs, 256, 0, s>>>(cent, static_cast<long long>(nc), hi, lo);
+  }
+  return launch_status();
+}
+
 template <typename T, int D>
 int run_cluster(const T* x, const int* init, int BH, int N, int C, int iters, int* assign,
                 float* cent, int* count, cudaStream_t s) {
@@ -480,8 +531,7 @@ VA_EXPORT int va_cluster(const void* x, const int32_t* init_idx, int B, int head
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == VA_BF16) {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    return d == 128 ? run_cluster<__nv_bfloat16, 128>(xb, init_idx, BH, N, C, iters, assign,
-                                                      centroid, count, s)
+    return d == 128 ? run_cluster_tc(xb, init_idx, BH, N, C, iters, assign, centroid, count, s)
                     : run_cluster<__nv_bfloat16, 64>(xb, init_idx, BH, N, C, iters, assign,
                                                      centroid, count, s);
   }

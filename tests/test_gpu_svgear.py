@@ -57,6 +57,7 @@ KM_CASES = [
     (1, 2, 517, 64, 7, "bf16"),
     (2, 1, 300, 128, 33, "f32"),
     (1, 3, 1000, 128, 100, "bf16"),
+    (1, 2, 1500, 128, 300, "bf16"),          # tensor-core path, ragged cluster tile
 ]
 
 
