@@ -1,0 +1,568 @@
+// SVG-EAR compensated attention on the 5th-generation tensor cores (bf16,
+// d = 128): one softmax per query over (1) virtual centroid keys kc_c with
+// logit bias ln n_c and values vc_c for every non-empty key cluster that is
+// not selected for the query's cluster, and (2) the exact keys of the
+// selected key clusters (SVG-EAR, gist.science 2603.08982, technical summary
+// sec. 2, ideas 1 and 2).
+//
+// Layout: Q, K and V are first gathered into cluster order, so a query
+// cluster is a contiguous row range of Qs and a key cluster one of Ks / Vs.
+// A work unit is one 128-row chunk of one query cluster; a CTA takes two
+// chunks (tiles t = 0, 1) whose key streams are interleaved entry by entry,
+// reusing the two-tile pipeline of attn_tc.cuh (TMA producer warp, one MMA
+// thread, one softmax warpgroup per tile; S_t and O_t in TMEM).
+//
+// Key stream of a query cluster p: nv virtual tiles (centroids 128j ..
+// 128j + 127, one TMA box each for K and V), then exact tiles of 16 slots.
+// A slot is 8 consecutive rows of one selected key cluster (an 8-row TMA box,
+// which lands on a whole 128B-swizzle atom, so slots assemble into the same
+// shared-memory layout as one 128-row box); a cluster of n_c keys takes
+// ceil(n_c / 8) slots and the rows past n_c are masked. The producer passes
+// each entry's 128-bit validity mask to the softmax through a small
+// shared-memory ring with its own full / empty barriers.
+#pragma once
+
+#include "attn_tc.cuh"
+
+namespace va {
+
+constexpr int CT_NM = 4;  // validity-mask ring entries
+// Register split of this kernel (launched at TC_LAUNCH_REGS per thread): the
+// producer's slot search needs more than the attention kernel's producer.
+constexpr int CT_REGS_DEC = 64;
+constexpr int CT_REGS_INC = 216;
+static_assert(128 * CT_REGS_DEC + 256 * CT_REGS_INC <= TC_THREADS * TC_LAUNCH_REGS,
+              "register split exceeds the launch allocation");
+
+struct CompArgs {
+  const int* choff;    // [BH][Cq + 1] offsets of 128-row query chunks per cluster
+  const int* qoff;     // [BH][Cq + 1] query cluster offsets in cluster order
+  const int* qperm;    // [BH][N] token of each cluster-ordered query row
+  const int* koff;     // [BH][Ck + 1] key cluster offsets in cluster order
+  const int* nk;       // [BH][Ck]
+  const int* seln;     // [BH][Cq] number of selected key clusters
+  const int* selc;     // [BH][Cq][Ck] selected key clusters (ascending)
+  const int* selbox;   // [BH][Cq][Ck + 1] exclusive prefix of ceil(n_c / 8) over selc
+  const float* vbias;  // [BH][Cq][nv * 128] virtual-key bias, log2 units (-inf: none)
+  __nv_bfloat16* out;  // [BH][N][128], token order
+  int N, Cq, Ck, nv;
+  float scale_log2;
+  long long wait_limit;
+};
+
+enum : int {
+  CB_Q_FULL = 0,                    // 2
+  CB_K_FULL = CB_Q_FULL + 2,
+  CB_K_EMPTY = CB_K_FULL + TC_NK,
+  CB_V_FULL = CB_K_EMPTY + TC_NK,
+  CB_V_EMPTY = CB_V_FULL + TC_NV,
+  CB_M_FULL = CB_V_EMPTY + TC_NV,   // CT_NM
+  CB_M_EMPTY = CB_M_FULL + CT_NM,   // CT_NM, 128 arrivals
+  CB_S_FULL = CB_M_EMPTY + CT_NM,   // 2
+  CB_P_FULL = CB_S_FULL + 2,        // 2, 128 arrivals
+  CB_O_DONE = CB_P_FULL + 2,        // 2
+  CB_DRAIN = CB_O_DONE + 2,
+  CB_COUNT = CB_DRAIN + 1
+};
+
+struct CompTile {
+  int p, r0, nrows, ns, nslots, n;  // cluster, first row, rows, selected, slots, blocks
+};
+
+// Entry u of the interleaved stream of two tiles with n0, n1 blocks.
+__device__ __forceinline__ void ct_entry(int u, int n0, int n1, int& t, int& j) {
+  const int nmin = min(n0, n1);
+  if (u < 2 * nmin) {
+    t = u & 1;
+    j = u >> 1;
+  } else {
+    t = n0 > n1 ? 0 : 1;
+    j = nmin + (u - 2 * nmin);
+  }
+}
+
+__device__ __forceinline__ int ct_index(int t, int j, int n0, int n1) {
+  const int nmin = min(n0, n1);
+  return j < nmin ? 2 * j + t : 2 * nmin + (j - nmin);
+}
+
+// Softmax of one tile (thread r owns row r of the tile).
+__device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const CompTile& T,
+                                           int n0, int n1, int bh, uint32_t tmem,
+                                           uint64_t* bars, const uint32_t* masks,
+                                           volatile int* abort_p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t tS = tmem + tile * 256 + lane_off;
+  const uint32_t tO = tS + 128;
+  const uint32_t bS = smem_u32(&bars[CB_S_FULL + tile]);
+  const uint32_t bP = smem_u32(&bars[CB_P_FULL + tile]);
+  const uint32_t bO = smem_u32(&bars[CB_O_DONE + tile]);
+  const long long lim = a.wait_limit;
+  const float sl2 = a.scale_log2;
+  const float* vb = a.vbias + (static_cast<long long>(bh) * a.Cq + T.p) * (a.nv * 128);
+
+  float m_used = -INFINITY, l = 0.f;
+  bool ok = true;
+  for (int j = 0; j < T.n; ++j) {
+    const int u = ct_index(tile, j, n0, n1);
+    const int ms = u % CT_NM;
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bS, j & 1, lim, abort_p));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bars[CB_M_FULL + ms]),
+                                                           (u / CT_NM) & 1, lim, abort_p));
+    if (!ok) break;
+    uint32_t mw[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) mw[w] = masks[ms * 4 + w];
+    mbar_arrive(smem_u32(&bars[CB_M_EMPTY + ms]));
+    tc_fence_after();
+    float s[128];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tS + c * 32, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+    }
+    tmem_wait_ld();
+    if (j < a.nv) {
+      // virtual keys: scaled logit + log2 n_c (-inf for selected or empty c)
+      const float4* b4 = reinterpret_cast<const float4*>(vb + j * 128);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float4 bb = __ldg(b4 + i);
+        ffma2_bc(s[4 * i], s[4 * i + 1], s[4 * i], s[4 * i + 1], sl2, 0.f);
+        ffma2_bc(s[4 * i + 2], s[4 * i + 3], s[4 * i + 2], s[4 * i + 3], sl2, 0.f);
+        s[4 * i] += bb.x;
+        s[4 * i + 1] += bb.y;
+        s[4 * i + 2] += bb.z;
+        s[4 * i + 3] += bb.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 128; ++i)
+        s[i] = ((mw[i >> 5] >> (i & 31)) & 1u) ? s[i] * sl2 : -INFINITY;
+    }
+    float m0 = fmax3(s[0], s[1], s[2]), m1 = fmax3(s[3], s[4], s[5]);
+    float m2 = fmax3(s[6], s[7], s[8]), m3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+    for (int i = 12; i < 124; i += 8) {
+      m0 = fmax3(m0, s[i], s[i + 1]);
+      m1 = fmax3(m1, s[i + 2], s[i + 3]);
+      m2 = fmax3(m2, s[i + 4], s[i + 5]);
+      m3 = fmax3(m3, s[i + 6], s[i + 7]);
+    }
+    const float m_cand = fmax3(fmax3(m0, m1, s[124]), fmax3(m2, m3, s[125]), fmaxf(s[126], s[127]));
+    const bool need = m_cand > m_used + TC_TAU;  // false while the block is all -inf
+    float alpha = 1.f;
+    if (need) {
+      alpha = ex2_approx(m_used - m_cand);
+      m_used = m_cand;
+      l *= alpha;
+    }
+    if (__any_sync(0xffffffffu, need && j > 0)) {
+      ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (j - 1) & 1, lim, abort_p));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + c * 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+        tmem_st32(tO + c * 32, v);
+      }
+    }
+    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+#pragma unroll
+    for (int i = 0; i < 128; i += 2) {
+      ffma2_bc(s[i], s[i + 1], s[i], s[i + 1], 1.f, neg_m);
+      s[i] = ex2_approx(s[i]);
+      s[i + 1] = ex2_approx(s[i + 1]);
+    }
+    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+    uint32_t pk[64];
+#pragma unroll
+    for (int i = 0; i < 128; i += 4) {
+      fadd2_acc(r0, r1, s[i], s[i + 1]);
+      fadd2_acc(r2, r3, s[i + 2], s[i + 3]);
+      pk[i / 2] = pack_bf16x2(s[i], s[i + 1]);
+      pk[i / 2 + 1] = pack_bf16x2(s[i + 2], s[i + 3]);
+    }
+    l += (r0 + r1) + (r2 + r3);
+    {
+      uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
+      uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[32]);
+      tmem_st32(tS, lo);
+      tmem_st32(tS + 32, hi);
+    }
+    tmem_wait_st();
+    tc_fence_before();
+    mbar_arrive(bP);
+  }
+  if (T.n > 0 && ok)
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (T.n - 1) & 1, lim, abort_p));
+  if (T.n > 0 && ok) {
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const bool live = r < T.nrows;
+    const int tok = live ? a.qperm[static_cast<long long>(bh) * a.N + T.r0 + r] : 0;
+    __nv_bfloat16* orow = a.out + (static_cast<long long>(bh) * a.N + tok) * 128;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v[32];
+      tmem_ld32(tO + c * 32, v);
+      tmem_wait_ld();
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(v[q4 * 8 + 0]) * inv, __uint_as_float(v[q4 * 8 + 1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(v[q4 * 8 + 2]) * inv, __uint_as_float(v[q4 * 8 + 3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(v[q4 * 8 + 4]) * inv, __uint_as_float(v[q4 * 8 + 5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(v[q4 * 8 + 6]) * inv, __uint_as_float(v[q4 * 8 + 7]) * inv);
+          dst[q4] = w;
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void ct_locate(const CompArgs& a, int bh, int chunk, CompTile& T) {
+  const int* co = a.choff + static_cast<long long>(bh) * (a.Cq + 1);
+  int lo = 0, hi = a.Cq - 1;  // last p with co[p] <= chunk (skips empty clusters)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (co[mid] <= chunk) lo = mid;
+    else hi = mid - 1;
+  }
+  const int* qo = a.qoff + static_cast<long long>(bh) * (a.Cq + 1);
+  const long long pc = static_cast<long long>(bh) * a.Cq + lo;
+  T.p = lo;
+  T.r0 = qo[lo] + (chunk - co[lo]) * 128;
+  T.nrows = min(128, qo[lo + 1] - T.r0);
+  T.ns = a.seln[pc];
+  T.nslots = a.selbox[pc * (a.Ck + 1) + T.ns];
+  T.n = a.nv + (T.nslots + 15) / 16;
+}
+
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    comp_tc_kernel(const __grid_constant__ CUtensorMap map_q,
+                   const __grid_constant__ CUtensorMap map_kc,
+                   const __grid_constant__ CUtensorMap map_vc,
+                   const __grid_constant__ CUtensorMap map_k8,
+                   const __grid_constant__ CUtensorMap map_v8, const CompArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[CB_COUNT];
+  __shared__ uint32_t masks[CT_NM * 4];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+  __shared__ CompTile tiles[2];
+
+  const int bh = blockIdx.y;
+  const int total = a.choff[static_cast<long long>(bh) * (a.Cq + 1) + a.Cq];
+  const int c0 = 2 * blockIdx.x;
+  if (c0 >= total) return;  // whole CTA, before any barrier or TMEM use
+  const bool has1 = c0 + 1 < total;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sQ0 = smem_u32(smem);
+  const uint32_t sK0 = sQ0 + 2 * TC_TILE_BYTES;
+  const uint32_t sV0 = sK0 + TC_NK * TC_TILE_BYTES;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (tid == 0) {
+    abort_flag = 0;
+    ct_locate(a, bh, c0, tiles[0]);
+    if (has1) ct_locate(a, bh, c0 + 1, tiles[1]);
+    else tiles[1] = CompTile{0, 0, 0, 0, 0, 0};
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(CB_Q_FULL + t), 1);
+      mbar_init(bar(CB_S_FULL + t), 1);
+      mbar_init(bar(CB_P_FULL + t), 128);
+      mbar_init(bar(CB_O_DONE + t), 1);
+    }
+    for (int s = 0; s < TC_NK; ++s) {
+      mbar_init(bar(CB_K_FULL + s), 1);
+      mbar_init(bar(CB_K_EMPTY + s), 1);
+    }
+    for (int s = 0; s < TC_NV; ++s) {
+      mbar_init(bar(CB_V_FULL + s), 1);
+      mbar_init(bar(CB_V_EMPTY + s), 1);
+    }
+    for (int s = 0; s < CT_NM; ++s) {
+      mbar_init(bar(CB_M_FULL + s), 1);
+      mbar_init(bar(CB_M_EMPTY + s), 128);
+    }
+    mbar_init(bar(CB_DRAIN), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_s), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+  volatile int* abort_p = &abort_flag;
+  const long long lim = a.wait_limit;
+  const CompTile T0 = tiles[0], T1 = tiles[1];
+  const int n0 = T0.n, n1 = T1.n, nent = n0 + n1;
+
+  if (warp >= 4) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(CT_REGS_INC));
+    const int tile = (warp - 4) >> 2;
+    if (tile == 0 || has1)
+      ct_softmax(a, tile, tile == 0 ? T0 : T1, n0, n1, bh, tmem, bars, masks, abort_p);
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CT_REGS_DEC));
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer --
+      // The whole warp walks the stream; lane 0 waits and arms the barriers,
+      // lanes 0..15 issue one slot's copies each.
+      int issued_k = 0, issued_v = 0;
+      if (lane == 0) {
+        tma_prefetch_desc(&map_q);
+        tma_prefetch_desc(&map_kc);
+        tma_prefetch_desc(&map_vc);
+        tma_prefetch_desc(&map_k8);
+        tma_prefetch_desc(&map_v8);
+        mbar_arrive_expect_tx(bar(CB_Q_FULL + 0), TC_TILE_BYTES);
+        tma_load_3d(sQ0, &map_q, bar(CB_Q_FULL + 0), 0, T0.r0, bh);
+        tma_load_3d(sQ0 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 0), 64, T0.r0, bh);
+        if (has1) {
+          const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
+          mbar_arrive_expect_tx(bar(CB_Q_FULL + 1), TC_TILE_BYTES);
+          tma_load_3d(sQ1, &map_q, bar(CB_Q_FULL + 1), 0, T1.r0, bh);
+          tma_load_3d(sQ1 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 1), 64, T1.r0, bh);
+        }
+      }
+      for (int u = 0; u < nent; ++u) {
+        int t, j;
+        ct_entry(u, n0, n1, t, j);
+        const CompTile& T = t == 0 ? T0 : T1;
+        const int sk = u % TC_NK, sv = u % TC_NV, ms = u % CT_NM;
+        const uint32_t sK = sK0 + sk * TC_TILE_BYTES, sV = sV0 + sv * TC_TILE_BYTES;
+        // slot of this lane (exact tiles): source row and valid row count
+        int src = 0, valid = 0;
+        if (j >= a.nv && lane < 16) {
+          const int slot = (j - a.nv) * 16 + lane;
+          if (slot < T.nslots) {
+            const long long pc = static_cast<long long>(bh) * a.Cq + T.p;
+            const int* sb = a.selbox + pc * (a.Ck + 1);
+            int lo = 0, hi = T.ns - 1;  // last selected s with sb[s] <= slot
+            while (lo < hi) {
+              const int mid = (lo + hi + 1) >> 1;
+              if (sb[mid] <= slot) lo = mid;
+              else hi = mid - 1;
+            }
+            const int c = a.selc[pc * a.Ck + lo];
+            const int b = slot - sb[lo];
+            const int* ko = a.koff + static_cast<long long>(bh) * (a.Ck + 1);
+            src = ko[c] + 8 * b;
+            valid = min(8, ko[c + 1] - src);
+          }
+        }
+        bool ok = true;
+        if (lane == 0) {
+          if (u >= TC_NK)
+            ok = mbar_wait_bounded(bar(CB_K_EMPTY + sk), ((u / TC_NK) & 1) ^ 1, lim, abort_p);
+          if (ok) mbar_arrive_expect_tx(bar(CB_K_FULL + sk), TC_TILE_BYTES);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (j < a.nv) {
+          if (lane == 0) {
+            tma_load_3d(sK, &map_kc, bar(CB_K_FULL + sk), 0, j * 128, bh);
+            tma_load_3d(sK + TC_HALF_BYTES, &map_kc, bar(CB_K_FULL + sk), 64, j * 128, bh);
+          }
+        } else if (lane < 16) {
+          tma_load_3d(sK + lane * 1024, &map_k8, bar(CB_K_FULL + sk), 0, src, bh);
+          tma_load_3d(sK + TC_HALF_BYTES + lane * 1024, &map_k8, bar(CB_K_FULL + sk), 64, src, bh);
+        }
+        if (lane == 0) issued_k = u + 1;
+        if (lane == 0) {
+          if (u >= TC_NV)
+            ok = mbar_wait_bounded(bar(CB_V_EMPTY + sv), ((u / TC_NV) & 1) ^ 1, lim, abort_p);
+          if (ok) mbar_arrive_expect_tx(bar(CB_V_FULL + sv), TC_TILE_BYTES);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        if (j < a.nv) {
+          if (lane == 0) {
+            tma_load_3d(sV, &map_vc, bar(CB_V_FULL + sv), 0, j * 128, bh);
+            tma_load_3d(sV + TC_HALF_BYTES, &map_vc, bar(CB_V_FULL + sv), 64, j * 128, bh);
+          }
+        } else if (lane < 16) {
+          tma_load_3d(sV + lane * 1024, &map_v8, bar(CB_V_FULL + sv), 0, src, bh);
+          tma_load_3d(sV + TC_HALF_BYTES + lane * 1024, &map_v8, bar(CB_V_FULL + sv), 64, src, bh);
+        }
+        if (lane == 0) issued_v = u + 1;
+        // validity mask of the entry's 128 key columns
+        const uint32_t byte = j < a.nv ? 0xFFu : ((1u << valid) - 1u) & 0xFFu;
+        uint32_t mwords[4];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t acc = 0;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            acc |= __shfl_sync(0xffffffffu, byte, 4 * w + q) << (8 * q);
+          mwords[w] = acc;
+        }
+        if (lane == 0) {
+          if (u >= CT_NM)
+            ok = mbar_wait_bounded(bar(CB_M_EMPTY + ms), ((u / CT_NM) & 1) ^ 1, lim, abort_p);
+          if (ok) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) masks[ms * 4 + w] = mwords[w];
+            mbar_arrive(bar(CB_M_FULL + ms));
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      if (lane == 0 && *abort_p) {
+        volatile int no_abort = 0;
+        mbar_wait_bounded(bar(CB_Q_FULL + 0), 0, lim, &no_abort);
+        if (has1) {
+          no_abort = 0;
+          mbar_wait_bounded(bar(CB_Q_FULL + 1), 0, lim, &no_abort);
+        }
+        for (int u = issued_k > TC_NK ? issued_k - TC_NK : 0; u < issued_k; ++u) {
+          no_abort = 0;
+          mbar_wait_bounded(bar(CB_K_FULL + u % TC_NK), (u / TC_NK) & 1, lim, &no_abort);
+        }
+        for (int u = issued_v > TC_NV ? issued_v - TC_NV : 0; u < issued_v; ++u) {
+          no_abort = 0;
+          mbar_wait_bounded(bar(CB_V_FULL + u % TC_NV), (u / TC_NV) & 1, lim, &no_abort);
+        }
+      }
+    } else if (warp == 1) {
+      // --------------------------------------------------------------- MMA --
+      if (lane == 0) {
+        const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
+        bool ok = mbar_wait_bounded(bar(CB_Q_FULL + 0), 0, lim, abort_p);
+        if (ok && has1) ok = mbar_wait_bounded(bar(CB_Q_FULL + 1), 0, lim, abort_p);
+        int pend[2] = {-1, -1};
+        int cnt[2] = {0, 0};
+        auto issue_pv = [&](int t) -> bool {
+          const int pu = pend[t];
+          const int jj = cnt[t] - 1;
+          if (!mbar_wait_bounded(bar(CB_P_FULL + t), jj & 1, lim, abort_p)) return false;
+          const int sv = pu % TC_NV;
+          if (!mbar_wait_bounded(bar(CB_V_FULL + sv), (pu / TC_NV) & 1, lim, abort_p)) return false;
+          tc_fence_after();
+          tc_issue_pv(tmem + t * 256 + 128, tmem + t * 256, sV0 + sv * TC_TILE_BYTES, jj > 0);
+          umma_commit(bar(CB_O_DONE + t));
+          umma_commit(bar(CB_V_EMPTY + sv));  // every entry is read by one tile only
+          pend[t] = -1;
+          return true;
+        };
+        for (int u = 0; ok && u < nent; ++u) {
+          int t, j;
+          ct_entry(u, n0, n1, t, j);
+          // A V stage is reloaded NV entries later: release stale pending PVs.
+          if (pend[0] >= 0 && pend[0] <= u - TC_NV && !(ok = issue_pv(0))) break;
+          if (pend[1] >= 0 && pend[1] <= u - TC_NV && !(ok = issue_pv(1))) break;
+          const int sk = u % TC_NK;
+          if (!(ok = mbar_wait_bounded(bar(CB_K_FULL + sk), (u / TC_NK) & 1, lim, abort_p))) break;
+          if (pend[t] >= 0 && !(ok = issue_pv(t))) break;
+          tc_fence_after();
+          tc_issue_qk(tmem + t * 256, t == 0 ? sQ0 : sQ1, sK0 + sk * TC_TILE_BYTES);
+          umma_commit(bar(CB_S_FULL + t));
+          umma_commit(bar(CB_K_EMPTY + sk));
+          pend[t] = u;
+          ++cnt[t];
+        }
+        if (ok && pend[0] >= 0) ok = issue_pv(0);
+        if (ok && pend[1] >= 0) ok = issue_pv(1);
+        if (!ok) {
+          umma_commit(bar(CB_DRAIN));
+          volatile int no_abort = 0;
+          mbar_wait_bounded(bar(CB_DRAIN), 0, lim, &no_abort);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------ preparation --
+
+// dst[bh][t] = src[bh][perm[bh][t]] for bf16 rows of 128 (one half-warp per row).
+__global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ src,
+                                   const int* __restrict__ perm, int N,
+                                   __nv_bfloat16* __restrict__ dst) {
+  const int bh = blockIdx.y;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 4);
+  const int c = threadIdx.x & 15;
+  if (t >= N) return;
+  const long long base = static_cast<long long>(bh) * N;
+  const int row = perm[base + t];
+  const uint4* s = reinterpret_cast<const uint4*>(src + (base + row) * 128);
+  uint4* d = reinterpret_cast<uint4*>(dst + (base + t) * 128);
+  d[c] = s[c];
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ x, long long n,
+                                   __nv_bfloat16* __restrict__ y) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) y[i] = __float2bfloat16_rn(x[i]);
+}
+
+// ceil(n_p / rows) chunks per query cluster.
+__global__ void chunk_count_kernel(const int* __restrict__ nq, int Cq, int rows,
+                                   int* __restrict__ nch) {
+  const int bh = blockIdx.y;
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= Cq) return;
+  const int n = nq[static_cast<long long>(bh) * Cq + p];
+  nch[static_cast<long long>(bh) * Cq + p] = (n + rows - 1) / rows;
+}
+
+// One warp per (bh, p): the slot prefix over the selected list and the
+// virtual-key bias row (log2 n_c for non-empty unselected c, else -inf).
+__global__ void comp_prep_kernel(const int* __restrict__ nk, const int* __restrict__ seln,
+                                 const int* __restrict__ selc, const uint8_t* __restrict__ sel,
+                                 int Cq, int Ck, int nv, int* __restrict__ selbox,
+                                 float* __restrict__ vbias) {
+  const int bh = blockIdx.y;
+  const int p = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (p >= Cq) return;
+  const long long pc = static_cast<long long>(bh) * Cq + p;
+  const int* nkb = nk + static_cast<long long>(bh) * Ck;
+  const int ns = seln[pc];
+  const int* sl = selc + pc * Ck;
+  int* sb = selbox + pc * (Ck + 1);
+  int base = 0;
+  for (int s0 = 0; s0 < ns; s0 += 32) {
+    const int s = s0 + lane;
+    const int boxes = s < ns ? (nkb[sl[s]] + 7) / 8 : 0;
+    int incl = boxes;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (s < ns) sb[s] = base + incl - boxes;
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) sb[ns] = base;
+  const uint8_t* sr = sel + pc * Ck;
+  float* vb = vbias + pc * (nv * 128);
+  for (int c = lane; c < nv * 128; c += 32) {
+    const int n = c < Ck ? nkb[c] : 0;
+    vb[c] = (n > 0 && !sr[c]) ? log2f(static_cast<float>(n)) : -INFINITY;
+  }
+}
+
+}  // namespace va

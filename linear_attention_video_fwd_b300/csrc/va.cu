@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "va.h"
 #include "common.cuh"
@@ -16,6 +17,7 @@
 #include "attn_tc.cuh"
 #include "svgear.cuh"
 #include "kmeans_tc.cuh"
+#include "comp_tc.cuh"
 
 #define VA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -82,6 +84,23 @@ EncodeTiledFn encode_fn() {
     cudaGetLastError();
   }
   return fn;
+}
+
+// 3-D map over a [BH, N, D] bf16 tensor: box of 64 dims x box_rows rows x 1
+// head, 128-byte swizzle; rows beyond N read as zeros.
+int encode_bf16_rows_box(CUtensorMap* map, const void* base, int BH, int N, int D, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return VA_ERR_CUDA;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(D) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? VA_OK : VA_ERR_CUDA;
 }
 
 // 3-D map over a [BH, N, D] bf16 tensor: box of 64 dims x 128 rows x 1 head,
@@ -549,6 +568,83 @@ VA_EXPORT int va_cluster(const void* x, const int32_t* init_idx, int B, int head
 
 namespace {
 
+// Compensated attention on the tensor cores (bf16, d = 128): cluster-ordered
+// copies of Q, K, V, bf16 centroids, per-cluster slot prefixes and virtual
+// biases, then comp_tc_kernel over pairs of 128-row query chunks.
+int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                      int Cq, int Ck, int BH, int N, const int* nq, const int* qoff,
+                      const int* qperm, const int* nk, const int* koff, const int* kperm,
+                      const float* kc, const float* vc, const int* seln, const int* selc,
+                      const uint8_t* sel, float scale, __nv_bfloat16* out, Scoped& scratch,
+                      cudaStream_t s) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int st;
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaFuncAttributes fa;
+    if ((st = cuda_status(cudaFuncGetAttributes(&fa, va::comp_tc_kernel)))) return st;
+    if (fa.numRegs != va::TC_LAUNCH_REGS) return VA_ERR_UNSUPPORTED;
+    if ((st = cuda_status(cudaFuncSetAttribute(va::comp_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               va::TC_SMEM_BYTES))))
+      return st;
+    configured[dev] = true;
+  }
+  const size_t bh = static_cast<size_t>(BH);
+  const int nv = (Ck + 127) / 128;
+  __nv_bfloat16 *qs, *ks, *vs, *kcb, *vcb;
+  int *selbox, *nch, *choff, *chfill;
+  float* vbias;
+  if ((st = scratch.alloc(&qs, bh * N * 128)) || (st = scratch.alloc(&ks, bh * N * 128)) ||
+      (st = scratch.alloc(&vs, bh * N * 128)) || (st = scratch.alloc(&kcb, bh * Ck * 128)) ||
+      (st = scratch.alloc(&vcb, bh * Ck * 128)) ||
+      (st = scratch.alloc(&selbox, bh * Cq * (Ck + 1))) ||
+      (st = scratch.alloc(&vbias, bh * Cq * nv * 128)) || (st = scratch.alloc(&nch, bh * Cq)) ||
+      (st = scratch.alloc(&choff, bh * (Cq + 1))) || (st = scratch.alloc(&chfill, bh * Cq)))
+    return st;
+  const dim3 gg((N + 7) / 8, BH);
+  va::gather_rows_kernel<<<gg, 128, 0, s>>>(q, qperm, N, qs);
+  va::gather_rows_kernel<<<gg, 128, 0, s>>>(k, kperm, N, ks);
+  va::gather_rows_kernel<<<gg, 128, 0, s>>>(v, kperm, N, vs);
+  const long long ncen = static_cast<long long>(bh) * Ck * 128;
+  va::f32_to_bf16_kernel<<<static_cast<unsigned>((ncen + 255) / 256), 256, 0, s>>>(kc, ncen, kcb);
+  va::f32_to_bf16_kernel<<<static_cast<unsigned>((ncen + 255) / 256), 256, 0, s>>>(vc, ncen, vcb);
+  va::comp_prep_kernel<<<dim3((Cq + 7) / 8, BH), 256, 0, s>>>(nk, seln, selc, sel, Cq, Ck, nv,
+                                                             selbox, vbias);
+  va::chunk_count_kernel<<<dim3((Cq + 255) / 256, BH), 256, 0, s>>>(nq, Cq, 128, nch);
+  va::km_offsets_kernel<<<BH, 1024, 0, s>>>(nch, Cq, choff, chfill);
+  if ((st = launch_status())) return st;
+  CUtensorMap mq, mkc, mvc, mk8, mv8;
+  if ((st = encode_bf16_rows_box(&mq, qs, BH, N, 128, 128)) ||
+      (st = encode_bf16_rows_box(&mkc, kcb, BH, Ck, 128, 128)) ||
+      (st = encode_bf16_rows_box(&mvc, vcb, BH, Ck, 128, 128)) ||
+      (st = encode_bf16_rows_box(&mk8, ks, BH, N, 128, 8)) ||
+      (st = encode_bf16_rows_box(&mv8, vs, BH, N, 128, 8)))
+    return st;
+  va::CompArgs a;
+  a.choff = choff;
+  a.qoff = qoff;
+  a.qperm = qperm;
+  a.koff = koff;
+  a.nk = nk;
+  a.seln = seln;
+  a.selc = selc;
+  a.selbox = selbox;
+  a.vbias = vbias;
+  a.out = out;
+  a.N = N;
+  a.Cq = Cq;
+  a.Ck = Ck;
+  a.nv = nv;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit = g_wait_limit;
+  const int max_chunks = (N + 127) / 128 + Cq;
+  va::comp_tc_kernel<<<dim3((max_chunks + 1) / 2, BH), va::TC_THREADS, va::TC_SMEM_BYTES, s>>>(
+      mq, mkc, mvc, mk8, mv8, a);
+  return launch_status();
+}
+
 template <typename T, int D>
 int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int Cq,
                    const int* kassign, int Ck, long long budget, float scale, int BH, int N,
@@ -597,10 +693,16 @@ int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int C
   if ((st = launch_status())) return st;
 
   // routing
+  uint8_t* sel = sel_out;
+  if (sel == nullptr && (st = scratch.alloc(&sel, bh * Cq * Ck))) return st;
   va::route_select_kernel<<<BH, 1024, 0, s>>>(err, nq, nk, Cq, Ck, budget, cut);
-  va::route_mark_kernel<<<dim3(Cq, BH), 256, 0, s>>>(err, nq, nk, Cq, Ck, cut, sel_out, seln,
-                                                     selc);
+  va::route_mark_kernel<<<dim3(Cq, BH), 256, 0, s>>>(err, nq, nk, Cq, Ck, cut, sel, seln, selc);
   if ((st = launch_status())) return st;
+
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) {
+    return comp_tensor_cores(q, k, v, Cq, Ck, BH, N, nq, qoff, qperm, nk, koff, kperm, kc, vc,
+                             seln, selc, sel, scale, out, scratch, s);
+  }
 
   // compensated attention: chunks of up to 64 queries of one query cluster
   va::comp_chunks_kernel<<<dim3((Cq + 255) / 256, BH), 256, 0, s>>>(nq, Cq, nch);
