@@ -233,6 +233,18 @@ int va_device_error(va_stream_t stream);
  * about 2 s at 2 GHz). Values < 1000 are rejected with VA_ERR_INVALID. */
 int va_set_wait_limit(int64_t cycles);
 
+/*
+ * Self-test of the bounded device waits used by every kernel (an interface
+ * for failure-detection tests; the paper has no counterpart). Launches one
+ * small CTA on `stream` that waits on a shared-memory mbarrier no thread
+ * ever arrives at, with the wait bounded by `cycles` clock64 cycles (1e3 to
+ * 1e10). The wait gives up, records VA_ERR_TIMEOUT in the device error word
+ * and the kernel returns normally, so the CUDA context stays usable;
+ * va_device_error() then reports VA_ERR_TIMEOUT once.
+ * Errors: VA_ERR_INVALID (cycles out of range), VA_ERR_CUDA (launch).
+ */
+int va_selftest_wait_timeout(int64_t cycles, va_stream_t stream);
+
 /* Static text for a status code. */
 const char* va_status_string(int status);
 

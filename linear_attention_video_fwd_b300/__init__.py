@@ -56,6 +56,7 @@ def _load():
                                 vp, vp, vp, vp],
         "va_device_error": [vp],
         "va_set_wait_limit": [i64],
+        "va_selftest_wait_timeout": [i64, vp],
         "va_status_string": [i32],
         "va_version": [],
     }
@@ -220,6 +221,11 @@ def compensate_route(q, k, v, qassign, Cq: int, kassign, Ck: int, density: float
 def device_error(stream=None) -> int:
     """va_device_error: sync the stream and return/clear the device error word."""
     return _lib.va_device_error(_stream(stream))
+
+
+def selftest_wait_timeout(cycles: int = 2_000_000, stream=None):
+    """va_selftest_wait_timeout: a bounded device wait that must give up."""
+    _check(_lib.va_selftest_wait_timeout(int(cycles), _stream(stream)), "va_selftest_wait_timeout")
 
 
 def set_wait_limit(cycles: int):

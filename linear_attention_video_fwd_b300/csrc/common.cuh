@@ -73,6 +73,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// One thread waits, bounded by `limit`, on an mbarrier that nothing arrives
+// at: the wait must give up and record VA_ERR_TIMEOUT (failure-path test).
+__global__ void wait_selftest_kernel(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    mbar_wait_bounded(smem_u32(&bar), 0, limit, &abort_flag);
+  }
+}
+
 // --------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

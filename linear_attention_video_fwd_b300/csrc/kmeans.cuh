@@ -5,9 +5,9 @@
 // raw head vectors with squared Euclidean distance is the reading used).
 //
 // One iteration: assign (nearest centroid, ties to the lowest index) ->
-// counts -> offsets -> member lists -> means. The means are summed in float64
-// over the members of each cluster; for bf16 inputs those sums are exact, so
-// the centroids do not depend on the (atomic, unordered) member order.
+// counts -> offsets -> member lists -> means. The member sums are exact
+// (64-bit fixed point for bf16 inputs, float64 for float32), so the centroids
+// do not depend on the (atomic, unordered) member order.
 #pragma once
 
 #include "common.cuh"
@@ -233,16 +233,31 @@ __global__ void km_count_kernel(const int* __restrict__ assign, int N, int C,
   atomicAdd(&count[static_cast<long long>(bh) * C + a], 1);
 }
 
-// One warp per cluster: mean of its members (float64 sums), written as fp32
-// to mean[bh][c]; |mean|^2 (fp32) to norm[bh][c] if norm != nullptr. An empty
-// cluster keeps mean[bh][c] when keep_empty, else gets zeros.
-// Grid: (ceil(C / 8), BH), 256 threads.
+// bf16 value as a signed fixed-point integer with 32 fraction bits: exact
+// for |x| >= 2^-25, truncated toward zero (error < 2^-32) below.
+__device__ __forceinline__ long long bf16_fixed32(uint32_t bits16) {
+  const uint32_t e = (bits16 >> 7) & 0xFFu;
+  if (e == 0) return 0;                        // zero and subnormals (|x| < 2^-126)
+  const long long mant = static_cast<long long>((bits16 & 0x7Fu) | 0x80u);
+  const int sh = static_cast<int>(e) - 102;    // value = mant * 2^(e - 134) * 2^32
+  const long long mag = sh >= 0 ? (mant << min(sh, 62)) : (sh > -63 ? (mant >> -sh) : 0);
+  return (bits16 & 0x8000u) ? -mag : mag;
+}
+
+// One warp per cluster: mean of its members, written as fp32 to mean[bh][c];
+// |mean|^2 (fp32) to norm[bh][c] if norm != nullptr. An empty cluster keeps
+// mean[bh][c] when keep_empty, else gets zeros. Sums are exact and
+// order-independent: 64-bit fixed point for bf16 (members with |x| < 2^-25
+// contribute with an error below 2^-32; |sum| must stay below 2^31), float64
+// for float32. Member indices are fetched 32 at a time so the row loads of a
+// cluster are independent. Grid: (ceil(C / 8), BH), 256 threads.
 template <typename T, int D>
 __global__ void km_means_kernel(const T* __restrict__ x, int N, int C,
                                 const int* __restrict__ off, const int* __restrict__ perm,
                                 float* __restrict__ mean, float* __restrict__ norm,
                                 int keep_empty) {
   constexpr int PER = D / 32;
+  constexpr bool kFixed = sizeof(T) == 2;
   const int bh = blockIdx.y;
   const int c = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -252,20 +267,37 @@ __global__ void km_means_kernel(const T* __restrict__ x, int N, int C,
   const int* pm = perm + static_cast<long long>(bh) * N;
   const T* xb = x + static_cast<long long>(bh) * N * D;
   float* m = mean + (static_cast<long long>(bh) * C + c) * D;
-  double acc[PER];
+  long long iacc[PER];
+  double dacc[PER];
 #pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.0;
-  for (int t = beg; t < end; ++t) {
-    const T* row = xb + static_cast<long long>(pm[t]) * D + lane * PER;
+  for (int e = 0; e < PER; ++e) {
+    iacc[e] = 0;
+    dacc[e] = 0.0;
+  }
+  for (int t0 = beg; t0 < end; t0 += 32) {
+    const int my = (t0 + lane < end) ? pm[t0 + lane] : 0;
+    const int cnt = min(32, end - t0);
+#pragma unroll 4
+    for (int q = 0; q < cnt; ++q) {
+      const int idx = __shfl_sync(0xffffffffu, my, q);
+      const T* row = xb + static_cast<long long>(idx) * D + lane * PER;
+      if constexpr (kFixed) {
+        const uint16_t* r16 = reinterpret_cast<const uint16_t*>(row);
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += static_cast<double>(to_f32(row[e]));
+        for (int e = 0; e < PER; ++e) iacc[e] += bf16_fixed32(r16[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < PER; ++e) dacc[e] += static_cast<double>(to_f32(row[e]));
+      }
+    }
   }
   float nrm = 0.f;
   if (end > beg) {
-    const double inv_n = static_cast<double>(end - beg);
+    const double n = static_cast<double>(end - beg);
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
-      const float mv = static_cast<float>(acc[e] / inv_n);
+      const double sum = kFixed ? static_cast<double>(iacc[e]) * 0x1p-32 : dacc[e];
+      const float mv = static_cast<float>(sum / n);
       m[lane * PER + e] = mv;
       nrm = fmaf(mv, mv, nrm);
     }

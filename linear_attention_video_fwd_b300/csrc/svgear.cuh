@@ -28,119 +28,245 @@
 namespace va {
 
 // ------------------------------------------------------------------ probe --
+//
+// Pass 1 splits the keys of every proxy over PR_SPLIT CTAs (partial max, sum
+// and unnormalised value sum, merged by probe_combine_kernel); pass 2 splits
+// the key clusters over PR_CSPLIT CTAs (a cluster's residual only needs the
+// merged m_p, Z_p, O_p and its own keys). A CTA holds PR_PG = 32 proxies; warp
+// w owns proxies 4w..4w+3: each lane computes their logits for keys 2 lane,
+// 2 lane + 1 of a 64-key tile, and their value sums for the DV = d / 32 dims
+// DV lane.. (register tiles of 4 x 2 and 4 x DV, shared-memory operands read
+// as vectors).
 
-constexpr int PR_PG = 16;  // query clusters per CTA
+constexpr int PR_PG = 32;  // query clusters (proxies) per CTA
 constexpr int PR_KT = 64;  // keys per tile
 constexpr int PR_THREADS = 256;
+constexpr int PR_SPLIT = 8;    // key splits of pass 1
+constexpr int PR_CSPLIT = 8;   // key-cluster splits of pass 2
 
 template <int D>
 constexpr int probe_smem_bytes(int Ck) {
-  return (D * PR_PG + D * PR_KT + PR_KT * D + PR_PG * PR_KT) * 4 + 2 * PR_KT * 4 + (Ck + 1) * 4;
+  return (D * PR_PG + D * PR_KT + PR_KT * D + PR_KT * PR_PG) * 4 + 2 * PR_KT * 4 + (Ck + 1) * 4;
 }
 
-// err[bh][p][c] for every non-empty p and c (other entries are left as the
-// caller initialised them). Grid: (ceil(Cq / PR_PG), BH), 256 threads;
-// thread (ty, tx): query cluster p0 + ty, keys tx*4..tx*4+3 of a tile and
-// dims tx*(D/16).. of the value accumulators.
+// acc[a][b] = qc_{4w+a} . k_{2 lane + b}
+template <int D>
+__device__ __forceinline__ void probe_logits(const float* qcT, const float* kT, int w, int lane,
+                                             float (&acc)[4][2]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a) acc[a][0] = acc[a][1] = 0.f;
+#pragma unroll 8
+  for (int dd = 0; dd < D; ++dd) {
+    const float4 qv = *reinterpret_cast<const float4*>(&qcT[dd * PR_PG + 4 * w]);
+    const float2 kv = *reinterpret_cast<const float2*>(&kT[dd * PR_KT + 2 * lane]);
+    const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      acc[a][0] = fmaf(qa[a], kv.x, acc[a][0]);
+      acc[a][1] = fmaf(qa[a], kv.y, acc[a][1]);
+    }
+  }
+}
+
+// out[e] = src[e], e < DV, as one vector load (src aligned to DV floats).
+template <int DV>
+__device__ __forceinline__ void load_vec(const float* src, float (&out)[DV]) {
+  if constexpr (DV == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(src);
+    out[0] = t.x;
+    out[1] = t.y;
+    out[2] = t.z;
+    out[3] = t.w;
+  } else if constexpr (DV == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(src);
+    out[0] = t.x;
+    out[1] = t.y;
+  } else {
+#pragma unroll
+    for (int e = 0; e < DV; ++e) out[e] = src[e];
+  }
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// part[bh][p][split] = {m, Z, O[0..D)} over keys of this split (O unnormalised).
+// Grid (ceil(Cq / PR_PG), PR_SPLIT, BH).
 template <typename T, int D>
 __global__ void __launch_bounds__(PR_THREADS)
-    probe_kernel(const T* __restrict__ k, const T* __restrict__ v, int N, int Cq, int Ck,
-                 const float* __restrict__ qc, const int* __restrict__ nq,
-                 const float* __restrict__ kc, const float* __restrict__ vc,
-                 const int* __restrict__ nk, const int* __restrict__ koff,
-                 const int* __restrict__ kperm, const int* __restrict__ kassign, float scale,
-                 float* __restrict__ err) {
-  constexpr int DV = D / 16;  // value dims per thread
+    probe_pass1_kernel(const T* __restrict__ k, const T* __restrict__ v, int N, int Cq,
+                       const float* __restrict__ qc, float scale, float* __restrict__ part) {
+  static_assert(D == 64 || D == 128, "the probe tiles assume d = 64 or 128");
+  constexpr int DV = D / 32;
   extern __shared__ float pr_smem[];
   float* qcT = pr_smem;                       // [D][PR_PG]
   float* kT = qcT + D * PR_PG;                // [D][PR_KT]
   float* vs = kT + D * PR_KT;                 // [PR_KT][D]
-  float* es = vs + PR_KT * D;                 // [PR_PG][PR_KT]
-  int* cid = reinterpret_cast<int*>(es + PR_PG * PR_KT);  // [PR_KT]
-  int* kidx = cid + PR_KT;                    // [PR_KT]
-  int* offs = kidx + PR_KT;                   // [Ck + 1]
-
-  const int bh = blockIdx.y;
+  float* es = vs + PR_KT * D;                 // [PR_KT][PR_PG]
+  const int bh = blockIdx.z, split = blockIdx.y;
   const int p0 = blockIdx.x * PR_PG;
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int p = p0 + ty;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const long long kvb = static_cast<long long>(bh) * N * D;
+  const int per = ((N + PR_SPLIT - 1) / PR_SPLIT + PR_KT - 1) / PR_KT * PR_KT;
+  const int jb = split * per, je = min(N, jb + per);
+  stage_transposed<float, D, PR_PG, PR_THREADS>(qcT, [&](int pp) -> const float* {
+    return p0 + pp < Cq ? qc + (static_cast<long long>(bh) * Cq + p0 + pp) * D : nullptr;
+  });
+  float m[4], Z[4], O[4][DV];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    m[a] = -INFINITY;
+    Z[a] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DV; ++e) O[a][e] = 0.f;
+  }
+  for (int j0 = jb; j0 < je; j0 += PR_KT) {
+    __syncthreads();
+    stage_transposed<T, D, PR_KT, PR_THREADS>(kT, [&](int kk) -> const T* {
+      return j0 + kk < je ? k + kvb + static_cast<long long>(j0 + kk) * D : nullptr;
+    });
+    stage_rows<T, D, PR_KT, PR_THREADS>(vs, [&](int kk) -> const T* {
+      return j0 + kk < je ? v + kvb + static_cast<long long>(j0 + kk) * D : nullptr;
+    });
+    __syncthreads();
+    float acc[4][2];
+    probe_logits<D>(qcT, kT, w, lane, acc);
+    const bool v0 = j0 + 2 * lane < je, v1 = j0 + 2 * lane + 1 < je;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const float l0 = v0 ? acc[a][0] * scale : -INFINITY;
+      const float l1 = v1 ? acc[a][1] * scale : -INFINITY;
+      const float mn = fmaxf(m[a], warp_max(fmaxf(l0, l1)));
+      const float alpha = expf(m[a] - mn);  // m = -inf on the first tile: alpha = 0
+      m[a] = mn;
+      const float e0 = expf(l0 - mn), e1 = expf(l1 - mn);
+      es[(2 * lane) * PR_PG + 4 * w + a] = e0;
+      es[(2 * lane + 1) * PR_PG + 4 * w + a] = e1;
+      Z[a] = Z[a] * alpha + warp_sum(e0 + e1);
+#pragma unroll
+      for (int e = 0; e < DV; ++e) O[a][e] *= alpha;
+    }
+    __syncwarp();
+#pragma unroll 4
+    for (int kk = 0; kk < PR_KT; ++kk) {
+      const float4 ev = *reinterpret_cast<const float4*>(&es[kk * PR_PG + 4 * w]);
+      const float ea[4] = {ev.x, ev.y, ev.z, ev.w};
+      float va4[DV];
+      load_vec<DV>(&vs[kk * D + DV * lane], va4);
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int e = 0; e < DV; ++e) O[a][e] = fmaf(ea[a], va4[e], O[a][e]);
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int p = p0 + 4 * w + a;
+    if (p < Cq) {
+      float* out = part + ((static_cast<long long>(bh) * Cq + p) * PR_SPLIT + split) * (D + 2);
+      if (lane == 0) {
+        out[0] = m[a];
+        out[1] = Z[a];
+      }
+      float* o4 = out + 2 + DV * lane;
+#pragma unroll
+      for (int e = 0; e < DV; ++e) o4[e] = O[a][e];
+    }
+  }
+}
+
+// mzo[bh][p] = {m_p, Z_p, O_p[0..D)} (O_p normalised) from the split partials.
+// Grid (Cq, BH), D threads.
+template <int D>
+__global__ void probe_combine_kernel(const float* __restrict__ part, int Cq,
+                                     float* __restrict__ mzo) {
+  const int bh = blockIdx.y, p = blockIdx.x, d = threadIdx.x;
+  const float* pp = part + (static_cast<long long>(bh) * Cq + p) * PR_SPLIT * (D + 2);
+  float m = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < PR_SPLIT; ++s) m = fmaxf(m, pp[s * (D + 2)]);
+  float Z = 0.f, O = 0.f;
+#pragma unroll
+  for (int s = 0; s < PR_SPLIT; ++s) {
+    const float ms = pp[s * (D + 2)];
+    if (ms == -INFINITY) continue;
+    const float wgt = expf(ms - m);
+    Z = fmaf(pp[s * (D + 2) + 1], wgt, Z);
+    O = fmaf(pp[s * (D + 2) + 2 + d], wgt, O);
+  }
+  float* out = mzo + (static_cast<long long>(bh) * Cq + p) * (D + 2);
+  if (d == 0) {
+    out[0] = m;
+    out[1] = Z;
+  }
+  out[2 + d] = O / Z;
+}
+
+// err[bh][p][c] for non-empty p and the clusters c of this CTA's cluster range
+// (keys in cluster order). Grid (ceil(Cq / PR_PG), PR_CSPLIT, BH).
+template <typename T, int D>
+__global__ void __launch_bounds__(PR_THREADS)
+    probe_pass2_kernel(const T* __restrict__ k, const T* __restrict__ v, int N, int Cq, int Ck,
+                       const float* __restrict__ qc, const int* __restrict__ nq,
+                       const float* __restrict__ kc, const float* __restrict__ vc,
+                       const int* __restrict__ nk, const int* __restrict__ koff,
+                       const int* __restrict__ kperm, const int* __restrict__ kassign,
+                       const float* __restrict__ mzo, float scale, float* __restrict__ err) {
+  static_assert(D == 64 || D == 128, "the probe tiles assume d = 64 or 128");
+  constexpr int DV = D / 32;
+  extern __shared__ float pr_smem[];
+  float* qcT = pr_smem;                       // [D][PR_PG]
+  float* kT = qcT + D * PR_PG;                // [D][PR_KT]
+  float* vs = kT + D * PR_KT;                 // [PR_KT][D]
+  float* es = vs + PR_KT * D;                 // [PR_KT][PR_PG]
+  int* cid = reinterpret_cast<int*>(es + PR_KT * PR_PG);  // [PR_KT]
+  int* kidx = cid + PR_KT;                    // [PR_KT]
+  int* offs = kidx + PR_KT;                   // [Ck + 1] (this range's part)
+
+  const int bh = blockIdx.z, split = blockIdx.y;
+  const int p0 = blockIdx.x * PR_PG;
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const long long kvb = static_cast<long long>(bh) * N * D;
   const int* ko = koff + static_cast<long long>(bh) * (Ck + 1);
   const int* kp = kperm + static_cast<long long>(bh) * N;
   const int* ka = kassign + static_cast<long long>(bh) * N;
+  const int cper = (Ck + PR_CSPLIT - 1) / PR_CSPLIT;
+  const int c_lo = min(Ck, split * cper), c_hi = min(Ck, c_lo + cper);
+  const int tb = ko[c_lo], te = ko[c_hi];
 
   stage_transposed<float, D, PR_PG, PR_THREADS>(qcT, [&](int pp) -> const float* {
     return p0 + pp < Cq ? qc + (static_cast<long long>(bh) * Cq + p0 + pp) * D : nullptr;
   });
-  for (int e = tid; e <= Ck; e += PR_THREADS) offs[e] = ko[e];
-
-  // ---- pass 1: m_p, Z_p, O_p over all keys (token order) -------------------
-  float m = -INFINITY, Z = 0.f;
-  float O[DV];
+  for (int e = tid; e <= c_hi - c_lo; e += PR_THREADS) offs[e] = ko[c_lo + e];
+  float m[4], invZ[4], O[4][DV], r[4][DV];
+  bool write[4];
 #pragma unroll
-  for (int e = 0; e < DV; ++e) O[e] = 0.f;
-  for (int j0 = 0; j0 < N; j0 += PR_KT) {
-    __syncthreads();
-    stage_transposed<T, D, PR_KT, PR_THREADS>(kT, [&](int kk) -> const T* {
-      return j0 + kk < N ? k + kvb + static_cast<long long>(j0 + kk) * D : nullptr;
-    });
-    stage_rows<T, D, PR_KT, PR_THREADS>(vs, [&](int kk) -> const T* {
-      return j0 + kk < N ? v + kvb + static_cast<long long>(j0 + kk) * D : nullptr;
-    });
-    __syncthreads();
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int dd = 0; dd < D; ++dd) {
-      const float qv = qcT[dd * PR_PG + ty];
-      const float4 kv = *reinterpret_cast<const float4*>(&kT[dd * PR_KT + tx * 4]);
-      acc[0] = fmaf(qv, kv.x, acc[0]);
-      acc[1] = fmaf(qv, kv.y, acc[1]);
-      acc[2] = fmaf(qv, kv.z, acc[2]);
-      acc[3] = fmaf(qv, kv.w, acc[3]);
+  for (int a = 0; a < 4; ++a) {
+    const int p = p0 + 4 * w + a;
+    const int pr = min(p, Cq - 1);
+    const float* mz = mzo + (static_cast<long long>(bh) * Cq + pr) * (D + 2);
+    m[a] = mz[0];
+    invZ[a] = 1.f / mz[1];
+#pragma unroll
+    for (int e = 0; e < DV; ++e) {
+      O[a][e] = mz[2 + DV * lane + e];
+      r[a][e] = 0.f;
     }
-    float tmax = -INFINITY;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      acc[b] = (j0 + tx * 4 + b < N) ? acc[b] * scale : -INFINITY;
-      tmax = fmaxf(tmax, acc[b]);
-    }
-#pragma unroll
-    for (int o = 8; o; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-    const float mn = fmaxf(m, tmax);
-    const float alpha = expf(m - mn);  // m = -inf on the first tile: alpha = 0
-    m = mn;
-    float ts = 0.f;
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const float e = expf(acc[b] - mn);
-      es[ty * PR_KT + tx * 4 + b] = e;
-      ts += e;
-    }
-#pragma unroll
-    for (int o = 8; o; o >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, o);
-    Z = Z * alpha + ts;
-    __syncwarp();
-#pragma unroll
-    for (int e = 0; e < DV; ++e) O[e] *= alpha;
-    for (int kk = 0; kk < PR_KT; ++kk) {
-      const float w = es[ty * PR_KT + kk];
-#pragma unroll
-      for (int e = 0; e < DV; ++e) O[e] = fmaf(w, vs[kk * D + tx * DV + e], O[e]);
-    }
+    write[a] = p < Cq && nq[static_cast<long long>(bh) * Cq + pr] > 0;
   }
-  const float invZ = 1.f / Z;
-#pragma unroll
-  for (int e = 0; e < DV; ++e) O[e] *= invZ;
-
-  // ---- pass 2: per key cluster residual, keys in cluster order -------------
-  const bool write = p < Cq && nq[static_cast<long long>(bh) * Cq + min(p, Cq - 1)] > 0;
-  float r[DV];
-#pragma unroll
-  for (int e = 0; e < DV; ++e) r[e] = 0.f;
-  for (int t0 = 0; t0 < N; t0 += PR_KT) {
+  for (int t0 = tb; t0 < te; t0 += PR_KT) {
     __syncthreads();
     for (int kk = tid; kk < PR_KT; kk += PR_THREADS) {
-      const int j = (t0 + kk < N) ? kp[t0 + kk] : -1;
+      const int j = (t0 + kk < te) ? kp[t0 + kk] : -1;
       kidx[kk] = j;
       cid[kk] = j >= 0 ? ka[j] : -1;
     }
@@ -152,49 +278,55 @@ __global__ void __launch_bounds__(PR_THREADS)
       return kidx[kk] >= 0 ? v + kvb + static_cast<long long>(kidx[kk]) * D : nullptr;
     });
     __syncthreads();
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int dd = 0; dd < D; ++dd) {
-      const float qv = qcT[dd * PR_PG + ty];
-      const float4 kv = *reinterpret_cast<const float4*>(&kT[dd * PR_KT + tx * 4]);
-      acc[0] = fmaf(qv, kv.x, acc[0]);
-      acc[1] = fmaf(qv, kv.y, acc[1]);
-      acc[2] = fmaf(qv, kv.z, acc[2]);
-      acc[3] = fmaf(qv, kv.w, acc[3]);
-    }
+    float acc[4][2];
+    probe_logits<D>(qcT, kT, w, lane, acc);
+    const bool v0 = t0 + 2 * lane < te, v1 = t0 + 2 * lane + 1 < te;
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
-      es[ty * PR_KT + tx * 4 + b] =
-          (t0 + tx * 4 + b < N) ? expf(fmaf(acc[b], scale, -m)) : 0.f;
+    for (int a = 0; a < 4; ++a) {
+      es[(2 * lane) * PR_PG + 4 * w + a] = v0 ? expf(fmaf(acc[a][0], scale, -m[a])) : 0.f;
+      es[(2 * lane + 1) * PR_PG + 4 * w + a] = v1 ? expf(fmaf(acc[a][1], scale, -m[a])) : 0.f;
+    }
     __syncwarp();
     for (int kk = 0; kk < PR_KT; ++kk) {
       const int c = cid[kk];
       if (c < 0) break;
-      const float w = es[ty * PR_KT + kk];
+      const float4 ev = *reinterpret_cast<const float4*>(&es[kk * PR_PG + 4 * w]);
+      const float ea[4] = {ev.x, ev.y, ev.z, ev.w};
+      float va4[DV];
+      load_vec<DV>(&vs[kk * D + DV * lane], va4);
 #pragma unroll
-      for (int e = 0; e < DV; ++e) r[e] = fmaf(w, vs[kk * D + tx * DV + e] - O[e], r[e]);
-      if (t0 + kk == offs[c + 1] - 1) {
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int e = 0; e < DV; ++e) r[a][e] = fmaf(ea[a], va4[e] - O[a][e], r[a][e]);
+      if (t0 + kk == offs[c - c_lo + 1] - 1) {
         // last key of cluster c: subtract the compensated term, then |r| / Z
-        const float* kcc = kc + (static_cast<long long>(bh) * Ck + c) * D;
-        const float* vcc = vc + (static_cast<long long>(bh) * Ck + c) * D;
-        float dot = 0.f;
-#pragma unroll
-        for (int e = 0; e < DV; ++e) dot = fmaf(qcT[(tx * DV + e) * PR_PG + ty], kcc[tx * DV + e], dot);
-#pragma unroll
-        for (int o = 8; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        const float wc = static_cast<float>(nk[static_cast<long long>(bh) * Ck + c]) *
-                         expf(fmaf(dot, scale, -m));
-        float n2 = 0.f;
+        const float* kcc = kc + (static_cast<long long>(bh) * Ck + c) * D + DV * lane;
+        const float* vcc = vc + (static_cast<long long>(bh) * Ck + c) * D + DV * lane;
+        float kca[DV], vca[DV];
 #pragma unroll
         for (int e = 0; e < DV; ++e) {
-          const float re = fmaf(-wc, vcc[tx * DV + e] - O[e], r[e]);
-          n2 = fmaf(re, re, n2);
-          r[e] = 0.f;
+          kca[e] = kcc[e];
+          vca[e] = vcc[e];
         }
+        const float ncf = static_cast<float>(nk[static_cast<long long>(bh) * Ck + c]);
 #pragma unroll
-        for (int o = 8; o; o >>= 1) n2 += __shfl_xor_sync(0xffffffffu, n2, o);
-        if (write && tx == 0)
-          err[(static_cast<long long>(bh) * Cq + p) * Ck + c] = sqrtf(n2) * invZ;
+        for (int a = 0; a < 4; ++a) {
+          float dot = 0.f;
+#pragma unroll
+          for (int e = 0; e < DV; ++e) dot = fmaf(qcT[(DV * lane + e) * PR_PG + 4 * w + a], kca[e], dot);
+          dot = warp_sum(dot);
+          const float wc = ncf * expf(fmaf(dot, scale, -m[a]));
+          float n2 = 0.f;
+#pragma unroll
+          for (int e = 0; e < DV; ++e) {
+            const float re = fmaf(-wc, vca[e] - O[a][e], r[a][e]);
+            n2 = fmaf(re, re, n2);
+            r[a][e] = 0.f;
+          }
+          n2 = warp_sum(n2);
+          if (write[a] && lane == 0)
+            err[(static_cast<long long>(bh) * Cq + p0 + 4 * w + a) * Ck + c] = sqrtf(n2) * invZ[a];
+        }
       }
     }
   }
@@ -210,22 +342,49 @@ __device__ __forceinline__ unsigned long long route_key(float ratio, int p, int 
          static_cast<unsigned long long>(p * Ck + c);
 }
 
+// Sort keys and costs of every (p, c) block: key = route_key(err / n_c, p, c)
+// and cost n_p n_c, or (~0, 0) for a block with an empty cluster.
+// Grid (ceil(Cq * Ck / 256), BH).
+__global__ void route_keys_kernel(const float* __restrict__ err, const int* __restrict__ nq,
+                                  const int* __restrict__ nk, int Cq, int Ck,
+                                  unsigned long long* __restrict__ keys,
+                                  unsigned long long* __restrict__ costs) {
+  const int bh = blockIdx.y;
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= Cq * Ck) return;
+  const int p = e / Ck, c = e - p * Ck;
+  const int np = nq[static_cast<long long>(bh) * Cq + p];
+  const int nc = nk[static_cast<long long>(bh) * Ck + c];
+  const long long i = static_cast<long long>(bh) * Cq * Ck + e;
+  if (np <= 0 || nc <= 0) {
+    keys[i] = ~0ull;
+    costs[i] = 0;
+    return;
+  }
+  const float ratio = __fdiv_rn(err[i], static_cast<float>(nc));
+  keys[i] = route_key(ratio, p, c, Ck);
+  costs[i] = static_cast<unsigned long long>(np) * static_cast<unsigned long long>(nc);
+}
+
+constexpr int RS_THREADS = 1024;
+constexpr int RS_SMEM_BYTES = (RS_THREADS / 32) * 256 * 8;
+
 // Per bh (one CTA of 1024 threads): the smallest key K whose prefix (all keys
 // <= K) costs more than the budget; blocks with key < K are computed exactly.
 // cut[bh] = ~0 when every valid block fits. Weighted MSB-first radix select,
-// 8 bits per pass.
-__global__ void __launch_bounds__(1024)
-    route_select_kernel(const float* __restrict__ err, const int* __restrict__ nq,
-                        const int* __restrict__ nk, int Cq, int Ck, long long budget,
-                        unsigned long long* __restrict__ cut) {
+// 8 bits per pass, with one private histogram per warp.
+__global__ void __launch_bounds__(RS_THREADS)
+    route_select_kernel(const unsigned long long* __restrict__ keys,
+                        const unsigned long long* __restrict__ costs, int total,
+                        long long budget, unsigned long long* __restrict__ cut) {
+  extern __shared__ unsigned long long rs_hist[];  // [32 warps][256]
   __shared__ unsigned long long hist[256];
   __shared__ unsigned long long s_prefix, s_mask;
   __shared__ long long s_remaining;
   __shared__ int s_done;
-  const int bh = blockIdx.x, tid = threadIdx.x;
-  const float* eb = err + static_cast<long long>(bh) * Cq * Ck;
-  const int* nqb = nq + static_cast<long long>(bh) * Cq;
-  const int* nkb = nk + static_cast<long long>(bh) * Ck;
+  const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5;
+  const unsigned long long* kb = keys + static_cast<long long>(bh) * total;
+  const unsigned long long* cb = costs + static_cast<long long>(bh) * total;
   if (tid == 0) {
     s_prefix = 0;
     s_mask = 0;
@@ -233,35 +392,37 @@ __global__ void __launch_bounds__(1024)
     s_done = 0;
   }
   for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int b = tid; b < 256; b += 1024) hist[b] = 0;
+    for (int b = tid; b < (RS_THREADS / 32) * 256; b += RS_THREADS) rs_hist[b] = 0;
     __syncthreads();
     if (s_done) break;
     const unsigned long long prefix = s_prefix, mask = s_mask;
-    const int total = Cq * Ck;
-    for (int e = tid; e < total; e += 1024) {
-      const int p = e / Ck, c = e - p * Ck;
-      const int np = nqb[p], nc = nkb[c];
-      if (np <= 0 || nc <= 0) continue;
-      const float ratio = __fdiv_rn(eb[e], static_cast<float>(nc));
-      const unsigned long long key = route_key(ratio, p, c, Ck);
-      if ((key & mask) != prefix) continue;
-      atomicAdd(&hist[(key >> shift) & 255u],
-                static_cast<unsigned long long>(np) * static_cast<unsigned long long>(nc));
+    unsigned long long* h = rs_hist + warp * 256;
+    for (int e = tid; e < total; e += RS_THREADS) {
+      const unsigned long long key = kb[e];
+      const unsigned long long cost = cb[e];
+      if (cost == 0 || (key & mask) != prefix) continue;
+      atomicAdd(&h[(key >> shift) & 255u], cost);
+    }
+    __syncthreads();
+    for (int b = tid; b < 256; b += RS_THREADS) {
+      unsigned long long sum = 0;
+      for (int w = 0; w < RS_THREADS / 32; ++w) sum += rs_hist[w * 256 + b];
+      hist[b] = sum;
     }
     __syncthreads();
     if (tid == 0) {
       long long cum = 0;
       int b = 0;
       for (; b < 256; ++b) {
-        const long long h = static_cast<long long>(hist[b]);
-        if (cum + h > s_remaining) break;
-        cum += h;
+        const long long hb = static_cast<long long>(hist[b]);
+        if (cum + hb > s_remaining) break;
+        cum += hb;
       }
       if (b == 256) {
-        // everything under this prefix fits
+        // everything under this prefix fits (only possible on the first pass:
+        // the whole set fits the budget)
         s_done = 1;
-        if (shift == 56) s_prefix = ~0ull;  // the whole set fits the budget
-        else s_prefix = prefix | ((1ull << (shift + 8)) - 1ull) ;
+        s_prefix = ~0ull;
       } else {
         s_remaining -= cum;
         s_prefix = prefix | (static_cast<unsigned long long>(b) << shift);

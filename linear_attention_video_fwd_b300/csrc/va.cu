@@ -28,7 +28,8 @@ int64_t g_wait_limit = 4000000000LL;
 struct Scoped {
   // Stream-ordered scratch allocations released at scope exit.
   cudaStream_t s;
-  void* ptrs[32];
+  static constexpr int kCap = 64;
+  void* ptrs[kCap];
   int n = 0;
   explicit Scoped(cudaStream_t st) : s(st) {}
   ~Scoped() {
@@ -39,6 +40,7 @@ struct Scoped {
     *p = nullptr;
     if (count == 0) count = 1;
     if (fault_injected()) return VA_ERR_OOM;
+    if (n >= kCap) return VA_ERR_OOM;
     void* raw = nullptr;
     cudaError_t e = cudaMallocAsync(&raw, count * sizeof(T), s);
     if (e != cudaSuccess) {
@@ -168,6 +170,12 @@ VA_EXPORT int va_device_error(va_stream_t stream) {
   e = cudaMemcpyToSymbol(va::g_err_word, &zero, sizeof(int));
   if (e != cudaSuccess) return cuda_status(e);
   return word;
+}
+
+VA_EXPORT int va_selftest_wait_timeout(int64_t cycles, va_stream_t stream) {
+  if (cycles < 1000 || cycles > 10000000000LL) return VA_ERR_INVALID;
+  va::wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(cycles);
+  return launch_status();
 }
 
 // ------------------------------------------------------------------ masks --
@@ -429,9 +437,15 @@ int set_smem_attrs() {
   if ((st = cuda_status(cudaFuncSetAttribute(va::km_assign_kernel<T, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              2 * D * va::KM_PT * 4))) ||
-      (st = cuda_status(cudaFuncSetAttribute(va::probe_kernel<T, D>,
+      (st = cuda_status(cudaFuncSetAttribute(va::probe_pass1_kernel<T, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              va::probe_smem_bytes<D>(kMaxClusters)))) ||
+      (st = cuda_status(cudaFuncSetAttribute(va::probe_pass2_kernel<T, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             va::probe_smem_bytes<D>(kMaxClusters)))) ||
+      (st = cuda_status(cudaFuncSetAttribute(va::route_select_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             va::RS_SMEM_BYTES))) ||
       (st = cuda_status(cudaFuncSetAttribute(va::comp_attn_kernel<T, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              va::comp_smem_bytes<D>(kMaxClusters)))))
@@ -687,15 +701,29 @@ int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int C
 
   // probe: err = NaN where a cluster is empty, else the proxy error
   if ((st = cuda_status(cudaMemsetAsync(err, 0xFF, sizeof(float) * bh * Cq * Ck, s)))) return st;
-  va::probe_kernel<T, D><<<dim3((Cq + va::PR_PG - 1) / va::PR_PG, BH), va::PR_THREADS,
-                           va::probe_smem_bytes<D>(Ck), s>>>(
-      k, v, N, Cq, Ck, qc, nq, kc, vc, nk, koff, kperm, kassign, scale, err);
+  float *part, *mzo;
+  if ((st = scratch.alloc(&part, bh * Cq * va::PR_SPLIT * (D + 2))) ||
+      (st = scratch.alloc(&mzo, bh * Cq * (D + 2))))
+    return st;
+  const int pg = (Cq + va::PR_PG - 1) / va::PR_PG;
+  va::probe_pass1_kernel<T, D><<<dim3(pg, va::PR_SPLIT, BH), va::PR_THREADS,
+                                 va::probe_smem_bytes<D>(0), s>>>(k, v, N, Cq, qc, scale, part);
+  va::probe_combine_kernel<D><<<dim3(Cq, BH), D, 0, s>>>(part, Cq, mzo);
+  va::probe_pass2_kernel<T, D><<<dim3(pg, va::PR_CSPLIT, BH), va::PR_THREADS,
+                                 va::probe_smem_bytes<D>(Ck), s>>>(
+      k, v, N, Cq, Ck, qc, nq, kc, vc, nk, koff, kperm, kassign, mzo, scale, err);
   if ((st = launch_status())) return st;
 
   // routing
   uint8_t* sel = sel_out;
   if (sel == nullptr && (st = scratch.alloc(&sel, bh * Cq * Ck))) return st;
-  va::route_select_kernel<<<BH, 1024, 0, s>>>(err, nq, nk, Cq, Ck, budget, cut);
+  unsigned long long *rkeys, *rcosts;
+  if ((st = scratch.alloc(&rkeys, bh * Cq * Ck)) || (st = scratch.alloc(&rcosts, bh * Cq * Ck)))
+    return st;
+  va::route_keys_kernel<<<dim3((Cq * Ck + 255) / 256, BH), 256, 0, s>>>(err, nq, nk, Cq, Ck,
+                                                                       rkeys, rcosts);
+  va::route_select_kernel<<<BH, va::RS_THREADS, va::RS_SMEM_BYTES, s>>>(rkeys, rcosts, Cq * Ck,
+                                                                        budget, cut);
   va::route_mark_kernel<<<dim3(Cq, BH), 256, 0, s>>>(err, nq, nk, Cq, Ck, cut, sel, seln, selc);
   if ((st = launch_status())) return st;
 
