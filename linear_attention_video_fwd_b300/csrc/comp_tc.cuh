@@ -29,7 +29,7 @@ namespace va {
 constexpr int CT_NM = 4;  // validity-mask ring entries
 // Register split of this kernel (launched at TC_LAUNCH_REGS per thread): the
 // producer's slot search needs more than the attention kernel's producer.
-constexpr int CT_REGS_DEC = 64;
+constexpr int CT_REGS_DEC = 72;
 constexpr int CT_REGS_INC = 216;
 static_assert(128 * CT_REGS_DEC + 256 * CT_REGS_INC <= TC_THREADS * TC_LAUNCH_REGS,
               "register split exceeds the launch allocation");
@@ -44,6 +44,9 @@ struct CompArgs {
   const int* selc;     // [BH][Cq][Ck] selected key clusters (ascending)
   const int* selbox;   // [BH][Cq][Ck + 1] exclusive prefix of ceil(n_c / 8) over selc
   const float* vbias;  // [BH][Cq][nv * 128] virtual-key bias, log2 units (-inf: none)
+  const int* slots;    // slot table: (first key row << 4) | valid rows, 16 per exact tile
+  const long long* slotbase;  // [BH] start of each (batch, head) in the slot table
+  const int* slotoff;  // [BH][Cq + 1] start of each query cluster's slots
   __nv_bfloat16* out;  // [BH][N][128], token order
   int N, Cq, Ck, nv;
   float scale_log2;
@@ -184,21 +187,20 @@ __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const Co
       s[i + 1] = ex2_approx(s[i + 1]);
     }
     float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-    uint32_t pk[64];
 #pragma unroll
-    for (int i = 0; i < 128; i += 4) {
-      fadd2_acc(r0, r1, s[i], s[i + 1]);
-      fadd2_acc(r2, r3, s[i + 2], s[i + 3]);
-      pk[i / 2] = pack_bf16x2(s[i], s[i + 1]);
-      pk[i / 2 + 1] = pack_bf16x2(s[i + 2], s[i + 3]);
+    for (int h = 0; h < 2; ++h) {  // pack and store P in two halves of 64 keys
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 64; i += 4) {
+        const int c = h * 64 + i;
+        fadd2_acc(r0, r1, s[c], s[c + 1]);
+        fadd2_acc(r2, r3, s[c + 2], s[c + 3]);
+        pk[i / 2] = pack_bf16x2(s[c], s[c + 1]);
+        pk[i / 2 + 1] = pack_bf16x2(s[c + 2], s[c + 3]);
+      }
+      tmem_st32(tS + h * 32, pk);
     }
     l += (r0 + r1) + (r2 + r3);
-    {
-      uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
-      uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[32]);
-      tmem_st32(tS, lo);
-      tmem_st32(tS + 32, hi);
-    }
     tmem_wait_st();
     tc_fence_before();
     mbar_arrive(bP);
@@ -350,25 +352,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const CompTile& T = t == 0 ? T0 : T1;
         const int sk = u % TC_NK, sv = u % TC_NV, ms = u % CT_NM;
         const uint32_t sK = sK0 + sk * TC_TILE_BYTES, sV = sV0 + sv * TC_TILE_BYTES;
-        // slot of this lane (exact tiles): source row and valid row count
+        // slot of this lane (exact tiles): source row and valid row count,
+        // from the slot table (16 slots per exact tile, padding slots valid 0)
         int src = 0, valid = 0;
         if (j >= a.nv && lane < 16) {
-          const int slot = (j - a.nv) * 16 + lane;
-          if (slot < T.nslots) {
-            const long long pc = static_cast<long long>(bh) * a.Cq + T.p;
-            const int* sb = a.selbox + pc * (a.Ck + 1);
-            int lo = 0, hi = T.ns - 1;  // last selected s with sb[s] <= slot
-            while (lo < hi) {
-              const int mid = (lo + hi + 1) >> 1;
-              if (sb[mid] <= slot) lo = mid;
-              else hi = mid - 1;
-            }
-            const int c = a.selc[pc * a.Ck + lo];
-            const int b = slot - sb[lo];
-            const int* ko = a.koff + static_cast<long long>(bh) * (a.Ck + 1);
-            src = ko[c] + 8 * b;
-            valid = min(8, ko[c + 1] - src);
-          }
+          const int sd = a.slots[a.slotbase[bh] +
+                                 a.slotoff[static_cast<long long>(bh) * (a.Cq + 1) + T.p] +
+                                 (j - a.nv) * 16 + lane];
+          src = sd >> 4;
+          valid = sd & 15;
         }
         bool ok = true;
         if (lane == 0) {
@@ -562,6 +554,62 @@ __global__ void comp_prep_kernel(const int* __restrict__ nk, const int* __restri
   for (int c = lane; c < nv * 128; c += 32) {
     const int n = c < Ck ? nkb[c] : 0;
     vb[c] = (n > 0 && !sr[c]) ? log2f(static_cast<float>(n)) : -INFINITY;
+  }
+}
+
+// Padded slot count per query cluster: 16 * ceil(slots / 16).
+__global__ void slot_count_kernel(const int* __restrict__ seln, const int* __restrict__ selbox,
+                                  int Cq, int Ck, int* __restrict__ cnt) {
+  const int bh = blockIdx.y;
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= Cq) return;
+  const long long pc = static_cast<long long>(bh) * Cq + p;
+  const int ns = selbox[pc * (Ck + 1) + seln[pc]];
+  cnt[pc] = (ns + 15) / 16 * 16;
+}
+
+// base[b] = sum of off[b'][Cq] for b' < b; base[BH] = total (one thread).
+__global__ void slot_base_kernel(const int* __restrict__ off, int Cq, int BH,
+                                 long long* __restrict__ base) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  long long acc = 0;
+  for (int b = 0; b < BH; ++b) {
+    base[b] = acc;
+    acc += off[static_cast<long long>(b) * (Cq + 1) + Cq];
+  }
+  base[BH] = acc;
+}
+
+// One thread per slot of one query cluster: (first key row << 4) | valid rows
+// for slot i < slots (a slot is 8 rows of one selected key cluster, in cluster
+// order), 0 for the padding up to a multiple of 16. Grid (Cq, BH).
+__global__ void slot_fill_kernel(const int* __restrict__ koff, const int* __restrict__ seln,
+                                 const int* __restrict__ selc, const int* __restrict__ selbox,
+                                 int Cq, int Ck, const long long* __restrict__ base,
+                                 const int* __restrict__ off, int* __restrict__ slots) {
+  const int bh = blockIdx.y, p = blockIdx.x;
+  const long long pc = static_cast<long long>(bh) * Cq + p;
+  const int ns = seln[pc];
+  const int* sb = selbox + pc * (Ck + 1);
+  const int* sl = selc + pc * Ck;
+  const int* ko = koff + static_cast<long long>(bh) * (Ck + 1);
+  const int nslots = sb[ns];
+  const int npad = (nslots + 15) / 16 * 16;
+  int* out = slots + base[bh] + off[static_cast<long long>(bh) * (Cq + 1) + p];
+  for (int i = threadIdx.x; i < npad; i += blockDim.x) {
+    int v = 0;
+    if (i < nslots) {
+      int lo = 0, hi = ns - 1;  // last selected s with sb[s] <= i
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sb[mid] <= i) lo = mid;
+        else hi = mid - 1;
+      }
+      const int c = sl[lo];
+      const int src = ko[c] + 8 * (i - sb[lo]);
+      v = (src << 4) | min(8, ko[c + 1] - src);
+    }
+    out[i] = v;
   }
 }
 

@@ -316,6 +316,96 @@ __global__ void km_means_kernel(const T* __restrict__ x, int N, int C,
   }
 }
 
+// Member sums of bf16 points as 64-bit fixed point (bf16_fixed32), balanced:
+// warp g sums the 32 cluster-ordered points perm[32g .. 32g + 31] of its
+// (batch, head), splitting at cluster changes, and adds each run into
+// sums[bh][c][0..D) with 64-bit integer atomics (exact, so the result does not
+// depend on the order). sums must be zeroed. Grid (ceil(N / 256), BH), 256
+// threads.
+template <int D>
+__global__ void km_sum_kernel(const __nv_bfloat16* __restrict__ x, int N, int C,
+                              const int* __restrict__ perm, const int* __restrict__ assign,
+                              unsigned long long* __restrict__ sums) {
+  constexpr int PER = D / 32;
+  const int bh = blockIdx.y;
+  const int t0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * 32;
+  const int lane = threadIdx.x & 31;
+  if (t0 >= N) return;
+  const long long nb = static_cast<long long>(bh) * N;
+  const int my = t0 + lane < N ? perm[nb + t0 + lane] : 0;
+  const int myc = t0 + lane < N ? assign[nb + my] : -1;
+  const int cnt = min(32, N - t0);
+  const uint16_t* xb = reinterpret_cast<const uint16_t*>(x) + nb * D + lane * PER;
+  long long acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0;
+  int cur = __shfl_sync(0xffffffffu, myc, 0);
+  for (int q = 0; q < cnt; ++q) {
+    const int idx = __shfl_sync(0xffffffffu, my, q);
+    const int c = __shfl_sync(0xffffffffu, myc, q);
+    if (c != cur) {
+      if (cur >= 0 && cur < C) {
+        unsigned long long* dst = sums + (static_cast<long long>(bh) * C + cur) * D + lane * PER;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) atomicAdd(dst + e, static_cast<unsigned long long>(acc[e]));
+      }
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = 0;
+      cur = c;
+    }
+    const uint16_t* row = xb + static_cast<long long>(idx) * D;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] += bf16_fixed32(row[e]);
+  }
+  if (cur >= 0 && cur < C) {
+    unsigned long long* dst = sums + (static_cast<long long>(bh) * C + cur) * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) atomicAdd(dst + e, static_cast<unsigned long long>(acc[e]));
+  }
+}
+
+// mean[bh][c] = sums / count (fp32), |mean|^2 to norm (if non-null), and the
+// bf16 split hi = bf16(mean), lo = bf16(mean - hi) (if non-null). An empty
+// cluster keeps mean (and its split) when keep_empty, else gets zeros.
+// One warp per cluster; grid (ceil(C / 8), BH), 256 threads.
+template <int D>
+__global__ void km_finalize_kernel(const unsigned long long* __restrict__ sums,
+                                   const int* __restrict__ count, int C, float* __restrict__ mean,
+                                   float* __restrict__ norm, __nv_bfloat16* __restrict__ hi,
+                                   __nv_bfloat16* __restrict__ lo, int keep_empty) {
+  constexpr int PER = D / 32;
+  const int bh = blockIdx.y;
+  const int c = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (c >= C) return;
+  const long long row = (static_cast<long long>(bh) * C + c) * D + lane * PER;
+  const int n = count[static_cast<long long>(bh) * C + c];
+  float nrm = 0.f;
+  if (n > 0 || !keep_empty) {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const float mv = n > 0 ? static_cast<float>(static_cast<double>(
+                                   static_cast<long long>(sums[row + e])) * 0x1p-32 / n)
+                             : 0.f;
+      mean[row + e] = mv;
+      nrm = fmaf(mv, mv, nrm);
+      if (hi != nullptr) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(mv);
+        hi[row + e] = h;
+        lo[row + e] = __float2bfloat16_rn(mv - __bfloat162float(h));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < PER; ++e) nrm = fmaf(mean[row + e], mean[row + e], nrm);
+  }
+  if (norm != nullptr) {
+#pragma unroll
+    for (int o2 = 16; o2; o2 >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o2);
+    if (lane == 0) norm[static_cast<long long>(bh) * C + c] = nrm;
+  }
+}
+
 // Initial centroids: cent[bh][c] = x[bh][init[bh][c]] (fp32), |c|^2 to cnorm.
 // Indices outside [0, N) are reported as VA_ERR_DEVICE (the row is zeroed).
 // One warp per centroid; grid (ceil(C / 8), BH).

@@ -43,10 +43,14 @@ constexpr int PR_KT = 64;  // keys per tile
 constexpr int PR_THREADS = 256;
 constexpr int PR_SPLIT = 8;    // key splits of pass 1
 constexpr int PR_CSPLIT = 8;   // key-cluster splits of pass 2
+// Row stride (floats) of the per-key weight tile es[key][proxy]: 36 keeps the
+// float4 rows of consecutive keys on different bank groups.
+constexpr int PR_ES_LD = PR_PG + 4;
+constexpr int PR_NO_KEY = 0x7fffffff;  // tile slot past the range's last key
 
 template <int D>
 constexpr int probe_smem_bytes(int Ck) {
-  return (D * PR_PG + D * PR_KT + PR_KT * D + PR_KT * PR_PG) * 4 + 2 * PR_KT * 4 + (Ck + 1) * 4;
+  return (D * PR_PG + D * PR_KT + PR_KT * D + PR_KT * PR_ES_LD) * 4 + 2 * PR_KT * 4 + (Ck + 1) * 4;
 }
 
 // acc[a][b] = qc_{4w+a} . k_{2 lane + b}
@@ -111,7 +115,7 @@ __global__ void __launch_bounds__(PR_THREADS)
   float* qcT = pr_smem;                       // [D][PR_PG]
   float* kT = qcT + D * PR_PG;                // [D][PR_KT]
   float* vs = kT + D * PR_KT;                 // [PR_KT][D]
-  float* es = vs + PR_KT * D;                 // [PR_KT][PR_PG]
+  float* es = vs + PR_KT * D;                 // [PR_KT][PR_ES_LD]
   const int bh = blockIdx.z, split = blockIdx.y;
   const int p0 = blockIdx.x * PR_PG;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -141,6 +145,7 @@ __global__ void __launch_bounds__(PR_THREADS)
     float acc[4][2];
     probe_logits<D>(qcT, kT, w, lane, acc);
     const bool v0 = j0 + 2 * lane < je, v1 = j0 + 2 * lane + 1 < je;
+    float e0[4], e1[4];
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       const float l0 = v0 ? acc[a][0] * scale : -INFINITY;
@@ -148,17 +153,20 @@ __global__ void __launch_bounds__(PR_THREADS)
       const float mn = fmaxf(m[a], warp_max(fmaxf(l0, l1)));
       const float alpha = expf(m[a] - mn);  // m = -inf on the first tile: alpha = 0
       m[a] = mn;
-      const float e0 = expf(l0 - mn), e1 = expf(l1 - mn);
-      es[(2 * lane) * PR_PG + 4 * w + a] = e0;
-      es[(2 * lane + 1) * PR_PG + 4 * w + a] = e1;
-      Z[a] = Z[a] * alpha + warp_sum(e0 + e1);
+      e0[a] = expf(l0 - mn);
+      e1[a] = expf(l1 - mn);
+      Z[a] = Z[a] * alpha + warp_sum(e0[a] + e1[a]);
 #pragma unroll
       for (int e = 0; e < DV; ++e) O[a][e] *= alpha;
     }
+    *reinterpret_cast<float4*>(&es[(2 * lane) * PR_ES_LD + 4 * w]) =
+        make_float4(e0[0], e0[1], e0[2], e0[3]);
+    *reinterpret_cast<float4*>(&es[(2 * lane + 1) * PR_ES_LD + 4 * w]) =
+        make_float4(e1[0], e1[1], e1[2], e1[3]);
     __syncwarp();
 #pragma unroll 4
     for (int kk = 0; kk < PR_KT; ++kk) {
-      const float4 ev = *reinterpret_cast<const float4*>(&es[kk * PR_PG + 4 * w]);
+      const float4 ev = *reinterpret_cast<const float4*>(&es[kk * PR_ES_LD + 4 * w]);
       const float ea[4] = {ev.x, ev.y, ev.z, ev.w};
       float va4[DV];
       load_vec<DV>(&vs[kk * D + DV * lane], va4);
@@ -227,8 +235,9 @@ __global__ void __launch_bounds__(PR_THREADS)
   float* qcT = pr_smem;                       // [D][PR_PG]
   float* kT = qcT + D * PR_PG;                // [D][PR_KT]
   float* vs = kT + D * PR_KT;                 // [PR_KT][D]
-  float* es = vs + PR_KT * D;                 // [PR_KT][PR_PG]
-  int* cid = reinterpret_cast<int*>(es + PR_KT * PR_PG);  // [PR_KT]
+  float* es = vs + PR_KT * D;                 // [PR_KT][PR_ES_LD]
+  int* cid = reinterpret_cast<int*>(es + PR_KT * PR_ES_LD);  // [PR_KT]: cluster, or
+                                              // -1 - cluster for its last key
   int* kidx = cid + PR_KT;                    // [PR_KT]
   int* offs = kidx + PR_KT;                   // [Ck + 1] (this range's part)
 
@@ -247,7 +256,10 @@ __global__ void __launch_bounds__(PR_THREADS)
     return p0 + pp < Cq ? qc + (static_cast<long long>(bh) * Cq + p0 + pp) * D : nullptr;
   });
   for (int e = tid; e <= c_hi - c_lo; e += PR_THREADS) offs[e] = ko[c_lo + e];
-  float m[4], invZ[4], O[4][DV], r[4][DV];
+  // Per cluster: E = sum e_j v_j and Zc = sum e_j over its keys; at its last
+  // key r = E - Zc O - w (vc - O) (the same residual, one subtraction per
+  // cluster instead of per key).
+  float m[4], invZ[4], O[4][DV], r[4][DV], zc[4];
   bool write[4];
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
@@ -261,6 +273,7 @@ __global__ void __launch_bounds__(PR_THREADS)
       O[a][e] = mz[2 + DV * lane + e];
       r[a][e] = 0.f;
     }
+    zc[a] = 0.f;
     write[a] = p < Cq && nq[static_cast<long long>(bh) * Cq + pr] > 0;
   }
   for (int t0 = tb; t0 < te; t0 += PR_KT) {
@@ -268,7 +281,12 @@ __global__ void __launch_bounds__(PR_THREADS)
     for (int kk = tid; kk < PR_KT; kk += PR_THREADS) {
       const int j = (t0 + kk < te) ? kp[t0 + kk] : -1;
       kidx[kk] = j;
-      cid[kk] = j >= 0 ? ka[j] : -1;
+      int c = PR_NO_KEY;
+      if (j >= 0) {
+        c = ka[j];
+        if (t0 + kk == offs[c - c_lo + 1] - 1) c = -1 - c;  // last key of cluster c
+      }
+      cid[kk] = c;
     }
     __syncthreads();
     stage_transposed<T, D, PR_KT, PR_THREADS>(kT, [&](int kk) -> const T* {
@@ -281,25 +299,33 @@ __global__ void __launch_bounds__(PR_THREADS)
     float acc[4][2];
     probe_logits<D>(qcT, kT, w, lane, acc);
     const bool v0 = t0 + 2 * lane < te, v1 = t0 + 2 * lane + 1 < te;
+    float e0[4], e1[4];
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-      es[(2 * lane) * PR_PG + 4 * w + a] = v0 ? expf(fmaf(acc[a][0], scale, -m[a])) : 0.f;
-      es[(2 * lane + 1) * PR_PG + 4 * w + a] = v1 ? expf(fmaf(acc[a][1], scale, -m[a])) : 0.f;
+      e0[a] = v0 ? expf(fmaf(acc[a][0], scale, -m[a])) : 0.f;
+      e1[a] = v1 ? expf(fmaf(acc[a][1], scale, -m[a])) : 0.f;
     }
+    *reinterpret_cast<float4*>(&es[(2 * lane) * PR_ES_LD + 4 * w]) =
+        make_float4(e0[0], e0[1], e0[2], e0[3]);
+    *reinterpret_cast<float4*>(&es[(2 * lane + 1) * PR_ES_LD + 4 * w]) =
+        make_float4(e1[0], e1[1], e1[2], e1[3]);
     __syncwarp();
     for (int kk = 0; kk < PR_KT; ++kk) {
-      const int c = cid[kk];
-      if (c < 0) break;
-      const float4 ev = *reinterpret_cast<const float4*>(&es[kk * PR_PG + 4 * w]);
+      const int cc = cid[kk];
+      if (cc == PR_NO_KEY) break;
+      const float4 ev = *reinterpret_cast<const float4*>(&es[kk * PR_ES_LD + 4 * w]);
       const float ea[4] = {ev.x, ev.y, ev.z, ev.w};
       float va4[DV];
       load_vec<DV>(&vs[kk * D + DV * lane], va4);
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
+      for (int a = 0; a < 4; ++a) {
+        zc[a] += ea[a];
 #pragma unroll
-        for (int e = 0; e < DV; ++e) r[a][e] = fmaf(ea[a], va4[e] - O[a][e], r[a][e]);
-      if (t0 + kk == offs[c - c_lo + 1] - 1) {
-        // last key of cluster c: subtract the compensated term, then |r| / Z
+        for (int e = 0; e < DV; ++e) r[a][e] = fmaf(ea[a], va4[e], r[a][e]);
+      }
+      if (cc < 0) {
+        const int c = -1 - cc;
+        // last key of cluster c: subtract Zc O and the compensated term, then |r| / Z
         const float* kcc = kc + (static_cast<long long>(bh) * Ck + c) * D + DV * lane;
         const float* vcc = vc + (static_cast<long long>(bh) * Ck + c) * D + DV * lane;
         float kca[DV], vca[DV];
@@ -319,10 +345,11 @@ __global__ void __launch_bounds__(PR_THREADS)
           float n2 = 0.f;
 #pragma unroll
           for (int e = 0; e < DV; ++e) {
-            const float re = fmaf(-wc, vca[e] - O[a][e], r[a][e]);
+            const float re = fmaf(-wc, vca[e] - O[a][e], fmaf(-zc[a], O[a][e], r[a][e]));
             n2 = fmaf(re, re, n2);
             r[a][e] = 0.f;
           }
+          zc[a] = 0.f;
           n2 = warp_sum(n2);
           if (write[a] && lane == 0)
             err[(static_cast<long long>(bh) * Cq + p0 + 4 * w + a) * Ck + c] = sqrtf(n2) * invZ[a];

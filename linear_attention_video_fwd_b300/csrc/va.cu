@@ -484,12 +484,14 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C
   float* cnorm = nullptr;
   int *off = nullptr, *fill = nullptr, *perm = nullptr;
   __nv_bfloat16 *hi = nullptr, *lo = nullptr;
+  unsigned long long* sums = nullptr;
   const size_t nc = static_cast<size_t>(BH) * C * 128;
   if ((st = scratch.alloc(&cnorm, static_cast<size_t>(BH) * C)) ||
       (st = scratch.alloc(&off, static_cast<size_t>(BH) * (C + 1))) ||
       (st = scratch.alloc(&fill, static_cast<size_t>(BH) * C)) ||
       (st = scratch.alloc(&perm, static_cast<size_t>(BH) * N)) ||
-      (st = scratch.alloc(&hi, nc)) || (st = scratch.alloc(&lo, nc)))
+      (st = scratch.alloc(&hi, nc)) || (st = scratch.alloc(&lo, nc)) ||
+      (st = scratch.alloc(&sums, nc)))
     return st;
   CUtensorMap mx, mh, ml;
   if ((st = encode_bf16_rows(&mx, x, BH, N, 128)) || (st = encode_bf16_rows(&mh, hi, BH, C, 128)) ||
@@ -509,8 +511,9 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C
     if (iters == 0) break;
     va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
     va::km_scatter_kernel<<<gn, 256, 0, s>>>(assign, N, C, off, fill, perm);
-    va::km_means_kernel<__nv_bfloat16, 128><<<gc, 256, 0, s>>>(x, N, C, off, perm, cent, cnorm, 1);
-    va::km_split_kernel<<<gs, 256, 0, s>>>(cent, static_cast<long long>(nc), hi, lo);
+    if ((st = cuda_status(cudaMemsetAsync(sums, 0, sizeof(unsigned long long) * nc, s)))) return st;
+    va::km_sum_kernel<128><<<gn, 256, 0, s>>>(x, N, C, perm, assign, sums);
+    va::km_finalize_kernel<128><<<gc, 256, 0, s>>>(sums, count, C, cent, cnorm, hi, lo, 1);
   }
   return launch_status();
 }
@@ -628,6 +631,26 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
                                                              selbox, vbias);
   va::chunk_count_kernel<<<dim3((Cq + 255) / 256, BH), 256, 0, s>>>(nq, Cq, 128, nch);
   va::km_offsets_kernel<<<BH, 1024, 0, s>>>(nch, Cq, choff, chfill);
+  // slot table: per query cluster, its selected clusters' 8-row slots padded
+  // to whole 16-slot tiles; one synchronisation reads its total size
+  int *slcnt, *sloff, *slfill, *slots;
+  long long* slbase;
+  if ((st = scratch.alloc(&slcnt, bh * Cq)) || (st = scratch.alloc(&sloff, bh * (Cq + 1))) ||
+      (st = scratch.alloc(&slfill, bh * Cq)) || (st = scratch.alloc(&slbase, bh + 1)))
+    return st;
+  va::slot_count_kernel<<<dim3((Cq + 255) / 256, BH), 256, 0, s>>>(seln, selbox, Cq, Ck, slcnt);
+  va::km_offsets_kernel<<<BH, 1024, 0, s>>>(slcnt, Cq, sloff, slfill);
+  va::slot_base_kernel<<<1, 1, 0, s>>>(sloff, Cq, BH, slbase);
+  if ((st = launch_status())) return st;
+  long long total_slots = 0;
+  if ((st = cuda_status(cudaMemcpyAsync(&total_slots, slbase + BH, sizeof(long long),
+                                        cudaMemcpyDeviceToHost, s))) ||
+      (st = cuda_status(cudaStreamSynchronize(s))))
+    return st;
+  if ((st = scratch.alloc(&slots, static_cast<size_t>(total_slots > 0 ? total_slots : 1))))
+    return st;
+  va::slot_fill_kernel<<<dim3(Cq, BH), 256, 0, s>>>(koff, seln, selc, selbox, Cq, Ck, slbase,
+                                                   sloff, slots);
   if ((st = launch_status())) return st;
   CUtensorMap mq, mkc, mvc, mk8, mv8;
   if ((st = encode_bf16_rows_box(&mq, qs, BH, N, 128, 128)) ||
@@ -646,6 +669,9 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   a.selc = selc;
   a.selbox = selbox;
   a.vbias = vbias;
+  a.slots = slots;
+  a.slotbase = slbase;
+  a.slotoff = sloff;
   a.out = out;
   a.N = N;
   a.Cq = Cq;
