@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -18,6 +19,7 @@
 #include "svgear.cuh"
 #include "kmeans_tc.cuh"
 #include "comp_tc.cuh"
+#include "probe_tc.cuh"
 
 #define VA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -685,6 +687,119 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   return launch_status();
 }
 
+// Error probe on the tensor cores (bf16, d = 128): padded cluster-ordered
+// K/V with group metadata, three bf16 pieces of the proxies, then pass 1
+// (split partials of m2, Z, O), their merge and pass 2 (err).
+int probe_tensor_cores(const __nv_bfloat16* k, const __nv_bfloat16* v, int Cq, int Ck, int BH,
+                       int N, const int* nq, const int* nk, const int* koff, const int* kperm,
+                       const float* qc, const float* vc, float scale, float* err,
+                       Scoped& scratch, cudaStream_t s) {
+  static bool configured[64] = {false};
+  static int num_sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int st;
+  if (dev < 0 || dev >= 64) return VA_ERR_UNSUPPORTED;
+  if (!configured[dev]) {
+    cudaFuncAttributes fa1, fa2;
+    if ((st = cuda_status(cudaFuncGetAttributes(&fa1, va::probe_tc_kernel<1>))) ||
+        (st = cuda_status(cudaFuncGetAttributes(&fa2, va::probe_tc_kernel<2>))))
+      return st;
+    if (fa1.numRegs != va::PT_LAUNCH_REGS || fa2.numRegs != va::PT_LAUNCH_REGS)
+      return VA_ERR_UNSUPPORTED;
+    if ((st = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<1>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               va::PT_SMEM_BYTES))) ||
+        (st = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<2>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               va::PT_SMEM_BYTES))) ||
+        (st = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
+                                                 dev))))
+      return st;
+    configured[dev] = true;
+  }
+  const size_t bh = static_cast<size_t>(BH);
+  const int Cqp = (Cq + 127) / 128 * 128;
+  const int ntiles = Cqp / 128;
+  // rows per head: every cluster padded to 16, plus 64 zero rows after them
+  const long long Npad = (static_cast<long long>(N) + 15LL * Ck + 64 + 15) / 16 * 16;
+  if (Npad > (1LL << 30) || static_cast<long long>(BH) * ntiles > 65535)
+    return VA_ERR_UNSUPPORTED;
+  const int G = static_cast<int>(Npad / 16);
+  const long long per_head = static_cast<long long>(BH) * ntiles;
+  const int NS = static_cast<int>(
+      std::max(1LL, std::min(static_cast<long long>(Ck), num_sms[dev] / per_head)));
+  int *cnt16, *kpoff, *kpfill, *gmeta;
+  __nv_bfloat16 *kpad, *vpad, *qp;
+  float *part, *mzo;
+  if ((st = scratch.alloc(&cnt16, bh * Ck)) || (st = scratch.alloc(&kpoff, bh * (Ck + 1))) ||
+      (st = scratch.alloc(&kpfill, bh * Ck)) ||
+      (st = scratch.alloc(&gmeta, bh * static_cast<size_t>(G))) ||
+      (st = scratch.alloc(&kpad, bh * static_cast<size_t>(Npad) * 128)) ||
+      (st = scratch.alloc(&vpad, bh * static_cast<size_t>(Npad) * 128)) ||
+      (st = scratch.alloc(&qp, bh * 3 * Cqp * 128)) ||
+      (st = scratch.alloc(&part, bh * Cq * NS * va::PT_ROW)) ||
+      (st = scratch.alloc(&mzo, bh * Cq * va::PT_ROW)))
+    return st;
+  const long long nbk = static_cast<long long>(bh) * Ck;
+  va::pad16_count_kernel<<<static_cast<unsigned>((nbk + 255) / 256), 256, 0, s>>>(
+      nk, static_cast<int>(nbk), cnt16);
+  va::km_offsets_kernel<<<BH, 1024, 0, s>>>(cnt16, Ck, kpoff, kpfill);
+  va::pad_gather_kernel<<<dim3(Ck + 1, BH), 128, 0, s>>>(k, v, N, Ck, nk, koff, kperm, kpoff,
+                                                        Npad, G, kpad, vpad, gmeta);
+  va::proxy_pieces_kernel<<<dim3(Cqp, BH), 128, 0, s>>>(qc, Cq, Cqp, qp);
+  if ((st = launch_status())) return st;
+  CUtensorMap mq, mk, mv;
+  if ((st = encode_bf16_rows_box(&mq, qp, BH, 3 * Cqp, 128, 128)) ||
+      (st = encode_bf16_rows_box(&mk, kpad, BH, static_cast<int>(Npad), 128, va::PT_KT)) ||
+      (st = encode_bf16_rows_box(&mv, vpad, BH, static_cast<int>(Npad), 128, va::PT_KT)))
+    return st;
+  va::ProbeArgs a;
+  a.gmeta = gmeta;
+  a.kpoff = kpoff;
+  a.nk = nk;
+  a.nq = nq;
+  a.mzo = mzo;
+  a.vc = vc;
+  a.part = part;
+  a.err = err;
+  a.Cq = Cq;
+  a.Ck = Ck;
+  a.Cqp = Cqp;
+  a.G = G;
+  a.NS = NS;
+  a.sl2 = scale * 1.4426950408889634f;
+  a.wait_limit = g_wait_limit;
+  const dim3 grid(NS, ntiles, BH);
+  va::probe_tc_kernel<1><<<grid, va::PT_THREADS, va::PT_SMEM_BYTES, s>>>(mq, mk, mv, a);
+  va::probe_tc_combine_kernel<<<dim3(Cq, BH), 128, 0, s>>>(part, Cq, NS, mzo);
+  va::probe_tc_kernel<2><<<grid, va::PT_THREADS, va::PT_SMEM_BYTES, s>>>(mq, mk, mv, a);
+  return launch_status();
+}
+
+// Error probe on the FP32 pipe (fp32 inputs or d = 64): pass 1 split
+// partials of m, Z, O, their merge, pass 2 err.
+template <typename T, int D>
+int probe_simt(const T* k, const T* v, int Cq, int Ck, int BH, int N, const int* nq,
+               const int* nk, const int* koff, const int* kperm, const int* kassign,
+               const float* qc, const float* kc, const float* vc, float scale, float* err,
+               Scoped& scratch, cudaStream_t s) {
+  const size_t bh = static_cast<size_t>(BH);
+  float *part, *mzo;
+  int st;
+  if ((st = scratch.alloc(&part, bh * Cq * va::PR_SPLIT * (D + 2))) ||
+      (st = scratch.alloc(&mzo, bh * Cq * (D + 2))))
+    return st;
+  const int pg = (Cq + va::PR_PG - 1) / va::PR_PG;
+  va::probe_pass1_kernel<T, D><<<dim3(pg, va::PR_SPLIT, BH), va::PR_THREADS,
+                                 va::probe_smem_bytes<D>(0), s>>>(k, v, N, Cq, qc, scale, part);
+  va::probe_combine_kernel<D><<<dim3(Cq, BH), D, 0, s>>>(part, Cq, mzo);
+  va::probe_pass2_kernel<T, D><<<dim3(pg, va::PR_CSPLIT, BH), va::PR_THREADS,
+                                 va::probe_smem_bytes<D>(Ck), s>>>(
+      k, v, N, Cq, Ck, qc, nq, kc, vc, nk, koff, kperm, kassign, mzo, scale, err);
+  return launch_status();
+}
+
 template <typename T, int D>
 int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int Cq,
                    const int* kassign, int Ck, long long budget, float scale, int BH, int N,
@@ -727,18 +842,13 @@ int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int C
 
   // probe: err = NaN where a cluster is empty, else the proxy error
   if ((st = cuda_status(cudaMemsetAsync(err, 0xFF, sizeof(float) * bh * Cq * Ck, s)))) return st;
-  float *part, *mzo;
-  if ((st = scratch.alloc(&part, bh * Cq * va::PR_SPLIT * (D + 2))) ||
-      (st = scratch.alloc(&mzo, bh * Cq * (D + 2))))
-    return st;
-  const int pg = (Cq + va::PR_PG - 1) / va::PR_PG;
-  va::probe_pass1_kernel<T, D><<<dim3(pg, va::PR_SPLIT, BH), va::PR_THREADS,
-                                 va::probe_smem_bytes<D>(0), s>>>(k, v, N, Cq, qc, scale, part);
-  va::probe_combine_kernel<D><<<dim3(Cq, BH), D, 0, s>>>(part, Cq, mzo);
-  va::probe_pass2_kernel<T, D><<<dim3(pg, va::PR_CSPLIT, BH), va::PR_THREADS,
-                                 va::probe_smem_bytes<D>(Ck), s>>>(
-      k, v, N, Cq, Ck, qc, nq, kc, vc, nk, koff, kperm, kassign, mzo, scale, err);
-  if ((st = launch_status())) return st;
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128)
+    st = probe_tensor_cores(k, v, Cq, Ck, BH, N, nq, nk, koff, kperm, qc, vc, scale, err, scratch,
+                            s);
+  else
+    st = probe_simt<T, D>(k, v, Cq, Ck, BH, N, nq, nk, koff, kperm, kassign, qc, kc, vc, scale,
+                          err, scratch, s);
+  if (st) return st;
 
   // routing
   uint8_t* sel = sel_out;

@@ -147,6 +147,10 @@ ROUTE_CASES = [
     (331, 64, 6, 13, 0.0, "f32", False),
     (400, 128, 4, 11, 1.0, "f32", True),
     (700, 128, 9, 40, 0.15, "bf16", False),
+    # tensor-core probe: a ragged second proxy tile, empty clusters, many splits
+    (2500, 128, 130, 150, 0.1, "bf16", True),
+    # clusters longer than a 64-key tile
+    (1500, 128, 3, 7, 0.3, "bf16", False),
 ]
 
 
