@@ -22,11 +22,17 @@
 // shared-memory ring with its own full / empty barriers.
 #pragma once
 
+#include <type_traits>
+
 #include "attn_tc.cuh"
 
 namespace va {
 
 constexpr int CT_NM = 4;  // validity-mask ring entries
+// K and V ring depths (two stages each, as in the attention kernel).
+constexpr int CT_NK = 2;
+constexpr int CT_NV = 2;
+constexpr int CT_SMEM_BYTES = 1024 + TC_TILE_BYTES * (2 + CT_NK + CT_NV);
 // Register split of this kernel (launched at TC_LAUNCH_REGS per thread): the
 // producer's slot search needs more than the attention kernel's producer.
 constexpr int CT_REGS_DEC = 72;
@@ -56,10 +62,10 @@ struct CompArgs {
 enum : int {
   CB_Q_FULL = 0,                    // 2
   CB_K_FULL = CB_Q_FULL + 2,
-  CB_K_EMPTY = CB_K_FULL + TC_NK,
-  CB_V_FULL = CB_K_EMPTY + TC_NK,
-  CB_V_EMPTY = CB_V_FULL + TC_NV,
-  CB_M_FULL = CB_V_EMPTY + TC_NV,   // CT_NM
+  CB_K_EMPTY = CB_K_FULL + CT_NK,
+  CB_V_FULL = CB_K_EMPTY + CT_NK,
+  CB_V_EMPTY = CB_V_FULL + CT_NV,
+  CB_M_FULL = CB_V_EMPTY + CT_NV,   // CT_NM
   CB_M_EMPTY = CB_M_FULL + CT_NM,   // CT_NM, 128 arrivals
   CB_S_FULL = CB_M_EMPTY + CT_NM,   // 2
   CB_P_FULL = CB_S_FULL + 2,        // 2, 128 arrivals
@@ -92,7 +98,7 @@ __device__ __forceinline__ int ct_index(int t, int j, int n0, int n1) {
 // Softmax of one tile (thread r owns row r of the tile).
 __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const CompTile& T,
                                            int n0, int n1, int bh, uint32_t tmem,
-                                           uint64_t* bars, const uint32_t* masks,
+                                           uint64_t* bars, const float4* bias_ring,
                                            volatile int* abort_p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;
@@ -105,7 +111,6 @@ __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const Co
   const uint32_t bO = smem_u32(&bars[CB_O_DONE + tile]);
   const long long lim = a.wait_limit;
   const float sl2 = a.scale_log2;
-  const float* vb = a.vbias + (static_cast<long long>(bh) * a.Cq + T.p) * (a.nv * 128);
 
   float m_used = -INFINITY, l = 0.f;
   bool ok = true;
@@ -116,10 +121,6 @@ __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const Co
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bars[CB_M_FULL + ms]),
                                                            (u / CT_NM) & 1, lim, abort_p));
     if (!ok) break;
-    uint32_t mw[4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) mw[w] = masks[ms * 4 + w];
-    mbar_arrive(smem_u32(&bars[CB_M_EMPTY + ms]));
     tc_fence_after();
     float s[128];
 #pragma unroll
@@ -130,24 +131,17 @@ __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const Co
       for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
     }
     tmem_wait_ld();
-    if (j < a.nv) {
-      // virtual keys: scaled logit + log2 n_c (-inf for selected or empty c)
-      const float4* b4 = reinterpret_cast<const float4*>(vb + j * 128);
+    // scaled logit plus the entry's column bias (log2 units): log2 n_c of a
+    // virtual key (-inf for a selected or empty cluster), 0 / -inf for a
+    // valid / padding row of an exact tile
+    const float4* brow = bias_ring + ms * 32;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float4 bb = __ldg(b4 + i);
-        ffma2_bc(s[4 * i], s[4 * i + 1], s[4 * i], s[4 * i + 1], sl2, 0.f);
-        ffma2_bc(s[4 * i + 2], s[4 * i + 3], s[4 * i + 2], s[4 * i + 3], sl2, 0.f);
-        s[4 * i] += bb.x;
-        s[4 * i + 1] += bb.y;
-        s[4 * i + 2] += bb.z;
-        s[4 * i + 3] += bb.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 128; ++i)
-        s[i] = ((mw[i >> 5] >> (i & 31)) & 1u) ? s[i] * sl2 : -INFINITY;
+    for (int i = 0; i < 32; ++i) {
+      const float4 bb = brow[i];
+      ffma2_v(s[4 * i], s[4 * i + 1], s[4 * i], s[4 * i + 1], sl2, bb.x, bb.y);
+      ffma2_v(s[4 * i + 2], s[4 * i + 3], s[4 * i + 2], s[4 * i + 3], sl2, bb.z, bb.w);
     }
+    mbar_arrive(smem_u32(&bars[CB_M_EMPTY + ms]));
     float m0 = fmax3(s[0], s[1], s[2]), m1 = fmax3(s[3], s[4], s[5]);
     float m2 = fmax3(s[6], s[7], s[8]), m3 = fmax3(s[9], s[10], s[11]);
 #pragma unroll
@@ -260,7 +254,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                    const __grid_constant__ CUtensorMap map_v8, const CompArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[CB_COUNT];
-  __shared__ uint32_t masks[CT_NM * 4];
+  __shared__ float4 bias_ring[CT_NM * 32];  // per entry: 128 column biases
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
   __shared__ CompTile tiles[2];
@@ -275,7 +269,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sQ0 = smem_u32(smem);
   const uint32_t sK0 = sQ0 + 2 * TC_TILE_BYTES;
-  const uint32_t sV0 = sK0 + TC_NK * TC_TILE_BYTES;
+  const uint32_t sV0 = sK0 + CT_NK * TC_TILE_BYTES;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -290,11 +284,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(bar(CB_P_FULL + t), 128);
       mbar_init(bar(CB_O_DONE + t), 1);
     }
-    for (int s = 0; s < TC_NK; ++s) {
+    for (int s = 0; s < CT_NK; ++s) {
       mbar_init(bar(CB_K_FULL + s), 1);
       mbar_init(bar(CB_K_EMPTY + s), 1);
     }
-    for (int s = 0; s < TC_NV; ++s) {
+    for (int s = 0; s < CT_NV; ++s) {
       mbar_init(bar(CB_V_FULL + s), 1);
       mbar_init(bar(CB_V_EMPTY + s), 1);
     }
@@ -322,7 +316,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(CT_REGS_INC));
     const int tile = (warp - 4) >> 2;
     if (tile == 0 || has1)
-      ct_softmax(a, tile, tile == 0 ? T0 : T1, n0, n1, bh, tmem, bars, masks, abort_p);
+      ct_softmax(a, tile, tile == 0 ? T0 : T1, n0, n1, bh, tmem, bars, bias_ring, abort_p);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CT_REGS_DEC));
     if (warp == 0) {
@@ -346,26 +340,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tma_load_3d(sQ1 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 1), 64, T1.r0, bh);
         }
       }
+      // Slot lists of the two tiles; the slot of the next entry is read one
+      // entry ahead, so its global-memory latency overlaps this entry's waits.
+      const int* slots_bh = a.slots + a.slotbase[bh];
+      const int* so = a.slotoff + static_cast<long long>(bh) * (a.Cq + 1);
+      const int* slot_list0 = slots_bh + so[T0.p];
+      const int* slot_list1 = slots_bh + so[T1.p];
+      const float* vb0 = a.vbias + (static_cast<long long>(bh) * a.Cq + T0.p) * (a.nv * 128);
+      const float* vb1 = a.vbias + (static_cast<long long>(bh) * a.Cq + T1.p) * (a.nv * 128);
+      auto slot_of = [&](int u) -> int {
+        int t, j;
+        ct_entry(u, n0, n1, t, j);
+        const int* sl = t == 0 ? slot_list0 : slot_list1;
+        return (j >= a.nv && lane < 16) ? sl[(j - a.nv) * 16 + lane] : 0;
+      };
+      int sd_next = nent > 0 ? slot_of(0) : 0;
       for (int u = 0; u < nent; ++u) {
         int t, j;
         ct_entry(u, n0, n1, t, j);
-        const CompTile& T = t == 0 ? T0 : T1;
-        const int sk = u % TC_NK, sv = u % TC_NV, ms = u % CT_NM;
+        const int sk = u % CT_NK, sv = u % CT_NV, ms = u % CT_NM;
         const uint32_t sK = sK0 + sk * TC_TILE_BYTES, sV = sV0 + sv * TC_TILE_BYTES;
         // slot of this lane (exact tiles): source row and valid row count,
         // from the slot table (16 slots per exact tile, padding slots valid 0)
-        int src = 0, valid = 0;
-        if (j >= a.nv && lane < 16) {
-          const int sd = a.slots[a.slotbase[bh] +
-                                 a.slotoff[static_cast<long long>(bh) * (a.Cq + 1) + T.p] +
-                                 (j - a.nv) * 16 + lane];
-          src = sd >> 4;
-          valid = sd & 15;
-        }
+        const int sd = sd_next;
+        if (u + 1 < nent) sd_next = slot_of(u + 1);
+        const int src = sd >> 4, valid = sd & 15;
         bool ok = true;
         if (lane == 0) {
-          if (u >= TC_NK)
-            ok = mbar_wait_bounded(bar(CB_K_EMPTY + sk), ((u / TC_NK) & 1) ^ 1, lim, abort_p);
+          if (u >= CT_NK)
+            ok = mbar_wait_bounded(bar(CB_K_EMPTY + sk), ((u / CT_NK) & 1) ^ 1, lim, abort_p);
           if (ok) mbar_arrive_expect_tx(bar(CB_K_FULL + sk), TC_TILE_BYTES);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -380,8 +383,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         if (lane == 0) issued_k = u + 1;
         if (lane == 0) {
-          if (u >= TC_NV)
-            ok = mbar_wait_bounded(bar(CB_V_EMPTY + sv), ((u / TC_NV) & 1) ^ 1, lim, abort_p);
+          if (u >= CT_NV)
+            ok = mbar_wait_bounded(bar(CB_V_EMPTY + sv), ((u / CT_NV) & 1) ^ 1, lim, abort_p);
           if (ok) mbar_arrive_expect_tx(bar(CB_V_FULL + sv), TC_TILE_BYTES);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -395,27 +398,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tma_load_3d(sV + TC_HALF_BYTES + lane * 1024, &map_v8, bar(CB_V_FULL + sv), 64, src, bh);
         }
         if (lane == 0) issued_v = u + 1;
-        // validity mask of the entry's 128 key columns
-        const uint32_t byte = j < a.nv ? 0xFFu : ((1u << valid) - 1u) & 0xFFu;
-        uint32_t mwords[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint32_t acc = 0;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            acc |= __shfl_sync(0xffffffffu, byte, 4 * w + q) << (8 * q);
-          mwords[w] = acc;
+        // column biases of the entry (lane l: columns 4l..4l+3, rows 4 (l & 1)..
+        // of slot l / 2): the virtual bias row, or 0 / -inf for valid / padding
+        // slot rows
+        const int vslot = __shfl_sync(0xffffffffu, valid, lane >> 1);
+        float4 brow;
+        if (j < a.nv) {
+          brow = __ldg(reinterpret_cast<const float4*>((t == 0 ? vb0 : vb1) + j * 128) + lane);
+        } else {
+          const int r0 = (lane & 1) * 4;
+          brow.x = r0 + 0 < vslot ? 0.f : -INFINITY;
+          brow.y = r0 + 1 < vslot ? 0.f : -INFINITY;
+          brow.z = r0 + 2 < vslot ? 0.f : -INFINITY;
+          brow.w = r0 + 3 < vslot ? 0.f : -INFINITY;
         }
-        if (lane == 0) {
-          if (u >= CT_NM)
-            ok = mbar_wait_bounded(bar(CB_M_EMPTY + ms), ((u / CT_NM) & 1) ^ 1, lim, abort_p);
-          if (ok) {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) masks[ms * 4 + w] = mwords[w];
-            mbar_arrive(bar(CB_M_FULL + ms));
-          }
-        }
+        if (lane == 0 && u >= CT_NM)
+          ok = mbar_wait_bounded(bar(CB_M_EMPTY + ms), ((u / CT_NM) & 1) ^ 1, lim, abort_p);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        bias_ring[ms * 32 + lane] = brow;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(CB_M_FULL + ms));
       }
       if (lane == 0 && *abort_p) {
         volatile int no_abort = 0;
@@ -424,13 +426,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           no_abort = 0;
           mbar_wait_bounded(bar(CB_Q_FULL + 1), 0, lim, &no_abort);
         }
-        for (int u = issued_k > TC_NK ? issued_k - TC_NK : 0; u < issued_k; ++u) {
+        for (int u = issued_k > CT_NK ? issued_k - CT_NK : 0; u < issued_k; ++u) {
           no_abort = 0;
-          mbar_wait_bounded(bar(CB_K_FULL + u % TC_NK), (u / TC_NK) & 1, lim, &no_abort);
+          mbar_wait_bounded(bar(CB_K_FULL + u % CT_NK), (u / CT_NK) & 1, lim, &no_abort);
         }
-        for (int u = issued_v > TC_NV ? issued_v - TC_NV : 0; u < issued_v; ++u) {
+        for (int u = issued_v > CT_NV ? issued_v - CT_NV : 0; u < issued_v; ++u) {
           no_abort = 0;
-          mbar_wait_bounded(bar(CB_V_FULL + u % TC_NV), (u / TC_NV) & 1, lim, &no_abort);
+          mbar_wait_bounded(bar(CB_V_FULL + u % CT_NV), (u / CT_NV) & 1, lim, &no_abort);
         }
       }
     } else if (warp == 1) {
@@ -439,39 +441,50 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
         bool ok = mbar_wait_bounded(bar(CB_Q_FULL + 0), 0, lim, abort_p);
         if (ok && has1) ok = mbar_wait_bounded(bar(CB_Q_FULL + 1), 0, lim, abort_p);
-        int pend[2] = {-1, -1};
-        int cnt[2] = {0, 0};
-        auto issue_pv = [&](int t) -> bool {
-          const int pu = pend[t];
-          const int jj = cnt[t] - 1;
+        // Per-tile state in scalars selected at compile time: an array indexed
+        // by the runtime tile number would live in local memory.
+        int pend0 = -1, pend1 = -1;  // entry whose PV is still to issue
+        int cnt0 = 0, cnt1 = 0;      // QKs issued
+        using Tile0 = std::integral_constant<int, 0>;
+        using Tile1 = std::integral_constant<int, 1>;
+        auto issue_pv = [&](auto tile) -> bool {
+          constexpr int t = decltype(tile)::value;
+          int& pend = t == 0 ? pend0 : pend1;
+          const int pu = pend;
+          const int jj = (t == 0 ? cnt0 : cnt1) - 1;
           if (!mbar_wait_bounded(bar(CB_P_FULL + t), jj & 1, lim, abort_p)) return false;
-          const int sv = pu % TC_NV;
-          if (!mbar_wait_bounded(bar(CB_V_FULL + sv), (pu / TC_NV) & 1, lim, abort_p)) return false;
+          const int sv = pu % CT_NV;
+          if (!mbar_wait_bounded(bar(CB_V_FULL + sv), (pu / CT_NV) & 1, lim, abort_p)) return false;
           tc_fence_after();
           tc_issue_pv(tmem + t * 256 + 128, tmem + t * 256, sV0 + sv * TC_TILE_BYTES, jj > 0);
           umma_commit(bar(CB_O_DONE + t));
           umma_commit(bar(CB_V_EMPTY + sv));  // every entry is read by one tile only
-          pend[t] = -1;
+          pend = -1;
+          return true;
+        };
+        auto issue_entry = [&](auto tile, int u) -> bool {
+          constexpr int t = decltype(tile)::value;
+          const int sk = u % CT_NK;
+          if (!mbar_wait_bounded(bar(CB_K_FULL + sk), (u / CT_NK) & 1, lim, abort_p)) return false;
+          if ((t == 0 ? pend0 : pend1) >= 0 && !issue_pv(tile)) return false;
+          tc_fence_after();
+          tc_issue_qk(tmem + t * 256, t == 0 ? sQ0 : sQ1, sK0 + sk * TC_TILE_BYTES);
+          umma_commit(bar(CB_S_FULL + t));
+          umma_commit(bar(CB_K_EMPTY + sk));
+          (t == 0 ? pend0 : pend1) = u;
+          ++(t == 0 ? cnt0 : cnt1);
           return true;
         };
         for (int u = 0; ok && u < nent; ++u) {
           int t, j;
           ct_entry(u, n0, n1, t, j);
           // A V stage is reloaded NV entries later: release stale pending PVs.
-          if (pend[0] >= 0 && pend[0] <= u - TC_NV && !(ok = issue_pv(0))) break;
-          if (pend[1] >= 0 && pend[1] <= u - TC_NV && !(ok = issue_pv(1))) break;
-          const int sk = u % TC_NK;
-          if (!(ok = mbar_wait_bounded(bar(CB_K_FULL + sk), (u / TC_NK) & 1, lim, abort_p))) break;
-          if (pend[t] >= 0 && !(ok = issue_pv(t))) break;
-          tc_fence_after();
-          tc_issue_qk(tmem + t * 256, t == 0 ? sQ0 : sQ1, sK0 + sk * TC_TILE_BYTES);
-          umma_commit(bar(CB_S_FULL + t));
-          umma_commit(bar(CB_K_EMPTY + sk));
-          pend[t] = u;
-          ++cnt[t];
+          if (pend0 >= 0 && pend0 <= u - CT_NV && !(ok = issue_pv(Tile0{}))) break;
+          if (pend1 >= 0 && pend1 <= u - CT_NV && !(ok = issue_pv(Tile1{}))) break;
+          ok = t == 0 ? issue_entry(Tile0{}, u) : issue_entry(Tile1{}, u);
         }
-        if (ok && pend[0] >= 0) ok = issue_pv(0);
-        if (ok && pend[1] >= 0) ok = issue_pv(1);
+        if (ok && pend0 >= 0) ok = issue_pv(Tile0{});
+        if (ok && pend1 >= 0) ok = issue_pv(Tile1{});
         if (!ok) {
           umma_commit(bar(CB_DRAIN));
           volatile int no_abort = 0;

@@ -8,14 +8,16 @@
 // exact-product bf16 MMAs accumulated in one fp32 TMEM accumulator (K = 256).
 // dist(i, c) = |c|^2 - 2 x_i . c; the argmin takes the lowest c on ties.
 //
-// One CTA per (batch*head, 128-point tile); 256 threads:
-//   warp 0      TMA producer: the point tile once, then the hi and lo halves
-//               of every 128-cluster tile into a ring of KA_NS stages;
-//   warp 1      MMA issuer: cluster tile t into TMEM accumulator t & 1;
+// One CTA per (batch*head, pair of 128-point tiles); 256 threads:
+//   warp 0      TMA producer: the two point tiles once, then the hi and lo
+//               halves of every 128-cluster tile into a ring of KA_NS stages
+//               (each cluster tile is fetched once for both point tiles);
+//   warp 1      MMA issuer: cluster tile t against point tile q into TMEM
+//               columns [256 (t & 1) + 128 q, +128);
 //   warps 2, 3  idle;
-//   warps 4..7  argmin epilogue, thread r owns point r (TMEM lane r); the
-//               accumulator is released right after tcgen05.ld, so the next
-//               tile's MMAs overlap this tile's comparisons.
+//   warps 4..7  argmin epilogue, thread r owns point r of both tiles (TMEM
+//               lane r); a buffer is released right after its tcgen05.ld, so
+//               the next cluster tile's MMAs overlap these comparisons.
 // Every mbarrier wait is bounded; see attn_tc.cuh for the timeout protocol.
 #pragma once
 
@@ -27,7 +29,8 @@ constexpr int KA_THREADS = 256;
 constexpr int KA_NS = 2;
 constexpr int KA_TILE = 128 * 128 * 2;   // 32 KB: 128 rows x 128 bf16
 constexpr int KA_HALF = KA_TILE / 2;
-constexpr int KA_SMEM_BYTES = 1024 + KA_TILE * (1 + 2 * KA_NS);
+constexpr int KA_PTS = 2;  // 128-point tiles per CTA
+constexpr int KA_SMEM_BYTES = 1024 + KA_TILE * (KA_PTS + 2 * KA_NS);
 
 enum : int {
   KB_X_FULL = 0,
@@ -63,10 +66,10 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
   __shared__ int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const uint32_t sX = smem_u32(smem);
-  const uint32_t sC0 = sX + KA_TILE;  // stage s: hi at sC0 + 2 s TILE, lo right after
+  const uint32_t sX = smem_u32(smem);  // point tile q at sX + q TILE
+  const uint32_t sC0 = sX + KA_PTS * KA_TILE;  // stage s: hi at sC0 + 2 s TILE, lo right after
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.y, i0 = blockIdx.x * 128;
+  const int bh = blockIdx.y, i0 = blockIdx.x * 128 * KA_PTS;
   const int ntiles = (C + 127) / 128;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_base_s), 256);
+    tmem_alloc(smem_u32(&tmem_base_s), 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -99,9 +102,11 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
       tma_prefetch_desc(&map_x);
       tma_prefetch_desc(&map_hi);
       tma_prefetch_desc(&map_lo);
-      mbar_arrive_expect_tx(bar(KB_X_FULL), KA_TILE);
-      tma_load_3d(sX, &map_x, bar(KB_X_FULL), 0, i0, bh);
-      tma_load_3d(sX + KA_HALF, &map_x, bar(KB_X_FULL), 64, i0, bh);
+      mbar_arrive_expect_tx(bar(KB_X_FULL), KA_PTS * KA_TILE);
+      for (int q = 0; q < KA_PTS; ++q) {
+        tma_load_3d(sX + q * KA_TILE, &map_x, bar(KB_X_FULL), 0, i0 + 128 * q, bh);
+        tma_load_3d(sX + q * KA_TILE + KA_HALF, &map_x, bar(KB_X_FULL), 64, i0 + 128 * q, bh);
+      }
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % KA_NS;
@@ -136,8 +141,11 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
           break;
         tc_fence_after();
         const uint32_t hi = sC0 + 2 * s * KA_TILE, lo = hi + KA_TILE;
-        ka_issue(tmem + b * 128, sX, hi, false);
-        ka_issue(tmem + b * 128, sX, lo, true);
+#pragma unroll
+        for (int q = 0; q < KA_PTS; ++q) {
+          ka_issue(tmem + b * 256 + q * 128, sX + q * KA_TILE, hi, false);
+          ka_issue(tmem + b * 256 + q * 128, sX + q * KA_TILE, lo, true);
+        }
         umma_commit(bar(KB_C_EMPTY + s));
         umma_commit(bar(KB_ACC_FULL + b));
       }
@@ -152,8 +160,13 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const float* cn = cnorm + static_cast<long long>(bh) * C;
-    float best = INFINITY;
-    int besti = 0x7fffffff;
+    float best[KA_PTS];
+    int besti[KA_PTS];
+#pragma unroll
+    for (int q = 0; q < KA_PTS; ++q) {
+      best[q] = INFINITY;
+      besti[q] = 0x7fffffff;
+    }
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
       const int b = t & 1;
@@ -161,52 +174,64 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
                       mbar_wait_bounded(bar(KB_ACC_FULL + b), (t >> 1) & 1, lim, abort_p));
       if (!ok) break;
       tc_fence_after();
-      float acc[128];
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t v[32];
-        tmem_ld32(tmem + b * 128 + lane_off + c4 * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) acc[c4 * 32 + i] = __uint_as_float(v[i]);
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(KB_ACC_EMPTY + b));
       const int c0 = t * 128;
       const int nc = min(128, C - c0);
-      if (nc == 128) {
+#pragma unroll 1
+      for (int q = 0; q < KA_PTS; ++q) {
+        float acc[128];
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          const float dist = fmaf(-2.f, acc[i], __ldg(cn + c0 + i));
-          if (dist < best) {
-            best = dist;
-            besti = c0 + i;
-          }
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t v[32];
+          tmem_ld32(tmem + b * 256 + q * 128 + lane_off + c4 * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c4 * 32 + i] = __uint_as_float(v[i]);
         }
-      } else {
+        tmem_wait_ld();
+        if (q == KA_PTS - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(KB_ACC_EMPTY + b));
+        }
+        float bq = best[q];
+        int iq = besti[q];
+        if (nc == 128) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          if (i < nc) {
+          for (int i = 0; i < 128; ++i) {
             const float dist = fmaf(-2.f, acc[i], __ldg(cn + c0 + i));
-            if (dist < best) {
-              best = dist;
-              besti = c0 + i;
+            if (dist < bq) {
+              bq = dist;
+              iq = c0 + i;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            if (i < nc) {
+              const float dist = fmaf(-2.f, acc[i], __ldg(cn + c0 + i));
+              if (dist < bq) {
+                bq = dist;
+                iq = c0 + i;
+              }
             }
           }
         }
+        best[q] = bq;
+        besti[q] = iq;
       }
     }
-    const int i = i0 + r;
-    if (ok && i < N) {
-      assign[static_cast<long long>(bh) * N + i] = besti;
-      atomicAdd(&count[static_cast<long long>(bh) * C + besti], 1);
+#pragma unroll
+    for (int q = 0; q < KA_PTS; ++q) {
+      const int i = i0 + 128 * q + r;
+      if (ok && i < N) {
+        assign[static_cast<long long>(bh) * N + i] = besti[q];
+        atomicAdd(&count[static_cast<long long>(bh) * C + besti[q]], 1);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 // c = hi + lo with hi = bf16(c) and lo = bf16(c - hi), for [rows, 128] fp32.

@@ -500,7 +500,7 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C
       (st = encode_bf16_rows(&ml, lo, BH, C, 128)))
     return st;
   const dim3 gc((C + 7) / 8, BH);
-  const dim3 ga((N + 127) / 128, BH);
+  const dim3 ga((N + 128 * va::KA_PTS - 1) / (128 * va::KA_PTS), BH);
   const dim3 gn((N + 255) / 256, BH);
   const unsigned gs = static_cast<unsigned>((nc + 255) / 256);
   va::km_init_kernel<__nv_bfloat16, 128><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
@@ -606,7 +606,7 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
     if (fa.numRegs != va::TC_LAUNCH_REGS) return VA_ERR_UNSUPPORTED;
     if ((st = cuda_status(cudaFuncSetAttribute(va::comp_tc_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::TC_SMEM_BYTES))))
+                                               va::CT_SMEM_BYTES))))
       return st;
     configured[dev] = true;
   }
@@ -682,7 +682,7 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit = g_wait_limit;
   const int max_chunks = (N + 127) / 128 + Cq;
-  va::comp_tc_kernel<<<dim3((max_chunks + 1) / 2, BH), va::TC_THREADS, va::TC_SMEM_BYTES, s>>>(
+  va::comp_tc_kernel<<<dim3((max_chunks + 1) / 2, BH), va::TC_THREADS, va::CT_SMEM_BYTES, s>>>(
       mq, mkc, mvc, mk8, mv8, a);
   return launch_status();
 }
