@@ -9,17 +9,20 @@
 // cluster is a contiguous row range of Qs and a key cluster one of Ks / Vs.
 // A work unit is one 128-row chunk of one query cluster; a CTA takes two
 // chunks (tiles t = 0, 1) whose key streams are interleaved entry by entry,
-// reusing the two-tile pipeline of attn_tc.cuh (TMA producer warp, one MMA
-// thread, one softmax warpgroup per tile; S_t and O_t in TMEM).
+// reusing the two-tile pipeline of attn_tc.cuh (one MMA thread, one softmax
+// warpgroup per tile, S_t and O_t in TMEM), with two TMA producer warps: one
+// for Q, K and the column biases, one for V.
 //
 // Key stream of a query cluster p: nv virtual tiles (centroids 128j ..
 // 128j + 127, one TMA box each for K and V), then exact tiles of 16 slots.
 // A slot is 8 consecutive rows of one selected key cluster (an 8-row TMA box,
 // which lands on a whole 128B-swizzle atom, so slots assemble into the same
 // shared-memory layout as one 128-row box); a cluster of n_c keys takes
-// ceil(n_c / 8) slots and the rows past n_c are masked. The producer passes
-// each entry's 128-bit validity mask to the softmax through a small
-// shared-memory ring with its own full / empty barriers.
+// ceil(n_c / 8) slots and the rows past n_c are masked. The K producer passes
+// each entry's 128 column biases (log2 n_c of a virtual key, -inf for a
+// selected or empty cluster; 0 / -inf for a valid / padding slot row) to the
+// softmax through a small shared-memory ring with its own full / empty
+// barriers; the softmax adds them with the logit scaling in one packed FMA.
 #pragma once
 
 #include <type_traits>
@@ -319,25 +322,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       ct_softmax(a, tile, tile == 0 ? T0 : T1, n0, n1, bh, tmem, bars, bias_ring, abort_p);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CT_REGS_DEC));
-    if (warp == 0) {
-      // ---------------------------------------------------------- producer --
-      // The whole warp walks the stream; lane 0 waits and arms the barriers,
-      // lanes 0..15 issue one slot's copies each.
-      int issued_k = 0, issued_v = 0;
+    if (warp == 0 || warp == 2) {
+      // --------------------------------------------------------- producers --
+      // Warp 0: the Q tiles, then the K copies and the column biases of every
+      // entry; warp 2: the V copies. Each walks the whole stream on its own,
+      // so K never waits behind a V stage (which frees only when an earlier
+      // PV completed). Lane 0 waits and arms the barriers, lanes 0..15 issue
+      // one slot's copies each.
+      const bool kw = warp == 0;
+      int issued = 0;
       if (lane == 0) {
-        tma_prefetch_desc(&map_q);
-        tma_prefetch_desc(&map_kc);
-        tma_prefetch_desc(&map_vc);
-        tma_prefetch_desc(&map_k8);
-        tma_prefetch_desc(&map_v8);
-        mbar_arrive_expect_tx(bar(CB_Q_FULL + 0), TC_TILE_BYTES);
-        tma_load_3d(sQ0, &map_q, bar(CB_Q_FULL + 0), 0, T0.r0, bh);
-        tma_load_3d(sQ0 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 0), 64, T0.r0, bh);
-        if (has1) {
-          const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
-          mbar_arrive_expect_tx(bar(CB_Q_FULL + 1), TC_TILE_BYTES);
-          tma_load_3d(sQ1, &map_q, bar(CB_Q_FULL + 1), 0, T1.r0, bh);
-          tma_load_3d(sQ1 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 1), 64, T1.r0, bh);
+        if (kw) {
+          tma_prefetch_desc(&map_q);
+          tma_prefetch_desc(&map_kc);
+          tma_prefetch_desc(&map_k8);
+          mbar_arrive_expect_tx(bar(CB_Q_FULL + 0), TC_TILE_BYTES);
+          tma_load_3d(sQ0, &map_q, bar(CB_Q_FULL + 0), 0, T0.r0, bh);
+          tma_load_3d(sQ0 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 0), 64, T0.r0, bh);
+          if (has1) {
+            const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
+            mbar_arrive_expect_tx(bar(CB_Q_FULL + 1), TC_TILE_BYTES);
+            tma_load_3d(sQ1, &map_q, bar(CB_Q_FULL + 1), 0, T1.r0, bh);
+            tma_load_3d(sQ1 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 1), 64, T1.r0, bh);
+          }
+        } else {
+          tma_prefetch_desc(&map_vc);
+          tma_prefetch_desc(&map_v8);
         }
       }
       // Slot lists of the two tiles; the slot of the next entry is read one
@@ -354,12 +364,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int* sl = t == 0 ? slot_list0 : slot_list1;
         return (j >= a.nv && lane < 16) ? sl[(j - a.nv) * 16 + lane] : 0;
       };
+      const CUtensorMap* map_c = kw ? &map_kc : &map_vc;  // centroid rows (virtual tiles)
+      const CUtensorMap* map_8 = kw ? &map_k8 : &map_v8;  // 8-row slots (exact tiles)
+      const int nst = kw ? CT_NK : CT_NV;
+      const int b_full = kw ? CB_K_FULL : CB_V_FULL, b_empty = kw ? CB_K_EMPTY : CB_V_EMPTY;
+      const uint32_t s0 = kw ? sK0 : sV0;
       int sd_next = nent > 0 ? slot_of(0) : 0;
       for (int u = 0; u < nent; ++u) {
         int t, j;
         ct_entry(u, n0, n1, t, j);
-        const int sk = u % CT_NK, sv = u % CT_NV, ms = u % CT_NM;
-        const uint32_t sK = sK0 + sk * TC_TILE_BYTES, sV = sV0 + sv * TC_TILE_BYTES;
+        const int st = u % nst;
+        const uint32_t dst = s0 + st * TC_TILE_BYTES;
         // slot of this lane (exact tiles): source row and valid row count,
         // from the slot table (16 slots per exact tile, padding slots valid 0)
         const int sd = sd_next;
@@ -367,40 +382,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int src = sd >> 4, valid = sd & 15;
         bool ok = true;
         if (lane == 0) {
-          if (u >= CT_NK)
-            ok = mbar_wait_bounded(bar(CB_K_EMPTY + sk), ((u / CT_NK) & 1) ^ 1, lim, abort_p);
-          if (ok) mbar_arrive_expect_tx(bar(CB_K_FULL + sk), TC_TILE_BYTES);
+          if (u >= nst)
+            ok = mbar_wait_bounded(bar(b_empty + st), ((u / nst) & 1) ^ 1, lim, abort_p);
+          if (ok) mbar_arrive_expect_tx(bar(b_full + st), TC_TILE_BYTES);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         if (j < a.nv) {
           if (lane == 0) {
-            tma_load_3d(sK, &map_kc, bar(CB_K_FULL + sk), 0, j * 128, bh);
-            tma_load_3d(sK + TC_HALF_BYTES, &map_kc, bar(CB_K_FULL + sk), 64, j * 128, bh);
+            tma_load_3d(dst, map_c, bar(b_full + st), 0, j * 128, bh);
+            tma_load_3d(dst + TC_HALF_BYTES, map_c, bar(b_full + st), 64, j * 128, bh);
           }
         } else if (lane < 16) {
-          tma_load_3d(sK + lane * 1024, &map_k8, bar(CB_K_FULL + sk), 0, src, bh);
-          tma_load_3d(sK + TC_HALF_BYTES + lane * 1024, &map_k8, bar(CB_K_FULL + sk), 64, src, bh);
+          tma_load_3d(dst + lane * 1024, map_8, bar(b_full + st), 0, src, bh);
+          tma_load_3d(dst + TC_HALF_BYTES + lane * 1024, map_8, bar(b_full + st), 64, src, bh);
         }
-        if (lane == 0) issued_k = u + 1;
-        if (lane == 0) {
-          if (u >= CT_NV)
-            ok = mbar_wait_bounded(bar(CB_V_EMPTY + sv), ((u / CT_NV) & 1) ^ 1, lim, abort_p);
-          if (ok) mbar_arrive_expect_tx(bar(CB_V_FULL + sv), TC_TILE_BYTES);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        if (j < a.nv) {
-          if (lane == 0) {
-            tma_load_3d(sV, &map_vc, bar(CB_V_FULL + sv), 0, j * 128, bh);
-            tma_load_3d(sV + TC_HALF_BYTES, &map_vc, bar(CB_V_FULL + sv), 64, j * 128, bh);
-          }
-        } else if (lane < 16) {
-          tma_load_3d(sV + lane * 1024, &map_v8, bar(CB_V_FULL + sv), 0, src, bh);
-          tma_load_3d(sV + TC_HALF_BYTES + lane * 1024, &map_v8, bar(CB_V_FULL + sv), 64, src, bh);
-        }
-        if (lane == 0) issued_v = u + 1;
+        if (lane == 0) issued = u + 1;
+        if (!kw) continue;
         // column biases of the entry (lane l: columns 4l..4l+3, rows 4 (l & 1)..
         // of slot l / 2): the virtual bias row, or 0 / -inf for valid / padding
         // slot rows
+        const int ms = u % CT_NM;
         const int vslot = __shfl_sync(0xffffffffu, valid, lane >> 1);
         float4 brow;
         if (j < a.nv) {
@@ -420,19 +421,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) mbar_arrive(bar(CB_M_FULL + ms));
       }
       if (lane == 0 && *abort_p) {
+        // Drain: only the last nst copies of a ring can still be in flight.
         volatile int no_abort = 0;
-        mbar_wait_bounded(bar(CB_Q_FULL + 0), 0, lim, &no_abort);
-        if (has1) {
-          no_abort = 0;
-          mbar_wait_bounded(bar(CB_Q_FULL + 1), 0, lim, &no_abort);
+        if (kw) {
+          mbar_wait_bounded(bar(CB_Q_FULL + 0), 0, lim, &no_abort);
+          if (has1) {
+            no_abort = 0;
+            mbar_wait_bounded(bar(CB_Q_FULL + 1), 0, lim, &no_abort);
+          }
         }
-        for (int u = issued_k > CT_NK ? issued_k - CT_NK : 0; u < issued_k; ++u) {
+        for (int u = issued > nst ? issued - nst : 0; u < issued; ++u) {
           no_abort = 0;
-          mbar_wait_bounded(bar(CB_K_FULL + u % CT_NK), (u / CT_NK) & 1, lim, &no_abort);
-        }
-        for (int u = issued_v > CT_NV ? issued_v - CT_NV : 0; u < issued_v; ++u) {
-          no_abort = 0;
-          mbar_wait_bounded(bar(CB_V_FULL + u % CT_NV), (u / CT_NV) & 1, lim, &no_abort);
+          mbar_wait_bounded(bar(b_full + u % nst), (u / nst) & 1, lim, &no_abort);
         }
       }
     } else if (warp == 1) {
