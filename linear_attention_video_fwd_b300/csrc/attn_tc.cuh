@@ -137,19 +137,6 @@ __device__ __forceinline__ void ffma2_bc(float& d0, float& d1, float a0, float a
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
 
-// (d0, d1) = (a0 * b + c0, a1 * b + c1) as one packed f32x2 FMA.
-__device__ __forceinline__ void ffma2_v(float& d0, float& d1, float a0, float a1, float b,
-                                        float c0, float c1) {
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rb, {%4, %4};\n\t"
-      "mov.b64 rc, {%5, %6};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
-      "mov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
-}
-
 // (s0, s1) += (a0, a1) as one packed f32x2 add.
 __device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float a1) {
   asm("{\n\t.reg .b64 ra, rs;\n\t"
