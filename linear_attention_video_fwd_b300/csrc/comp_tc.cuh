@@ -77,6 +77,14 @@ enum : int {
   CB_COUNT = CB_DRAIN + 1
 };
 
+// Row maps of the cluster-ordered K and V with box heights 8 << i (i < 5):
+// a run of 2^i consecutive slots with contiguous source rows is one copy.
+constexpr int CT_NBOX = 5;
+struct CompSlotMaps {
+  CUtensorMap k[CT_NBOX];
+  CUtensorMap v[CT_NBOX];
+};
+
 struct CompTile {
   int p, r0, nrows, ns, nslots, n;  // cluster, first row, rows, selected, slots, blocks
 };
@@ -253,8 +261,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     comp_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_kc,
                    const __grid_constant__ CUtensorMap map_vc,
-                   const __grid_constant__ CUtensorMap map_k8,
-                   const __grid_constant__ CUtensorMap map_v8, const CompArgs a) {
+                   const __grid_constant__ CompSlotMaps maps, const CompArgs a) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[CB_COUNT];
   __shared__ float4 bias_ring[CT_NM * 32];  // per entry: 128 column biases
@@ -335,7 +342,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (kw) {
           tma_prefetch_desc(&map_q);
           tma_prefetch_desc(&map_kc);
-          tma_prefetch_desc(&map_k8);
+          for (int i = 0; i < CT_NBOX; ++i) tma_prefetch_desc(&maps.k[i]);
           mbar_arrive_expect_tx(bar(CB_Q_FULL + 0), TC_TILE_BYTES);
           tma_load_3d(sQ0, &map_q, bar(CB_Q_FULL + 0), 0, T0.r0, bh);
           tma_load_3d(sQ0 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 0), 64, T0.r0, bh);
@@ -347,7 +354,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         } else {
           tma_prefetch_desc(&map_vc);
-          tma_prefetch_desc(&map_v8);
+          for (int i = 0; i < CT_NBOX; ++i) tma_prefetch_desc(&maps.v[i]);
         }
       }
       // Slot lists of the two tiles; the slot of the next entry is read one
@@ -365,7 +372,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         return (j >= a.nv && lane < 16) ? sl[(j - a.nv) * 16 + lane] : 0;
       };
       const CUtensorMap* map_c = kw ? &map_kc : &map_vc;  // centroid rows (virtual tiles)
-      const CUtensorMap* map_8 = kw ? &map_k8 : &map_v8;  // 8-row slots (exact tiles)
+      const CUtensorMap* map_slots = kw ? maps.k : maps.v;  // slot runs (exact tiles)
       const int nst = kw ? CT_NK : CT_NV;
       const int b_full = kw ? CB_K_FULL : CB_V_FULL, b_empty = kw ? CB_K_EMPTY : CB_V_EMPTY;
       const uint32_t s0 = kw ? sK0 : sV0;
@@ -392,9 +399,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             tma_load_3d(dst, map_c, bar(b_full + st), 0, j * 128, bh);
             tma_load_3d(dst + TC_HALF_BYTES, map_c, bar(b_full + st), 64, j * 128, bh);
           }
-        } else if (lane < 16) {
-          tma_load_3d(dst + lane * 1024, map_8, bar(b_full + st), 0, src, bh);
-          tma_load_3d(dst + TC_HALF_BYTES + lane * 1024, map_8, bar(b_full + st), 64, src, bh);
+        } else {
+          // Runs of slots with contiguous source rows (slot l continues slot
+          // l - 1 when its first row is 8 further) are copied as greedy
+          // power-of-two pieces, each one box of 8 * 2^i rows issued by the
+          // lane of its first slot; together they cover the 16 slots once.
+          const int prev = __shfl_up_sync(0xffffffffu, src, 1);
+          const bool starts_run = lane < 16 && (lane == 0 || src != prev + 8);
+          const uint32_t starts = __ballot_sync(0xffffffffu, starts_run);
+          if (lane < 16) {
+            const uint32_t upto = starts & ((2u << lane) - 1u);
+            const int r0 = 31 - __clz(upto);
+            const uint32_t above = starts & ~((2u << lane) - 1u);
+            const int r1 = above ? __ffs(above) - 1 : 16;
+            const int n = r1 - r0, pos = lane - r0;
+            int lg = -1;
+            for (int at = 0; at < n;) {
+              const int l2 = 31 - __clz(n - at);
+              if (at == pos) lg = l2;
+              at += 1 << l2;
+            }
+            if (lg >= 0) {
+              tma_load_3d(dst + lane * 1024, map_slots + lg, bar(b_full + st), 0, src, bh);
+              tma_load_3d(dst + TC_HALF_BYTES + lane * 1024, map_slots + lg, bar(b_full + st), 64,
+                          src, bh);
+            }
+          }
         }
         if (lane == 0) issued = u + 1;
         if (!kw) continue;

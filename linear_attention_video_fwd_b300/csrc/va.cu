@@ -654,13 +654,16 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   va::slot_fill_kernel<<<dim3(Cq, BH), 256, 0, s>>>(koff, seln, selc, selbox, Cq, Ck, slbase,
                                                    sloff, slots);
   if ((st = launch_status())) return st;
-  CUtensorMap mq, mkc, mvc, mk8, mv8;
+  CUtensorMap mq, mkc, mvc;
+  va::CompSlotMaps slot_maps;
   if ((st = encode_bf16_rows_box(&mq, qs, BH, N, 128, 128)) ||
       (st = encode_bf16_rows_box(&mkc, kcb, BH, Ck, 128, 128)) ||
-      (st = encode_bf16_rows_box(&mvc, vcb, BH, Ck, 128, 128)) ||
-      (st = encode_bf16_rows_box(&mk8, ks, BH, N, 128, 8)) ||
-      (st = encode_bf16_rows_box(&mv8, vs, BH, N, 128, 8)))
+      (st = encode_bf16_rows_box(&mvc, vcb, BH, Ck, 128, 128)))
     return st;
+  for (int i = 0; i < va::CT_NBOX; ++i)
+    if ((st = encode_bf16_rows_box(&slot_maps.k[i], ks, BH, N, 128, 8 << i)) ||
+        (st = encode_bf16_rows_box(&slot_maps.v[i], vs, BH, N, 128, 8 << i)))
+      return st;
   va::CompArgs a;
   a.choff = choff;
   a.qoff = qoff;
@@ -683,7 +686,7 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   a.wait_limit = g_wait_limit;
   const int max_chunks = (N + 127) / 128 + Cq;
   va::comp_tc_kernel<<<dim3((max_chunks + 1) / 2, BH), va::TC_THREADS, va::CT_SMEM_BYTES, s>>>(
-      mq, mkc, mvc, mk8, mv8, a);
+      mq, mkc, mvc, slot_maps, a);
   return launch_status();
 }
 
