@@ -8,16 +8,20 @@
 // exact-product bf16 MMAs accumulated in one fp32 TMEM accumulator (K = 256).
 // dist(i, c) = |c|^2 - 2 x_i . c; the argmin takes the lowest c on ties.
 //
-// One CTA per (batch*head, pair of 128-point tiles); 256 threads:
-//   warp 0      TMA producer: the two point tiles once, then the hi and lo
-//               halves of every 128-cluster tile into a ring of KA_NS stages
-//               (each cluster tile is fetched once for both point tiles);
-//   warp 1      MMA issuer: cluster tile t against point tile q into TMEM
-//               columns [256 (t & 1) + 128 q, +128);
+// Persistent CTAs with resident centroids: CTA (split, chunk, batch*head)
+// holds the hi and lo halves of one chunk of 256 clusters in shared memory
+// (128 KB) and streams its share of the 128-point tiles through a two-stage
+// TMA ring; the accumulators of consecutive point tiles alternate between two
+// TMEM halves, so the argmin of one tile overlaps the MMAs of the next. With
+// several chunks the per-chunk (distance, index) results are merged by
+// ka_merge_kernel in chunk order (strict <, so the lowest index still wins
+// ties). 256 threads:
+//   warp 0      TMA producer: the centroid chunk once, then the point tiles;
+//   warp 1      MMA issuer: point tile i against cluster tiles 0, 1 into TMEM
+//               columns [256 (i & 1) + 128 t, +128);
 //   warps 2, 3  idle;
-//   warps 4..7  argmin epilogue, thread r owns point r of both tiles (TMEM
-//               lane r); a buffer is released right after its tcgen05.ld, so
-//               the next cluster tile's MMAs overlap these comparisons.
+//   warps 4..7  argmin epilogue, thread r owns point r of the tile (TMEM lane
+//               r); the accumulators are released right after tcgen05.ld.
 // Every mbarrier wait is bounded; see attn_tc.cuh for the timeout protocol.
 #pragma once
 
@@ -26,17 +30,17 @@
 namespace va {
 
 constexpr int KA_THREADS = 256;
-constexpr int KA_NS = 2;
+constexpr int KA_CHUNK = 256;            // clusters resident per CTA
 constexpr int KA_TILE = 128 * 128 * 2;   // 32 KB: 128 rows x 128 bf16
 constexpr int KA_HALF = KA_TILE / 2;
-constexpr int KA_PTS = 2;  // 128-point tiles per CTA
-constexpr int KA_SMEM_BYTES = 1024 + KA_TILE * (KA_PTS + 2 * KA_NS);
+constexpr int KA_NX = 2;                 // point-tile ring stages
+constexpr int KA_SMEM_BYTES = 1024 + KA_TILE * (4 + KA_NX);
 
 enum : int {
-  KB_X_FULL = 0,
-  KB_C_FULL = 1,
-  KB_C_EMPTY = KB_C_FULL + KA_NS,
-  KB_ACC_FULL = KB_C_EMPTY + KA_NS,   // 2
+  KB_C_FULL = 0,
+  KB_X_FULL = 1,
+  KB_X_EMPTY = KB_X_FULL + KA_NX,
+  KB_ACC_FULL = KB_X_EMPTY + KA_NX,   // 2
   KB_ACC_EMPTY = KB_ACC_FULL + 2,     // 2, 128 arrivals
   KB_DRAIN = KB_ACC_EMPTY + 2,
   KB_COUNT = KB_DRAIN + 1
@@ -54,31 +58,48 @@ __device__ __forceinline__ void ka_issue(uint32_t d_tmem, uint32_t sA, uint32_t 
   }
 }
 
+// Point tiles [t_lo, t_hi) of split blockIdx.x over the ntiles of a head.
+__device__ __forceinline__ void ka_range(int ntiles, int nsplit, int split, int& t_lo, int& t_hi) {
+  const int per = (ntiles + nsplit - 1) / nsplit;
+  t_lo = min(ntiles, split * per);
+  t_hi = min(ntiles, t_lo + per);
+}
+
+// Grid (nsplit, nchunks, BH). With one chunk the result is the assignment
+// (assign, count += 1); with several, (pdist, pidx)[bh][chunk][i] for the merge.
 __global__ void __launch_bounds__(KA_THREADS, 1)
     km_assign_tc_kernel(const __grid_constant__ CUtensorMap map_x,
                         const __grid_constant__ CUtensorMap map_hi,
                         const __grid_constant__ CUtensorMap map_lo,
-                        const float* __restrict__ cnorm, int N, int C, int* __restrict__ assign,
-                        int* __restrict__ count, long long lim) {
+                        const float* __restrict__ cnorm, int N, int C,
+                        int* __restrict__ assign, int* __restrict__ count,
+                        float* __restrict__ pdist, int* __restrict__ pidx, long long lim) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[KB_COUNT];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
+  __shared__ float cn_s[KA_CHUNK];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const uint32_t sX = smem_u32(smem);  // point tile q at sX + q TILE
-  const uint32_t sC0 = sX + KA_PTS * KA_TILE;  // stage s: hi at sC0 + 2 s TILE, lo right after
+  const uint32_t sHi = smem_u32(smem);          // cluster tile t: hi at sHi + t TILE
+  const uint32_t sLo = sHi + 2 * KA_TILE;       // lo at sLo + t TILE
+  const uint32_t sX0 = sLo + 2 * KA_TILE;       // point-tile stage s at sX0 + s TILE
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.y, i0 = blockIdx.x * 128 * KA_PTS;
-  const int ntiles = (C + 127) / 128;
+  const int split = blockIdx.x, chunk = blockIdx.y, bh = blockIdx.z;
+  const int nchunks = gridDim.y;
+  const int c0 = chunk * KA_CHUNK;
+  const int ntiles = (N + 127) / 128;
+  int t_lo, t_hi;
+  ka_range(ntiles, gridDim.x, split, t_lo, t_hi);
+  const int nt = t_hi - t_lo;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (tid == 0) {
     abort_flag = 0;
-    mbar_init(bar(KB_X_FULL), 1);
-    for (int s = 0; s < KA_NS; ++s) {
-      mbar_init(bar(KB_C_FULL + s), 1);
-      mbar_init(bar(KB_C_EMPTY + s), 1);
+    mbar_init(bar(KB_C_FULL), 1);
+    for (int s = 0; s < KA_NX; ++s) {
+      mbar_init(bar(KB_X_FULL + s), 1);
+      mbar_init(bar(KB_X_EMPTY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(KB_ACC_FULL + b), 1);
@@ -87,6 +108,9 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
     mbar_init(bar(KB_DRAIN), 1);
     fence_barrier_init();
   }
+  // |c|^2 of the chunk; +inf past C, so those columns never win
+  for (int c = tid; c < KA_CHUNK; c += KA_THREADS)
+    cn_s[c] = c0 + c < C ? cnorm[static_cast<long long>(bh) * C + c0 + c] : INFINITY;
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_s), 512);
     tmem_relinquish();
@@ -98,55 +122,55 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
   volatile int* abort_p = &abort_flag;
 
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && nt > 0) {
       tma_prefetch_desc(&map_x);
       tma_prefetch_desc(&map_hi);
       tma_prefetch_desc(&map_lo);
-      mbar_arrive_expect_tx(bar(KB_X_FULL), KA_PTS * KA_TILE);
-      for (int q = 0; q < KA_PTS; ++q) {
-        tma_load_3d(sX + q * KA_TILE, &map_x, bar(KB_X_FULL), 0, i0 + 128 * q, bh);
-        tma_load_3d(sX + q * KA_TILE + KA_HALF, &map_x, bar(KB_X_FULL), 64, i0 + 128 * q, bh);
+      mbar_arrive_expect_tx(bar(KB_C_FULL), 4 * KA_TILE);
+      for (int t = 0; t < 2; ++t) {
+        tma_load_3d(sHi + t * KA_TILE, &map_hi, bar(KB_C_FULL), 0, c0 + 128 * t, bh);
+        tma_load_3d(sHi + t * KA_TILE + KA_HALF, &map_hi, bar(KB_C_FULL), 64, c0 + 128 * t, bh);
+        tma_load_3d(sLo + t * KA_TILE, &map_lo, bar(KB_C_FULL), 0, c0 + 128 * t, bh);
+        tma_load_3d(sLo + t * KA_TILE + KA_HALF, &map_lo, bar(KB_C_FULL), 64, c0 + 128 * t, bh);
       }
       int issued = 0;
-      for (int t = 0; t < ntiles; ++t) {
-        const int s = t % KA_NS;
-        if (t >= KA_NS &&
-            !mbar_wait_bounded(bar(KB_C_EMPTY + s), ((t / KA_NS) & 1) ^ 1, lim, abort_p))
+      for (int i = 0; i < nt; ++i) {
+        const int s = i % KA_NX;
+        if (i >= KA_NX &&
+            !mbar_wait_bounded(bar(KB_X_EMPTY + s), ((i / KA_NX) & 1) ^ 1, lim, abort_p))
           break;
-        const uint32_t hi = sC0 + 2 * s * KA_TILE, lo = hi + KA_TILE;
-        mbar_arrive_expect_tx(bar(KB_C_FULL + s), 2 * KA_TILE);
-        tma_load_3d(hi, &map_hi, bar(KB_C_FULL + s), 0, t * 128, bh);
-        tma_load_3d(hi + KA_HALF, &map_hi, bar(KB_C_FULL + s), 64, t * 128, bh);
-        tma_load_3d(lo, &map_lo, bar(KB_C_FULL + s), 0, t * 128, bh);
-        tma_load_3d(lo + KA_HALF, &map_lo, bar(KB_C_FULL + s), 64, t * 128, bh);
-        issued = t + 1;
+        const int row = (t_lo + i) * 128;
+        mbar_arrive_expect_tx(bar(KB_X_FULL + s), KA_TILE);
+        tma_load_3d(sX0 + s * KA_TILE, &map_x, bar(KB_X_FULL + s), 0, row, bh);
+        tma_load_3d(sX0 + s * KA_TILE + KA_HALF, &map_x, bar(KB_X_FULL + s), 64, row, bh);
+        issued = i + 1;
       }
       if (*abort_p) {
         volatile int no_abort = 0;
-        mbar_wait_bounded(bar(KB_X_FULL), 0, lim, &no_abort);
-        for (int t = issued > KA_NS ? issued - KA_NS : 0; t < issued; ++t) {
+        mbar_wait_bounded(bar(KB_C_FULL), 0, lim, &no_abort);
+        for (int i = issued > KA_NX ? issued - KA_NX : 0; i < issued; ++i) {
           no_abort = 0;
-          mbar_wait_bounded(bar(KB_C_FULL + t % KA_NS), (t / KA_NS) & 1, lim, &no_abort);
+          mbar_wait_bounded(bar(KB_X_FULL + i % KA_NX), (i / KA_NX) & 1, lim, &no_abort);
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = mbar_wait_bounded(bar(KB_X_FULL), 0, lim, abort_p);
-      for (int t = 0; ok && t < ntiles; ++t) {
-        const int s = t % KA_NS, b = t & 1;
-        if (!(ok = mbar_wait_bounded(bar(KB_C_FULL + s), (t / KA_NS) & 1, lim, abort_p))) break;
-        if (t >= 2 &&
-            !(ok = mbar_wait_bounded(bar(KB_ACC_EMPTY + b), ((t >> 1) & 1) ^ 1, lim, abort_p)))
+    if (lane == 0 && nt > 0) {
+      bool ok = mbar_wait_bounded(bar(KB_C_FULL), 0, lim, abort_p);
+      for (int i = 0; ok && i < nt; ++i) {
+        const int s = i % KA_NX, b = i & 1;
+        if (!(ok = mbar_wait_bounded(bar(KB_X_FULL + s), (i / KA_NX) & 1, lim, abort_p))) break;
+        if (i >= 2 &&
+            !(ok = mbar_wait_bounded(bar(KB_ACC_EMPTY + b), ((i >> 1) & 1) ^ 1, lim, abort_p)))
           break;
         tc_fence_after();
-        const uint32_t hi = sC0 + 2 * s * KA_TILE, lo = hi + KA_TILE;
+        const uint32_t sX = sX0 + s * KA_TILE;
 #pragma unroll
-        for (int q = 0; q < KA_PTS; ++q) {
-          ka_issue(tmem + b * 256 + q * 128, sX + q * KA_TILE, hi, false);
-          ka_issue(tmem + b * 256 + q * 128, sX + q * KA_TILE, lo, true);
+        for (int t = 0; t < 2; ++t) {
+          ka_issue(tmem + b * 256 + t * 128, sX, sHi + t * KA_TILE, false);
+          ka_issue(tmem + b * 256 + t * 128, sX, sLo + t * KA_TILE, true);
         }
-        umma_commit(bar(KB_C_EMPTY + s));
+        umma_commit(bar(KB_X_EMPTY + s));
         umma_commit(bar(KB_ACC_FULL + b));
       }
       if (!ok) {
@@ -159,71 +183,48 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const float* cn = cnorm + static_cast<long long>(bh) * C;
-    float best[KA_PTS];
-    int besti[KA_PTS];
-#pragma unroll
-    for (int q = 0; q < KA_PTS; ++q) {
-      best[q] = INFINITY;
-      besti[q] = 0x7fffffff;
-    }
-    bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      const int b = t & 1;
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait_bounded(bar(KB_ACC_FULL + b), (t >> 1) & 1, lim, abort_p));
-      if (!ok) break;
+    for (int i = 0; i < nt; ++i) {
+      const int b = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(KB_ACC_FULL + b), (i >> 1) & 1, lim,
+                                                      abort_p)))
+        break;
       tc_fence_after();
-      const int c0 = t * 128;
-      const int nc = min(128, C - c0);
+      float best = INFINITY;
+      int besti = 0x7fffffff;
 #pragma unroll 1
-      for (int q = 0; q < KA_PTS; ++q) {
+      for (int t = 0; t < 2; ++t) {
         float acc[128];
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           uint32_t v[32];
-          tmem_ld32(tmem + b * 256 + q * 128 + lane_off + c4 * 32, v);
+          tmem_ld32(tmem + b * 256 + t * 128 + lane_off + c4 * 32, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[c4 * 32 + i] = __uint_as_float(v[i]);
+          for (int k = 0; k < 32; ++k) acc[c4 * 32 + k] = __uint_as_float(v[k]);
         }
         tmem_wait_ld();
-        if (q == KA_PTS - 1) {
+        if (t == 1) {
           tc_fence_before();
           mbar_arrive(bar(KB_ACC_EMPTY + b));
         }
-        float bq = best[q];
-        int iq = besti[q];
-        if (nc == 128) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            const float dist = fmaf(-2.f, acc[i], __ldg(cn + c0 + i));
-            if (dist < bq) {
-              bq = dist;
-              iq = c0 + i;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            if (i < nc) {
-              const float dist = fmaf(-2.f, acc[i], __ldg(cn + c0 + i));
-              if (dist < bq) {
-                bq = dist;
-                iq = c0 + i;
-              }
-            }
+        for (int k = 0; k < 128; ++k) {
+          const float dist = fmaf(-2.f, acc[k], cn_s[t * 128 + k]);
+          if (dist < best) {
+            best = dist;
+            besti = c0 + t * 128 + k;
           }
         }
-        best[q] = bq;
-        besti[q] = iq;
       }
-    }
-#pragma unroll
-    for (int q = 0; q < KA_PTS; ++q) {
-      const int i = i0 + 128 * q + r;
-      if (ok && i < N) {
-        assign[static_cast<long long>(bh) * N + i] = besti[q];
-        atomicAdd(&count[static_cast<long long>(bh) * C + besti[q]], 1);
+      const int p = (t_lo + i) * 128 + r;
+      if (p < N) {
+        if (nchunks == 1) {
+          assign[static_cast<long long>(bh) * N + p] = besti;
+          atomicAdd(&count[static_cast<long long>(bh) * C + besti], 1);
+        } else {
+          const long long o = (static_cast<long long>(bh) * nchunks + chunk) * N + p;
+          pdist[o] = best;
+          pidx[o] = besti;
+        }
       }
     }
   }
@@ -232,6 +233,33 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// Argmin over the chunks' results in chunk order (strict <: the lowest index
+// wins ties, as in one pass over all clusters); assign and count += 1.
+// Grid (ceil(N / 256), BH).
+__global__ void ka_merge_kernel(const float* __restrict__ pdist, const int* __restrict__ pidx,
+                                int N, int C, int nchunks, int* __restrict__ assign,
+                                int* __restrict__ count) {
+  const int bh = blockIdx.y;
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;
+  if (p >= N) return;
+  float best = INFINITY;
+  int besti = 0x7fffffff;
+  for (int ch = 0; ch < nchunks; ++ch) {
+    const long long o = (static_cast<long long>(bh) * nchunks + ch) * N + p;
+    const float d = pdist[o];
+    if (d < best) {
+      best = d;
+      besti = pidx[o];
+    }
+  }
+  if (besti >= 0 && besti < C) {
+    assign[static_cast<long long>(bh) * N + p] = besti;
+    atomicAdd(&count[static_cast<long long>(bh) * C + besti], 1);
+  } else {
+    raise_error(VA_ERR_DEVICE);
+  }
 }
 
 // c = hi + lo with hi = bf16(c) and lo = bf16(c - hi), for [rows, 128] fp32.

@@ -471,17 +471,29 @@ int cluster_lists(const int* assign, int BH, int N, int C, int* count, int* off,
 int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C, int iters,
                    int* assign, float* cent, int* count, cudaStream_t s) {
   static bool configured[64] = {false};
+  static int num_sms[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   int st;
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
+  if (dev < 0 || dev >= 64) return VA_ERR_UNSUPPORTED;
+  if (!configured[dev]) {
     if ((st = set_smem_attrs<__nv_bfloat16, 128>()) ||
         (st = cuda_status(cudaFuncSetAttribute(va::km_assign_tc_kernel,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::KA_SMEM_BYTES))))
+                                               va::KA_SMEM_BYTES))) ||
+        (st = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
+                                                 dev))))
       return st;
     configured[dev] = true;
   }
+  // assignment grid: resident chunks of 256 clusters, point tiles split so
+  // that the persistent CTAs fill about one wave
+  const int nchunks = (C + va::KA_CHUNK - 1) / va::KA_CHUNK;
+  const int ntiles = (N + 127) / 128;
+  const long long per_wave = static_cast<long long>(BH) * nchunks;
+  const int nsplit = static_cast<int>(
+      std::max(1LL, std::min(static_cast<long long>(ntiles), num_sms[dev] / per_wave)));
+  if (nchunks > 65535) return VA_ERR_UNSUPPORTED;
   Scoped scratch(s);
   float* cnorm = nullptr;
   int *off = nullptr, *fill = nullptr, *perm = nullptr;
@@ -495,12 +507,18 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C
       (st = scratch.alloc(&hi, nc)) || (st = scratch.alloc(&lo, nc)) ||
       (st = scratch.alloc(&sums, nc)))
     return st;
+  float* pdist = nullptr;
+  int* pidx = nullptr;
+  if (nchunks > 1) {
+    const size_t np = static_cast<size_t>(BH) * nchunks * N;
+    if ((st = scratch.alloc(&pdist, np)) || (st = scratch.alloc(&pidx, np))) return st;
+  }
   CUtensorMap mx, mh, ml;
   if ((st = encode_bf16_rows(&mx, x, BH, N, 128)) || (st = encode_bf16_rows(&mh, hi, BH, C, 128)) ||
       (st = encode_bf16_rows(&ml, lo, BH, C, 128)))
     return st;
   const dim3 gc((C + 7) / 8, BH);
-  const dim3 ga((N + 128 * va::KA_PTS - 1) / (128 * va::KA_PTS), BH);
+  const dim3 ga(nsplit, nchunks, BH);
   const dim3 gn((N + 255) / 256, BH);
   const unsigned gs = static_cast<unsigned>((nc + 255) / 256);
   va::km_init_kernel<__nv_bfloat16, 128><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
@@ -509,7 +527,10 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C
   for (int it = 0; it < rounds; ++it) {
     if ((st = cuda_status(cudaMemsetAsync(count, 0, sizeof(int) * BH * C, s)))) return st;
     va::km_assign_tc_kernel<<<ga, va::KA_THREADS, va::KA_SMEM_BYTES, s>>>(
-        mx, mh, ml, cnorm, N, C, assign, count, g_wait_limit);
+        mx, mh, ml, cnorm, N, C, assign, count, pdist, pidx, g_wait_limit);
+    if (nchunks > 1)
+      va::ka_merge_kernel<<<dim3((N + 255) / 256, BH), 256, 0, s>>>(pdist, pidx, N, C, nchunks,
+                                                                   assign, count);
     if (iters == 0) break;
     va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
     va::km_scatter_kernel<<<gn, 256, 0, s>>>(assign, N, C, off, fill, perm);
