@@ -393,72 +393,96 @@ __global__ void route_keys_kernel(const float* __restrict__ err, const int* __re
   costs[i] = static_cast<unsigned long long>(np) * static_cast<unsigned long long>(nc);
 }
 
-constexpr int RS_THREADS = 1024;
-constexpr int RS_SMEM_BYTES = (RS_THREADS / 32) * 256 * 8;
 
-// Per bh (one CTA of 1024 threads): the smallest key K whose prefix (all keys
-// <= K) costs more than the budget; blocks with key < K are computed exactly.
-// cut[bh] = ~0 when every valid block fits. Weighted MSB-first radix select,
-// 8 bits per pass, with one private histogram per warp.
+// Weighted MSB-first radix select, 8 bits per pass, spread over many CTAs:
+// per bh, the smallest key K whose prefix (all keys <= K) costs more than the
+// budget; blocks with key < K are computed exactly, cut[bh] = ~0 when every
+// valid block fits. State per bh: {prefix, mask, remaining budget, done}.
+// Each pass: every CTA adds the costs of its slice's keys that match the
+// prefix into a per-bh global histogram of the next 8 bits (64-bit integer
+// sums, so the result does not depend on the order); the last CTA to finish
+// scans the histogram, extends the prefix and clears the histogram.
+constexpr int RS_THREADS = 256;
+constexpr int RS_PER_CTA = 4096;  // keys per CTA and pass
+
+// state[bh] = {0, 0, budget, 0}; hist and the CTA counters zeroed.
+__global__ void route_init_kernel(long long budget, int BH, unsigned long long* __restrict__ state,
+                                  unsigned long long* __restrict__ hist,
+                                  unsigned int* __restrict__ counter) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < BH * 256) hist[i] = 0;
+  if (i < BH) {
+    state[4 * i + 0] = 0;
+    state[4 * i + 1] = 0;
+    state[4 * i + 2] = static_cast<unsigned long long>(budget);
+    state[4 * i + 3] = 0;
+    counter[i] = 0;
+  }
+}
+
+// One pass at bit offset `shift`. Grid (ceil(total / RS_PER_CTA), BH), RS_THREADS.
 __global__ void __launch_bounds__(RS_THREADS)
-    route_select_kernel(const unsigned long long* __restrict__ keys,
-                        const unsigned long long* __restrict__ costs, int total,
-                        long long budget, unsigned long long* __restrict__ cut) {
-  extern __shared__ unsigned long long rs_hist[];  // [32 warps][256]
-  __shared__ unsigned long long hist[256];
-  __shared__ unsigned long long s_prefix, s_mask;
-  __shared__ long long s_remaining;
-  __shared__ int s_done;
-  const int bh = blockIdx.x, tid = threadIdx.x, warp = tid >> 5;
+    route_pass_kernel(const unsigned long long* __restrict__ keys,
+                      const unsigned long long* __restrict__ costs, int total, int shift,
+                      unsigned long long* __restrict__ state, unsigned long long* __restrict__ hist,
+                      unsigned int* __restrict__ counter) {
+  __shared__ unsigned long long h[256];
+  __shared__ int s_last;
+  const int bh = blockIdx.y, tid = threadIdx.x;
+  unsigned long long* st = state + 4 * bh;
+  if (st[3]) return;  // uniform: every key already fits
+  const unsigned long long prefix = st[0], mask = st[1];
+  h[tid] = 0;
+  __syncthreads();
   const unsigned long long* kb = keys + static_cast<long long>(bh) * total;
   const unsigned long long* cb = costs + static_cast<long long>(bh) * total;
+  const int e0 = blockIdx.x * RS_PER_CTA, e1 = min(total, e0 + RS_PER_CTA);
+  for (int e = e0 + tid; e < e1; e += RS_THREADS) {
+    const unsigned long long key = kb[e];
+    const unsigned long long cost = cb[e];
+    if (cost == 0 || (key & mask) != prefix) continue;
+    atomicAdd(&h[(key >> shift) & 255u], cost);
+  }
+  __syncthreads();
+  unsigned long long* gh = hist + 256 * static_cast<long long>(bh);
+  if (h[tid] != 0) atomicAdd(&gh[tid], h[tid]);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&counter[bh], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // last CTA of this bh: read the complete histogram, extend the prefix
+  h[tid] = atomicExch(&gh[tid], 0ull);
+  __syncthreads();
   if (tid == 0) {
-    s_prefix = 0;
-    s_mask = 0;
-    s_remaining = budget;
-    s_done = 0;
+    long long remaining = static_cast<long long>(st[2]);
+    long long cum = 0;
+    int b = 0;
+    for (; b < 256; ++b) {
+      const long long hb = static_cast<long long>(h[b]);
+      if (cum + hb > remaining) break;
+      cum += hb;
+    }
+    if (b == 256) {
+      // everything under this prefix fits (only possible on the first pass:
+      // the whole set fits the budget)
+      st[0] = ~0ull;
+      st[3] = 1;
+    } else {
+      st[2] = static_cast<unsigned long long>(remaining - cum);
+      st[0] = prefix | (static_cast<unsigned long long>(b) << shift);
+      st[1] = mask | (255ull << shift);
+    }
+    counter[bh] = 0;
   }
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int b = tid; b < (RS_THREADS / 32) * 256; b += RS_THREADS) rs_hist[b] = 0;
-    __syncthreads();
-    if (s_done) break;
-    const unsigned long long prefix = s_prefix, mask = s_mask;
-    unsigned long long* h = rs_hist + warp * 256;
-    for (int e = tid; e < total; e += RS_THREADS) {
-      const unsigned long long key = kb[e];
-      const unsigned long long cost = cb[e];
-      if (cost == 0 || (key & mask) != prefix) continue;
-      atomicAdd(&h[(key >> shift) & 255u], cost);
-    }
-    __syncthreads();
-    for (int b = tid; b < 256; b += RS_THREADS) {
-      unsigned long long sum = 0;
-      for (int w = 0; w < RS_THREADS / 32; ++w) sum += rs_hist[w * 256 + b];
-      hist[b] = sum;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      long long cum = 0;
-      int b = 0;
-      for (; b < 256; ++b) {
-        const long long hb = static_cast<long long>(hist[b]);
-        if (cum + hb > s_remaining) break;
-        cum += hb;
-      }
-      if (b == 256) {
-        // everything under this prefix fits (only possible on the first pass:
-        // the whole set fits the budget)
-        s_done = 1;
-        s_prefix = ~0ull;
-      } else {
-        s_remaining -= cum;
-        s_prefix = prefix | (static_cast<unsigned long long>(b) << shift);
-        s_mask = mask | (255ull << shift);
-      }
-    }
-    __syncthreads();
-  }
-  if (tid == 0) cut[bh] = s_prefix;
+}
+
+// cut[bh] = state prefix after the last pass.
+__global__ void route_cut_kernel(const unsigned long long* __restrict__ state, int BH,
+                                 unsigned long long* __restrict__ cut) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < BH) cut[i] = state[4 * i];
 }
 
 // sel[bh][p][c] = 1 for exactly computed blocks (if sel != nullptr) and the

@@ -445,9 +445,6 @@ int set_smem_attrs() {
       (st = cuda_status(cudaFuncSetAttribute(va::probe_pass2_kernel<T, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              va::probe_smem_bytes<D>(kMaxClusters)))) ||
-      (st = cuda_status(cudaFuncSetAttribute(va::route_select_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             va::RS_SMEM_BYTES))) ||
       (st = cuda_status(cudaFuncSetAttribute(va::comp_attn_kernel<T, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              va::comp_smem_bytes<D>(kMaxClusters)))))
@@ -882,8 +879,17 @@ int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int C
     return st;
   va::route_keys_kernel<<<dim3((Cq * Ck + 255) / 256, BH), 256, 0, s>>>(err, nq, nk, Cq, Ck,
                                                                        rkeys, rcosts);
-  va::route_select_kernel<<<BH, va::RS_THREADS, va::RS_SMEM_BYTES, s>>>(rkeys, rcosts, Cq * Ck,
-                                                                        budget, cut);
+  unsigned long long *rstate, *rhist;
+  unsigned int* rcount;
+  if ((st = scratch.alloc(&rstate, bh * 4)) || (st = scratch.alloc(&rhist, bh * 256)) ||
+      (st = scratch.alloc(&rcount, bh)))
+    return st;
+  va::route_init_kernel<<<(BH * 256 + 255) / 256, 256, 0, s>>>(budget, BH, rstate, rhist, rcount);
+  const dim3 gsel((Cq * Ck + va::RS_PER_CTA - 1) / va::RS_PER_CTA, BH);
+  for (int shift = 56; shift >= 0; shift -= 8)
+    va::route_pass_kernel<<<gsel, va::RS_THREADS, 0, s>>>(rkeys, rcosts, Cq * Ck, shift, rstate,
+                                                           rhist, rcount);
+  va::route_cut_kernel<<<(BH + 255) / 256, 256, 0, s>>>(rstate, BH, cut);
   va::route_mark_kernel<<<dim3(Cq, BH), 256, 0, s>>>(err, nq, nk, Cq, Ck, cut, sel, seln, selc);
   if ((st = launch_status())) return st;
 
