@@ -249,7 +249,8 @@ __device__ __forceinline__ long long bf16_fixed32(uint32_t bits16) {
 // mean[bh][c] when keep_empty, else gets zeros. Sums are exact and
 // order-independent: 64-bit fixed point for bf16 (members with |x| < 2^-25
 // contribute with an error below 2^-32; |sum| must stay below 2^31), float64
-// for float32. Member indices are fetched 32 at a time so the row loads of a
+// for float32. The bf16 mean is the fp32 sum divided in fp32 (within one ulp
+// of the exact mean). Member indices are fetched 32 at a time so the row loads of a
 // cluster are independent. Grid: (ceil(C / 8), BH), 256 threads.
 template <typename T, int D>
 __global__ void km_means_kernel(const T* __restrict__ x, int N, int C,
@@ -293,11 +294,14 @@ __global__ void km_means_kernel(const T* __restrict__ x, int N, int C,
   }
   float nrm = 0.f;
   if (end > beg) {
-    const double n = static_cast<double>(end - beg);
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
-      const double sum = kFixed ? static_cast<double>(iacc[e]) * 0x1p-32 : dacc[e];
-      const float mv = static_cast<float>(sum / n);
+      // fixed point: the exact sum rounded to fp32, then an IEEE fp32 division
+      // (at most one ulp from the exact mean; no fp64 on the bf16 path, whose
+      // rate is a small fraction of fp32's on this part)
+      const float mv =
+          kFixed ? __fdiv_rn(static_cast<float>(iacc[e]) * 0x1p-32f, static_cast<float>(end - beg))
+                 : static_cast<float>(dacc[e] / static_cast<double>(end - beg));
       m[lane * PER + e] = mv;
       nrm = fmaf(mv, mv, nrm);
     }
@@ -384,9 +388,11 @@ __global__ void km_finalize_kernel(const unsigned long long* __restrict__ sums,
   if (n > 0 || !keep_empty) {
 #pragma unroll
     for (int e = 0; e < PER; ++e) {
-      const float mv = n > 0 ? static_cast<float>(static_cast<double>(
-                                   static_cast<long long>(sums[row + e])) * 0x1p-32 / n)
-                             : 0.f;
+      // exact fixed-point sum rounded to fp32, then an IEEE fp32 division
+      const float mv =
+          n > 0 ? __fdiv_rn(static_cast<float>(static_cast<long long>(sums[row + e])) * 0x1p-32f,
+                            static_cast<float>(n))
+                : 0.f;
       mean[row + e] = mv;
       nrm = fmaf(mv, mv, nrm);
       if (hi != nullptr) {

@@ -4,8 +4,8 @@ Bars (readings of SVG-EAR, gist.science 2603.08982, technical summary sec. 2):
 * k-means: given the same centroids, assignments are bit-exact except points
   whose best and chosen distances are within 1e-4 relative (near-ties, which
   float32 may order either way; counted and bounded); counts equal the
-  histogram of the assignment; centroids are the member means (float32
-  rounding of the exact mean).
+  histogram of the assignment; centroids are the member means (within one
+  float32 ulp of the exact mean, checked at 2e-7 relative).
 * probe: err within 1e-3 relative (plus a small absolute floor) of the float64
   oracle run on the GPU's clusters.
 * routing: bit-exact against the oracle's selection rule applied to the GPU's
