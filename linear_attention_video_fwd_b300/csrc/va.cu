@@ -853,12 +853,32 @@ int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int C
   if ((st = cluster_lists(qassign, BH, N, Cq, nq, qoff, qfill, qperm, s)) ||
       (st = cluster_lists(kassign, BH, N, Ck, nk, koff, kfill, kperm, s)))
     return st;
-  va::km_means_kernel<T, D><<<dim3((Cq + 7) / 8, BH), 256, 0, s>>>(q, N, Cq, qoff, qperm, qc,
-                                                                  nullptr, 0);
-  va::km_means_kernel<T, D><<<dim3((Ck + 7) / 8, BH), 256, 0, s>>>(k, N, Ck, koff, kperm, kc,
-                                                                  nullptr, 0);
-  va::km_means_kernel<T, D><<<dim3((Ck + 7) / 8, BH), 256, 0, s>>>(v, N, Ck, koff, kperm, vc,
-                                                                  nullptr, 0);
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) {
+    // balanced exact sums over the cluster-ordered members, then the means
+    unsigned long long* sums;
+    const size_t cmax = static_cast<size_t>(Cq > Ck ? Cq : Ck);
+    if ((st = scratch.alloc(&sums, bh * cmax * D))) return st;
+    struct MeanJob { const T* x; const int* perm; const int* assign; const int* count; int C;
+                     float* mean; };
+    const MeanJob jobs[3] = {{q, qperm, qassign, nq, Cq, qc}, {k, kperm, kassign, nk, Ck, kc},
+                             {v, kperm, kassign, nk, Ck, vc}};
+    for (const MeanJob& jb : jobs) {
+      if ((st = cuda_status(
+               cudaMemsetAsync(sums, 0, sizeof(unsigned long long) * bh * jb.C * D, s))))
+        return st;
+      va::km_sum_kernel<D><<<dim3((N + 255) / 256, BH), 256, 0, s>>>(jb.x, N, jb.C, jb.perm,
+                                                                     jb.assign, sums);
+      va::km_finalize_kernel<D><<<dim3((jb.C + 7) / 8, BH), 256, 0, s>>>(
+          sums, jb.count, jb.C, jb.mean, nullptr, nullptr, nullptr, 0);
+    }
+  } else {
+    va::km_means_kernel<T, D><<<dim3((Cq + 7) / 8, BH), 256, 0, s>>>(q, N, Cq, qoff, qperm, qc,
+                                                                    nullptr, 0);
+    va::km_means_kernel<T, D><<<dim3((Ck + 7) / 8, BH), 256, 0, s>>>(k, N, Ck, koff, kperm, kc,
+                                                                    nullptr, 0);
+    va::km_means_kernel<T, D><<<dim3((Ck + 7) / 8, BH), 256, 0, s>>>(v, N, Ck, koff, kperm, vc,
+                                                                    nullptr, 0);
+  }
   if ((st = launch_status())) return st;
 
   // probe: err = NaN where a cluster is empty, else the proxy error
