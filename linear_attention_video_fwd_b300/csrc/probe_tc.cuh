@@ -69,9 +69,9 @@ static_assert(128 * PT_REGS_DEC + 256 * PT_REGS_INC <= PT_THREADS * PT_LAUNCH_RE
               "register split exceeds the launch allocation");
 
 struct ProbeArgs {
-  const int* gmeta;   // [BH][G] per 16-row group: valid rows | PT_G_FIRST | PT_G_LAST
+  const int* gmeta;   // [BH][G] per 16-row group: valid rows | PT_G_FIRST | PT_G_LAST |
+                      // cluster << 8
   const int* kpoff;   // [BH][Ck + 1] first padded row of each key cluster
-  const int* nk;      // [BH][Ck] key-cluster sizes
   const int* nq;      // [BH][Cq] query-cluster sizes
   const float* mzo;   // pass 2: [BH][Cq][PT_ROW] merged {m2, Z, O / Z}
   const float* vc;    // pass 2: [BH][Ck][128] value means
@@ -127,7 +127,8 @@ template <int PASS>
 __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, int split,
                                            int g_lo, int g_hi, int nt, uint32_t tmem,
                                            uint64_t* bars, float (*zc_s)[128],
-                                           float (*w_s)[128], volatile int* abort_p) {
+                                           float (*w_s)[128], float (*vc_s)[128], int* cid_s,
+                                           volatile int* abort_p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;
   const int p = pt * 128 + r;
@@ -137,8 +138,8 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
   const int nval0 = PASS == 1 ? nt : 0;
   const int ne = nval0 + nt;
   const int* gm = a.gmeta + static_cast<long long>(bh) * a.G;
-  float m2 = -INFINITY, Z = 0.f, zc = 0.f, ls = 0.f;
-  int nv = 0;
+  float m2 = -INFINITY, Z = 0.f, zc = 0.f, ls = 0.f, vc_pre = 0.f;
+  int nv = 0, cur_c = 0;
   if constexpr (PASS == 2)
     m2 = a.mzo[(static_cast<long long>(bh) * a.Cq + min(p, a.Cq - 1)) * PT_ROW];
   int ci = -1;
@@ -220,6 +221,9 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
           zc = 0.f;
           ls = 0.f;
           nv = 0;
+          cur_c = mg >> 8;
+          // value mean of the cluster, read now and published at its end
+          vc_pre = a.vc[(static_cast<long long>(bh) * a.Ck + cur_c) * 128 + r];
         }
         float gs = 0.f;
 #pragma unroll
@@ -239,10 +243,25 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
           const float nf = static_cast<float>(nv);
           zc_s[slot][r] = zc;
           w_s[slot][r] = nf * exp2f(fmaf(ls / nf, sl2, -m2));
+          vc_s[slot][r] = vc_pre;
+          if (r == 0) cid_s[slot] = cur_c;
           mbar_arrive(smem_u32(&bars[PB_ZF + slot]));
         }
       }
       if (!ok) break;
+    }
+  }
+  if constexpr (PASS == 2) {
+    // sentinel after the last cluster: the residual warpgroup stops there
+    if (ok) {
+      const int cn = ci + 1, slot = cn & 1;
+      if (cn >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bars[PB_EE + slot]),
+                                                        ((cn - 2) >> 1) & 1, lim, abort_p));
+      if (ok) {
+        if (r == 0) cid_s[slot] = -1;
+        mbar_arrive(smem_u32(&bars[PB_ZF + slot]));
+      }
     }
   }
   if constexpr (PASS == 1) {
@@ -279,10 +298,14 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
   }
 }
 
-// Residual warpgroup (pass 2): thread r owns proxy row r; clusters in order.
-__device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, int c_lo, int c_hi,
-                                            uint32_t tmem, uint64_t* bars, float (*zc_s)[128],
-                                            const float (*w_s)[128], volatile int* abort_p) {
+// Residual warpgroup (pass 2): thread r owns proxy row r. The softmax
+// publishes each finished cluster through a slot of shared memory (its id,
+// Zc and w_c per row, and its value mean), then a sentinel id -1 after the
+// last one.
+__device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, uint32_t tmem,
+                                            uint64_t* bars, const float (*zc_s)[128],
+                                            const float (*w_s)[128], const float (*vc_s)[128],
+                                            const int* cid_s, volatile int* abort_p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;
   const int p = pt * 128 + r;
@@ -299,25 +322,22 @@ __device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, 
     O[i + 1] = t.y;
   }
   const bool write = p < a.Cq && a.nq[static_cast<long long>(bh) * a.Cq + pr] > 0;
-  const int* nkb = a.nk + static_cast<long long>(bh) * a.Ck;
   float* errr = a.err + (static_cast<long long>(bh) * a.Cq + pr) * a.Ck;
-  int ci = -1;
-  for (int c = c_lo; c < c_hi; ++c) {
-    const int n = nkb[c];
-    if (n == 0) continue;
-    ++ci;
+  for (int ci = 0;; ++ci) {
     const int slot = ci & 1;
     const uint32_t ph = (ci >> 1) & 1;
-    bool ok = __all_sync(0xffffffffu,
-                         mbar_wait_bounded(smem_u32(&bars[PB_EF + slot]), ph, lim, abort_p));
-    if (ok)
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait_bounded(smem_u32(&bars[PB_ZF + slot]), ph, lim, abort_p));
-    if (!ok) break;
+    if (!__all_sync(0xffffffffu,
+                    mbar_wait_bounded(smem_u32(&bars[PB_ZF + slot]), ph, lim, abort_p)))
+      break;
+    const int c = cid_s[slot];
+    if (c < 0) break;  // sentinel: no more clusters
+    if (!__all_sync(0xffffffffu,
+                    mbar_wait_bounded(smem_u32(&bars[PB_EF + slot]), ph, lim, abort_p)))
+      break;
     tc_fence_after();
     const float zc = zc_s[slot][r];
     const float w = w_s[slot][r];
-    const float* vcc = a.vc + (static_cast<long long>(bh) * a.Ck + c) * 128;
+    const float4* vc4 = reinterpret_cast<const float4*>(vc_s[slot]);
     const uint32_t tE = tmem + PT_T_ACC + slot * 128 + lane_off;
     float n2 = 0.f;
 #pragma unroll
@@ -327,7 +347,7 @@ __device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, 
       tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
-        const float4 vv = *reinterpret_cast<const float4*>(vcc + q * 32 + i);
+        const float4 vv = vc4[(q * 32 + i) / 4];
         const float vcv[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -352,8 +372,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   __shared__ __align__(8) uint64_t bars[PB_COUNT];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
-  __shared__ float zc_s[2][128];  // per E buffer: Zc and w_c of each proxy row
-  __shared__ float w_s[2][128];
+  __shared__ float zc_s[2][128];  // per E buffer: Zc and w_c of each proxy row,
+  __shared__ float w_s[2][128];   // the cluster's value mean and its id
+  __shared__ __align__(16) float vc_s[2][128];
+  __shared__ int cid_s[2];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -407,9 +429,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   if (warp >= 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PT_REGS_INC));
     if (warp < 8) {
-      pt_softmax<PASS>(a, bh, pt, split, g_lo, g_hi, nt, tmem, bars, zc_s, w_s, abort_p);
+      pt_softmax<PASS>(a, bh, pt, split, g_lo, g_hi, nt, tmem, bars, zc_s, w_s, vc_s, cid_s,
+                       abort_p);
     } else if constexpr (PASS == 2) {
-      pt_residual(a, bh, pt, c_lo, c_hi, tmem, bars, zc_s, w_s, abort_p);
+      pt_residual(a, bh, pt, tmem, bars, zc_s, w_s, vc_s, cid_s, abort_p);
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PT_REGS_DEC));
@@ -624,7 +647,7 @@ __global__ void pad_gather_kernel(const __nv_bfloat16* __restrict__ k,
     for (int g = threadIdx.x; g < ng; g += blockDim.x) {
       const int valid = min(16, n - 16 * g);
       gmeta[static_cast<long long>(bh) * G + (kp[c] >> 4) + g] =
-          valid | (g == 0 ? PT_G_FIRST : 0) | (g == ng - 1 ? PT_G_LAST : 0);
+          valid | (g == 0 ? PT_G_FIRST : 0) | (g == ng - 1 ? PT_G_LAST : 0) | (c << 8);
     }
   }
 }

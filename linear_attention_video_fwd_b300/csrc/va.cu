@@ -778,7 +778,6 @@ int probe_tensor_cores(const __nv_bfloat16* k, const __nv_bfloat16* v, int Cq, i
   va::ProbeArgs a;
   a.gmeta = gmeta;
   a.kpoff = kpoff;
-  a.nk = nk;
   a.nq = nq;
   a.mzo = mzo;
   a.vc = vc;
