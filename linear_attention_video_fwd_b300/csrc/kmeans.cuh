@@ -203,19 +203,27 @@ __global__ void km_offsets_kernel(const int* __restrict__ count, int C, int* __r
 
 // perm[off[a_i] + k] = i (member lists; order within a cluster unspecified).
 // Assignment values outside [0, C) are reported as VA_ERR_DEVICE and skipped.
+// Lanes of a warp with the same cluster take their slots with one atomic
+// (neighbouring tokens often share a cluster). Whole warps: blockDim is a
+// multiple of 32.
 __global__ void km_scatter_kernel(const int* __restrict__ assign, int N, int C,
                                   const int* __restrict__ off, int* __restrict__ fill,
                                   int* __restrict__ perm) {
   const int bh = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= N) return;
-  const int a = assign[static_cast<long long>(bh) * N + i];
-  if (a < 0 || a >= C) {
-    raise_error(VA_ERR_DEVICE);
-    return;
-  }
-  const int pos = off[static_cast<long long>(bh) * (C + 1) + a] +
-                  atomicAdd(&fill[static_cast<long long>(bh) * C + a], 1);
+  const int lane = threadIdx.x & 31;
+  const bool inr = i < N;
+  const int a = inr ? assign[static_cast<long long>(bh) * N + i] : -1;
+  const bool valid = inr && a >= 0 && a < C;
+  if (inr && !valid) raise_error(VA_ERR_DEVICE);
+  const unsigned grp = __match_any_sync(0xffffffffu, valid ? a : -1);
+  if (!valid) return;
+  const int leader = __ffs(grp) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(&fill[static_cast<long long>(bh) * C + a], __popc(grp));
+  base = __shfl_sync(grp, base, leader);
+  const int pos = off[static_cast<long long>(bh) * (C + 1) + a] + base +
+                  __popc(grp & ((1u << lane) - 1u));
   perm[static_cast<long long>(bh) * N + pos] = i;
 }
 
@@ -224,13 +232,14 @@ __global__ void km_count_kernel(const int* __restrict__ assign, int N, int C,
                                 int* __restrict__ count) {
   const int bh = blockIdx.y;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= N) return;
-  const int a = assign[static_cast<long long>(bh) * N + i];
-  if (a < 0 || a >= C) {
-    raise_error(VA_ERR_DEVICE);
-    return;
-  }
-  atomicAdd(&count[static_cast<long long>(bh) * C + a], 1);
+  const int lane = threadIdx.x & 31;
+  const bool inr = i < N;
+  const int a = inr ? assign[static_cast<long long>(bh) * N + i] : -1;
+  const bool valid = inr && a >= 0 && a < C;
+  if (inr && !valid) raise_error(VA_ERR_DEVICE);
+  const unsigned grp = __match_any_sync(0xffffffffu, valid ? a : -1);
+  if (valid && lane == __ffs(grp) - 1)
+    atomicAdd(&count[static_cast<long long>(bh) * C + a], __popc(grp));
 }
 
 // bf16 value as a signed fixed-point integer with 32 fraction bits: exact
