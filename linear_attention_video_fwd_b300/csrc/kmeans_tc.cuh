@@ -46,6 +46,12 @@ enum : int {
   KB_COUNT = KB_DRAIN + 1
 };
 
+__device__ __forceinline__ float ka_min3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // D (+)= A[128 x 128] . B[128 x 128]^T, both K-major 128B-swizzled halves.
 __device__ __forceinline__ void ka_issue(uint32_t d_tmem, uint32_t sA, uint32_t sB,
                                          bool accumulate) {
@@ -78,7 +84,7 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
   __shared__ __align__(8) uint64_t bars[KB_COUNT];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_flag;
-  __shared__ float cn_s[KA_CHUNK];
+  __shared__ __align__(8) float cn_s[KA_CHUNK];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sHi = smem_u32(smem);          // cluster tile t: hi at sHi + t TILE
@@ -206,13 +212,27 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
           tc_fence_before();
           mbar_arrive(bar(KB_ACC_EMPTY + b));
         }
+        // distances, two per packed FMA (columns past C have |c|^2 = +inf)
 #pragma unroll
-        for (int k = 0; k < 128; ++k) {
-          const float dist = fmaf(-2.f, acc[k], cn_s[t * 128 + k]);
-          if (dist < best) {
-            best = dist;
-            besti = c0 + t * 128 + k;
-          }
+        for (int k = 0; k < 128; k += 2) {
+          const float2 n2 = *reinterpret_cast<const float2*>(&cn_s[t * 128 + k]);
+          ffma2_v(acc[k], acc[k + 1], acc[k], acc[k + 1], -2.f, n2.x, n2.y);
+        }
+        // the tile's minimum, then the lowest column that attains it (the
+        // same choice as a strict-< scan in column order)
+        float m0 = ka_min3(acc[0], acc[1], acc[2]), m1 = ka_min3(acc[3], acc[4], acc[5]);
+#pragma unroll
+        for (int k = 6; k < 126; k += 4) {
+          m0 = ka_min3(m0, acc[k], acc[k + 1]);
+          m1 = ka_min3(m1, acc[k + 2], acc[k + 3]);
+        }
+        const float mn = ka_min3(m0, m1, fminf(acc[126], acc[127]));
+        int kmin = 0;
+#pragma unroll
+        for (int k = 127; k >= 0; --k) kmin = acc[k] == mn ? k : kmin;
+        if (mn < best) {  // earlier tiles win ties
+          best = mn;
+          besti = c0 + t * 128 + kmin;
         }
       }
       const int p = (t_lo + i) * 128 + r;
