@@ -27,6 +27,33 @@ namespace {
 
 int64_t g_wait_limit = 4000000000LL;
 
+// Scratch memory pool of the library, one per device: stream-ordered, and
+// with no release threshold, so memory freed at the end of a call stays
+// mapped for the next one instead of going back to the driver at every
+// synchronisation (the pool keeps the peak scratch of the process).
+cudaMemPool_t scratch_pool() {
+  static cudaMemPool_t pools[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (pools[dev] == nullptr) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    uint64_t keep = ~0ull;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[dev] = pool;
+  }
+  return pools[dev];
+}
+
 struct Scoped {
   // Stream-ordered scratch allocations released at scope exit.
   cudaStream_t s;
@@ -44,7 +71,9 @@ struct Scoped {
     if (fault_injected()) return VA_ERR_OOM;
     if (n >= kCap) return VA_ERR_OOM;
     void* raw = nullptr;
-    cudaError_t e = cudaMallocAsync(&raw, count * sizeof(T), s);
+    cudaMemPool_t pool = scratch_pool();
+    cudaError_t e = pool != nullptr ? cudaMallocFromPoolAsync(&raw, count * sizeof(T), pool, s)
+                                    : cudaMallocAsync(&raw, count * sizeof(T), s);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return e == cudaErrorMemoryAllocation ? VA_ERR_OOM : VA_ERR_CUDA;
@@ -652,7 +681,9 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   va::chunk_count_kernel<<<dim3((Cq + 255) / 256, BH), 256, 0, s>>>(nq, Cq, 128, nch);
   va::km_offsets_kernel<<<BH, 1024, 0, s>>>(nch, Cq, choff, chfill);
   // slot table: per query cluster, its selected clusters' 8-row slots padded
-  // to whole 16-slot tiles; one synchronisation reads its total size
+  // to whole 16-slot tiles. Its size is only known on the device; it is
+  // allocated for the bound sum_c ceil(n_c / 8) + 15 <= N / 8 + Ck + 16 slots
+  // per query cluster, so no synchronisation is needed.
   int *slcnt, *sloff, *slfill, *slots;
   long long* slbase;
   if ((st = scratch.alloc(&slcnt, bh * Cq)) || (st = scratch.alloc(&sloff, bh * (Cq + 1))) ||
@@ -662,13 +693,9 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   va::km_offsets_kernel<<<BH, 1024, 0, s>>>(slcnt, Cq, sloff, slfill);
   va::slot_base_kernel<<<1, 1, 0, s>>>(sloff, Cq, BH, slbase);
   if ((st = launch_status())) return st;
-  long long total_slots = 0;
-  if ((st = cuda_status(cudaMemcpyAsync(&total_slots, slbase + BH, sizeof(long long),
-                                        cudaMemcpyDeviceToHost, s))) ||
-      (st = cuda_status(cudaStreamSynchronize(s))))
-    return st;
-  if ((st = scratch.alloc(&slots, static_cast<size_t>(total_slots > 0 ? total_slots : 1))))
-    return st;
+  const size_t slot_bound =
+      bh * static_cast<size_t>(Cq) * (static_cast<size_t>(N) / 8 + static_cast<size_t>(Ck) + 16);
+  if ((st = scratch.alloc(&slots, slot_bound))) return st;
   va::slot_fill_kernel<<<dim3(Cq, BH), 256, 0, s>>>(koff, seln, selc, selbox, Cq, Ck, slbase,
                                                    sloff, slots);
   if ((st = launch_status())) return st;
