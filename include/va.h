@@ -178,6 +178,26 @@ int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mas
                        int dtype, va_stream_t stream);
 
 /*
+ * The same attention with q, k, v, out (and lse, if not NULL) in HOST memory,
+ * laid out as above; the library owns the device copies. The (batch, head)
+ * slices go through a ring of device buffers in chunks: host-to-device
+ * copies, the attention kernel and device-to-host copies run on three
+ * internal streams ordered by events, so the transfers of one chunk overlap
+ * the attention of another. The result is bit-identical to
+ * va_sparse_attn_fwd on device copies of the same inputs.
+ * Asynchronous on `stream` like the device call: the work starts after what
+ * `stream` already holds, and later work on `stream` follows it. The host
+ * buffers must stay valid, and out / lse must not be read, until `stream`
+ * has completed (cudaStreamSynchronize). Page-locked host memory is needed
+ * for the copies to overlap; pageable memory works with copies that stall
+ * the host. Calls on one device are serialised on the internal streams.
+ * Errors: as va_sparse_attn_fwd, plus VA_ERR_OOM (device buffers).
+ */
+int va_sparse_attn_fwd_host(const void* q, const void* k, const void* v, const va_mask* mask,
+                            void* out, float* lse, int B, int heads, int N, int d, float scale,
+                            int dtype, va_stream_t stream);
+
+/*
  * Lloyd k-means per (batch, head) on x [B, heads, N, d] (squared Euclidean
  * distance), SVG-EAR's semantic clustering:
  *   centroid <- x[init_idx]; repeat iters times: assign each token to the

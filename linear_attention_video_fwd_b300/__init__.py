@@ -51,6 +51,7 @@ def _load():
         "va_mask_to_host": [vp, i32p, i32p],
         "va_mask_free": [vp],
         "va_sparse_attn_fwd": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp],
+        "va_sparse_attn_fwd_host": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp],
         "va_cluster": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp],
         "va_compensate_route": [vp, vp, vp, vp, i32, vp, i32, f64, f32, i32, i32, i32, i32, i32,
                                 vp, vp, vp, vp],
@@ -177,6 +178,29 @@ def sparse_attn_fwd(q, k, v, mask: Mask, scale: float | None = None, out=None, l
     _check(_lib.va_sparse_attn_fwd(_ptr(q), _ptr(k), _ptr(v), mask.handle, _ptr(out), _ptr(lse),
                                    B, Hh, N, d, float(scale), _dtype_code(q), _stream(stream)),
            "va_sparse_attn_fwd")
+    return out, lse
+
+
+def sparse_attn_fwd_host(q, k, v, mask: Mask, scale: float | None = None, out=None, lse=None,
+                         stream=None):
+    """va_sparse_attn_fwd_host on [B, heads, N, d] CPU tensors (pin them for overlapped
+    copies). Asynchronous on `stream` (default: the current CUDA stream): synchronise
+    it before reading out / lse. Returns (out, lse or None)."""
+    import torch
+    for t in (q, k, v, out, lse):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise VAError(ERR_INVALID, "tensor argument (needs contiguous CPU tensors)")
+    B, Hh, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise VAError(ERR_INVALID, "q/k/v shapes or dtypes differ")
+    if out is None:
+        out = torch.empty_like(q, pin_memory=q.is_pinned())
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(_lib.va_sparse_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), mask.handle, _ptr(out),
+                                        _ptr(lse), B, Hh, N, d, float(scale), _dtype_code(q),
+                                        _stream(stream)),
+           "va_sparse_attn_fwd_host")
     return out, lse
 
 

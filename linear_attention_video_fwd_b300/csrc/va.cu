@@ -452,6 +452,138 @@ VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, co
   return VA_ERR_UNSUPPORTED;
 }
 
+// Host-buffer attention: (batch*head) chunks move through a ring of device
+// buffers; host->device copies, the attention kernel and device->host copies
+// run on three streams ordered by events, so the transfers of one chunk
+// overlap the attention of another.
+namespace {
+
+constexpr int kHostRing = 3;
+
+struct HostStreams {
+  cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, in_ready[kHostRing] = {}, in_free[kHostRing] = {},
+              out_free[kHostRing] = {}, done[3] = {};
+  std::mutex enqueue;  // one call at a time enqueues on these streams
+};
+
+// Streams and events of the current device, created on first use.
+int host_streams(HostStreams** out) {
+  static HostStreams per_dev[64];
+  static bool ready[64] = {false};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return VA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  HostStreams& h = per_dev[dev];
+  if (!ready[dev]) {
+    int st;
+    const unsigned fl = cudaEventDisableTiming;
+    if ((st = cuda_status(cudaStreamCreateWithFlags(&h.h2d, cudaStreamNonBlocking))) ||
+        (st = cuda_status(cudaStreamCreateWithFlags(&h.comp, cudaStreamNonBlocking))) ||
+        (st = cuda_status(cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking))) ||
+        (st = cuda_status(cudaEventCreateWithFlags(&h.start, fl))))
+      return st;
+    for (int t = 0; t < 3; ++t)
+      if ((st = cuda_status(cudaEventCreateWithFlags(&h.done[t], fl)))) return st;
+    for (int j = 0; j < kHostRing; ++j)
+      if ((st = cuda_status(cudaEventCreateWithFlags(&h.in_ready[j], fl))) ||
+          (st = cuda_status(cudaEventCreateWithFlags(&h.in_free[j], fl))) ||
+          (st = cuda_status(cudaEventCreateWithFlags(&h.out_free[j], fl))))
+        return st;
+    ready[dev] = true;
+  }
+  *out = &h;
+  return VA_OK;
+}
+
+}  // namespace
+
+VA_EXPORT int va_sparse_attn_fwd_host(const void* q, const void* k, const void* v,
+                                      const va_mask* m, void* out, float* lse, int B, int heads,
+                                      int N, int d, float scale, int dtype, va_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || m == nullptr || out == nullptr)
+    return VA_ERR_INVALID;
+  if (B < 1 || heads < 1 || N != m->N || N < 1 || d < 1) return VA_ERR_INVALID;
+  if (!std::isfinite(scale)) return VA_ERR_INVALID;
+  if (dtype != VA_BF16 && dtype != VA_F32) return VA_ERR_UNSUPPORTED;
+  const int64_t BH64 = static_cast<int64_t>(B) * heads;
+  if (BH64 * N >= (1LL << 31)) return VA_ERR_UNSUPPORTED;
+  const int BH = static_cast<int>(BH64);
+  HostStreams* h = nullptr;
+  int st;
+  if ((st = host_streams(&h))) return st;
+  std::lock_guard<std::mutex> lock(h->enqueue);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // chunks of `hc` (batch*head) slices: about 12 chunks, at least one slice
+  const int hc = BH >= 12 ? BH / 12 : 1;
+  const int nch = (BH + hc - 1) / hc;
+  const size_t esz = dtype == VA_BF16 ? 2 : 4;
+  const size_t slice = static_cast<size_t>(N) * d * esz;   // one (b, h) of q, k, v or out
+  const size_t lslice = static_cast<size_t>(N) * sizeof(float);
+  Scoped scratch(s);
+  uint8_t* buf[kHostRing][4];
+  float* lbuf[kHostRing] = {};
+  for (int j = 0; j < kHostRing; ++j) {
+    for (int t = 0; t < 4; ++t)
+      if ((st = scratch.alloc(&buf[j][t], slice * hc))) return st;
+    if (lse != nullptr && (st = scratch.alloc(&lbuf[j], lslice * hc / sizeof(float)))) return st;
+  }
+  // fork from the caller's stream (the scratch is allocated there) ...
+  if ((st = cuda_status(cudaEventRecord(h->start, s))) ||
+      (st = cuda_status(cudaStreamWaitEvent(h->h2d, h->start, 0))) ||
+      (st = cuda_status(cudaStreamWaitEvent(h->comp, h->start, 0))) ||
+      (st = cuda_status(cudaStreamWaitEvent(h->d2h, h->start, 0))))
+    return st;
+  // ... and join back on every exit, so the scratch is released on the
+  // caller's stream only after all three streams are done with it
+  auto join = [&](int status) -> int {
+    cudaStream_t side[3] = {h->h2d, h->comp, h->d2h};
+    for (int t = 0; t < 3; ++t) {
+      const int js = cuda_status(cudaEventRecord(h->done[t], side[t]));
+      const int ws = js ? js : cuda_status(cudaStreamWaitEvent(s, h->done[t], 0));
+      if (status == VA_OK) status = ws;
+    }
+    return status;
+  };
+  const uint8_t* hin[3] = {static_cast<const uint8_t*>(q), static_cast<const uint8_t*>(k),
+                           static_cast<const uint8_t*>(v)};
+  for (int i = 0; i < nch; ++i) {
+    const int j = i % kHostRing;
+    const int b0 = i * hc, nb = std::min(hc, BH - b0);
+    const size_t off = static_cast<size_t>(b0) * slice, bytes = static_cast<size_t>(nb) * slice;
+    // inputs of slot j are free once the attention of chunk i - ring finished
+    if (i >= kHostRing && (st = cuda_status(cudaStreamWaitEvent(h->h2d, h->in_free[j], 0))))
+      return join(st);
+    for (int t = 0; t < 3; ++t)
+      if ((st = cuda_status(cudaMemcpyAsync(buf[j][t], hin[t] + off, bytes,
+                                            cudaMemcpyHostToDevice, h->h2d))))
+        return join(st);
+    if ((st = cuda_status(cudaEventRecord(h->in_ready[j], h->h2d))) ||
+        (st = cuda_status(cudaStreamWaitEvent(h->comp, h->in_ready[j], 0))))
+      return join(st);
+    // output of slot j is free once the copy-out of chunk i - ring finished
+    if (i >= kHostRing && (st = cuda_status(cudaStreamWaitEvent(h->comp, h->out_free[j], 0))))
+      return join(st);
+    if ((st = va_sparse_attn_fwd(buf[j][0], buf[j][1], buf[j][2], m, buf[j][3],
+                                 lse != nullptr ? lbuf[j] : nullptr, 1, nb, N, d, scale, dtype,
+                                 reinterpret_cast<va_stream_t>(h->comp))))
+      return join(st);
+    if ((st = cuda_status(cudaEventRecord(h->in_free[j], h->comp))) ||
+        (st = cuda_status(cudaStreamWaitEvent(h->d2h, h->in_free[j], 0))) ||
+        (st = cuda_status(cudaMemcpyAsync(static_cast<uint8_t*>(out) + off, buf[j][3], bytes,
+                                          cudaMemcpyDeviceToHost, h->d2h))))
+      return join(st);
+    if (lse != nullptr &&
+        (st = cuda_status(cudaMemcpyAsync(lse + static_cast<size_t>(b0) * N, lbuf[j],
+                                          static_cast<size_t>(nb) * lslice,
+                                          cudaMemcpyDeviceToHost, h->d2h))))
+      return join(st);
+    if ((st = cuda_status(cudaEventRecord(h->out_free[j], h->d2h)))) return join(st);
+  }
+  return join(VA_OK);
+}
+
 // ------------------------------------------------------------ clustering --
 
 namespace {

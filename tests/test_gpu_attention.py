@@ -117,3 +117,45 @@ def test_attention_rejects_bad_arguments(va, dev):
         va.sparse_attn_fwd(q, q, q, m64)
     assert e.value.status == va.ERR_UNSUPPORTED
     assert va.device_error() == va.OK
+
+
+@pytest.mark.parametrize("pinned,with_lse,dtype", [(True, True, "bf16"), (False, False, "bf16"),
+                                                   (True, True, "f32")])
+def test_host_buffers_match_device_call(va, dev, pinned, with_lse, dtype):
+    # va_sparse_attn_fwd_host (host q/k/v/out, pipelined chunks) must give the
+    # device call's result bit for bit: every (batch, head) runs the same kernel.
+    T, H, W = 5, 6, 11                                    # N = 330: ragged last block
+    B, Hh, d = 3, 5, 128                                  # 15 slices: chunks of one slice
+    q, k, v = synth.iid_qkv(B, Hh, T * H * W, d, seed=17)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    qh, kh, vh = (torch.from_numpy(x).to(tdt) for x in (q, k, v))
+    if pinned:
+        qh, kh, vh = qh.pin_memory(), kh.pin_memory(), vh.pin_memory()
+    m = _mask(va, OM.RADIAL, T, H, W, OM.MaskParams(block=128, w0=9))
+    lse_d = torch.empty((B, Hh, T * H * W), dtype=torch.float32, device=dev) if with_lse else None
+    out_d, _ = va.sparse_attn_fwd(qh.to(dev), kh.to(dev), vh.to(dev), m, lse=lse_d)
+    lse_h = torch.empty((B, Hh, T * H * W), dtype=torch.float32) if with_lse else None
+    if with_lse and pinned:
+        lse_h = lse_h.pin_memory()
+    out_h, _ = va.sparse_attn_fwd_host(qh, kh, vh, m, lse=lse_h)
+    torch.cuda.synchronize()
+    assert va.device_error() == va.OK
+    assert torch.equal(out_h, out_d.cpu())
+    if with_lse:
+        assert torch.equal(lse_h, lse_d.cpu())
+    m.free()
+
+
+def test_host_buffers_full_size(va, dev):
+    # Wan-shaped radial workload through the host entry, bit-exact against the
+    # device call (12 slices, one per chunk).
+    T, H, W = 21, 30, 52
+    q, k, v = cached_video_qkv(1, 12, T, H, W, 128, seed=1235)
+    qh, kh, vh = (torch.from_numpy(x).to(torch.bfloat16).pin_memory() for x in (q, k, v))
+    m = _mask(va, OM.RADIAL, T, H, W, OM.MaskParams(block=128))
+    out_d, _ = va.sparse_attn_fwd(qh.to(dev), kh.to(dev), vh.to(dev), m)
+    out_h, _ = va.sparse_attn_fwd_host(qh, kh, vh, m)
+    torch.cuda.synchronize()
+    assert va.device_error() == va.OK
+    assert torch.equal(out_h, out_d.cpu())
+    m.free()
