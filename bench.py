@@ -502,13 +502,90 @@ def run_reference(args, world, rank):
     }
 
 
+def run_linear(args, world, rank, local, mixed):
+    """Linear attention (or LinVideo's mixed attention, r = 0.5 with the radial
+    mask) on the Wan-shaped inputs."""
+    import torch
+    import linear_attention_video_fwd_b300 as va
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS["wan_radial"]
+    T, H, W, heads = wl["T"], wl["H"], wl["W"], wl["heads"]
+    N = T * H * W
+    q, k, v = make_inputs(wl, seed=1235 + rank)
+    qt, kt, vt = (torch.from_numpy(x).to(dev, torch.bfloat16) for x in (q, k, v))
+    out = torch.empty_like(qt)
+    stream = torch.cuda.current_stream()
+    r = 0.5
+    mask = va.mask_build(1, T, H, W, block=128) if mixed else None  # radial
+
+    def call():
+        if mixed:
+            va.mixed_attn_fwd(qt, kt, vt, mask, r, out=out)
+        else:
+            va.linear_attn_fwd(qt, kt, vt, out=out)
+
+    total_ms, launch_ms, clocks = timed_region(args, world, local, call, stream)
+    if va.device_error() != va.OK:
+        raise RuntimeError("device error in the timed region")
+    ms_per_step = total_ms / args.steps
+    call_ms = float(np.mean(launch_ms))
+    tensor_bytes = qt.numel() * qt.element_size()
+    io_bytes = 4 * tensor_bytes                       # read Q, K, V; write O
+    lin_flops = 4.0 * N * D * (D + 1) * BATCH * heads  # phi(K)^T [V | 1] and phi(Q) [S | z]
+    pk, src = peaks()
+    cfg = {"workload": ("LinVideo mixed attention r=0.5 (radial block-sparse + linear)"
+                        if mixed else "linear attention forward, elu+1 feature map"),
+           "B": BATCH, "heads": heads, "grid_THW": [T, H, W], "tokens": N, "head_dim": D,
+           "l2": "inputs larger than L2 (Q+K+V+O = 403 MB per call vs 126 MB L2), no flush",
+           "parallelism": "replicas: one independent workload per GPU"}
+    line = {"n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded Fourier-mode Q/K + N(0,0.5^2), V~N(0,1))",
+            "config": cfg, "gpu_launches": args.steps * (4 if mixed else 3), "clocks": clocks}
+    if mixed:
+        rp, col = mask.csr()
+        blk = 128
+        sizes = np.minimum(blk, N - np.arange((N + blk - 1) // blk) * blk)
+        live = sum(int(sizes[i]) * int(sizes[col[rp[i]:rp[i + 1]]].sum())
+                   for i in range(len(rp) - 1))
+        att_flops = 4.0 * D * live * BATCH * heads
+        flops = att_flops + lin_flops
+        tf = flops / (call_ms * 1e-3) / 1e12
+        line.update({
+            "metric": "LinVideo mixed attention (r=0.5) effective TFLOP/s + ms/call at 32,760 tok",
+            "value": round(world * flops * args.steps / (total_ms * 1e-3) / 1e12, 2),
+            "unit": UNIT,
+            "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16_tflops"],
+                         "unit": UNIT, "frac": round(tf / pk["bf16_tflops"], 4),
+                         "peak_source": "%s bf16 dense burst" % src,
+                         "kernel": "whole call (attention + linear attention)", "traffic": None}})
+        mask.free()
+    else:
+        gbs = io_bytes / (call_ms * 1e-3) / 1e9
+        line.update({
+            "metric": "linear attention forward achieved GB/s + ms/call at 32,760 tok",
+            "value": round(world * io_bytes * args.steps / (total_ms * 1e-3) / 1e9, 1),
+            "unit": "GB/s",
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
+                         "peak_source": "%s copy bandwidth" % src,
+                         "kernel": "whole call (lin_state + lin_prep + lin_out)",
+                         "algorithmic_bytes": io_bytes, "flops": lin_flops, "traffic": None}})
+    head = {k2: line.pop(k2) for k2 in ("metric", "value", "unit")}
+    return {**head, **line}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["svgear"], default="wan_radial")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["svgear", "linear", "mixed"],
+                    default="wan_radial")
     ap.add_argument("--oracle-rows", type=int, default=512,
                     help="query rows per head in the CPU-oracle baseline sample")
     ap.add_argument("--reference-rows", type=int, default=16,
@@ -524,6 +601,8 @@ def main():
         line = run_reference(args, world, rank)
     elif args.workload == "svgear":
         line = run_svgear(args, world, rank, local)
+    elif args.workload in ("linear", "mixed"):
+        line = run_linear(args, world, rank, local, args.workload == "mixed")
     else:
         line = run_ours(args, world, rank, local)
     if rank == 0 and line is not None:

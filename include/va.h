@@ -198,6 +198,38 @@ int va_sparse_attn_fwd_host(const void* q, const void* k, const void* v, const v
                             int dtype, va_stream_t stream);
 
 /*
+ * Linear attention forward (LinVideo, gist.science 2510.08318, technical
+ * summary sec. 1: attention in O(N) instead of O(N^2)). Non-causal, with the
+ * feature map phi(x) = elu(x) + 1 (the page names none; this is the positive
+ * map of Katharopoulos et al. 2020). For every batch b, head h, query i:
+ *   out_i = sum_j (phi(q_i) . phi(k_j)) v_j / sum_j (phi(q_i) . phi(k_j))
+ * computed as phi(q_i)^T S / phi(q_i)^T z with S = sum_j phi(k_j) v_j^T and
+ * z = sum_j phi(k_j) (one read of K and V, one of Q). q, k, v, out:
+ * [B, heads, N, d] device arrays. Supported: VA_BF16 with d = 128 (fp32
+ * accumulation, bf16 output). Errors: VA_ERR_INVALID (null or misaligned
+ * pointers, B, heads or N < 1), VA_ERR_UNSUPPORTED (other dtype or d),
+ * VA_ERR_OOM, VA_ERR_CUDA.
+ */
+int va_linear_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int heads,
+                       int N, int d, int dtype, va_stream_t stream);
+
+/*
+ * LinVideo's mixed attention of one layer (technical summary sec. 2 A: a
+ * scalar r in [0, 1] selects quadratic attention at r = 1 and linear
+ * attention at r = 0):
+ *   out_i = r * att_i + (1 - r) * lin_i
+ * with att the block-sparse softmax attention of va_sparse_attn_fwd under
+ * `mask` (the dense mask gives full attention) and lin that of
+ * va_linear_attn_fwd. r = 1 runs the attention only, r = 0 the linear
+ * attention only. The attention part is rounded to bf16 before the blend.
+ * Supported: VA_BF16, d = 128, mask block 128. Errors: as the two calls, and
+ * VA_ERR_INVALID for r outside [0, 1] or N != the mask's N.
+ */
+int va_mixed_attn_fwd(const void* q, const void* k, const void* v, const va_mask* mask, float r,
+                      void* out, int B, int heads, int N, int d, float scale, int dtype,
+                      va_stream_t stream);
+
+/*
  * Lloyd k-means per (batch, head) on x [B, heads, N, d] (squared Euclidean
  * distance), SVG-EAR's semantic clustering:
  *   centroid <- x[init_idx]; repeat iters times: assign each token to the

@@ -52,6 +52,8 @@ def _load():
         "va_mask_free": [vp],
         "va_sparse_attn_fwd": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp],
         "va_sparse_attn_fwd_host": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp],
+        "va_linear_attn_fwd": [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp],
+        "va_mixed_attn_fwd": [vp, vp, vp, vp, f32, vp, i32, i32, i32, i32, f32, i32, vp],
         "va_cluster": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp],
         "va_compensate_route": [vp, vp, vp, vp, i32, vp, i32, f64, f32, i32, i32, i32, i32, i32,
                                 vp, vp, vp, vp],
@@ -202,6 +204,39 @@ def sparse_attn_fwd_host(q, k, v, mask: Mask, scale: float | None = None, out=No
                                         _stream(stream)),
            "va_sparse_attn_fwd_host")
     return out, lse
+
+
+def linear_attn_fwd(q, k, v, out=None, stream=None):
+    """va_linear_attn_fwd on [B, heads, N, d] CUDA tensors. Returns out."""
+    import torch
+    _require_cuda(q, k, v, out)
+    B, Hh, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise VAError(ERR_INVALID, "q/k/v shapes or dtypes differ")
+    if out is None:
+        out = torch.empty_like(q)
+    _check(_lib.va_linear_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hh, N, d,
+                                   _dtype_code(q), _stream(stream)),
+           "va_linear_attn_fwd")
+    return out
+
+
+def mixed_attn_fwd(q, k, v, mask: Mask, r: float, scale: float | None = None, out=None,
+                   stream=None):
+    """va_mixed_attn_fwd: r * block-sparse attention + (1 - r) * linear attention."""
+    import torch
+    _require_cuda(q, k, v, out)
+    B, Hh, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise VAError(ERR_INVALID, "q/k/v shapes or dtypes differ")
+    if out is None:
+        out = torch.empty_like(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(_lib.va_mixed_attn_fwd(_ptr(q), _ptr(k), _ptr(v), mask.handle, float(r), _ptr(out), B,
+                                  Hh, N, d, float(scale), _dtype_code(q), _stream(stream)),
+           "va_mixed_attn_fwd")
+    return out
 
 
 def cluster(x, C: int, iters: int, init_idx, assign=None, centroid=None, count=None,

@@ -1,0 +1,438 @@
+// Linear attention and LinVideo's mixed attention (LinVideo, gist.science
+// 2510.08318, technical summary sec. 1: O(n) linear attention; sec. 2 A: per
+// layer a scalar r mixes quadratic (r = 1) and linear (r = 0) attention) on
+// the 5th-generation tensor cores, bf16, head_dim 128. Feature map
+// phi(x) = elu(x) + 1; non-causal:
+//   lin_i = phi(q_i)^T S / phi(q_i)^T z,  S = sum_j phi(k_j) v_j^T,  z = sum_j phi(k_j)
+//   mix_i = r att_i + (1 - r) lin_i
+//
+// Three kernels, each HBM-bound (one read of K and V, one of Q, one write of
+// the output):
+//   lin_state_kernel  CTA (split, batch*head) streams 128-token tiles of K
+//                     and V through rings of LN_NS stages; a warpgroup applies phi to the K tile in place
+//                     (tokens >= N get 0), then S += phi(K)^T V and
+//                     z += phi(K)^T 1 on the tensor cores (TMEM), and the
+//                     split's partial {S, z} goes to global memory;
+//   lin_prep_kernel   sums the partials and writes [S | z]^T (144 x 128, rows
+//                     past 128 zero) as bf16 pieces hi + lo (16 significant
+//                     bits, so the product keeps fp32-level accuracy);
+//   lin_out_kernel    persistent CTAs keep the pieces resident and stream
+//                     128-token tiles of Q; num | den = phi(Q) [S | z] on the
+//                     tensor cores, the epilogue writes num / den (mixed with
+//                     the attention output already in `out` when r < 1).
+// Every mbarrier wait is bounded; on a timeout the CTA records
+// VA_ERR_TIMEOUT, drains its copies and MMAs and frees its TMEM.
+#pragma once
+
+#include "common.cuh"
+
+namespace va {
+
+constexpr int LN_TILE = 128 * 128 * 2;   // 32 KB: 128 tokens x 128 dims bf16
+constexpr int LN_HALF = LN_TILE / 2;     // 128 rows x 64 dims
+constexpr int LN_NEXT = 144;             // rows of [S | z]^T (128 + z + padding)
+constexpr int LN_PIECE = LN_NEXT * 128 * 2;   // 36 KB: one bf16 piece of [S | z]^T
+constexpr int LN_PIECE_HALF = LN_PIECE / 2;   // 144 rows x 64 dims
+constexpr int LN_ROW = 129;              // partial row: S[dim][0..128) and z[dim]
+constexpr int LN_STATE_THREADS = 384;
+constexpr int LN_OUT_THREADS = 512;
+constexpr int LN_NS = 3;                 // ring stages (K and V, or Q)
+constexpr int LN_STATE_SMEM = 1024 + 2 * LN_NS * LN_TILE + 4096;    // K, V rings + ones
+constexpr int LN_OUT_SMEM = 1024 + 2 * LN_PIECE + LN_NS * LN_TILE;  // pieces + Q ring
+
+__device__ __forceinline__ float lin_phi(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+
+// phi in place on one 64-dim half h of a 128-token bf16 tile (two
+// 128B-swizzled halves); the thread owns token row r of that half, rows with
+// token >= N become 0. Two warpgroups (h = 0, 1) cover a tile. The 16-byte
+// chunks of a row are visited in a rotated order so the warp's accesses fall
+// on distinct banks (the swizzle only permutes chunks within a row, and phi is
+// elementwise); all eight loads are issued before the stores.
+__device__ __forceinline__ void lin_phi_half(uint8_t* tile, int h, int r, bool valid) {
+  uint4 w[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    w[c] = *reinterpret_cast<const uint4*>(tile + h * LN_HALF + r * 128 + ((c + r) & 7) * 16);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint32_t* e = reinterpret_cast<uint32_t*>(&w[c]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = lin_phi(__uint_as_float(e[i] << 16));
+      const float hi = lin_phi(__uint_as_float(e[i] & 0xffff0000u));
+      e[i] = valid ? pack_bf16x2(lo, hi) : 0u;
+    }
+    *reinterpret_cast<uint4*>(tile + h * LN_HALF + r * 128 + ((c + r) & 7) * 16) = w[c];
+  }
+}
+
+enum : int {
+  LS_KF = 0,                   // LN_NS: K tile loaded
+  LS_VF = LS_KF + LN_NS,       // LN_NS: V tile loaded
+  LS_PHI = LS_VF + LN_NS,      // LN_NS: phi(K) written (256 arrivals)
+  LS_EMPTY = LS_PHI + LN_NS,   // LN_NS: K and V tiles consumed by the MMAs
+  LS_DONE = LS_EMPTY + LN_NS,  // accumulators complete
+  LS_DRAIN = LS_DONE + 1,
+  LS_COUNT = LS_DRAIN + 1
+};
+
+// Token tiles [t_lo, t_hi) of split `split` of `nsplit` over ntiles.
+__device__ __forceinline__ void lin_range(int ntiles, int nsplit, int split, int& t_lo, int& t_hi) {
+  const int per = (ntiles + nsplit - 1) / nsplit;
+  t_lo = min(ntiles, split * per);
+  t_hi = min(ntiles, t_lo + per);
+}
+
+// Grid (nsplit, BH), 256 threads. part[bh][split][dim][0..129) = {S row, z}.
+__global__ void __launch_bounds__(LN_STATE_THREADS, 1)
+    lin_state_kernel(const __grid_constant__ CUtensorMap map_k,
+                     const __grid_constant__ CUtensorMap map_v, int N, float* __restrict__ part,
+                     long long lim) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[LS_COUNT];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* kt = smem;                    // stage s at kt + s TILE
+  uint8_t* vt = smem + LN_NS * LN_TILE;
+  uint8_t* ones = smem + 2 * LN_NS * LN_TILE;  // 16 rows x 128 tokens of 1.0 (K-major halves)
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, bh = blockIdx.y, nsplit = gridDim.x;
+  const int ntiles = (N + 127) / 128;
+  int t_lo, t_hi;
+  lin_range(ntiles, nsplit, split, t_lo, t_hi);
+  const int nt = t_hi - t_lo;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  if (tid == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < LN_NS; ++s) {
+      mbar_init(bar(LS_KF + s), 1);
+      mbar_init(bar(LS_VF + s), 1);
+      mbar_init(bar(LS_PHI + s), 256);
+      mbar_init(bar(LS_EMPTY + s), 1);
+    }
+    mbar_init(bar(LS_DONE), 1);
+    mbar_init(bar(LS_DRAIN), 1);
+    fence_barrier_init();
+  }
+  for (int i = tid; i < 4096 / 4; i += LN_STATE_THREADS)
+    reinterpret_cast<uint32_t*>(ones)[i] = 0x3f803f80u;  // bf16 1.0 pairs
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_s), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;  // S at [0, 128), z at [128, 144)
+  volatile int* abort_p = &abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0 && nt > 0) {
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+      int issued = 0;
+      for (int u = 0; u < nt; ++u) {
+        const int s = u % LN_NS, row = (t_lo + u) * 128;
+        if (u >= LN_NS &&
+            !mbar_wait_bounded(bar(LS_EMPTY + s), ((u / LN_NS) & 1) ^ 1, lim, abort_p))
+          break;
+        mbar_arrive_expect_tx(bar(LS_KF + s), LN_TILE);
+        tma_load_3d(smem_u32(kt + s * LN_TILE), &map_k, bar(LS_KF + s), 0, row, bh);
+        tma_load_3d(smem_u32(kt + s * LN_TILE + LN_HALF), &map_k, bar(LS_KF + s), 64, row, bh);
+        mbar_arrive_expect_tx(bar(LS_VF + s), LN_TILE);
+        tma_load_3d(smem_u32(vt + s * LN_TILE), &map_v, bar(LS_VF + s), 0, row, bh);
+        tma_load_3d(smem_u32(vt + s * LN_TILE + LN_HALF), &map_v, bar(LS_VF + s), 64, row, bh);
+        issued = u + 1;
+      }
+      if (*abort_p) {
+        volatile int no_abort = 0;
+        for (int u = issued > LN_NS ? issued - LN_NS : 0; u < issued; ++u) {
+          no_abort = 0;
+          mbar_wait_bounded(bar(LS_KF + u % LN_NS), (u / LN_NS) & 1, lim, &no_abort);
+          no_abort = 0;
+          mbar_wait_bounded(bar(LS_VF + u % LN_NS), (u / LN_NS) & 1, lim, &no_abort);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nt > 0) {
+      // S (+)= phi(K)^T V: A = phi(K) and B = V, both MN-major (dims contiguous),
+      // K = 16 tokens per MMA; z (+)= phi(K)^T 1 with a K-major ones tile, N = 16.
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, 1, 1);
+      constexpr uint32_t id_z = idesc_bf16_f32(128, 16, 1, 0);
+      const uint32_t sOnes = smem_u32(ones);
+      bool ok = true;
+      for (int u = 0; u < nt; ++u) {
+        const int s = u % LN_NS;
+        const uint32_t ph = (u / LN_NS) & 1;
+        if (!(ok = mbar_wait_bounded(bar(LS_PHI + s), ph, lim, abort_p))) break;
+        if (!(ok = mbar_wait_bounded(bar(LS_VF + s), ph, lim, abort_p))) break;
+        tc_fence_after();
+        const uint32_t sK = smem_u32(kt + s * LN_TILE), sV = smem_u32(vt + s * LN_TILE);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t a = sw128_desc(sK + k * 2048, LN_HALF, 1024);
+          umma_ss(tmem, a, sw128_desc(sV + k * 2048, LN_HALF, 1024), id_s, (u | k) ? 1u : 0u);
+          umma_ss(tmem + 128, a, sw128_desc(sOnes + (k >> 2) * 2048 + (k & 3) * 32, 16, 1024),
+                  id_z, (u | k) ? 1u : 0u);
+        }
+        umma_commit(bar(LS_EMPTY + s));
+      }
+      if (ok) umma_commit(bar(LS_DONE));
+      else {
+        umma_commit(bar(LS_DRAIN));
+        volatile int no_abort = 0;
+        mbar_wait_bounded(bar(LS_DRAIN), 0, lim, &no_abort);
+      }
+    }
+  } else if (warp >= 4) {
+    const int r = (warp & 3) * 32 + lane, h = (warp - 4) >> 2;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int u = 0; u < nt; ++u) {
+      const int s = u % LN_NS;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(LS_KF + s), (u / LN_NS) & 1, lim,
+                                                          abort_p))))
+        break;
+      lin_phi_half(kt + s * LN_TILE, h, r, (t_lo + u) * 128 + r < N);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(LS_PHI + s));
+    }
+    if (h == 0) {  // the epilogue is warps 4..7
+      float* out = part + ((static_cast<long long>(bh) * nsplit + split) * 128 + r) * LN_ROW;
+      if (nt == 0) {
+        for (int n = 0; n < LN_ROW; ++n) out[n] = 0.f;
+      } else if (ok && __all_sync(0xffffffffu, mbar_wait_bounded(bar(LS_DONE), 0, lim, abort_p))) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) out[c * 32 + i] = __uint_as_float(v[i]);
+        }
+        uint32_t zv[16];
+        tmem_ld16(tmem + lane_off + 128, zv);
+        tmem_wait_ld();
+        out[128] = __uint_as_float(zv[0]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// [S | z]^T of each batch*head from the split partials, as bf16 pieces:
+// piece[bh][p][n][dim], p = 0 hi, 1 lo, n < 128 S[dim][n], n = 128 z[dim],
+// n > 128 zero. Grid (LN_NEXT, BH), 128 threads (one per dim).
+__global__ void lin_prep_kernel(const float* __restrict__ part, int nsplit,
+                                __nv_bfloat16* __restrict__ piece) {
+  const int n = blockIdx.x, bh = blockIdx.y, dim = threadIdx.x;
+  float acc = 0.f;
+  if (n <= 128) {
+    const float* pp = part + static_cast<long long>(bh) * nsplit * 128 * LN_ROW;
+    for (int s = 0; s < nsplit; ++s) acc += pp[(static_cast<long long>(s) * 128 + dim) * LN_ROW + n];
+  }
+  const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
+  const long long o = ((static_cast<long long>(bh) * 2) * LN_NEXT + n) * 128 + dim;
+  piece[o] = hi;
+  piece[o + static_cast<long long>(LN_NEXT) * 128] = lo;
+}
+
+enum : int {
+  LO_PF = 0,                 // pieces loaded
+  LO_QF = 1,                 // LN_NS: Q tile loaded
+  LO_PHI = LO_QF + LN_NS,    // LN_NS: phi(Q) written (256 arrivals)
+  LO_QE = LO_PHI + LN_NS,    // LN_NS: Q tile consumed by the MMAs
+  LO_AF = LO_QE + LN_NS,     // 2: accumulator full
+  LO_AE = LO_AF + 2,         // 2: accumulator read (128 arrivals)
+  LO_DRAIN = LO_AE + 2,
+  LO_COUNT = LO_DRAIN + 1
+};
+
+// Grid (nsplit, BH), 512 threads: warp 0 TMA producer, warp 1 MMA issuer,
+// warps 4..7 and 12..15 phi(Q) in place (dims 0..63 and 64..127), warps 8..11
+// epilogue (thread r owns token row r of the tile). out = num / den, or r_mix * out + (1 - r_mix) * num / den when
+// mix != 0 (out then holds the attention output on entry).
+__global__ void __launch_bounds__(LN_OUT_THREADS, 1)
+    lin_out_kernel(const __grid_constant__ CUtensorMap map_q,
+                   const __grid_constant__ CUtensorMap map_p, int N, __nv_bfloat16* __restrict__ out,
+                   int mix, float r_mix, long long lim) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[LO_COUNT];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_flag;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* pc = smem;                    // piece p at pc + p PIECE
+  uint8_t* qt = smem + 2 * LN_PIECE;     // Q stage s at qt + s TILE
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x, bh = blockIdx.y;
+  const int ntiles = (N + 127) / 128;
+  int t_lo, t_hi;
+  lin_range(ntiles, gridDim.x, split, t_lo, t_hi);
+  const int nt = t_hi - t_lo;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(bar(LO_PF), 1);
+    for (int s = 0; s < LN_NS; ++s) {
+      mbar_init(bar(LO_QF + s), 1);
+      mbar_init(bar(LO_PHI + s), 256);
+      mbar_init(bar(LO_QE + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(LO_AF + b), 1);
+      mbar_init(bar(LO_AE + b), 128);
+    }
+    mbar_init(bar(LO_DRAIN), 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_base_s), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;  // accumulator b at [256 b, 256 b + 144)
+  volatile int* abort_p = &abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0 && nt > 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_p);
+      mbar_arrive_expect_tx(bar(LO_PF), 2 * LN_PIECE);
+      for (int p = 0; p < 2; ++p)
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(smem_u32(pc + p * LN_PIECE + h * LN_PIECE_HALF), &map_p, bar(LO_PF), 64 * h,
+                      p * LN_NEXT, bh);
+      int issued = 0;
+      for (int u = 0; u < nt; ++u) {
+        const int s = u % LN_NS, row = (t_lo + u) * 128;
+        if (u >= LN_NS &&
+            !mbar_wait_bounded(bar(LO_QE + s), ((u / LN_NS) & 1) ^ 1, lim, abort_p))
+          break;
+        mbar_arrive_expect_tx(bar(LO_QF + s), LN_TILE);
+        tma_load_3d(smem_u32(qt + s * LN_TILE), &map_q, bar(LO_QF + s), 0, row, bh);
+        tma_load_3d(smem_u32(qt + s * LN_TILE + LN_HALF), &map_q, bar(LO_QF + s), 64, row, bh);
+        issued = u + 1;
+      }
+      if (*abort_p) {
+        volatile int no_abort = 0;
+        mbar_wait_bounded(bar(LO_PF), 0, lim, &no_abort);
+        for (int u = issued > LN_NS ? issued - LN_NS : 0; u < issued; ++u) {
+          no_abort = 0;
+          mbar_wait_bounded(bar(LO_QF + u % LN_NS), (u / LN_NS) & 1, lim, &no_abort);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nt > 0) {
+      // num | den = phi(Q) [S | z]: A = phi(Q) K-major, B = [S | z]^T K-major
+      // (144 rows), two pieces accumulated in fp32.
+      constexpr uint32_t id = idesc_bf16_f32(128, LN_NEXT, 0, 0);
+      const uint32_t sP = smem_u32(pc);
+      bool ok = mbar_wait_bounded(bar(LO_PF), 0, lim, abort_p);
+      for (int u = 0; ok && u < nt; ++u) {
+        const int s = u % LN_NS, b = u & 1;
+        if (!(ok = mbar_wait_bounded(bar(LO_PHI + s), (u / LN_NS) & 1, lim, abort_p))) break;
+        if (u >= 2 &&
+            !(ok = mbar_wait_bounded(bar(LO_AE + b), ((u >> 1) & 1) ^ 1, lim, abort_p)))
+          break;
+        tc_fence_after();
+        const uint32_t sQ = smem_u32(qt + s * LN_TILE);
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            umma_ss(tmem + b * 256,
+                    sw128_desc(sQ + (k >> 2) * LN_HALF + (k & 3) * 32, 16, 1024),
+                    sw128_desc(sP + p * LN_PIECE + (k >> 2) * LN_PIECE_HALF + (k & 3) * 32, 16, 1024),
+                    id, (p | k) ? 1u : 0u);
+        umma_commit(bar(LO_QE + s));
+        umma_commit(bar(LO_AF + b));
+      }
+      if (!ok) {
+        umma_commit(bar(LO_DRAIN));
+        volatile int no_abort = 0;
+        mbar_wait_bounded(bar(LO_DRAIN), 0, lim, &no_abort);
+      }
+    }
+  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
+    const int r = (warp & 3) * 32 + lane, h = warp >= 12 ? 1 : 0;
+    for (int u = 0; u < nt; ++u) {
+      const int s = u % LN_NS;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait_bounded(bar(LO_QF + s), (u / LN_NS) & 1, lim, abort_p)))
+        break;
+      lin_phi_half(qt + s * LN_TILE, h, r, true);
+      fence_proxy_async_smem();
+      mbar_arrive(bar(LO_PHI + s));
+    }
+  } else if (warp >= 8) {
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    for (int u = 0; u < nt; ++u) {
+      const int b = u & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_AF + b), (u >> 1) & 1, lim, abort_p)))
+        break;
+      tc_fence_after();
+      const uint32_t tA = tmem + b * 256 + lane_off;
+      uint32_t dv[16];
+      tmem_ld16(tA + 128, dv);
+      tmem_wait_ld();
+      const float inv = 1.f / __uint_as_float(dv[0]);
+      const int tok = (t_lo + u) * 128 + r;
+      __nv_bfloat16* orow = out + (static_cast<long long>(bh) * N + tok) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tA + c * 32, v);
+        tmem_wait_ld();
+        if (c == 3) {
+          tc_fence_before();
+          mbar_arrive(bar(LO_AE + b));
+        }
+        if (tok < N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            float o[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(v[q4 * 8 + e]) * inv;
+            if (mix) {
+              const uint4 a = dst[q4];
+              const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                o[2 * e] = fmaf(r_mix, __uint_as_float(aw[e] << 16) - o[2 * e], o[2 * e]);
+                o[2 * e + 1] =
+                    fmaf(r_mix, __uint_as_float(aw[e] & 0xffff0000u) - o[2 * e + 1], o[2 * e + 1]);
+              }
+            }
+            uint4 w;
+            w.x = pack_bf16x2(o[0], o[1]);
+            w.y = pack_bf16x2(o[2], o[3]);
+            w.z = pack_bf16x2(o[4], o[5]);
+            w.w = pack_bf16x2(o[6], o[7]);
+            dst[q4] = w;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace va

@@ -20,6 +20,7 @@
 #include "kmeans_tc.cuh"
 #include "comp_tc.cuh"
 #include "probe_tc.cuh"
+#include "linear_tc.cuh"
 
 #define VA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -582,6 +583,98 @@ VA_EXPORT int va_sparse_attn_fwd_host(const void* q, const void* k, const void* 
     if ((st = cuda_status(cudaEventRecord(h->out_free[j], h->d2h)))) return join(st);
   }
   return join(VA_OK);
+}
+
+// ------------------------------------------------- linear / mixed attention --
+
+namespace {
+
+// Linear attention (bf16, d = 128) of every (batch, head): split state sums,
+// their merge into bf16 pieces of [S | z]^T, then the output; with mix != 0
+// the output kernel blends r * out (the attention already there) with the
+// linear result.
+int run_linear(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+               __nv_bfloat16* out, int BH, int N, int mix, float r, cudaStream_t s) {
+  static bool configured[64] = {false};
+  static int num_sms[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int st;
+  if (dev < 0 || dev >= 64) return VA_ERR_UNSUPPORTED;
+  if (!configured[dev]) {
+    if ((st = cuda_status(cudaFuncSetAttribute(va::lin_state_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               va::LN_STATE_SMEM))) ||
+        (st = cuda_status(cudaFuncSetAttribute(va::lin_out_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               va::LN_OUT_SMEM))) ||
+        (st = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
+                                                 dev))))
+      return st;
+    configured[dev] = true;
+  }
+  const int ntiles = (N + 127) / 128;
+  const int nsplit = std::max(1, std::min(ntiles, num_sms[dev] / BH));
+  Scoped scratch(s);
+  float* part;
+  __nv_bfloat16* piece;
+  const size_t bh = static_cast<size_t>(BH);
+  if ((st = scratch.alloc(&part, bh * nsplit * 128 * va::LN_ROW)) ||
+      (st = scratch.alloc(&piece, bh * 2 * va::LN_NEXT * 128)))
+    return st;
+  CUtensorMap mk, mv, mq, mp;
+  if ((st = encode_bf16_rows(&mk, k, BH, N, 128)) || (st = encode_bf16_rows(&mv, v, BH, N, 128)) ||
+      (st = encode_bf16_rows(&mq, q, BH, N, 128)) ||
+      (st = encode_bf16_rows_box(&mp, piece, BH, 2 * va::LN_NEXT, 128, va::LN_NEXT)))
+    return st;
+  va::lin_state_kernel<<<dim3(nsplit, BH), va::LN_STATE_THREADS, va::LN_STATE_SMEM, s>>>(
+      mk, mv, N, part, g_wait_limit);
+  va::lin_prep_kernel<<<dim3(va::LN_NEXT, BH), 128, 0, s>>>(part, nsplit, piece);
+  va::lin_out_kernel<<<dim3(nsplit, BH), va::LN_OUT_THREADS, va::LN_OUT_SMEM, s>>>(
+      mq, mp, N, out, mix, r, g_wait_limit);
+  return launch_status();
+}
+
+int check_linear_args(const void* q, const void* k, const void* v, const void* out, int B,
+                      int heads, int N, int d, int dtype, int* BH) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return VA_ERR_INVALID;
+  if (B < 1 || heads < 1 || N < 1) return VA_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VA_ERR_INVALID;
+  if (dtype != VA_BF16 || d != 128) return VA_ERR_UNSUPPORTED;
+  const int64_t BH64 = static_cast<int64_t>(B) * heads;
+  if (BH64 > 65535 || BH64 * N >= (1LL << 31)) return VA_ERR_UNSUPPORTED;
+  *BH = static_cast<int>(BH64);
+  return VA_OK;
+}
+
+}  // namespace
+
+VA_EXPORT int va_linear_attn_fwd(const void* q, const void* k, const void* v, void* out, int B,
+                                 int heads, int N, int d, int dtype, va_stream_t stream) {
+  int BH = 0;
+  const int st = check_linear_args(q, k, v, out, B, heads, N, d, dtype, &BH);
+  if (st) return st;
+  using T = __nv_bfloat16;
+  return run_linear(static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+                    static_cast<T*>(out), BH, N, 0, 0.f, reinterpret_cast<cudaStream_t>(stream));
+}
+
+VA_EXPORT int va_mixed_attn_fwd(const void* q, const void* k, const void* v, const va_mask* m,
+                                float r, void* out, int B, int heads, int N, int d, float scale,
+                                int dtype, va_stream_t stream) {
+  int BH = 0;
+  int st = check_linear_args(q, k, v, out, B, heads, N, d, dtype, &BH);
+  if (st) return st;
+  if (m == nullptr || N != m->N) return VA_ERR_INVALID;
+  if (!(r >= 0.f && r <= 1.f)) return VA_ERR_INVALID;
+  using T = __nv_bfloat16;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (r > 0.f &&
+      (st = va_sparse_attn_fwd(q, k, v, m, out, nullptr, B, heads, N, d, scale, dtype, stream)))
+    return st;
+  if (r == 1.f) return VA_OK;
+  return run_linear(static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+                    static_cast<T*>(out), BH, N, r > 0.f ? 1 : 0, r, s);
 }
 
 // ------------------------------------------------------------ clustering --
