@@ -249,6 +249,20 @@ int va_cluster(const void* x, const int32_t* init_idx, int B, int heads, int N, 
                va_stream_t stream);
 
 /*
+ * va_cluster warm-started from given centroids instead of seed indices: the
+ * clusters of the previous denoising step, say, so that a few iterations
+ * refine them (SVG-EAR clusters queries and keys at every step; nearby steps
+ * have nearby activations). centroid_init: device float32 [B, heads, C, d],
+ * 16-byte aligned; it may be the same array as `centroid`. Starting from the
+ * float copies of x[init_idx] gives exactly va_cluster's result, and k
+ * iterations from the centroids after m give exactly the result after m + k.
+ * Other arguments, outputs and errors as va_cluster.
+ */
+int va_cluster_from(const void* x, const float* centroid_init, int B, int heads, int N, int d,
+                    int C, int iters, int dtype, int32_t* assign, float* centroid,
+                    int32_t* count, va_stream_t stream);
+
+/*
  * SVG-EAR compensated sparse attention with error-aware routing.
  * A block is (query cluster p, key cluster c); n_p, n_c are cluster sizes and
  * qc_p, kc_c, vc_c member means (float32) of q, k, v.

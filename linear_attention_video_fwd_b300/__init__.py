@@ -55,6 +55,7 @@ def _load():
         "va_linear_attn_fwd": [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp],
         "va_mixed_attn_fwd": [vp, vp, vp, vp, f32, vp, i32, i32, i32, i32, f32, i32, vp],
         "va_cluster": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp],
+        "va_cluster_from": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp],
         "va_compensate_route": [vp, vp, vp, vp, i32, vp, i32, f64, f32, i32, i32, i32, i32, i32,
                                 vp, vp, vp, vp],
         "va_device_error": [vp],
@@ -257,6 +258,31 @@ def cluster(x, C: int, iters: int, init_idx, assign=None, centroid=None, count=N
     _check(_lib.va_cluster(_ptr(x), _ptr(init_idx), B, Hh, N, d, C, iters, _dtype_code(x),
                            _ptr(assign), _ptr(centroid), _ptr(count), _stream(stream)),
            "va_cluster")
+    return assign, centroid, count
+
+
+def cluster_from(x, centroid_init, iters: int, assign=None, centroid=None, count=None,
+                 stream=None):
+    """va_cluster_from: Lloyd k-means warm-started from float32 centroids
+    [B, heads, C, d] (may be passed again as `centroid`). Returns (assign, centroid, count)."""
+    import torch
+    _require_cuda(x, centroid_init, assign, centroid, count)
+    B, Hh, N, d = x.shape
+    if centroid_init.dtype != torch.float32 or centroid_init.dim() != 4 or \
+            tuple(centroid_init.shape[:2]) != (B, Hh) or centroid_init.shape[3] != d:
+        raise VAError(ERR_INVALID, "centroid_init must be float32 [B, heads, C, d]")
+    C = centroid_init.shape[2]
+    dev = x.device
+    if assign is None:
+        assign = torch.empty((B, Hh, N), dtype=torch.int32, device=dev)
+    if centroid is None:
+        centroid = torch.empty((B, Hh, C, d), dtype=torch.float32, device=dev)
+    if count is None:
+        count = torch.empty((B, Hh, C), dtype=torch.int32, device=dev)
+    _check(_lib.va_cluster_from(_ptr(x), _ptr(centroid_init), B, Hh, N, d, C, iters,
+                                _dtype_code(x), _ptr(assign), _ptr(centroid), _ptr(count),
+                                _stream(stream)),
+           "va_cluster_from")
     return assign, centroid, count
 
 

@@ -424,6 +424,31 @@ __global__ void km_finalize_kernel(const unsigned long long* __restrict__ sums,
 // Initial centroids: cent[bh][c] = x[bh][init[bh][c]] (fp32), |c|^2 to cnorm.
 // Indices outside [0, N) are reported as VA_ERR_DEVICE (the row is zeroed).
 // One warp per centroid; grid (ceil(C / 8), BH).
+// Warm start: cent = c0 (skipped when they alias) and cnorm = |c0|^2, with
+// the same per-lane order of accumulation as km_init_kernel, so a warm start
+// from the float copies of the seed rows reproduces a seeded run exactly.
+// Grid (ceil(C / 8), BH), 256 threads.
+template <int D>
+__global__ void km_warm_kernel(const float* __restrict__ c0, int C, float* __restrict__ cent,
+                               float* __restrict__ cnorm) {
+  constexpr int PER = D / 32;
+  const int bh = blockIdx.y;
+  const int c = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (c >= C) return;
+  const long long row = (static_cast<long long>(bh) * C + c) * D + lane * PER;
+  float nrm = 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const float v = c0[row + e];
+    if (c0 != cent) cent[row + e] = v;
+    nrm = fmaf(v, v, nrm);
+  }
+#pragma unroll
+  for (int o2 = 16; o2; o2 >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o2);
+  if (lane == 0) cnorm[static_cast<long long>(bh) * C + c] = nrm;
+}
+
 template <typename T, int D>
 __global__ void km_init_kernel(const T* __restrict__ x, const int* __restrict__ init, int N,
                                int C, float* __restrict__ cent, float* __restrict__ cnorm) {

@@ -719,8 +719,8 @@ int cluster_lists(const int* assign, int BH, int N, int C, int* count, int* off,
 }
 
 // bf16, d = 128: distances on the tensor cores (split-bf16 centroids).
-int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C, int iters,
-                   int* assign, float* cent, int* count, cudaStream_t s) {
+int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int BH, int N, int C,
+                   int iters, int* assign, float* cent, int* count, cudaStream_t s) {
   static bool configured[64] = {false};
   static int num_sms[64] = {0};
   int dev = 0;
@@ -772,7 +772,10 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C
   const dim3 ga(nsplit, nchunks, BH);
   const dim3 gn((N + 255) / 256, BH);
   const unsigned gs = static_cast<unsigned>((nc + 255) / 256);
-  va::km_init_kernel<__nv_bfloat16, 128><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
+  if (c0 != nullptr)
+    va::km_warm_kernel<128><<<gc, 256, 0, s>>>(c0, C, cent, cnorm);
+  else
+    va::km_init_kernel<__nv_bfloat16, 128><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
   va::km_split_kernel<<<gs, 256, 0, s>>>(cent, static_cast<long long>(nc), hi, lo);
   const int rounds = iters > 0 ? iters : 1;
   for (int it = 0; it < rounds; ++it) {
@@ -793,8 +796,8 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, int BH, int N, int C
 }
 
 template <typename T, int D>
-int run_cluster(const T* x, const int* init, int BH, int N, int C, int iters, int* assign,
-                float* cent, int* count, cudaStream_t s) {
+int run_cluster(const T* x, const int* init, const float* c0, int BH, int N, int C, int iters,
+                int* assign, float* cent, int* count, cudaStream_t s) {
   int st = set_smem_attrs<T, D>();
   if (st) return st;
   Scoped scratch(s);
@@ -808,7 +811,10 @@ int run_cluster(const T* x, const int* init, int BH, int N, int C, int iters, in
   const dim3 gc((C + 7) / 8, BH);
   const dim3 ga((N + va::KM_PT - 1) / va::KM_PT, BH);
   const dim3 gn((N + 255) / 256, BH);
-  va::km_init_kernel<T, D><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
+  if (c0 != nullptr)
+    va::km_warm_kernel<D><<<gc, 256, 0, s>>>(c0, C, cent, cnorm);
+  else
+    va::km_init_kernel<T, D><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
   const int rounds = iters > 0 ? iters : 1;
   for (int it = 0; it < rounds; ++it) {
     if ((st = cuda_status(cudaMemsetAsync(count, 0, sizeof(int) * BH * C, s)))) return st;
@@ -824,37 +830,58 @@ int run_cluster(const T* x, const int* init, int BH, int N, int C, int iters, in
 
 }  // namespace
 
-VA_EXPORT int va_cluster(const void* x, const int32_t* init_idx, int B, int heads, int N, int d,
-                         int C, int iters, int dtype, int32_t* assign, float* centroid,
-                         int32_t* count, va_stream_t stream) {
-  if (x == nullptr || init_idx == nullptr || assign == nullptr || centroid == nullptr ||
-      count == nullptr)
+namespace {
+
+// Seeded (init_idx) or warm-started (c0) Lloyd k-means; exactly one is set.
+int cluster_entry(const void* x, const int32_t* init_idx, const float* c0, int B, int heads,
+                  int N, int d, int C, int iters, int dtype, int32_t* assign, float* centroid,
+                  int32_t* count, va_stream_t stream) {
+  if (x == nullptr || assign == nullptr || centroid == nullptr || count == nullptr)
     return VA_ERR_INVALID;
   if (B < 1 || heads < 1 || N < 1 || C < 1 || C > N || iters < 0) return VA_ERR_INVALID;
   if (!aligned16(x) || !aligned16(centroid) || (reinterpret_cast<uintptr_t>(assign) & 3u) ||
-      (reinterpret_cast<uintptr_t>(count) & 3u) || (reinterpret_cast<uintptr_t>(init_idx) & 3u))
+      (reinterpret_cast<uintptr_t>(count) & 3u) || (reinterpret_cast<uintptr_t>(init_idx) & 3u) ||
+      (reinterpret_cast<uintptr_t>(c0) & 15u))
     return VA_ERR_INVALID;
   if (C > kMaxClusters || (d != 64 && d != 128)) return VA_ERR_UNSUPPORTED;
   const int64_t BH64 = static_cast<int64_t>(B) * heads;
   if (BH64 > 65535 || BH64 * N * d >= (1LL << 40)) return VA_ERR_UNSUPPORTED;
   const int BH = static_cast<int>(BH64);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int* ii = init_idx;
   if (dtype == VA_BF16) {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    return d == 128 ? run_cluster_tc(xb, init_idx, BH, N, C, iters, assign, centroid, count, s)
-                    : run_cluster<__nv_bfloat16, 64>(xb, init_idx, BH, N, C, iters, assign,
+    return d == 128 ? run_cluster_tc(xb, ii, c0, BH, N, C, iters, assign, centroid, count, s)
+                    : run_cluster<__nv_bfloat16, 64>(xb, ii, c0, BH, N, C, iters, assign,
                                                      centroid, count, s);
   }
   if (dtype == VA_F32) {
     const float* xf = static_cast<const float*>(x);
-    return d == 128 ? run_cluster<float, 128>(xf, init_idx, BH, N, C, iters, assign, centroid,
+    return d == 128 ? run_cluster<float, 128>(xf, ii, c0, BH, N, C, iters, assign, centroid,
                                               count, s)
-                    : run_cluster<float, 64>(xf, init_idx, BH, N, C, iters, assign, centroid,
+                    : run_cluster<float, 64>(xf, ii, c0, BH, N, C, iters, assign, centroid,
                                              count, s);
   }
   return VA_ERR_UNSUPPORTED;
 }
 
+}  // namespace
+
+VA_EXPORT int va_cluster(const void* x, const int32_t* init_idx, int B, int heads, int N, int d,
+                         int C, int iters, int dtype, int32_t* assign, float* centroid,
+                         int32_t* count, va_stream_t stream) {
+  if (init_idx == nullptr) return VA_ERR_INVALID;
+  return cluster_entry(x, init_idx, nullptr, B, heads, N, d, C, iters, dtype, assign, centroid,
+                       count, stream);
+}
+
+VA_EXPORT int va_cluster_from(const void* x, const float* centroid_init, int B, int heads, int N,
+                              int d, int C, int iters, int dtype, int32_t* assign,
+                              float* centroid, int32_t* count, va_stream_t stream) {
+  if (centroid_init == nullptr) return VA_ERR_INVALID;
+  return cluster_entry(x, nullptr, centroid_init, B, heads, N, d, C, iters, dtype, assign,
+                       centroid, count, stream);
+}
 // -------------------------------------------- compensation and routing --
 
 namespace {

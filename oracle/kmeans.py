@@ -72,6 +72,21 @@ def lloyd(x, init_idx, iters: int):
     return a, c, np.bincount(a, minlength=C)
 
 
+def lloyd_from(x, c0, iters: int):
+    """Lloyd iterations from given centroids c0 [C, d] (a warm start, e.g. the
+    previous denoising step's clusters); otherwise the same steps as lloyd."""
+    x = np.asarray(x, dtype=np.float64)
+    c = np.asarray(c0, dtype=np.float64).copy()
+    C = c.shape[0]
+    if iters == 0:
+        a = assign(x, c)
+        return a, c, np.bincount(a, minlength=C)
+    for _ in range(iters):
+        a = assign(x, c)
+        c = update(x, a, c)
+    return a, c, np.bincount(a, minlength=C)
+
+
 def inertia(x, a, c) -> float:
     """Sum of squared distances of points to their assigned centroid."""
     x = np.asarray(x, dtype=np.float64)

@@ -245,3 +245,34 @@ def test_svgear_full_size(va, dev):
     h = 3                                                  # probe on one head
     pr = S.probe(q[0, h], k[0, h], v[0, h], qa[0, h], Cq, ka[0, h], Ck, scale)
     _check_err(err[0, h], pr["err"])
+
+
+@pytest.mark.parametrize("B,Hh,N,d,C", [(1, 2, 1500, 128, 300),   # tensor-core path, 2 chunks
+                                         (2, 1, 517, 64, 7)])     # FMA path
+def test_kmeans_warm_start_from_seed_rows_equals_seeded(va, dev, B, Hh, N, d, C):
+    # warm start (reuse across denoising steps): starting from the float copies
+    # of the seed rows is the seeded run, bit for bit
+    x = torch.from_numpy(synth.iid_qkv(B, Hh, N, d, seed=51)[0]).to(dev, torch.bfloat16)
+    init = torch.from_numpy(synth.init_indices(B, Hh, N, C, seed=52)).to(dev)
+    c0 = torch.stack([torch.stack([x[b, h, init[b, h].long()].float() for h in range(Hh)])
+                      for b in range(B)]).contiguous()
+    for iters in (0, 3):
+        a1, c1, n1 = va.cluster(x, C, iters, init)
+        a2, c2, n2 = va.cluster_from(x, c0, iters)
+        torch.cuda.synchronize()
+        assert va.device_error() == va.OK
+        assert torch.equal(a1, a2) and torch.equal(c1, c2) and torch.equal(n1, n2)
+
+
+def test_kmeans_warm_start_continues_the_iteration(va, dev):
+    # 4 iterations from the centroids after 6 give the result after 10
+    q, _, _ = cached_video_qkv(1, 2, 8, 32, 32, 128, seed=53)
+    x = torch.from_numpy(q).to(dev, torch.bfloat16)
+    N, C = x.shape[2], 256
+    init = torch.from_numpy(synth.init_indices(1, 2, N, C, seed=54)).to(dev)
+    a10, c10, n10 = va.cluster(x, C, 10, init)
+    _, c6, _ = va.cluster(x, C, 6, init)
+    a, c, n = va.cluster_from(x, c6, 4, centroid=c6)     # in place
+    torch.cuda.synchronize()
+    assert va.device_error() == va.OK
+    assert torch.equal(a, a10) and torch.equal(c, c10) and torch.equal(n, n10)

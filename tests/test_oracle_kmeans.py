@@ -92,3 +92,25 @@ def test_inertia_never_increases():
         val = KM.inertia(x, a, c)
         assert val <= prev + 1e-9
         prev = val
+
+
+def test_warm_start_from_seed_rows_equals_seeded_lloyd():
+    # a warm start from the seed points themselves is the seeded run
+    rng = np.random.default_rng(31)
+    x = rng.normal(size=(300, 6))
+    idx = rng.choice(300, size=9, replace=False)
+    for iters in (0, 1, 4):
+        a1, c1, n1 = KM.lloyd(x, idx, iters)
+        a2, c2, n2 = KM.lloyd_from(x, x[idx], iters)
+        assert np.array_equal(a1, a2) and np.array_equal(c1, c2) and np.array_equal(n1, n2)
+
+
+def test_warm_start_continues_the_iteration():
+    # k more iterations from the centroids after m equal m + k iterations
+    rng = np.random.default_rng(32)
+    x = rng.normal(size=(400, 5))
+    idx = rng.choice(400, size=12, replace=False)
+    _, c3, _ = KM.lloyd(x, idx, 3)
+    a5, c5, n5 = KM.lloyd(x, idx, 5)
+    b5, d5, m5 = KM.lloyd_from(x, c3, 2)
+    assert np.array_equal(a5, b5) and np.allclose(c5, d5, rtol=0, atol=0) and np.array_equal(n5, m5)
