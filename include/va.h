@@ -230,6 +230,45 @@ int va_mixed_attn_fwd(const void* q, const void* k, const void* v, const va_mask
                       va_stream_t stream);
 
 /*
+ * LIPAR inter-frame pruning (LIPAR summary, sec. 2 B; readings, as the page
+ * gives no formulas). x: device latent [B, T*H*W, C] of `dtype` (token
+ * n = t*H*W + h*W + w). Per batch:
+ *   changed(t, h, w) = t == 0 or max_c |x[t,h,w,c] - x[t-1,h,w,c]| >= tau
+ *   keep(t, h, w)    = t == 0 or changed anywhere in the 3 x 3 spatial
+ *                      neighbourhood of (h, w) in frame t (motion check)
+ * Outputs (device, caller-owned): keep uint8 [B, N]; order int32 [B, N] whose
+ * first count[b] entries list the kept tokens in token order (the compacted
+ * sequence); src int32 [B, N], the compacted slot that restores token n (its
+ * own slot if kept, else src of the same (h, w) in frame t - 1); count int32
+ * [B]. The decisions use the largest channel difference, exact in float32.
+ * Errors: VA_ERR_INVALID (null or misaligned pointers, sizes < 1, NaN tau),
+ * VA_ERR_UNSUPPORTED (dtype, sizes), VA_ERR_OOM, VA_ERR_CUDA.
+ */
+int va_lipar_prune(const void* x, int B, int T, int H, int W, int C, float tau, int dtype,
+                   uint8_t* keep, int32_t* order, int32_t* src, int32_t* count,
+                   va_stream_t stream);
+
+/*
+ * Compaction of a [B, heads, N, d] device tensor to the kept tokens of
+ * va_lipar_prune: out[b, h, k] = x[b, h, order[b, k]] for k < count[b] (rows
+ * from count[b] on are left as they are), so out holds the shorter sequence
+ * that attention then runs on. d * element size must be a multiple of 16
+ * bytes; x and out 16-byte aligned. Errors: VA_ERR_INVALID,
+ * VA_ERR_UNSUPPORTED, VA_ERR_CUDA.
+ */
+int va_lipar_gather(const void* x, const int32_t* order, const int32_t* count, int B, int heads,
+                    int N, int d, int dtype, void* out, va_stream_t stream);
+
+/*
+ * Restoration (LIPAR summary, sec. 2 B): out[b, h, n] = y[b, h, src[b, n]]
+ * expands a compacted [B, heads, N, d] result (first count[b] rows valid) to
+ * the full sequence, a pruned token taking the result of its previous-frame
+ * source. Same layout rules and errors as va_lipar_gather.
+ */
+int va_lipar_restore(const void* y, const int32_t* src, int B, int heads, int N, int d, int dtype,
+                     void* out, va_stream_t stream);
+
+/*
  * Lloyd k-means per (batch, head) on x [B, heads, N, d] (squared Euclidean
  * distance), SVG-EAR's semantic clustering:
  *   centroid <- x[init_idx]; repeat iters times: assign each token to the

@@ -56,6 +56,9 @@ def _load():
         "va_mixed_attn_fwd": [vp, vp, vp, vp, f32, vp, i32, i32, i32, i32, f32, i32, vp],
         "va_cluster": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp],
         "va_cluster_from": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp],
+        "va_lipar_prune": [vp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, vp, vp],
+        "va_lipar_gather": [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp],
+        "va_lipar_restore": [vp, vp, i32, i32, i32, i32, i32, vp, vp],
         "va_compensate_route": [vp, vp, vp, vp, i32, vp, i32, f64, f32, i32, i32, i32, i32, i32,
                                 vp, vp, vp, vp],
         "va_device_error": [vp],
@@ -284,6 +287,51 @@ def cluster_from(x, centroid_init, iters: int, assign=None, centroid=None, count
                                 _stream(stream)),
            "va_cluster_from")
     return assign, centroid, count
+
+
+def lipar_prune(x, T: int, H: int, W: int, tau: float, stream=None):
+    """va_lipar_prune on a [B, T*H*W, C] CUDA latent.
+    Returns (keep uint8 [B, N], order int32 [B, N], src int32 [B, N], count int32 [B])."""
+    import torch
+    _require_cuda(x)
+    B, N, C = x.shape
+    if N != T * H * W:
+        raise VAError(ERR_INVALID, "x must be [B, T*H*W, C]")
+    dev = x.device
+    keep = torch.empty((B, N), dtype=torch.uint8, device=dev)
+    order = torch.empty((B, N), dtype=torch.int32, device=dev)
+    src = torch.empty((B, N), dtype=torch.int32, device=dev)
+    count = torch.empty((B,), dtype=torch.int32, device=dev)
+    _check(_lib.va_lipar_prune(_ptr(x), B, T, H, W, C, float(tau), _dtype_code(x), _ptr(keep),
+                               _ptr(order), _ptr(src), _ptr(count), _stream(stream)),
+           "va_lipar_prune")
+    return keep, order, src, count
+
+
+def lipar_gather(x, order, count, out=None, stream=None):
+    """va_lipar_gather: compacted copy of a [B, heads, N, d] CUDA tensor."""
+    import torch
+    _require_cuda(x, order, count, out)
+    B, Hh, N, d = x.shape
+    if out is None:
+        out = torch.zeros_like(x)
+    _check(_lib.va_lipar_gather(_ptr(x), _ptr(order), _ptr(count), B, Hh, N, d, _dtype_code(x),
+                                _ptr(out), _stream(stream)),
+           "va_lipar_gather")
+    return out
+
+
+def lipar_restore(y, src, out=None, stream=None):
+    """va_lipar_restore: full-length [B, heads, N, d] result from a compacted one."""
+    import torch
+    _require_cuda(y, src, out)
+    B, Hh, N, d = y.shape
+    if out is None:
+        out = torch.empty_like(y)
+    _check(_lib.va_lipar_restore(_ptr(y), _ptr(src), B, Hh, N, d, _dtype_code(y), _ptr(out),
+                                 _stream(stream)),
+           "va_lipar_restore")
+    return out
 
 
 def compensate_route(q, k, v, qassign, Cq: int, kassign, Ck: int, density: float,

@@ -21,6 +21,7 @@
 #include "comp_tc.cuh"
 #include "probe_tc.cuh"
 #include "linear_tc.cuh"
+#include "lipar.cuh"
 
 #define VA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -675,6 +676,88 @@ VA_EXPORT int va_mixed_attn_fwd(const void* q, const void* k, const void* v, con
   if (r == 1.f) return VA_OK;
   return run_linear(static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
                     static_cast<T*>(out), BH, N, r > 0.f ? 1 : 0, r, s);
+}
+
+// ------------------------------------------------------------------ LIPAR --
+
+VA_EXPORT int va_lipar_prune(const void* x, int B, int T, int H, int W, int C, float tau,
+                             int dtype, uint8_t* keep, int32_t* order, int32_t* src,
+                             int32_t* count, va_stream_t stream) {
+  if (x == nullptr || keep == nullptr || order == nullptr || src == nullptr || count == nullptr)
+    return VA_ERR_INVALID;
+  if (B < 1 || T < 1 || H < 1 || W < 1 || C < 1 || std::isnan(tau)) return VA_ERR_INVALID;
+  if (dtype != VA_BF16 && dtype != VA_F32) return VA_ERR_UNSUPPORTED;
+  const int64_t N64 = static_cast<int64_t>(T) * H * W;
+  if (N64 >= (1LL << 31) || static_cast<int64_t>(B) * N64 * C >= (1LL << 40) || B > 65535)
+    return VA_ERR_UNSUPPORTED;
+  const size_t esz = dtype == VA_BF16 ? 2 : 4;
+  if ((reinterpret_cast<uintptr_t>(x) & (esz - 1)) ||
+      (reinterpret_cast<uintptr_t>(order) & 3u) || (reinterpret_cast<uintptr_t>(src) & 3u) ||
+      (reinterpret_cast<uintptr_t>(count) & 3u))
+    return VA_ERR_INVALID;
+  const int N = static_cast<int>(N64), F = H * W;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Scoped scratch(s);
+  uint8_t* changed;
+  int* slot;
+  int st;
+  if ((st = scratch.alloc(&changed, static_cast<size_t>(B) * N)) ||
+      (st = scratch.alloc(&slot, static_cast<size_t>(B) * N)))
+    return st;
+  const dim3 gw((N + 7) / 8, B), gt((N + 255) / 256, B);
+  if (dtype == VA_BF16)
+    va::lp_changed_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), N, F, C, tau, changed);
+  else
+    va::lp_changed_kernel<float><<<gw, 256, 0, s>>>(static_cast<const float*>(x), N, F, C, tau,
+                                                    changed);
+  va::lp_keep_kernel<<<gt, 256, 0, s>>>(changed, N, H, W, keep);
+  va::lp_compact_kernel<<<B, 1024, 0, s>>>(keep, N, slot, order, count);
+  va::lp_src_kernel<<<dim3((F + 255) / 256, B), 256, 0, s>>>(slot, T, F, src);
+  return launch_status();
+}
+
+namespace {
+
+int lipar_rows_check(const void* a, const void* b, int B, int heads, int N, int d, int dtype,
+                     int* row16) {
+  if (a == nullptr || b == nullptr) return VA_ERR_INVALID;
+  if (B < 1 || heads < 1 || N < 1 || d < 1) return VA_ERR_INVALID;
+  if (dtype != VA_BF16 && dtype != VA_F32) return VA_ERR_UNSUPPORTED;
+  const int64_t bytes = static_cast<int64_t>(d) * (dtype == VA_BF16 ? 2 : 4);
+  if (bytes % 16 != 0) return VA_ERR_UNSUPPORTED;
+  if (!aligned16(a) || !aligned16(b)) return VA_ERR_INVALID;
+  const int64_t BH = static_cast<int64_t>(B) * heads;
+  if (BH > 65535 || BH * N >= (1LL << 40)) return VA_ERR_UNSUPPORTED;
+  *row16 = static_cast<int>(bytes / 16);
+  return VA_OK;
+}
+
+}  // namespace
+
+VA_EXPORT int va_lipar_gather(const void* x, const int32_t* order, const int32_t* count, int B,
+                              int heads, int N, int d, int dtype, void* out,
+                              va_stream_t stream) {
+  int row16 = 0;
+  int st = lipar_rows_check(x, out, B, heads, N, d, dtype, &row16);
+  if (st) return st;
+  if (order == nullptr || count == nullptr) return VA_ERR_INVALID;
+  va::lp_gather_kernel<<<dim3((N + 7) / 8, B * heads), 256, 0,
+                         reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(x), order, count, heads, N, row16, static_cast<uint4*>(out));
+  return launch_status();
+}
+
+VA_EXPORT int va_lipar_restore(const void* y, const int32_t* src, int B, int heads, int N, int d,
+                               int dtype, void* out, va_stream_t stream) {
+  int row16 = 0;
+  int st = lipar_rows_check(y, out, B, heads, N, d, dtype, &row16);
+  if (st) return st;
+  if (src == nullptr) return VA_ERR_INVALID;
+  va::lp_restore_kernel<<<dim3((N + 7) / 8, B * heads), 256, 0,
+                          reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(y), src, heads, N, row16, static_cast<uint4*>(out));
+  return launch_status();
 }
 
 // ------------------------------------------------------------ clustering --
