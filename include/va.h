@@ -178,6 +178,35 @@ int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mas
                        int dtype, va_stream_t stream);
 
 /*
+ * Block-sparse attention backward: the gradients of va_sparse_attn_fwd's
+ * output for an upstream gradient dout = dL/dout (Radial Attention, hyper.ai
+ * news page: LoRA fine-tuning for 4x longer videos trains through the same
+ * masked attention; the page gives no formulas, these are the chain rule of
+ * the forward's definition). With p_ij = exp(scale q_i . k_j - lse_i) on the
+ * live blocks (j < N) and delta_i = dout_i . out_i:
+ *   ds_ij = p_ij (dout_i . v_j - delta_i)
+ *   dq_i  = scale sum_j ds_ij k_j,  dk_j = scale sum_i ds_ij q_i,
+ *   dv_j  = sum_i p_ij dout_i
+ * q, k, v, out, dout, dq, dk, dv: [B, heads, N, d] device arrays of `dtype`
+ * (out and lse as the forward call with the same q, k, v, mask and scale
+ * returned them); lse: [B, heads, N] float32. A row the forward gave
+ * lse = -inf contributes nothing. dq, dk, dv are written (not accumulated)
+ * and must not overlap the inputs. Each gradient row is reduced in a fixed
+ * order (no atomics): results are deterministic. Uses the mask's transposed
+ * block lists (built by va_mask_build) for dk and dv, and 8 * B * heads *
+ * ceil(N / block) * block bytes of stream-ordered scratch.
+ * Supported: as the forward (VA_BF16, d = 128, block 128 on tcgen05; VA_F32,
+ * d in {64, 128}, block in {64, 128} on the FMA pipes), B * heads <= 65535.
+ * Errors: VA_ERR_INVALID (null or misaligned pointers, N != T*H*W of the
+ * mask, B or heads < 1, non-finite scale), VA_ERR_UNSUPPORTED,
+ * VA_ERR_OOM (scratch), VA_ERR_CUDA.
+ */
+int va_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, const va_mask* mask, void* dq,
+                       void* dk, void* dv, int B, int heads, int N, int d, float scale,
+                       int dtype, va_stream_t stream);
+
+/*
  * The same attention with q, k, v, out (and lse, if not NULL) in HOST memory,
  * laid out as above; the library owns the device copies. The (batch, head)
  * slices go through a ring of device buffers in chunks: host-to-device

@@ -52,6 +52,8 @@ def _load():
         "va_mask_free": [vp],
         "va_sparse_attn_fwd": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp],
         "va_sparse_attn_fwd_host": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp],
+        "va_sparse_attn_bwd": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
+                               i32, vp],
         "va_linear_attn_fwd": [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp],
         "va_mixed_attn_fwd": [vp, vp, vp, vp, f32, vp, i32, i32, i32, i32, f32, i32, vp],
         "va_cluster": [vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp],
@@ -185,6 +187,31 @@ def sparse_attn_fwd(q, k, v, mask: Mask, scale: float | None = None, out=None, l
                                    B, Hh, N, d, float(scale), _dtype_code(q), _stream(stream)),
            "va_sparse_attn_fwd")
     return out, lse
+
+
+def sparse_attn_bwd(q, k, v, out, dout, lse, mask: Mask, scale: float | None = None, dq=None,
+                    dk=None, dv=None, stream=None):
+    """va_sparse_attn_bwd on [B, heads, N, d] CUDA tensors: the gradients of
+    sparse_attn_fwd's output (out, lse from the forward call) for the upstream
+    gradient dout. Returns (dq, dk, dv)."""
+    import torch
+    _require_cuda(q, k, v, out, dout, lse, dq, dk, dv)
+    B, Hh, N, d = q.shape
+    for t in (k, v, out, dout):
+        if t.shape != q.shape or t.dtype != q.dtype:
+            raise VAError(ERR_INVALID, "q/k/v/out/dout shapes or dtypes differ")
+    if lse is None or lse.shape != (B, Hh, N) or lse.dtype != torch.float32:
+        raise VAError(ERR_INVALID, "lse must be float32 [B, heads, N]")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(_lib.va_sparse_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                   mask.handle, _ptr(dq), _ptr(dk), _ptr(dv), B, Hh, N, d,
+                                   float(scale), _dtype_code(q), _stream(stream)),
+           "va_sparse_attn_bwd")
+    return dq, dk, dv
 
 
 def sparse_attn_fwd_host(q, k, v, mask: Mask, scale: float | None = None, out=None, lse=None,

@@ -22,6 +22,9 @@ namespace va {
 struct MaskDesc {
   int kind, T, F, N, block, nb;
   int w0, local, period, anchor0, rot_stride, step;
+  // 1: count and fill the transposed lists (for key block I, the query blocks
+  // J that see it), which the backward's key-side kernels walk.
+  int transpose = 0;
 };
 
 __device__ __forceinline__ bool run_pair_live(const MaskDesc& m, int ti, int lo_i, int hi_i,
@@ -73,7 +76,7 @@ __global__ void mask_count_kernel(MaskDesc m, int* __restrict__ cnt,
   long long kt = 0;
   for (int J0 = 0; J0 < m.nb; J0 += 32) {
     const int J = J0 + lane;
-    const bool live = J < m.nb && block_pair_live(m, I, J);
+    const bool live = J < m.nb && (m.transpose ? block_pair_live(m, J, I) : block_pair_live(m, I, J));
     c += __popc(__ballot_sync(0xffffffffu, live));
     if (live) kt += min(m.N, (J + 1) * m.block) - J * m.block;
   }
@@ -149,7 +152,7 @@ __global__ void mask_fill_kernel(MaskDesc m, const int* __restrict__ row_ptr,
   const int end = row_ptr[I + 1];
   for (int J0 = 0; J0 < m.nb; J0 += 32) {
     const int J = J0 + lane;
-    const bool live = J < m.nb && block_pair_live(m, I, J);
+    const bool live = J < m.nb && (m.transpose ? block_pair_live(m, J, I) : block_pair_live(m, I, J));
     const unsigned bal = __ballot_sync(0xffffffffu, live);
     const int pos = base + __popc(bal & ((1u << lane) - 1u));
     if (live) {

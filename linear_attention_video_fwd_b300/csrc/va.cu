@@ -22,6 +22,8 @@
 #include "probe_tc.cuh"
 #include "linear_tc.cuh"
 #include "lipar.cuh"
+#include "attn_bwd_simt.cuh"
+#include "attn_bwd_tc.cuh"
 
 #define VA_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -170,6 +172,11 @@ struct va_mask {
   int32_t* pcol = nullptr;     // device [nnz]: merged rows, entry J << 2 | live bits
   int32_t* plen = nullptr;     // device [npairs]: merged length per pair
   int32_t* porder = nullptr;   // device [npairs]: pairs by descending work
+  // transposed lists for the backward: for key block J, the query blocks
+  // that see it (ascending), and key blocks by descending list length
+  int32_t* t_ptr = nullptr;    // device [nqb + 1]
+  int32_t* t_row = nullptr;    // device [nnz]
+  int32_t* t_order = nullptr;  // device [nqb]
   int device = 0;
 };
 
@@ -316,6 +323,24 @@ VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params*
       va_mask_free(m);
       return st;
     }
+    // The transposed lists reuse the count / scan / fill kernels with the
+    // roles of query and key blocks swapped; the live pairs are the same, so
+    // their number is already known.
+    if ((st = cuda_status(cudaMalloc(&m->t_ptr, sizeof(int32_t) * (md.nb + 1)))) ||
+        (st = cuda_status(cudaMalloc(&m->t_order, sizeof(int32_t) * md.nb))) ||
+        (st = cuda_status(cudaMalloc(&m->t_row, sizeof(int32_t) * (m->nnz > 0 ? m->nnz : 1))))) {
+      va_mask_free(m);
+      return st;
+    }
+    va::MaskDesc mt = md;
+    mt.transpose = 1;
+    va::mask_count_kernel<<<blocks, threads, 0, s>>>(mt, cnt, keytok);
+    va::mask_scan_kernel<<<1, 1024, 0, s>>>(mt, cnt, keytok, m->t_ptr, summary, m->t_order, hist);
+    va::mask_fill_kernel<<<blocks, threads, 0, s>>>(mt, m->t_ptr, m->t_row);
+    if ((st = launch_status())) {
+      va_mask_free(m);
+      return st;
+    }
   }
   if ((st = cuda_status(cudaStreamSynchronize(s)))) {
     va_mask_free(m);
@@ -363,6 +388,9 @@ VA_EXPORT int va_mask_free(va_mask* m) {
   if (m->pcol) cudaFree(m->pcol);
   if (m->plen) cudaFree(m->plen);
   if (m->porder) cudaFree(m->porder);
+  if (m->t_ptr) cudaFree(m->t_ptr);
+  if (m->t_row) cudaFree(m->t_row);
+  if (m->t_order) cudaFree(m->t_order);
   delete m;
   return VA_OK;
 }
@@ -452,6 +480,129 @@ VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, co
     return VA_ERR_UNSUPPORTED;
   }
   return VA_ERR_UNSUPPORTED;
+}
+
+// --------------------------------------------------------------- backward --
+
+namespace {
+
+template <typename T, int D, int BLK>
+int launch_bwd_simt(const void* q, const void* k, const void* v, const void* g, const va_mask* m,
+                    const float* delta, const float* lse2, void* dq, void* dk, void* dv, int BH,
+                    int N, int Np, float scale, cudaStream_t s) {
+  dim3 grid(m->nqb * (BLK / va::BWS_ROWS), BH);
+  const float sl2 = scale * 1.4426950408889634f;
+  va::bwd_dq_simt_kernel<T, D, BLK><<<grid, va::BWS_ROWS * 4, 0, s>>>(
+      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+      static_cast<const T*>(g), delta, lse2, m->row_ptr, m->col, static_cast<T*>(dq), N, Np,
+      scale, sl2);
+  va::bwd_dkdv_simt_kernel<T, D, BLK><<<grid, va::BWS_ROWS * 4, 0, s>>>(
+      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+      static_cast<const T*>(g), delta, lse2, m->t_ptr, m->t_row, static_cast<T*>(dk),
+      static_cast<T*>(dv), N, Np, scale, sl2);
+  return launch_status();
+}
+
+int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, const va_mask* m,
+                  const float* delta, const float* lse2, void* dq, void* dk, void* dv, int BH,
+                  int N, int Np, float scale, cudaStream_t s) {
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !configured[dev]) {
+    int st;
+    if ((st = cuda_status(cudaFuncSetAttribute(va::bwd_dkdv_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               va::BW_SMEM_BYTES))) ||
+        (st = cuda_status(cudaFuncSetAttribute(va::bwd_dq_tc_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               va::BW_SMEM_BYTES))))
+      return st;
+    configured[dev] = true;
+  }
+  CUtensorMap mq, mk, mv, mg;
+  int st;
+  if ((st = encode_bf16_rows(&mq, q, BH, N, 128)) || (st = encode_bf16_rows(&mk, k, BH, N, 128)) ||
+      (st = encode_bf16_rows(&mv, v, BH, N, 128)) || (st = encode_bf16_rows(&mg, g, BH, N, 128)))
+    return st;
+  const long long grid = static_cast<long long>(m->nqb) * BH;
+  if (grid > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
+  va::BwArgs a;
+  a.delta = delta;
+  a.lse2 = lse2;
+  a.N = N;
+  a.Np = Np;
+  a.nb = m->nqb;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit = g_wait_limit;
+  a.ptr = m->t_ptr;
+  a.idx = m->t_row;
+  a.order = m->t_order;
+  a.d0 = static_cast<__nv_bfloat16*>(dv);
+  a.d1 = static_cast<__nv_bfloat16*>(dk);
+  va::bwd_dkdv_tc_kernel<<<static_cast<unsigned>(grid), va::BW_THREADS, va::BW_SMEM_BYTES, s>>>(
+      mq, mk, mv, mg, a);
+  a.ptr = m->row_ptr;
+  a.idx = m->col;
+  a.order = m->order;
+  a.d0 = static_cast<__nv_bfloat16*>(dq);
+  a.d1 = nullptr;
+  va::bwd_dq_tc_kernel<<<static_cast<unsigned>(grid), va::BW_THREADS, va::BW_SMEM_BYTES, s>>>(
+      mq, mk, mv, mg, a);
+  return launch_status();
+}
+
+}  // namespace
+
+VA_EXPORT int va_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                                 const void* dout, const float* lse, const va_mask* m, void* dq,
+                                 void* dk, void* dv, int B, int heads, int N, int d, float scale,
+                                 int dtype, va_stream_t stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || dout == nullptr ||
+      lse == nullptr || m == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+    return VA_ERR_INVALID;
+  if (B < 1 || heads < 1 || N != m->N || m->t_ptr == nullptr) return VA_ERR_INVALID;
+  for (const void* p : {q, k, v, out, dout, static_cast<const void*>(dq),
+                        static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if (!aligned16(p)) return VA_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return VA_ERR_INVALID;
+  if (!std::isfinite(scale)) return VA_ERR_INVALID;
+  const int64_t BH64 = static_cast<int64_t>(B) * heads;
+  if (BH64 > 65535) return VA_ERR_UNSUPPORTED;
+  if (BH64 * N >= (1LL << 31)) return VA_ERR_UNSUPPORTED;
+  const int BH = static_cast<int>(BH64);
+  const int blk = m->p.block;
+  const int Np = m->nqb * blk;
+  const bool tc = dtype == VA_BF16 && d == 128 && blk == 128;
+  const bool simt = dtype == VA_F32 && (d == 64 || d == 128) && (blk == 64 || blk == 128);
+  if (!tc && !simt) return VA_ERR_UNSUPPORTED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  Scoped scratch(s);
+  float* delta = nullptr;
+  float* lse2 = nullptr;
+  int st;
+  const size_t rows = static_cast<size_t>(BH) * Np;
+  if ((st = scratch.alloc(&delta, rows)) || (st = scratch.alloc(&lse2, rows))) return st;
+  dim3 pgrid((Np + 7) / 8, BH);
+  if (tc) {
+    va::bwd_prep_kernel<__nv_bfloat16><<<pgrid, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, N,
+        Np, d, delta, lse2);
+    if ((st = launch_status())) return st;
+    return launch_bwd_tc(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
+  }
+  va::bwd_prep_kernel<float><<<pgrid, 256, 0, s>>>(static_cast<const float*>(out),
+                                                   static_cast<const float*>(dout), lse, N, Np,
+                                                   d, delta, lse2);
+  if ((st = launch_status())) return st;
+  if (d == 64 && blk == 64)
+    return launch_bwd_simt<float, 64, 64>(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
+  if (d == 64 && blk == 128)
+    return launch_bwd_simt<float, 64, 128>(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
+  if (d == 128 && blk == 64)
+    return launch_bwd_simt<float, 128, 64>(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
+  return launch_bwd_simt<float, 128, 128>(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
 }
 
 // Host-buffer attention: (batch*head) chunks move through a ring of device

@@ -29,7 +29,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 _MASK64 = (1 << 64) - 1
 
 # tensor ids of the streams
-Q, K, V, MODES, INIT = 1, 2, 3, 4, 5
+Q, K, V, MODES, INIT, GRAD = 1, 2, 3, 4, 5, 6
 
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -201,6 +201,17 @@ def iid_qkv(B: int, heads: int, N: int, d: int, seed: int, dtype: str = "f32"):
                 x[b, h] = normals_f32(stream_key(seed, tensor, b, h), N * d).reshape(N, d)
         out.append(round_bf16_(x) if dtype == "bf16" else x)
     return tuple(out)
+
+
+def upstream_grad(B: int, heads: int, N: int, d: int, seed: int, dtype: str = "bf16",
+                  std: float = 1.0) -> np.ndarray:
+    """An upstream gradient dL/dO of shape [B, heads, N, d]: i.i.d. N(0, std^2)
+    float32, bf16-representable (RNE) when dtype is "bf16"."""
+    x = np.empty((B, heads, N, d), dtype=np.float32)
+    for b in range(B):
+        for h in range(heads):
+            x[b, h] = normals_f32(stream_key(seed, GRAD, b, h), N * d, std).reshape(N, d)
+    return round_bf16_(x) if dtype == "bf16" else x
 
 
 def init_indices(B: int, heads: int, N: int, C: int, seed: int, tensor: int = INIT) -> np.ndarray:
