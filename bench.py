@@ -20,6 +20,10 @@ pairs of |I| * |J|, real tokens only) * B * heads per call, and ms per call.
   svgear          one SVG-EAR step on the Wan shape: k-means of Q (256
                   clusters) and K (1,024 clusters), 10 iterations each, then
                   va_compensate_route at 15% density
+  linear, mixed   linear attention (GB/s) and LinVideo's mixed attention at
+                  r = 0.5 with the radial mask, on the Wan-shaped inputs
+  backward        the attention backward (dq, dk, dv) of the Wan radial
+                  workload: 2.5x the forward's FLOPs per call
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                        [--workload NAME]
@@ -578,13 +582,124 @@ def run_linear(args, world, rank, local, mixed):
     return {**head, **line}
 
 
+def run_bwd(args, world, rank, local):
+    """The block-sparse attention backward on the Wan radial workload: one
+    va_sparse_attn_bwd call per step (row preprocess, dK/dV kernel, dQ kernel),
+    with out and lse from one forward call before timing."""
+    import torch
+    import linear_attention_video_fwd_b300 as va
+    from oracle import attention as OA
+    from oracle import attention_bwd as OB
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = WORKLOADS["wan_radial"]
+    T, H, W, heads = wl["T"], wl["H"], wl["W"], wl["heads"]
+    N = T * H * W
+    q, k, v = make_inputs(wl, seed=1235 + rank)
+    g = synth.upstream_grad(BATCH, heads, N, D, seed=1235 + rank)
+    qt, kt, vt, gt = (torch.from_numpy(x).to(dev, torch.bfloat16) for x in (q, k, v, g))
+    mask = va.mask_build(va.RADIAL, T, H, W, block=BLOCK)
+    lse = torch.empty((BATCH, heads, N), dtype=torch.float32, device=dev)
+    out, _ = va.sparse_attn_fwd(qt, kt, vt, mask, lse=lse)
+    dq, dk, dv = (torch.empty_like(qt) for _ in range(3))
+    fwd_flops = 4.0 * D * mask.live_pairs * BATCH * heads
+    flops = 2.5 * fwd_flops          # S, dP, dV, dK, dQ: five products per live pair
+    stream = torch.cuda.current_stream()
+
+    def call():
+        va.sparse_attn_bwd(qt, kt, vt, out, gt, lse, mask, dq=dq, dk=dk, dv=dv)
+
+    total_ms, launch_ms, clocks = timed_region(args, world, local, call, stream)
+    if va.device_error() != va.OK:
+        raise RuntimeError("device error in the timed region")
+    ms_per_step = total_ms / args.steps
+    call_ms = float(np.mean(launch_ms))
+
+    # end to end: host q, k, v, out, dout, lse in; host dq, dk, dv out
+    host_in = [x.to("cpu").pin_memory() for x in (qt, kt, vt, out, gt, lse)]
+    host_out = [torch.empty(qt.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
+    dev_in = [qt, kt, vt, out, gt, lse]
+
+    def e2e_call():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        call()
+        for h_, d_ in zip(host_out, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        e2e_call()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+    pk, src = peaks()
+    tf = flops / (call_ms * 1e-3) / 1e12
+    line = {
+        "metric": "block-sparse attn backward effective TFLOP/s + ms/call at 32,760 tok",
+        "value": round(world * flops * args.steps / (total_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Fourier-mode Q/K + N(0,0.5^2), V~N(0,1), dO~N(0,1))",
+        "config": dict(workload_config("wan_radial", wl),
+                       workload="Wan-2.1-1.3B-shaped radial block-sparse attention backward "
+                                "(dq, dk, dv from out, lse, dO)",
+                       l2="inputs larger than L2 (Q+K+V+O+dO+dQ+dK+dV = 805 MB per call), "
+                          "no flush",
+                       parallelism="replicas: one independent workload per GPU"),
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16_tflops"],
+                     "unit": UNIT, "frac": round(tf / pk["bf16_tflops"], 4),
+                     "peak_source": "%s bf16 dense burst" % src,
+                     "frac_of_sustained": round(tf / pk["bf16_tflops_sustained"], 4),
+                     "flops_per_launch": flops, "launch_ms_mean": round(call_ms, 4),
+                     "kernel": "whole call (bwd_prep + bwd_dkdv_tc + bwd_dq_tc)",
+                     "traffic": None},
+        "gpu_launches": args.steps * 3,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        bm = oracle_block_mask(wl)
+        rows = OA.sample_rows(N, BLOCK, 64, seed=8)
+        live_keys = (bm * np.minimum(BLOCK, N - np.arange(bm.shape[0]) * BLOCK)[None, :]).sum(1)
+        oflops = 6.0 * D * float(live_keys[rows // BLOCK].sum()) * BATCH * heads
+        t0 = time.perf_counter()
+        OB.block_sparse_attention_grad(q, k, v, g, bm, BLOCK, 1.0 / np.sqrt(D), rows=rows,
+                                       keys=np.array([], dtype=np.int64))
+        secs = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT,
+                                "cores": threads_used(), "kind": "oracle",
+                                "seconds": round(secs, 2),
+                                "sample": "dq of %d seeded query rows x %d heads (float64 "
+                                          "oracle: logits, dP and dQ products, 6*d FLOPs per "
+                                          "live pair)" % (len(rows), heads)}
+    mask.free()
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["svgear", "linear", "mixed"],
+    ap.add_argument("--workload",
+                    choices=sorted(WORKLOADS) + ["svgear", "linear", "mixed", "backward"],
                     default="wan_radial")
     ap.add_argument("--oracle-rows", type=int, default=512,
                     help="query rows per head in the CPU-oracle baseline sample")
@@ -603,6 +718,8 @@ def main():
         line = run_svgear(args, world, rank, local)
     elif args.workload in ("linear", "mixed"):
         line = run_linear(args, world, rank, local, args.workload == "mixed")
+    elif args.workload == "backward":
+        line = run_bwd(args, world, rank, local)
     else:
         line = run_ours(args, world, rank, local)
     if rank == 0 and line is not None:
