@@ -34,7 +34,8 @@ namespace va {
 
 constexpr int BW_THREADS = 384;
 constexpr int BW_NS = 2;  // ring stages
-constexpr int BW_SMEM_BYTES = 1024 + TC_TILE_BYTES * (2 + 2 * BW_NS);
+constexpr int BW_ROWVEC = 1024;  // per stage: lse2 and delta of one 128-row block
+constexpr int BW_SMEM_BYTES = 1024 + TC_TILE_BYTES * (2 + 2 * BW_NS) + BW_NS * BW_ROWVEC;
 
 struct BwArgs {
   const int* ptr;    // CSR (query side) or transposed CSR (key side) offsets
@@ -111,6 +112,16 @@ __device__ __forceinline__ void bw_store64(uint32_t taddr, float mul, __nv_bfloa
   }
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to shared memory, completing on `bar`.
+__device__ __forceinline__ void bw_bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void bw_load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                              int row, int bh) {
   tma_load_3d(dst, map, bar, 0, row, bh);
@@ -158,12 +169,16 @@ __device__ __forceinline__ void bw_setup(uint64_t* bars, uint32_t* tmem_base_s, 
 }
 
 // Producer of both kernels: the resident pair of tiles at block `own`, then
-// the streamed pair for every entry of the list.
+// the streamed pair for every entry of the list. With rv0 != nullptr each
+// entry also brings the 128 floats of rv0 and rv1 at its block (the lse2 and
+// delta rows of a query block) to sX + stage * BW_ROWVEC.
 __device__ __forceinline__ void bw_produce(const CUtensorMap* r0, const CUtensorMap* r1,
                                            const CUtensorMap* s0, const CUtensorMap* s1,
                                            uint32_t sR, uint32_t sA, uint32_t sB, int own,
                                            const int* list, int n, int bh, uint64_t* bars,
-                                           long long lim, volatile int* abort_p) {
+                                           long long lim, volatile int* abort_p,
+                                           const float* rv0 = nullptr,
+                                           const float* rv1 = nullptr, uint32_t sX = 0) {
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   tma_prefetch_desc(r0);
   tma_prefetch_desc(r1);
@@ -178,9 +193,13 @@ __device__ __forceinline__ void bw_produce(const CUtensorMap* r0, const CUtensor
     if (u >= BW_NS &&
         !mbar_wait_bounded(bar(KA_EMPTY + s), ((u / BW_NS) & 1) ^ 1, lim, abort_p))
       break;
-    mbar_arrive_expect_tx(bar(KA_FULL + s), 2 * TC_TILE_BYTES);
+    mbar_arrive_expect_tx(bar(KA_FULL + s), 2 * TC_TILE_BYTES + (rv0 ? BW_ROWVEC : 0));
     bw_load_tile(sA + s * TC_TILE_BYTES, s0, bar(KA_FULL + s), blk * TC_BLK, bh);
     bw_load_tile(sB + s * TC_TILE_BYTES, s1, bar(KA_FULL + s), blk * TC_BLK, bh);
+    if (rv0 != nullptr) {
+      bw_bulk_load(sX + s * BW_ROWVEC, rv0 + blk * TC_BLK, 512, bar(KA_FULL + s));
+      bw_bulk_load(sX + s * BW_ROWVEC + 512, rv1 + blk * TC_BLK, 512, bar(KA_FULL + s));
+    }
     issued = u + 1;
   }
   if (*abort_p) {
@@ -222,6 +241,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sK = smem_u32(smem), sV = sK + TC_TILE_BYTES;
   const uint32_t sQ0 = sV + TC_TILE_BYTES, sG0 = sQ0 + BW_NS * TC_TILE_BYTES;
+  const uint32_t sX = sG0 + BW_NS * TC_TILE_BYTES;  // lse2 | delta per stage
+  const float* rowvec = reinterpret_cast<const float*>(smem + (sX - sK));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x / a.nb;
   const int J = a.order[blockIdx.x % a.nb];
@@ -237,7 +258,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (warp == 0) {
     if (lane == 0 && n > 0)
       bw_produce(&map_k, &map_v, &map_q, &map_g, sK, sQ0, sG0, J, list, n, bh, bars, lim,
-                 abort_p);
+                 abort_p, a.lse2 + static_cast<long long>(bh) * a.Np,
+                 a.delta + static_cast<long long>(bh) * a.Np, sX);
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       bool ok = mbar_wait_bounded(bar(KA_RES), 0, lim, abort_p) &&
@@ -277,12 +299,17 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const int wq = warp & 3, r = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t col = lane_off + h * 64;
-    const float* l2b = a.lse2 + static_cast<long long>(bh) * a.Np + h * 64;
-    const float* dlb = a.delta + static_cast<long long>(bh) * a.Np + h * 64;
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int u = 0; u < n; ++u) {
-      const int q0 = list[u] * TC_BLK;
+      // lse2 and delta of this query block's 64 columns, staged with its tiles
+      // (the stage cannot be refilled before this iteration's dS is written)
+      const int s = u % BW_NS;
+      const float* l2b = rowvec + s * (BW_ROWVEC / 4) + h * 64;
+      const float* dlb = l2b + 128;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(KA_FULL + s), (u / BW_NS) & 1,
+                                                          lim, abort_p))))
+        break;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(KA_S), u & 1, lim, abort_p))))
         break;
       tc_fence_after();
@@ -290,7 +317,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       bw_ld64(tS + col, p);
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
-        const float4 l = __ldg(reinterpret_cast<const float4*>(l2b + q0 + c));
+        const float4 l = *reinterpret_cast<const float4*>(l2b + c);
         p[c] = ex2_approx(fmaf(p[c], sl2, -l.x));
         p[c + 1] = ex2_approx(fmaf(p[c + 1], sl2, -l.y));
         p[c + 2] = ex2_approx(fmaf(p[c + 2], sl2, -l.z));
@@ -306,7 +333,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       bw_ld64(tDP + col, ds);
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
-        const float4 dl = __ldg(reinterpret_cast<const float4*>(dlb + q0 + c));
+        const float4 dl = *reinterpret_cast<const float4*>(dlb + c);
         ds[c] = p[c] * (ds[c] - dl.x);
         ds[c + 1] = p[c + 1] * (ds[c + 1] - dl.y);
         ds[c + 2] = p[c + 2] * (ds[c + 2] - dl.z);
