@@ -15,14 +15,15 @@
 
 namespace va {
 
-// Per row of a [BH, N] grid padded to Np rows per head: delta = g . o in
-// float32 and lse2 = lse * log2(e). Padding rows, and rows that saw no key
-// (lse = -inf), get lse2 = +inf (so every recomputed p is 0) and delta = 0.
+// Per row of a [BH, N] grid padded to Np rows per head, both negated so the
+// kernels add them: ndelta = -(g . o) in float32 and nlse2 = -lse * log2(e).
+// Padding rows, and rows that saw no key (lse = -inf), get nlse2 = -inf (so
+// every recomputed p is 0) and ndelta = 0.
 // One warp per row; grid (ceil(Np / 8), BH), 256 threads.
 template <typename T>
 __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ g,
                                 const float* __restrict__ lse, int N, int Np, int D,
-                                float* __restrict__ delta, float* __restrict__ lse2) {
+                                float* __restrict__ ndelta, float* __restrict__ nlse2) {
   const int bh = blockIdx.y;
   const int n = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -30,8 +31,8 @@ __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ g
   const long long out = static_cast<long long>(bh) * Np + n;
   if (n >= N) {
     if (lane == 0) {
-      delta[out] = 0.f;
-      lse2[out] = INFINITY;
+      ndelta[out] = 0.f;
+      nlse2[out] = -INFINITY;
     }
     return;
   }
@@ -43,8 +44,8 @@ __global__ void bwd_prep_kernel(const T* __restrict__ o, const T* __restrict__ g
   if (lane == 0) {
     const float l = lse[static_cast<long long>(bh) * N + n];
     const bool dead = l == -INFINITY;
-    delta[out] = dead ? 0.f : acc;
-    lse2[out] = dead ? INFINITY : l * 1.4426950408889634f;
+    ndelta[out] = dead ? 0.f : -acc;
+    nlse2[out] = dead ? -INFINITY : -l * 1.4426950408889634f;
   }
 }
 
@@ -58,8 +59,8 @@ constexpr int BWS_ROWS = 64;
 template <typename T, int D, int BLK>
 __global__ void __launch_bounds__(BWS_ROWS * 4)
     bwd_dq_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                       const T* __restrict__ g, const float* __restrict__ delta,
-                       const float* __restrict__ lse2, const int* __restrict__ row_ptr,
+                       const T* __restrict__ g, const float* __restrict__ ndelta,
+                       const float* __restrict__ nlse2, const int* __restrict__ row_ptr,
                        const int* __restrict__ col, T* __restrict__ dq, int N, int Np,
                        float scale, float scale_log2) {
   constexpr int TPR = 4, DQ = D / TPR, BN = 32, NT = BWS_ROWS * TPR;
@@ -80,8 +81,8 @@ __global__ void __launch_bounds__(BWS_ROWS * 4)
     gr[i] = row_ok ? to_f32(g[at]) : 0.f;
     acc[i] = 0.f;
   }
-  const float l2 = lse2[bh * Np + row];   // +inf on padding rows
-  const float dl = delta[bh * Np + row];
+  const float nl2 = nlse2[bh * Np + row];   // -inf on padding rows
+  const float ndl = ndelta[bh * Np + row];
   for (int e = row_ptr[I]; e < row_ptr[I + 1]; ++e) {
     const int kstart = col[e] * BLK;
     const int kcount = min(BLK, N - kstart);
@@ -107,8 +108,8 @@ __global__ void __launch_bounds__(BWS_ROWS * 4)
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         dp += __shfl_xor_sync(0xffffffffu, dp, 1);
         dp += __shfl_xor_sync(0xffffffffu, dp, 2);
-        const float p = (s0 + j < kcount) ? exp2f(fmaf(s, scale_log2, -l2)) : 0.f;
-        const float ds = p * (dp - dl);
+        const float p = (s0 + j < kcount) ? exp2f(fmaf(s, scale_log2, nl2)) : 0.f;
+        const float ds = p * (dp + ndl);
 #pragma unroll
         for (int i = 0; i < DQ; ++i) acc[i] = fmaf(ds, ks[j][TPR * i + u], acc[i]);
       }
@@ -123,13 +124,13 @@ __global__ void __launch_bounds__(BWS_ROWS * 4)
 
 // dk and dv for 64 rows of key block J of head bh (blockIdx = (J * BLK / 64
 // + part, bh)), walking the query blocks of the transposed CSR. Four threads
-// share a key row; queries, their upstream gradients, lse2 and delta are
+// share a key row; queries, their upstream gradients, nlse2 and ndelta are
 // staged 32 at a time.
 template <typename T, int D, int BLK>
 __global__ void __launch_bounds__(BWS_ROWS * 4)
     bwd_dkdv_simt_kernel(const T* __restrict__ q, const T* __restrict__ k,
                          const T* __restrict__ v, const T* __restrict__ g,
-                         const float* __restrict__ delta, const float* __restrict__ lse2,
+                         const float* __restrict__ ndelta, const float* __restrict__ nlse2,
                          const int* __restrict__ t_ptr, const int* __restrict__ t_row,
                          T* __restrict__ dk, T* __restrict__ dv, int N, int Np, float scale,
                          float scale_log2) {
@@ -166,9 +167,9 @@ __global__ void __launch_bounds__(BWS_ROWS * 4)
         gs[ii][c] = ok ? to_f32(gb[at]) : 0.f;
       }
       if (tid < BN) {
-        // padded rows hold lse2 = +inf and delta = 0
-        ls[tid] = lse2[bh * Np + qstart + s0 + tid];
-        dls[tid] = delta[bh * Np + qstart + s0 + tid];
+        // padded rows hold nlse2 = -inf and ndelta = 0
+        ls[tid] = nlse2[bh * Np + qstart + s0 + tid];
+        dls[tid] = ndelta[bh * Np + qstart + s0 + tid];
       }
       __syncthreads();
 #pragma unroll 4
@@ -183,8 +184,8 @@ __global__ void __launch_bounds__(BWS_ROWS * 4)
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         dp += __shfl_xor_sync(0xffffffffu, dp, 1);
         dp += __shfl_xor_sync(0xffffffffu, dp, 2);
-        const float p = exp2f(fmaf(s, scale_log2, -ls[ii]));
-        const float ds = p * (dp - dls[ii]);
+        const float p = exp2f(fmaf(s, scale_log2, ls[ii]));
+        const float ds = p * (dp + dls[ii]);
 #pragma unroll
         for (int i = 0; i < DQ; ++i) {
           av[i] = fmaf(p, gs[ii][TPR * i + u], av[i]);

@@ -2,7 +2,7 @@
 // + TMEM + TMA), bf16, head_dim 128, 128-token blocks. The gradients are
 // those of the float32 kernels' header (chain rule of the attention
 // definition); p is recomputed from the forward's lse, in the log2 domain:
-// p = exp2(scale_log2 s - lse2), lse2 = lse log2(e) (+inf on padding rows).
+// p = exp2(scale_log2 s + nlse2), nlse2 = -lse log2(e) (-inf on padding rows).
 //
 // Two kernels, each one CTA per (batch*head, 128-token block), longest list
 // first, no atomics (the results are deterministic):
@@ -34,15 +34,15 @@ namespace va {
 
 constexpr int BW_THREADS = 384;
 constexpr int BW_NS = 2;  // ring stages
-constexpr int BW_ROWVEC = 1024;  // per stage: lse2 and delta of one 128-row block
+constexpr int BW_ROWVEC = 1024;  // per stage: nlse2 and ndelta of one 128-row block
 constexpr int BW_SMEM_BYTES = 1024 + TC_TILE_BYTES * (2 + 2 * BW_NS) + BW_NS * BW_ROWVEC;
 
 struct BwArgs {
   const int* ptr;    // CSR (query side) or transposed CSR (key side) offsets
   const int* idx;    // the blocks of each list
   const int* order;  // blocks by descending list length
-  const float* delta;  // [BH, Np]
-  const float* lse2;   // [BH, Np]
+  const float* ndelta;  // [BH, Np]: -(dO . O)
+  const float* nlse2;   // [BH, Np]: -lse log2(e)
   __nv_bfloat16* d0;   // dq (query side) or dv (key side)
   __nv_bfloat16* d1;   // dk (key side)
   int N, Np, nb;
@@ -112,6 +112,18 @@ __device__ __forceinline__ void bw_store64(uint32_t taddr, float mul, __nv_bfloa
   }
 }
 
+// (d0, d1) = (a0 * b0, a1 * b1) as one packed f32x2 multiply.
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0,
+                                      float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
 // from global to shared memory, completing on `bar`.
 __device__ __forceinline__ void bw_bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -170,8 +182,8 @@ __device__ __forceinline__ void bw_setup(uint64_t* bars, uint32_t* tmem_base_s, 
 
 // Producer of both kernels: the resident pair of tiles at block `own`, then
 // the streamed pair for every entry of the list. With rv0 != nullptr each
-// entry also brings the 128 floats of rv0 and rv1 at its block (the lse2 and
-// delta rows of a query block) to sX + stage * BW_ROWVEC.
+// entry also brings the 128 floats of rv0 and rv1 at its block (the nlse2 and
+// ndelta rows of a query block) to sX + stage * BW_ROWVEC.
 __device__ __forceinline__ void bw_produce(const CUtensorMap* r0, const CUtensorMap* r1,
                                            const CUtensorMap* s0, const CUtensorMap* s1,
                                            uint32_t sR, uint32_t sA, uint32_t sB, int own,
@@ -241,7 +253,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sK = smem_u32(smem), sV = sK + TC_TILE_BYTES;
   const uint32_t sQ0 = sV + TC_TILE_BYTES, sG0 = sQ0 + BW_NS * TC_TILE_BYTES;
-  const uint32_t sX = sG0 + BW_NS * TC_TILE_BYTES;  // lse2 | delta per stage
+  const uint32_t sX = sG0 + BW_NS * TC_TILE_BYTES;  // nlse2 | ndelta per stage
   const float* rowvec = reinterpret_cast<const float*>(smem + (sX - sK));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x / a.nb;
@@ -258,8 +270,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (warp == 0) {
     if (lane == 0 && n > 0)
       bw_produce(&map_k, &map_v, &map_q, &map_g, sK, sQ0, sG0, J, list, n, bh, bars, lim,
-                 abort_p, a.lse2 + static_cast<long long>(bh) * a.Np,
-                 a.delta + static_cast<long long>(bh) * a.Np, sX);
+                 abort_p, a.nlse2 + static_cast<long long>(bh) * a.Np,
+                 a.ndelta + static_cast<long long>(bh) * a.Np, sX);
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       bool ok = mbar_wait_bounded(bar(KA_RES), 0, lim, abort_p) &&
@@ -302,7 +314,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int u = 0; u < n; ++u) {
-      // lse2 and delta of this query block's 64 columns, staged with its tiles
+      // nlse2 and ndelta of this query block's 64 columns, staged with its tiles
       // (the stage cannot be refilled before this iteration's dS is written)
       const int s = u % BW_NS;
       const float* l2b = rowvec + s * (BW_ROWVEC / 4) + h * 64;
@@ -318,10 +330,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
         const float4 l = *reinterpret_cast<const float4*>(l2b + c);
-        p[c] = ex2_approx(fmaf(p[c], sl2, -l.x));
-        p[c + 1] = ex2_approx(fmaf(p[c + 1], sl2, -l.y));
-        p[c + 2] = ex2_approx(fmaf(p[c + 2], sl2, -l.z));
-        p[c + 3] = ex2_approx(fmaf(p[c + 3], sl2, -l.w));
+        ffma2_v(p[c], p[c + 1], p[c], p[c + 1], sl2, l.x, l.y);
+        ffma2_v(p[c + 2], p[c + 3], p[c + 2], p[c + 3], sl2, l.z, l.w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[c + i] = ex2_approx(p[c + i]);
       }
       bw_st_packed(tS + col, p);
       tc_fence_before();
@@ -334,10 +346,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 64; c += 4) {
         const float4 dl = *reinterpret_cast<const float4*>(dlb + c);
-        ds[c] = p[c] * (ds[c] - dl.x);
-        ds[c + 1] = p[c + 1] * (ds[c + 1] - dl.y);
-        ds[c + 2] = p[c + 2] * (ds[c + 2] - dl.z);
-        ds[c + 3] = p[c + 3] * (ds[c + 3] - dl.w);
+        fadd2_acc(ds[c], ds[c + 1], dl.x, dl.y);
+        fadd2_acc(ds[c + 2], ds[c + 3], dl.z, dl.w);
+        fmul2(ds[c], ds[c + 1], ds[c], ds[c + 1], p[c], p[c + 1]);
+        fmul2(ds[c + 2], ds[c + 3], ds[c + 2], ds[c + 3], p[c + 2], p[c + 3]);
       }
       bw_st_packed(tDP + col, ds);
       tc_fence_before();
@@ -437,8 +449,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t col = lane_off + h * 64;
     const int row = I * TC_BLK + r;
-    const float l2 = a.lse2[static_cast<long long>(bh) * a.Np + row];  // +inf on padding rows
-    const float dl = a.delta[static_cast<long long>(bh) * a.Np + row];
+    const float nl2 = a.nlse2[static_cast<long long>(bh) * a.Np + row];  // -inf on padding rows
+    const float ndl = a.ndelta[static_cast<long long>(bh) * a.Np + row];
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int u = 0; u < n; ++u) {
@@ -452,14 +464,25 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(KA_P));
 #pragma unroll
-      for (int c = 0; c < 64; ++c) p[c] = c < kvalid ? ex2_approx(fmaf(p[c], sl2, -l2)) : 0.f;
+      for (int c = 0; c < 64; c += 2) {
+        ffma2_bc(p[c], p[c + 1], p[c], p[c + 1], sl2, nl2);
+        p[c] = ex2_approx(p[c]);
+        p[c + 1] = ex2_approx(p[c + 1]);
+      }
+      if (kvalid < 64) {  // warp-uniform: only the ragged last key block
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = c < kvalid ? p[c] : 0.f;
+      }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(KA_DP), u & 1, lim, abort_p))))
         break;
       tc_fence_after();
       float ds[64];
       bw_ld64(tDP + col, ds);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) ds[c] = p[c] * (ds[c] - dl);
+      for (int c = 0; c < 64; c += 2) {
+        ffma2_bc(ds[c], ds[c + 1], ds[c], ds[c + 1], 1.f, ndl);
+        fmul2(ds[c], ds[c + 1], ds[c], ds[c + 1], p[c], p[c + 1]);
+      }
       bw_st_packed(tDP + col, ds);
       tc_fence_before();
       mbar_arrive(bar(KA_DS));

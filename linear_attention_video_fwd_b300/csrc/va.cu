@@ -488,23 +488,23 @@ namespace {
 
 template <typename T, int D, int BLK>
 int launch_bwd_simt(const void* q, const void* k, const void* v, const void* g, const va_mask* m,
-                    const float* delta, const float* lse2, void* dq, void* dk, void* dv, int BH,
+                    const float* ndelta, const float* nlse2, void* dq, void* dk, void* dv, int BH,
                     int N, int Np, float scale, cudaStream_t s) {
   dim3 grid(m->nqb * (BLK / va::BWS_ROWS), BH);
   const float sl2 = scale * 1.4426950408889634f;
   va::bwd_dq_simt_kernel<T, D, BLK><<<grid, va::BWS_ROWS * 4, 0, s>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
-      static_cast<const T*>(g), delta, lse2, m->row_ptr, m->col, static_cast<T*>(dq), N, Np,
+      static_cast<const T*>(g), ndelta, nlse2, m->row_ptr, m->col, static_cast<T*>(dq), N, Np,
       scale, sl2);
   va::bwd_dkdv_simt_kernel<T, D, BLK><<<grid, va::BWS_ROWS * 4, 0, s>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
-      static_cast<const T*>(g), delta, lse2, m->t_ptr, m->t_row, static_cast<T*>(dk),
+      static_cast<const T*>(g), ndelta, nlse2, m->t_ptr, m->t_row, static_cast<T*>(dk),
       static_cast<T*>(dv), N, Np, scale, sl2);
   return launch_status();
 }
 
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, const va_mask* m,
-                  const float* delta, const float* lse2, void* dq, void* dk, void* dv, int BH,
+                  const float* ndelta, const float* nlse2, void* dq, void* dk, void* dv, int BH,
                   int N, int Np, float scale, cudaStream_t s) {
   static bool configured[64] = {false};
   int dev = 0;
@@ -528,8 +528,8 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, co
   const long long grid = static_cast<long long>(m->nqb) * BH;
   if (grid > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
   va::BwArgs a;
-  a.delta = delta;
-  a.lse2 = lse2;
+  a.ndelta = ndelta;
+  a.nlse2 = nlse2;
   a.N = N;
   a.Np = Np;
   a.nb = m->nqb;
@@ -579,30 +579,30 @@ VA_EXPORT int va_sparse_attn_bwd(const void* q, const void* k, const void* v, co
   if (!tc && !simt) return VA_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Scoped scratch(s);
-  float* delta = nullptr;
-  float* lse2 = nullptr;
+  float* ndelta = nullptr;
+  float* nlse2 = nullptr;
   int st;
   const size_t rows = static_cast<size_t>(BH) * Np;
-  if ((st = scratch.alloc(&delta, rows)) || (st = scratch.alloc(&lse2, rows))) return st;
+  if ((st = scratch.alloc(&ndelta, rows)) || (st = scratch.alloc(&nlse2, rows))) return st;
   dim3 pgrid((Np + 7) / 8, BH);
   if (tc) {
     va::bwd_prep_kernel<__nv_bfloat16><<<pgrid, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, N,
-        Np, d, delta, lse2);
+        Np, d, ndelta, nlse2);
     if ((st = launch_status())) return st;
-    return launch_bwd_tc(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
+    return launch_bwd_tc(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);
   }
   va::bwd_prep_kernel<float><<<pgrid, 256, 0, s>>>(static_cast<const float*>(out),
                                                    static_cast<const float*>(dout), lse, N, Np,
-                                                   d, delta, lse2);
+                                                   d, ndelta, nlse2);
   if ((st = launch_status())) return st;
   if (d == 64 && blk == 64)
-    return launch_bwd_simt<float, 64, 64>(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
+    return launch_bwd_simt<float, 64, 64>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);
   if (d == 64 && blk == 128)
-    return launch_bwd_simt<float, 64, 128>(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
+    return launch_bwd_simt<float, 64, 128>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);
   if (d == 128 && blk == 64)
-    return launch_bwd_simt<float, 128, 64>(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
-  return launch_bwd_simt<float, 128, 128>(q, k, v, dout, m, delta, lse2, dq, dk, dv, BH, N, Np, scale, s);
+    return launch_bwd_simt<float, 128, 64>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);
+  return launch_bwd_simt<float, 128, 128>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);
 }
 
 // Host-buffer attention: (batch*head) chunks move through a ring of device
