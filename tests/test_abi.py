@@ -62,6 +62,23 @@ def test_validation_before_device_work(lib):
     assert lib.va_set_wait_limit(ctypes.c_int64(4000000000)) == 0
 
 
+def test_validation_of_the_other_entries(lib):
+    # Every entry rejects null pointers on the host, before any CUDA call.
+    f, vp = ctypes.c_float, ctypes.c_void_p
+    n = None
+    assert lib.va_sparse_attn_bwd(n, n, n, n, n, n, n, n, n, n, 1, 1, 1, 128, f(1.0), 1, n) == -1
+    assert lib.va_sparse_attn_fwd_host(n, n, n, n, n, n, 1, 1, 1, 128, f(1.0), 1, n) == -1
+    assert lib.va_linear_attn_fwd(n, n, n, n, 1, 1, 1, 128, 1, n) == -1
+    assert lib.va_mixed_attn_fwd(n, n, n, n, f(0.5), n, 1, 1, 1, 128, f(1.0), 1, n) == -1
+    assert lib.va_cluster_from(n, n, 1, 1, 16, 128, 4, 1, 1, n, n, n, n) == -1
+    assert lib.va_lipar_prune(n, 1, 2, 3, 4, 16, f(0.5), 1, n, n, n, n, n) == -1
+    assert lib.va_lipar_gather(n, n, n, 1, 1, 24, 128, 1, n, n) == -1
+    assert lib.va_lipar_restore(n, n, 1, 1, 24, 128, 1, n, n) == -1
+    # misaligned device pointers are rejected the same way (never dereferenced)
+    odd = vp(0x1001)
+    assert lib.va_linear_attn_fwd(odd, odd, odd, odd, 1, 1, 1, 128, 1, n) == -1
+
+
 def test_python_binding_imports():
     import linear_attention_video_fwd_b300 as va
     assert va.status_string(va.ERR_OOM) == "device allocation failed"
