@@ -94,12 +94,24 @@ typedef struct va_mask_params {
  * return it as a library-owned handle holding a device CSR:
  *   row_ptr[nqb + 1] (int32), col_idx[nnz] (int32, strictly ascending per row),
  *   nqb = ceil(T*H*W / block).
+ * Sources: the radial rule follows the Radial Attention news page (hyper.ai:
+ * static mask, window shrinking exponentially with temporal distance,
+ * O(n log n)); the LVSA rule follows the LVSA review (secrett2633 blog,
+ * sec. 3 and Fig. 2: local frame window plus periodic anchor frames that
+ * rotate with the denoising step); block pooling follows its sec. 1
+ * ("block-sparse attention"). The pages give no formulas: the token rules
+ * above va_mask_params are readings of them.
  * The mask is identical for every batch element and head. The result is
- * bit-exact (integer arithmetic only). This call synchronises `stream` once
- * (to size col_idx); the handle is ready when it returns.
- * Errors: VA_ERR_INVALID (null out/params, non-positive sizes, N >= 2^31,
- * block outside 1..4096, negative local/period/w0), VA_ERR_OOM, VA_ERR_CUDA.
+ * bit-exact (integer arithmetic only). The handle's arrays live on the
+ * device current at the call; the attention calls reject a mask from another
+ * device. This call synchronises `stream` once (to size col_idx); the handle
+ * is ready when it returns.
+ * Errors: VA_ERR_INVALID (null out/params, non-positive sizes, N >= 2^30,
+ * block outside 1..4096, negative local/period/w0), VA_ERR_UNSUPPORTED
+ * (nqb > VA_MASK_MAX_BLOCKS, or more than 2^31 - 1 live block pairs, which
+ * int32 row offsets cannot index), VA_ERR_OOM, VA_ERR_CUDA.
  */
+#define VA_MASK_MAX_BLOCKS 65536
 int va_mask_build(int kind, int T, int H, int W, const va_mask_params* params, int step,
                   va_mask** out, va_stream_t stream);
 
@@ -150,7 +162,8 @@ int va_mask_free(va_mask* mask);
  * VA_ERR_INVALID is returned (call again with a larger array).
  * Errors: VA_ERR_INVALID (as va_mask_build; null row_ptr/nnz; col_idx NULL
  * with col_capacity > 0; capacity too small), VA_ERR_UNSUPPORTED (grid too
- * large for the static scratch), VA_ERR_CUDA.
+ * large for the static scratch, or nnz > 2^31 - 1: *nnz is set, row_ptr is
+ * not usable and col_idx is untouched), VA_ERR_CUDA.
  */
 #define VA_STATIC_MAX_BLOCKS 65536
 int va_mask_build_static(int kind, int T, int H, int W, const va_mask_params* params, int step,
@@ -158,7 +171,13 @@ int va_mask_build_static(int kind, int T, int H, int W, const va_mask_params* pa
                          va_stream_t stream);
 
 /*
- * Block-sparse attention forward. For every batch b, head h and query token i
+ * Block-sparse attention forward (LVSA review, secrett2633 blog, sec. 1:
+ * attention computed only on the live blocks of a block-sparse mask; Radial
+ * Attention news page, hyper.ai: the same computation under the static
+ * radial mask; LinVideo, gist.science 2510.08318, technical summary sec. 1:
+ * this quadratic attention is the cost that dominates video generation). The
+ * pages name softmax attention without a variant, so this is the textbook
+ * masked form. For every batch b, head h and query token i
  * with block I = i / block:
  *   l_j   = scale * q_i . k_j   for keys j in live key blocks of row I, j < N
  *   o_i   = sum_j exp(l_j - m) v_j / sum_j exp(l_j - m),  m = max_j l_j
@@ -170,8 +189,8 @@ int va_mask_build_static(int kind, int T, int H, int W, const va_mask_params* pa
  * Supported: VA_BF16 with d = 128 and block 128 (tcgen05 tensor-core kernel);
  * VA_F32 with d in {64, 128} and block in {64, 128} (float32 FMA kernel).
  * Errors: VA_ERR_INVALID (null pointers, N != T*H*W of the mask, B or heads
- * < 1, misaligned pointers), VA_ERR_UNSUPPORTED (other dtype/d/block),
- * VA_ERR_CUDA (launch failure).
+ * < 1, misaligned pointers, a mask built on another device), VA_ERR_UNSUPPORTED
+ * (other dtype/d/block), VA_ERR_CUDA (launch failure).
  */
 int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mask* mask,
                        void* out, float* lse, int B, int heads, int N, int d, float scale,
@@ -198,8 +217,8 @@ int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mas
  * Supported: as the forward (VA_BF16, d = 128, block 128 on tcgen05; VA_F32,
  * d in {64, 128}, block in {64, 128} on the FMA pipes), B * heads <= 65535.
  * Errors: VA_ERR_INVALID (null or misaligned pointers, N != T*H*W of the
- * mask, B or heads < 1, non-finite scale), VA_ERR_UNSUPPORTED,
- * VA_ERR_OOM (scratch), VA_ERR_CUDA.
+ * mask, B or heads < 1, non-finite scale, a mask built on another device),
+ * VA_ERR_UNSUPPORTED, VA_ERR_OOM (scratch), VA_ERR_CUDA.
  */
 int va_sparse_attn_bwd(const void* q, const void* k, const void* v, const void* out,
                        const void* dout, const float* lse, const va_mask* mask, void* dq,
@@ -252,7 +271,8 @@ int va_linear_attn_fwd(const void* q, const void* k, const void* v, void* out, i
  * va_linear_attn_fwd. r = 1 runs the attention only, r = 0 the linear
  * attention only. The attention part is rounded to bf16 before the blend.
  * Supported: VA_BF16, d = 128, mask block 128. Errors: as the two calls, and
- * VA_ERR_INVALID for r outside [0, 1] or N != the mask's N.
+ * VA_ERR_INVALID for r outside [0, 1], N != the mask's N or a mask built on
+ * another device.
  */
 int va_mixed_attn_fwd(const void* q, const void* k, const void* v, const va_mask* mask, float r,
                       void* out, int B, int heads, int N, int d, float scale, int dtype,
@@ -299,7 +319,9 @@ int va_lipar_restore(const void* y, const int32_t* src, int B, int heads, int N,
 
 /*
  * Lloyd k-means per (batch, head) on x [B, heads, N, d] (squared Euclidean
- * distance), SVG-EAR's semantic clustering:
+ * distance): SVG-EAR's clustering of query and key tokens by semantic
+ * similarity (SVG-EAR, gist.science 2603.08982, technical summary sec. 2,
+ * idea 1; the page names no algorithm, Lloyd's is the reading):
  *   centroid <- x[init_idx]; repeat iters times: assign each token to the
  *   nearest centroid (ties: lowest index), then replace each centroid by the
  *   mean of its members (an empty cluster keeps its centroid).

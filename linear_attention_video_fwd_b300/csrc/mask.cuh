@@ -150,6 +150,11 @@ __global__ void mask_fill_kernel(MaskDesc m, const int* __restrict__ row_ptr,
   if (I >= m.nb) return;
   int base = row_ptr[I];
   const int end = row_ptr[I + 1];
+  if (base < 0 || end < base) {
+    // offsets that wrapped or run backwards: write nothing
+    if (lane == 0) raise_error(VA_ERR_DEVICE);
+    return;
+  }
   for (int J0 = 0; J0 < m.nb; J0 += 32) {
     const int J = J0 + lane;
     const bool live = J < m.nb && (m.transpose ? block_pair_live(m, J, I) : block_pair_live(m, I, J));

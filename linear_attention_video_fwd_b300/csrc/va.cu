@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -93,6 +94,26 @@ struct Scoped {
     return f != nullptr && std::strstr(f, "alloc") != nullptr;
   }
 };
+
+// One-time configuration of a device (kernel attributes, SM counts), run
+// under a lock so that host threads calling concurrently neither race on the
+// flags nor launch before the attributes are set. A failed configuration is
+// retried on the next call.
+struct DeviceOnce {
+  std::mutex mu;
+  std::atomic<bool> done[64];
+};
+
+template <typename Fn>
+int device_once(DeviceOnce& once, int dev, Fn&& fn) {
+  if (dev < 0 || dev >= 64) return VA_ERR_UNSUPPORTED;
+  if (once.done[dev].load(std::memory_order_acquire)) return VA_OK;
+  std::lock_guard<std::mutex> lock(once.mu);
+  if (once.done[dev].load(std::memory_order_relaxed)) return VA_OK;
+  const int st = fn();
+  if (st == VA_OK) once.done[dev].store(true, std::memory_order_release);
+  return st;
+}
 
 int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return VA_OK;
@@ -180,6 +201,24 @@ struct va_mask {
   int device = 0;
 };
 
+namespace {
+
+// A mask's arrays live on the device it was built on: a kernel running on
+// another device must not be handed them.
+int check_mask_device(const va_mask* m) {
+  int dev = 0;
+  const int st = cuda_status(cudaGetDevice(&dev));
+  if (st) return st;
+  return dev == m->device ? VA_OK : VA_ERR_INVALID;
+}
+
+// Mask limits shared by both builds: at most VA_MASK_MAX_BLOCKS blocks per
+// side (the count and fill kernels test every block pair), and int32 CSR
+// offsets, so at most INT32_MAX live block pairs.
+constexpr int64_t kMaxMaskNnz = 0x7fffffffLL;
+
+}  // namespace
+
 VA_EXPORT int va_version(void) { return 100; }
 
 VA_EXPORT const char* va_status_string(int status) {
@@ -233,6 +272,7 @@ VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params*
   const va_mask_params p = *params;
   if (p.block < 1 || p.block > 4096) return VA_ERR_INVALID;
   if (p.w0 < 0 || p.local < 0 || p.period < 0) return VA_ERR_INVALID;
+  if ((N64 + p.block - 1) / p.block > VA_MASK_MAX_BLOCKS) return VA_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   va::MaskDesc md;
@@ -282,7 +322,7 @@ VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params*
       return st;
     }
     const int threads = 256;
-    const int blocks = (md.nb * 32 + threads - 1) / threads;
+    const int blocks = static_cast<int>((static_cast<int64_t>(md.nb) * 32 + threads - 1) / threads);
     va::mask_count_kernel<<<blocks, threads, 0, s>>>(md, cnt, keytok);
     va::mask_scan_kernel<<<1, 1024, 0, s>>>(md, cnt, keytok, m->row_ptr, summary, m->order, hist);
     if ((st = launch_status())) {
@@ -298,6 +338,11 @@ VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params*
     }
     m->nnz = host_summary[0];
     m->live_pairs = host_summary[1];
+    if (m->nnz > kMaxMaskNnz) {
+      // int32 row offsets cannot index the list: stop before any fill
+      va_mask_free(m);
+      return VA_ERR_UNSUPPORTED;
+    }
     if ((st = cuda_status(cudaMalloc(&m->col, sizeof(int32_t) * (m->nnz > 0 ? m->nnz : 1))))) {
       va_mask_free(m);
       return st;
@@ -411,23 +456,22 @@ int launch_simt(const void* q, const void* k, const void* v, const va_mask* m, v
 
 int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, void* out, float* lse,
               int BH, int N, float scale, cudaStream_t s) {
-  static bool configured[64] = {false};
+  static DeviceOnce once;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
+  int st = cuda_status(cudaGetDevice(&dev));
+  if (st) return st;
+  st = device_once(once, dev, [] {
     // The kernel's setmaxnreg split assumes this exact per-thread register
     // count at launch; anything else could leave the increase waiting.
     cudaFuncAttributes fa;
-    int st = cuda_status(cudaFuncGetAttributes(&fa, va::attn_tc_kernel));
-    if (st) return st;
+    int r = cuda_status(cudaFuncGetAttributes(&fa, va::attn_tc_kernel));
+    if (r) return r;
     if (fa.numRegs != va::TC_LAUNCH_REGS) return VA_ERR_UNSUPPORTED;
-    st = cuda_status(cudaFuncSetAttribute(
+    return cuda_status(cudaFuncSetAttribute(
         va::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, va::TC_SMEM_BYTES));
-    if (st) return st;
-    configured[dev] = true;
-  }
+  });
+  if (st) return st;
   CUtensorMap mq, mk, mv;
-  int st;
   if ((st = encode_bf16_rows(&mq, q, BH, N, 128)) || (st = encode_bf16_rows(&mk, k, BH, N, 128)) ||
       (st = encode_bf16_rows(&mv, v, BH, N, 128)))
     return st;
@@ -461,6 +505,7 @@ VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, co
   if (B < 1 || heads < 1 || N != m->N) return VA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VA_ERR_INVALID;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u)) return VA_ERR_INVALID;
+  if (int dst = check_mask_device(m)) return dst;
   if (!std::isfinite(scale)) return VA_ERR_INVALID;
   const int64_t BH64 = static_cast<int64_t>(B) * heads;
   if (BH64 > 65535 && dtype == VA_F32) return VA_ERR_UNSUPPORTED;
@@ -506,22 +551,23 @@ int launch_bwd_simt(const void* q, const void* k, const void* v, const void* g, 
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, const va_mask* m,
                   const float* ndelta, const float* nlse2, void* dq, void* dk, void* dv, int BH,
                   int N, int Np, float scale, cudaStream_t s) {
-  static bool configured[64] = {false};
+  static DeviceOnce once;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 64 && !configured[dev]) {
-    int st;
-    if ((st = cuda_status(cudaFuncSetAttribute(va::bwd_dkdv_tc_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::BW_SMEM_BYTES))) ||
-        (st = cuda_status(cudaFuncSetAttribute(va::bwd_dq_tc_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::BW_SMEM_BYTES))))
-      return st;
-    configured[dev] = true;
-  }
+  int st = cuda_status(cudaGetDevice(&dev));
+  if (st) return st;
+  st = device_once(once, dev, [] {
+    int r;
+    if ((r = cuda_status(cudaFuncSetAttribute(va::bwd_dkdv_tc_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::BW_SMEM_BYTES))) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::bwd_dq_tc_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::BW_SMEM_BYTES))))
+      return r;
+    return VA_OK;
+  });
+  if (st) return st;
   CUtensorMap mq, mk, mv, mg;
-  int st;
   if ((st = encode_bf16_rows(&mq, q, BH, N, 128)) || (st = encode_bf16_rows(&mk, k, BH, N, 128)) ||
       (st = encode_bf16_rows(&mv, v, BH, N, 128)) || (st = encode_bf16_rows(&mg, g, BH, N, 128)))
     return st;
@@ -563,6 +609,7 @@ VA_EXPORT int va_sparse_attn_bwd(const void* q, const void* k, const void* v, co
       lse == nullptr || m == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
     return VA_ERR_INVALID;
   if (B < 1 || heads < 1 || N != m->N || m->t_ptr == nullptr) return VA_ERR_INVALID;
+  if (int dst = check_mask_device(m)) return dst;
   for (const void* p : {q, k, v, out, dout, static_cast<const void*>(dq),
                         static_cast<const void*>(dk), static_cast<const void*>(dv)})
     if (!aligned16(p)) return VA_ERR_INVALID;
@@ -659,6 +706,7 @@ VA_EXPORT int va_sparse_attn_fwd_host(const void* q, const void* k, const void* 
     return VA_ERR_INVALID;
   if (B < 1 || heads < 1 || N != m->N || N < 1 || d < 1) return VA_ERR_INVALID;
   if (!std::isfinite(scale)) return VA_ERR_INVALID;
+  if (int dst = check_mask_device(m)) return dst;
   if (dtype != VA_BF16 && dtype != VA_F32) return VA_ERR_UNSUPPORTED;
   const int64_t BH64 = static_cast<int64_t>(B) * heads;
   if (BH64 * N >= (1LL << 31)) return VA_ERR_UNSUPPORTED;
@@ -747,24 +795,25 @@ namespace {
 // linear result.
 int run_linear(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
                __nv_bfloat16* out, int BH, int N, int mix, float r, cudaStream_t s) {
-  static bool configured[64] = {false};
+  static DeviceOnce once;
   static int num_sms[64] = {0};
   int dev = 0;
-  cudaGetDevice(&dev);
-  int st;
-  if (dev < 0 || dev >= 64) return VA_ERR_UNSUPPORTED;
-  if (!configured[dev]) {
-    if ((st = cuda_status(cudaFuncSetAttribute(va::lin_state_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::LN_STATE_SMEM))) ||
-        (st = cuda_status(cudaFuncSetAttribute(va::lin_out_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::LN_OUT_SMEM))) ||
-        (st = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
-                                                 dev))))
-      return st;
-    configured[dev] = true;
-  }
+  int st = cuda_status(cudaGetDevice(&dev));
+  if (st) return st;
+  st = device_once(once, dev, [dev] {
+    int r;
+    if ((r = cuda_status(cudaFuncSetAttribute(va::lin_state_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::LN_STATE_SMEM))) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::lin_out_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::LN_OUT_SMEM))) ||
+        (r = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
+                                                dev))))
+      return r;
+    return VA_OK;
+  });
+  if (st) return st;
   const int ntiles = (N + 127) / 128;
   const int nsplit = std::max(1, std::min(ntiles, num_sms[dev] / BH));
   Scoped scratch(s);
@@ -819,6 +868,7 @@ VA_EXPORT int va_mixed_attn_fwd(const void* q, const void* k, const void* v, con
   if (st) return st;
   if (m == nullptr || N != m->N) return VA_ERR_INVALID;
   if (!(r >= 0.f && r <= 1.f)) return VA_ERR_INVALID;
+  if ((st = check_mask_device(m))) return st;
   using T = __nv_bfloat16;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (r > 0.f &&
@@ -919,26 +969,27 @@ constexpr int kMaxClusters = 4096;
 
 template <typename T, int D>
 int set_smem_attrs() {
-  static bool done[64] = {false};
+  static DeviceOnce once;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && done[dev]) return VA_OK;
-  int st;
-  if ((st = cuda_status(cudaFuncSetAttribute(va::km_assign_kernel<T, D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             2 * D * va::KM_PT * 4))) ||
-      (st = cuda_status(cudaFuncSetAttribute(va::probe_pass1_kernel<T, D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             va::probe_smem_bytes<D>(kMaxClusters)))) ||
-      (st = cuda_status(cudaFuncSetAttribute(va::probe_pass2_kernel<T, D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             va::probe_smem_bytes<D>(kMaxClusters)))) ||
-      (st = cuda_status(cudaFuncSetAttribute(va::comp_attn_kernel<T, D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             va::comp_smem_bytes<D>(kMaxClusters)))))
-    return st;
-  if (dev >= 0 && dev < 64) done[dev] = true;
-  return VA_OK;
+  int st = cuda_status(cudaGetDevice(&dev));
+  if (st) return st;
+  return device_once(once, dev, [] {
+    int r;
+    if ((r = cuda_status(cudaFuncSetAttribute(va::km_assign_kernel<T, D>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              2 * D * va::KM_PT * 4))) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::probe_pass1_kernel<T, D>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::probe_smem_bytes<D>(kMaxClusters)))) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::probe_pass2_kernel<T, D>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::probe_smem_bytes<D>(kMaxClusters)))) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::comp_attn_kernel<T, D>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::comp_smem_bytes<D>(kMaxClusters)))))
+      return r;
+    return VA_OK;
+  });
 }
 
 // Member lists of an assignment: count -> offsets -> perm (order within a
@@ -955,22 +1006,23 @@ int cluster_lists(const int* assign, int BH, int N, int C, int* count, int* off,
 // bf16, d = 128: distances on the tensor cores (split-bf16 centroids).
 int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int BH, int N, int C,
                    int iters, int* assign, float* cent, int* count, cudaStream_t s) {
-  static bool configured[64] = {false};
+  static DeviceOnce once;
   static int num_sms[64] = {0};
   int dev = 0;
-  cudaGetDevice(&dev);
-  int st;
-  if (dev < 0 || dev >= 64) return VA_ERR_UNSUPPORTED;
-  if (!configured[dev]) {
-    if ((st = set_smem_attrs<__nv_bfloat16, 128>()) ||
-        (st = cuda_status(cudaFuncSetAttribute(va::km_assign_tc_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::KA_SMEM_BYTES))) ||
-        (st = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
-                                                 dev))))
-      return st;
-    configured[dev] = true;
-  }
+  int st = cuda_status(cudaGetDevice(&dev));
+  if (st) return st;
+  st = device_once(once, dev, [dev] {
+    int r;
+    if ((r = set_smem_attrs<__nv_bfloat16, 128>()) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::km_assign_tc_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::KA_SMEM_BYTES))) ||
+        (r = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
+                                                dev))))
+      return r;
+    return VA_OK;
+  });
+  if (st) return st;
   // assignment grid: resident chunks of 256 clusters, point tiles split so
   // that the persistent CTAs fill about one wave
   const int nchunks = (C + va::KA_CHUNK - 1) / va::KA_CHUNK;
@@ -1129,20 +1181,19 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
                       const float* kc, const float* vc, const int* seln, const int* selc,
                       const uint8_t* sel, float scale, __nv_bfloat16* out, Scoped& scratch,
                       cudaStream_t s) {
-  static bool configured[64] = {false};
+  static DeviceOnce once;
   int dev = 0;
-  cudaGetDevice(&dev);
-  int st;
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
+  int st = cuda_status(cudaGetDevice(&dev));
+  if (st) return st;
+  st = device_once(once, dev, [] {
     cudaFuncAttributes fa;
-    if ((st = cuda_status(cudaFuncGetAttributes(&fa, va::comp_tc_kernel)))) return st;
+    int r = cuda_status(cudaFuncGetAttributes(&fa, va::comp_tc_kernel));
+    if (r) return r;
     if (fa.numRegs != va::TC_LAUNCH_REGS) return VA_ERR_UNSUPPORTED;
-    if ((st = cuda_status(cudaFuncSetAttribute(va::comp_tc_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::CT_SMEM_BYTES))))
-      return st;
-    configured[dev] = true;
-  }
+    return cuda_status(cudaFuncSetAttribute(
+        va::comp_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, va::CT_SMEM_BYTES));
+  });
+  if (st) return st;
   const size_t bh = static_cast<size_t>(BH);
   const int nv = (Ck + 127) / 128;
   __nv_bfloat16 *qs, *ks, *vs, *kcb, *vcb;
@@ -1228,30 +1279,31 @@ int probe_tensor_cores(const __nv_bfloat16* k, const __nv_bfloat16* v, int Cq, i
                        int N, const int* nq, const int* nk, const int* koff, const int* kperm,
                        const float* qc, const float* vc, float scale, float* err,
                        Scoped& scratch, cudaStream_t s) {
-  static bool configured[64] = {false};
+  static DeviceOnce once;
   static int num_sms[64] = {0};
   int dev = 0;
-  cudaGetDevice(&dev);
-  int st;
-  if (dev < 0 || dev >= 64) return VA_ERR_UNSUPPORTED;
-  if (!configured[dev]) {
+  int st = cuda_status(cudaGetDevice(&dev));
+  if (st) return st;
+  st = device_once(once, dev, [dev] {
     cudaFuncAttributes fa1, fa2;
-    if ((st = cuda_status(cudaFuncGetAttributes(&fa1, va::probe_tc_kernel<1>))) ||
-        (st = cuda_status(cudaFuncGetAttributes(&fa2, va::probe_tc_kernel<2>))))
-      return st;
+    int r;
+    if ((r = cuda_status(cudaFuncGetAttributes(&fa1, va::probe_tc_kernel<1>))) ||
+        (r = cuda_status(cudaFuncGetAttributes(&fa2, va::probe_tc_kernel<2>))))
+      return r;
     if (fa1.numRegs != va::PT_LAUNCH_REGS || fa2.numRegs != va::PT_LAUNCH_REGS)
       return VA_ERR_UNSUPPORTED;
-    if ((st = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<1>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::PT_SMEM_BYTES))) ||
-        (st = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<2>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               va::PT_SMEM_BYTES))) ||
-        (st = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
-                                                 dev))))
-      return st;
-    configured[dev] = true;
-  }
+    if ((r = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<1>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::PT_SMEM_BYTES))) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<2>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              va::PT_SMEM_BYTES))) ||
+        (r = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
+                                                dev))))
+      return r;
+    return VA_OK;
+  });
+  if (st) return st;
   const size_t bh = static_cast<size_t>(BH);
   const int Cqp = (Cq + 127) / 128 * 128;
   const int ntiles = Cqp / 128;
@@ -1581,7 +1633,7 @@ VA_EXPORT int va_mask_build_static(int kind, int T, int H, int W, const va_mask_
   // The previous call's contents stay in the array: start the summary at zero.
   if ((st = cuda_status(cudaMemsetAsync(summary, 0, 2 * sizeof(long long), s)))) return st;
   const int threads = 256;
-  const int blocks = (md.nb * 32 + threads - 1) / threads;
+  const int blocks = static_cast<int>((static_cast<int64_t>(md.nb) * 32 + threads - 1) / threads);
   va::mask_count_kernel<<<blocks, threads, 0, s>>>(md, cnt, keytok);
   va::mask_scan_kernel<<<1, 1024, 0, s>>>(md, cnt, keytok, row_ptr, summary, order, hist);
   if ((st = launch_status())) return st;
@@ -1591,6 +1643,8 @@ VA_EXPORT int va_mask_build_static(int kind, int T, int H, int W, const va_mask_
       (st = cuda_status(cudaStreamSynchronize(s))))
     return st;
   *nnz = host_summary[0];
+  // int32 row offsets cannot index more live pairs: row_ptr is not usable
+  if (host_summary[0] > kMaxMaskNnz) return VA_ERR_UNSUPPORTED;
   if (host_summary[0] > col_capacity) return VA_ERR_INVALID;
   if (host_summary[0] > 0) {
     va::mask_fill_kernel<<<blocks, threads, 0, s>>>(md, row_ptr, col_idx);

@@ -82,3 +82,34 @@ def test_validation_of_the_other_entries(lib):
 def test_python_binding_imports():
     import linear_attention_video_fwd_b300 as va
     assert va.status_string(va.ERR_OOM) == "device allocation failed"
+
+
+def test_mask_size_limits_are_checked_on_the_host(lib):
+    # Grids beyond the documented limits return before any device work, so
+    # these calls need no GPU: N >= 2^30 is invalid, more than
+    # VA_MASK_MAX_BLOCKS blocks per side is unsupported (the count kernel tests
+    # every block pair), for the allocating and the allocation-free build.
+    class P(ctypes.Structure):
+        _fields_ = [(n, ctypes.c_int32) for n in
+                    ("block", "w0", "local", "period", "anchor0", "rot_stride")]
+
+    with open(os.path.join(ROOT, "include", "va.h")) as f:
+        max_blocks = int(re.search(r"#define VA_MASK_MAX_BLOCKS (\d+)", f.read()).group(1))
+    assert max_blocks == 65536
+    out = ctypes.c_void_p(0)
+    p1 = P(1, 0, 1, 0, 0, 1)
+    assert lib.va_mask_build(1, 1 << 10, 1 << 10, 1 << 10, ctypes.byref(p1), 0,
+                             ctypes.byref(out), None) == -1           # N = 2^30
+    assert lib.va_mask_build(1, 1, 1, max_blocks + 1, ctypes.byref(p1), 0,
+                             ctypes.byref(out), None) == -2           # one block too many
+    assert out.value is None
+    nnz = ctypes.c_int64(-1)
+    fn = lib.va_mask_build_static
+    fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                   ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                   ctypes.POINTER(ctypes.c_int64), ctypes.c_void_p]
+    fake = ctypes.c_void_p(0x10000)                  # never dereferenced: rejected first
+    assert fn(1, 1, 1, max_blocks + 1, ctypes.byref(p1), 0, fake, fake, 0,
+              ctypes.byref(nnz), None) == -2
+    assert fn(1, 1 << 10, 1 << 10, 1 << 10, ctypes.byref(p1), 0, fake, fake, 0,
+              ctypes.byref(nnz), None) == -1

@@ -78,3 +78,21 @@ def test_mask_allocation_failure_is_reported(va, monkeypatch):
     monkeypatch.delenv("VA_FAULT_INJECT")
     m = va.mask_build(va.RADIAL, 4, 4, 4, block=16)
     assert m.nnz > 0
+
+
+def test_mask_limits_on_blocks_and_live_pairs(va):
+    # At most VA_MASK_MAX_BLOCKS = 65,536 blocks per side. The dense mask of
+    # 65,536 one-token blocks has 2^32 live block pairs, more than int32 row
+    # offsets can index: the build stops after counting, before any list is
+    # filled or sized, and reports the grid as unsupported.
+    with pytest.raises(va.VAError) as e:
+        va.mask_build(va.DENSE, 1, 1, 65537, block=1)
+    assert e.value.status == va.ERR_UNSUPPORTED
+    with pytest.raises(va.VAError) as e:
+        va.mask_build(va.DENSE, 1, 1, 65536, block=1)
+    assert e.value.status == va.ERR_UNSUPPORTED
+    assert va.device_error() == va.OK
+    m = va.mask_build(va.DENSE, 1, 1, 4096, block=1)              # works again afterwards
+    assert m.nnz == 4096 * 4096
+    m.free()
+    assert va.device_error() == va.OK

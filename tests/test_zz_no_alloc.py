@@ -26,28 +26,42 @@ CASES = [
 ]
 
 
-def _static_build(va, case, capacity):
-    kind, T, H, W, block, w0, local, period, a0, rho, step = case
-    lib = va.lib()
-    fn = lib.va_mask_build_static
+def _static_fn(va):
+    fn = va.lib().va_mask_build_static
     fn.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                    ctypes.POINTER(va._MaskParams), ctypes.c_int, ctypes.c_void_p,
                    ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(ctypes.c_int64),
                    ctypes.c_void_p]
     fn.restype = ctypes.c_int
+    return fn
+
+
+def _outputs(case, capacity):
+    """Caller-owned output arrays, filled with garbage to catch unwritten slots."""
+    kind, T, H, W, block = case[:5]
     nqb = -(-(T * H * W) // block)
     dev = torch.device("cuda", 0)
-    # The caller owns the outputs; fill them with garbage to catch unwritten slots.
     row_ptr = torch.full((nqb + 1,), -7, dtype=torch.int32, device=dev)
     col = torch.full((max(capacity, 1),), -7, dtype=torch.int32, device=dev)
+    return row_ptr, col
+
+
+def _call(va, case, row_ptr, col, capacity):
+    kind, T, H, W, block, w0, local, period, a0, rho, step = case
     nnz = ctypes.c_int64(-1)
     p = va._MaskParams(block, w0, local, period, a0, rho)
     stream = torch.cuda.current_stream()
-    st = fn(kind, T, H, W, ctypes.byref(p), step, ctypes.c_void_p(row_ptr.data_ptr()),
-            ctypes.c_void_p(col.data_ptr()), capacity, ctypes.byref(nnz),
-            ctypes.c_void_p(stream.cuda_stream))
+    st = _static_fn(va)(kind, T, H, W, ctypes.byref(p), step,
+                        ctypes.c_void_p(row_ptr.data_ptr()), ctypes.c_void_p(col.data_ptr()),
+                        capacity, ctypes.byref(nnz), ctypes.c_void_p(stream.cuda_stream))
     torch.cuda.synchronize()
-    return st, nnz.value, row_ptr.cpu().numpy(), col.cpu().numpy()
+    return st, nnz.value
+
+
+def _static_build(va, case, capacity):
+    row_ptr, col = _outputs(case, capacity)
+    st, nnz = _call(va, case, row_ptr, col, capacity)
+    return st, nnz, row_ptr.cpu().numpy(), col.cpu().numpy()
 
 
 def _reference(va, case):
@@ -82,4 +96,43 @@ def test_static_build_reports_size_and_limits(va):
     assert st == va.ERR_UNSUPPORTED                            # beyond the static scratch
     st, nnz, rp, col = _static_build(va, case, len(want_col))  # works again afterwards
     assert st == va.OK and np.array_equal(col[:nnz], want_col)
+    assert va.device_error() == va.OK
+
+
+def test_static_build_allocates_nothing(va, monkeypatch):
+    # The property the entry point exists for. (1) With every library scratch
+    # allocation made to fail (VA_FAULT_INJECT=alloc), the allocating build
+    # fails and the static build still succeeds with the same CSR. (2) Around
+    # a warmed-up call (its kernels already loaded), the device's free memory
+    # does not move.
+    case = CASES[1]
+    want_rp, want_col = _reference(va, case)
+    row_ptr, col = _outputs(case, len(want_col))
+    assert _call(va, case, row_ptr, col, len(want_col)) == (va.OK, len(want_col))
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    monkeypatch.setenv("VA_FAULT_INJECT", "alloc")
+    with pytest.raises(va.VAError) as e:
+        _reference(va, case)
+    assert e.value.status == va.ERR_OOM
+    st, nnz = _call(va, case, row_ptr, col, len(want_col))
+    monkeypatch.delenv("VA_FAULT_INJECT")
+    assert st == va.OK and nnz == len(want_col)
+    for _ in range(3):
+        assert _call(va, case, row_ptr, col, len(want_col)) == (va.OK, len(want_col))
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before, (free_before, free_after)
+    assert np.array_equal(row_ptr.cpu().numpy(), want_rp)
+    assert np.array_equal(col.cpu().numpy(), want_col)
+    assert va.device_error() == va.OK
+
+
+def test_static_build_rejects_more_live_pairs_than_int32_offsets(va):
+    # The dense mask of 65,536 one-token blocks (the block limit) has 2^32 live
+    # block pairs: the count is reported, row_ptr is unusable and col_idx is
+    # left untouched.
+    case = (0, 1, 1, 65536, 1, 0, 1, 0, 0, 1, 0)
+    st, nnz, _, col = _static_build(va, case, 16)
+    assert st == va.ERR_UNSUPPORTED and nnz == 1 << 32
+    assert (col == -7).all()
     assert va.device_error() == va.OK
