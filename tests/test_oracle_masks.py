@@ -164,3 +164,61 @@ def test_radial_is_n_log_n():
     assert (steps > 1.0).all() and (steps < 2.0).all()
     # dense attention would give a ratio of T (64 at the last point)
     assert ratios[-1] < 10
+
+
+def test_live_pair_tokens_hand_count_on_a_ragged_grid(golden):
+    # The FLOP count behind every TFLOP/s figure: 4 * d * live_pair_tokens.
+    g = golden("lvsa_ragged_live_pairs.txt")
+    T, H, W, block, local, period, a0 = map(int, g[1])
+    want = np.array([[int(x) for x in row] for row in g[3:6]], dtype=bool)
+    p = M.MaskParams(block=block, local=local, period=period, anchor0=a0)
+    bm = M.block_mask_literal(M.LVSA, T, H, W, p)
+    assert np.array_equal(bm, want)
+    assert M.live_pair_tokens(bm, block, T * H * W) == int(g[7][0])
+
+
+@pytest.mark.parametrize("N,block", [(12, 5), (300, 128), (257, 64), (1, 128), (128, 128)])
+def test_live_pair_tokens_equals_token_expansion_count(N, block):
+    # Independent route: expand the block matrix to its N x N token mask and
+    # count the live entries; padding past N never counts.
+    rng = np.random.default_rng(N + block)
+    nb = M.num_blocks(N, block)
+    bm = rng.random((nb, nb)) < 0.4
+    assert M.live_pair_tokens(bm, block, N) == int(M.expand_to_tokens(bm, block, N).sum())
+
+
+def _literal_block_row(kind, T, H, W, p, step, I):
+    """Row I of the pooled block mask by literal enumeration of its token pairs."""
+    N = T * H * W
+    nb = M.num_blocks(N, p.block)
+    rows = np.arange(I * p.block, min(N, (I + 1) * p.block))
+    live = M.token_live(kind, T, H, W, p, step, rows[:, None], np.arange(N)[None, :])
+    padded = np.zeros((len(rows), nb * p.block), dtype=bool)
+    padded[:, :N] = live
+    return padded.reshape(len(rows), nb, p.block).any(axis=(0, 2))
+
+
+FULL_GRIDS = [
+    # kind, T, H, W, params, steps: the full-size workloads, where the oracle's
+    # block_mask takes the frame-run route
+    (M.RADIAL, 21, 30, 52, M.MaskParams(block=128), (0,)),
+    (M.LVSA, 126, 30, 52, M.MaskParams(block=128, local=2, period=8, rot_stride=1), (0, 1, 2, 3)),
+    (M.RADIAL, 33, 45, 80, M.MaskParams(block=128), (0,)),
+]
+
+
+@pytest.mark.parametrize("grid", FULL_GRIDS, ids=["wan_radial", "lvsa_long", "hunyuan_radial"])
+def test_frame_run_pooling_matches_literal_rows_at_full_size(grid):
+    # Spot check of block_mask_segments against literal token enumeration on
+    # whole block rows of the full-size grids: the first, second, a middle, a
+    # frame-straddling and the ragged last row.
+    kind, T, H, W, p, steps = grid
+    N = T * H * W
+    nb = M.num_blocks(N, p.block)
+    F = H * W
+    straddle = next(I for I in range(nb) if (I * p.block) // F != (min(N, (I + 1) * p.block) - 1) // F)
+    for step in steps:
+        seg = M.block_mask_segments(kind, T, H, W, p, step)
+        for I in sorted({0, 1, nb // 2, straddle, nb - 1}):
+            lit = _literal_block_row(kind, T, H, W, p, step, I)
+            assert np.array_equal(seg[I], lit), (step, I)
