@@ -223,15 +223,33 @@ def oracle_block_mask(wl):
 
 
 def oracle_sample(wl, q, k, v, bm, rows):
-    """Run the float64 oracle on `rows` of every head; returns (seconds, live FLOPs done)."""
+    """Run the float64 oracle on `rows` of every head; returns (seconds, live
+    FLOPs done, output rows [B, heads, R, d])."""
     from oracle import attention as OA
     N = q.shape[2]
     live_keys_per_block = (bm * np.array([min(N, (b + 1) * BLOCK) - b * BLOCK
                                           for b in range(bm.shape[0])])[None, :]).sum(1)
     flops = 4.0 * D * float(live_keys_per_block[rows // BLOCK].sum()) * BATCH * wl["heads"]
     t0 = time.perf_counter()
-    OA.block_sparse_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(D), rows=rows)
-    return time.perf_counter() - t0, flops
+    o, _ = OA.block_sparse_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(D), rows=rows)
+    return time.perf_counter() - t0, flops, o
+
+
+def parity_record(got, want, what, max_abs=2e-2, mean_abs=2e-3, relative=False):
+    """Element-wise comparison of sampled output rows with the oracle, taken
+    outside the timed region. With `relative` the bars scale with the
+    reference (gradients): max-abs <= max_abs * max|want|, mean-abs <=
+    mean_abs * mean|want|."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    err = np.abs(got - want)
+    mx, mn = float(err.max()), float(err.mean())
+    bar_max = max_abs * float(np.abs(want).max()) if relative else max_abs
+    bar_mean = mean_abs * float(np.abs(want).mean()) if relative else mean_abs
+    return {"compared": what, "max_abs": mx, "mean_abs": mn,
+            "bar": {"max_abs": bar_max, "mean_abs": bar_mean},
+            "finite": bool(np.isfinite(got).all()),
+            "pass": bool(np.isfinite(got).all() and mx <= bar_max and mn <= bar_mean)}
 
 
 def timed_region(args, world, local, call, stream):
@@ -348,16 +366,21 @@ def run_ours(args, world, rank, local):
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0:
         bm = oracle_block_mask(wl)
-        rows = OA.sample_rows(N, BLOCK, args.oracle_rows, seed=7)
-        secs, oflops = oracle_sample(wl, q, k, v, bm, rows)
-        line["cpu_baseline"] = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT,
-                                "cores": threads_used(), "kind": "oracle",
-                                "seconds": round(secs, 2),
-                                "sample": "%d seeded query rows x %d heads of the same workload "
-                                          "(float64 numpy oracle, masked dense rows)"
-                                          % (len(rows), heads)}
+        full = world == 1 and not args.no_cpu_baseline
+        rows = OA.sample_rows(N, BLOCK, args.oracle_rows if full else 64, seed=7)
+        secs, oflops, want = oracle_sample(wl, q, k, v, bm, rows)
+        got = out[:, :, torch.from_numpy(rows).to(dev)].float().cpu().numpy()
+        line["parity"] = parity_record(got, want, "output rows %d x %d heads vs the float64 "
+                                       "oracle (last timed call)" % (len(rows), heads))
+        if full:
+            line["cpu_baseline"] = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT,
+                                    "cores": threads_used(), "kind": "oracle",
+                                    "seconds": round(secs, 2),
+                                    "sample": "%d seeded query rows x %d heads of the same "
+                                              "workload (float64 numpy oracle, masked dense "
+                                              "rows)" % (len(rows), heads)}
     mask.free()
     return line
 
@@ -469,7 +492,85 @@ def run_svgear(args, world, rank, local):
         "gpu_launches": None,
         "clocks": clocks,
     }
+    if rank == 0:
+        line.update(svgear_checks(args, world, va, q, k, v, qt, kt, vt, qa, ka, qinit, kinit,
+                                  out, sel, Cq, Ck, N))
     return line
+
+
+def svgear_checks(args, world, va, q, k, v, qt, kt, vt, qa, ka, qinit, kinit, out, sel, Cq, Ck,
+                  N):
+    """Outside the timed region: the step's output and routing against the
+    float64 oracle (given the step's own clusters), the last k-means step
+    against the oracle's argmin, and the oracle's compensated attention timed
+    on the same rows as the CPU baseline."""
+    import torch
+    from oracle import attention as OA
+    from oracle import kmeans as KM
+    from oracle import svgear as S
+    heads = q.shape[1]
+    scale = 1.0 / np.sqrt(D)
+    dev = qt.device
+    err = torch.empty((BATCH, heads, Cq, Ck), dtype=torch.float32, device=dev)
+    sel2 = torch.empty_like(sel)
+    out2, _, _ = va.compensate_route(qt, kt, vt, qa, Cq, ka, Ck, SVG["density"], err=err, sel=sel2)
+    qa9 = torch.empty_like(qa)
+    qc9 = torch.empty((BATCH, heads, Cq, D), dtype=torch.float32, device=dev)
+    qn9 = torch.empty((BATCH, heads, Cq), dtype=torch.int32, device=dev)
+    va.cluster(qt, Cq, SVG["iters"] - 1, qinit, qa9, qc9, qn9)
+    if va.device_error() != va.OK:
+        raise RuntimeError("device error in the parity calls")
+    # Member lists are built with atomics, so a repeated call may sum keys in
+    # another order (last-bit differences, and near-cut routing flips): kept
+    # as information, not as a pass criterion.
+    same = bool(torch.equal(out2, out)) and bool(torch.equal(sel2, sel))
+    qa_h, ka_h = qa.cpu().numpy(), ka.cpu().numpy()
+    err_h, sel_h = err.cpu().numpy(), sel.cpu().numpy().astype(bool)
+    sel2_h = sel2.cpu().numpy().astype(bool)
+    rows = OA.sample_rows(N, BLOCK, 64, seed=9)
+    got = out[:, :, torch.from_numpy(rows).to(dev)].float().cpu().numpy()
+    want = np.empty_like(got, dtype=np.float64)
+    route_exact = True
+    oflops, secs = 0.0, 0.0
+    for h in range(heads):
+        nq, _ = S.cluster_stats(q[0, h], qa_h[0, h], Cq)
+        nk, _ = S.cluster_stats(k[0, h], ka_h[0, h], Ck)
+        # routing rule on the same call's own float32 errors, bit for bit
+        route_exact &= bool(np.array_equal(sel2_h[0, h], S.route(err_h[0, h], nq, nk, N,
+                                                                 SVG["density"])))
+        t0 = time.perf_counter()
+        want[0, h] = S.compensated_attention(q[0, h], k[0, h], v[0, h], qa_h[0, h], ka_h[0, h],
+                                             Ck, sel_h[0, h], scale, rows=rows)
+        secs += time.perf_counter() - t0
+        for i in rows:
+            s_row = sel_h[0, h][qa_h[0, h, i]]
+            oflops += 4.0 * D * (float(s_row[ka_h[0, h]].sum()) + float((~s_row & (nk > 0)).sum()))
+    rec = parity_record(got, want, "compensated output rows %d x %d heads vs the float64 oracle "
+                        "on the step's clusters and selection" % (len(rows), heads))
+    near = 0
+    qc9_h, qa9_h = qc9.cpu().numpy().astype(np.float64), qa9.cpu().numpy()
+    for h in (0, heads - 1):
+        # the 10th assignment is the oracle's argmin under the GPU's 9th centroids
+        d2 = KM.sq_distances(q[0, h], qc9_h[0, h])
+        want_a = np.argmin(d2, axis=1)
+        bad = np.nonzero(qa_h[0, h] != want_a)[0]
+        gap = d2[bad, qa_h[0, h][bad]] - d2[bad, want_a[bad]]
+        scl = (q[0, h][bad].astype(np.float64) ** 2).sum(1) + (qc9_h[0, h][want_a[bad]] ** 2).sum(1)
+        if (gap > 1e-4 * scl).any():
+            route_exact = False
+        near += len(bad)
+    rec.update({"routing_bit_exact": route_exact, "kmeans_near_ties_2_heads": near,
+                "repeat_call_identical": same})
+    rec["pass"] = bool(rec["pass"] and route_exact)
+    extra = {"parity": rec}
+    if world == 1 and not args.no_cpu_baseline:
+        extra["cpu_baseline"] = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT,
+                                 "cores": threads_used(), "kind": "oracle",
+                                 "seconds": round(secs, 2),
+                                 "sample": "compensated attention (exact keys of the selected "
+                                           "clusters + virtual keys) of %d query rows x %d "
+                                           "heads, float64 oracle" % (len(rows), heads)}
+    return extra
 
 
 def run_reference(args, world, rank):
@@ -487,7 +588,7 @@ def run_reference(args, world, rank):
         oracle_sample(wl, q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=1000 + i))
     secs, fl = 0.0, 0.0
     for i in range(args.steps):
-        s, f = oracle_sample(wl, q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=2000 + i))
+        s, f, _ = oracle_sample(wl, q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=2000 + i))
         secs += s
         fl += f
     value = fl / secs / 1e12
@@ -578,6 +679,38 @@ def run_linear(args, world, rank, local, mixed):
                          "peak_source": "%s copy bandwidth" % src,
                          "kernel": "whole call (lin_state + lin_prep + lin_out)",
                          "algorithmic_bytes": io_bytes, "flops": lin_flops, "traffic": None}})
+    if rank == 0:
+        from oracle import attention as OA
+        from oracle import linear as OL
+        rows = OA.sample_rows(N, BLOCK, 64, seed=10)
+        got = out[:, :, torch.from_numpy(rows).to(dev)].float().cpu().numpy()
+        t0 = time.perf_counter()
+        if mixed:
+            bm = oracle_block_mask(wl)
+            want = OL.mixed_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(D), r, rows=rows)
+        else:
+            want = OL.linear_attention(q, k, v, rows=rows)
+        secs = time.perf_counter() - t0
+        line["parity"] = parity_record(got, want, "output rows %d x %d heads vs the float64 "
+                                       "oracle (last timed call)" % (len(rows), heads))
+        if world == 1 and not args.no_cpu_baseline:
+            if mixed:
+                live_keys = (bm * np.minimum(BLOCK, N - np.arange(bm.shape[0]) * BLOCK)[None, :]).sum(1)
+                oflops = (4.0 * D * float(live_keys[rows // BLOCK].sum())
+                          + 4.0 * N * D * len(rows)) * BATCH * heads
+                base = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT}
+            else:
+                # the oracle's time for R rows, scaled to a whole call's rows,
+                # against the call's algorithmic bytes
+                full_secs = secs * N / len(rows)
+                base = {"value": round(io_bytes / full_secs / 1e9, 4), "unit": "GB/s"}
+            line["cpu_baseline"] = dict(base, cores=threads_used(), kind="oracle",
+                                        seconds=round(secs, 2),
+                                        sample="%d query rows x %d heads (float64 oracle, "
+                                               "pairwise weights%s)"
+                                               % (len(rows), heads,
+                                                  ", plus the masked softmax rows" if mixed
+                                                  else "; scaled to all rows"))
     head = {k2: line.pop(k2) for k2 in ("metric", "value", "unit")}
     return {**head, **line}
 
@@ -679,9 +812,14 @@ def run_bwd(args, world, rank, local):
         live_keys = (bm * np.minimum(BLOCK, N - np.arange(bm.shape[0]) * BLOCK)[None, :]).sum(1)
         oflops = 6.0 * D * float(live_keys[rows // BLOCK].sum()) * BATCH * heads
         t0 = time.perf_counter()
-        OB.block_sparse_attention_grad(q, k, v, g, bm, BLOCK, 1.0 / np.sqrt(D), rows=rows,
-                                       keys=np.array([], dtype=np.int64))
+        want_dq, _, _ = OB.block_sparse_attention_grad(q, k, v, g, bm, BLOCK, 1.0 / np.sqrt(D),
+                                                       rows=rows,
+                                                       keys=np.array([], dtype=np.int64))
         secs = time.perf_counter() - t0
+        got_dq = dq[:, :, torch.from_numpy(rows).to(dev)].float().cpu().numpy()
+        line["parity"] = parity_record(got_dq, want_dq, "dq rows %d x %d heads vs the float64 "
+                                       "gradient oracle (last timed call)" % (len(rows), heads),
+                                       max_abs=3e-2, mean_abs=1e-2, relative=True)
         line["cpu_baseline"] = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT,
                                 "cores": threads_used(), "kind": "oracle",
                                 "seconds": round(secs, 2),

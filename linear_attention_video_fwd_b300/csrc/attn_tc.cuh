@@ -87,6 +87,9 @@ enum : int {
   B_COUNT = B_DRAIN + 1
 };
 
+// S = Q K^T over the 128 dims (8 steps of K = 16) into TMEM at s_tmem; Q and
+// K are 128B-swizzled K-major tiles (two 64-dim halves). Used by the kernels
+// whose issue loops are not grouped.
 __device__ __forceinline__ void tc_issue_qk(uint32_t s_tmem, uint32_t sQ, uint32_t sK) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll
@@ -96,6 +99,7 @@ __device__ __forceinline__ void tc_issue_qk(uint32_t s_tmem, uint32_t sQ, uint32
   }
 }
 
+// O (+)= P V with P from TMEM at p_tmem and V an MN-major tile at sV.
 __device__ __forceinline__ void tc_issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t sV,
                                             bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
@@ -104,6 +108,82 @@ __device__ __forceinline__ void tc_issue_pv(uint32_t o_tmem, uint32_t p_tmem, ui
     umma_ts(o_tmem, p_tmem + k * 8, sw128_desc(sV + k * 2048, TC_HALF_BYTES, 1024), idesc,
             (accumulate || k > 0) ? 1u : 0u);
   }
+}
+
+// The tensor pipe accepts an MMA about as fast as it runs one (64 cycles for
+// 128 x 128 x 16), so every instruction the issuing thread spends between
+// two MMAs of a product is idle pipe. A product's eight K = 16 steps are
+// therefore issued from one asm block, with descriptors precomputed: a step
+// changes only the start address field (low 14 bits) of a 128B-swizzled
+// tile's descriptor, i.e. low word + (byte offset >> 4), with no carry since
+// shared-memory addresses stay below 256 KB.
+
+// S = Q K^T: A and B are K-major tiles, steps 16 elements (32 B) apart
+// within a 64-wide half and TC_HALF_BYTES between the halves.
+__device__ __forceinline__ void tc_qk_group(uint32_t d, uint32_t alo, uint32_t blo, uint32_t hi) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#define TC_QK_OFS(k) ((((k) >> 2) * TC_HALF_BYTES + ((k) & 3) * 32) >> 4)
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+      "mov.b64 a, {%4, %2};\n\tmov.b64 b, {%5, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pf;\n\t"
+      "mov.b64 a, {%6, %2};\n\tmov.b64 b, {%7, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t"
+      "mov.b64 a, {%8, %2};\n\tmov.b64 b, {%9, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t"
+      "mov.b64 a, {%10, %2};\n\tmov.b64 b, {%11, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t"
+      "mov.b64 a, {%12, %2};\n\tmov.b64 b, {%13, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t"
+      "mov.b64 a, {%14, %2};\n\tmov.b64 b, {%15, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t"
+      "mov.b64 a, {%16, %2};\n\tmov.b64 b, {%17, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t"
+      "mov.b64 a, {%18, %2};\n\tmov.b64 b, {%19, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t}"
+      ::"r"(d), "r"(idesc), "r"(hi), "r"(0u),
+      "r"(alo + TC_QK_OFS(0)), "r"(blo + TC_QK_OFS(0)), "r"(alo + TC_QK_OFS(1)),
+      "r"(blo + TC_QK_OFS(1)), "r"(alo + TC_QK_OFS(2)), "r"(blo + TC_QK_OFS(2)),
+      "r"(alo + TC_QK_OFS(3)), "r"(blo + TC_QK_OFS(3)), "r"(alo + TC_QK_OFS(4)),
+      "r"(blo + TC_QK_OFS(4)), "r"(alo + TC_QK_OFS(5)), "r"(blo + TC_QK_OFS(5)),
+      "r"(alo + TC_QK_OFS(6)), "r"(blo + TC_QK_OFS(6)), "r"(alo + TC_QK_OFS(7)),
+      "r"(blo + TC_QK_OFS(7))
+      : "memory");
+#undef TC_QK_OFS
+}
+
+// O (+)= P V: A (P, bf16 pairs) from TMEM columns p + 8k, B (V) an MN-major
+// tile whose start advances 16 rows (2048 B) per step. The first step
+// accumulates only if `accumulate`.
+__device__ __forceinline__ void tc_pv_group(uint32_t d, uint32_t p, uint32_t blo, uint32_t hi,
+                                            bool accumulate) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 pf, %3, 0;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+      "mov.b64 b, {%5, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], b, %1, pf;\n\t"
+      "mov.b64 b, {%7, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], b, %1, pt;\n\t"
+      "mov.b64 b, {%9, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], b, %1, pt;\n\t"
+      "mov.b64 b, {%11, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], b, %1, pt;\n\t"
+      "mov.b64 b, {%13, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%12], b, %1, pt;\n\t"
+      "mov.b64 b, {%15, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%14], b, %1, pt;\n\t"
+      "mov.b64 b, {%17, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%16], b, %1, pt;\n\t"
+      "mov.b64 b, {%19, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%18], b, %1, pt;\n\t}"
+      ::"r"(d), "r"(idesc), "r"(hi), "r"(accumulate ? 1u : 0u),
+      "r"(p + 0), "r"(blo + 0 * 128), "r"(p + 8), "r"(blo + 1 * 128),
+      "r"(p + 16), "r"(blo + 2 * 128), "r"(p + 24), "r"(blo + 3 * 128),
+      "r"(p + 32), "r"(blo + 4 * 128), "r"(p + 40), "r"(blo + 5 * 128),
+      "r"(p + 48), "r"(blo + 6 * 128), "r"(p + 56), "r"(blo + 7 * 128)
+      : "memory");
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -428,6 +508,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
       bool ok = mbar_wait_bounded(bar(B_Q_FULL + 0), 0, lim, abort_p);
       if (ok && has1) ok = mbar_wait_bounded(bar(B_Q_FULL + 1), 0, lim, abort_p);
+      // Descriptor halves of the Q tiles and of stage 0 of the K and V rings;
+      // a stage's descriptor is the low word + stage * (tile bytes >> 4).
+      const uint64_t dq0 = sw128_desc(sQ0, 16, 1024), dq1 = sw128_desc(sQ1, 16, 1024);
+      const uint64_t dk = sw128_desc(sK0, 16, 1024);
+      const uint64_t dv = sw128_desc(sV0, TC_HALF_BYTES, 1024);
+      const uint32_t q_lo[2] = {static_cast<uint32_t>(dq0), static_cast<uint32_t>(dq1)};
+      const uint32_t k_lo = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
+      const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
       int pend[2] = {-1, -1};   // union entry whose PV is still to issue, per tile
       int cnt[2] = {0, 0};      // QKs issued per tile
       uint32_t outst = 0;       // per V stage, 2 bits: tiles still to read it
@@ -439,7 +527,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int sv = pu % TC_NV;
         if (!mbar_wait_bounded(bar(B_V_FULL + sv), (pu / TC_NV) & 1, lim, abort_p)) return false;
         tc_fence_after();
-        tc_issue_pv(tmem + t * 256 + 128, tmem + t * 256, sV0 + sv * TC_TILE_BYTES, jj > 0);
+        tc_pv_group(tmem + t * 256 + 128, tmem + t * 256, v_lo + sv * (TC_TILE_BYTES >> 4), v_hi,
+                    jj > 0);
         umma_commit(bar(B_O_DONE + t));
         outst &= ~(1u << (2 * sv + t));
         if (((outst >> (2 * sv)) & 3u) == 0) umma_commit(bar(B_V_EMPTY + sv));
@@ -456,7 +545,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int t = 0; t < 2; ++t) {
           if (pend[t] >= 0 && !(ok = issue_pv(t))) break;
           if ((f >> t) & 1u) {
-            tc_issue_qk(tmem + t * 256, t == 0 ? sQ0 : sQ1, sK0 + sk * TC_TILE_BYTES);
+            tc_qk_group(tmem + t * 256, q_lo[t], k_lo + sk * (TC_TILE_BYTES >> 4), k_hi);
             umma_commit(bar(B_S_FULL + t));
             pend[t] = u;
             ++cnt[t];
