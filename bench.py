@@ -66,6 +66,9 @@ WORKLOADS = {
     "hunyuan_dense": dict(T=33, H=45, W=80, heads=24, kind="dense", params={}, step=0,
                           seed=1239, desc="HunyuanVideo-720p-shaped attention forward with the "
                           "all-ones mask on the same block-sparse kernel", mask="dense"),
+    "wan_radial_d64": dict(T=21, H=30, W=52, heads=12, kind="radial", params={}, step=0,
+                           seed=1235, d=64, desc="Wan-shaped radial block-sparse attention "
+                           "forward with head_dim 64", mask="radial, W0=H*W"),
 }
 METRIC = "block-sparse attn effective TFLOP/s + ms/call at 32,760 tok; % of B300 BF16 peak"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_tc_wan_radial_traffic.json")
@@ -85,11 +88,12 @@ def workload_metric(name, wl):
 
 def workload_config(name, wl):
     N = wl["T"] * wl["H"] * wl["W"]
+    d = wl.get("d", D)
     return {"workload": wl["desc"], "B": BATCH, "heads": wl["heads"],
-            "grid_THW": [wl["T"], wl["H"], wl["W"]], "tokens": N, "head_dim": D,
+            "grid_THW": [wl["T"], wl["H"], wl["W"]], "tokens": N, "head_dim": d,
             "block": BLOCK, "mask": wl["mask"],
             "l2": "inputs larger than L2 (Q+K+V+O = %d MB per call vs 126 MB L2), no flush"
-                  % round(4 * BATCH * wl["heads"] * N * D * 2 / 1e6)}
+                  % round(4 * BATCH * wl["heads"] * N * d * 2 / 1e6)}
 
 
 def peaks():
@@ -211,8 +215,8 @@ def threads_used() -> int:
 
 def make_inputs(wl, seed):
     import synth
-    return synth.video_qkv(BATCH, wl["heads"], wl["T"], wl["H"], wl["W"], D, seed=seed,
-                           dtype="bf16")
+    return synth.video_qkv(BATCH, wl["heads"], wl["T"], wl["H"], wl["W"], wl.get("d", D),
+                           seed=seed, dtype="bf16")
 
 
 def oracle_block_mask(wl):
@@ -226,12 +230,12 @@ def oracle_sample(wl, q, k, v, bm, rows):
     """Run the float64 oracle on `rows` of every head; returns (seconds, live
     FLOPs done, output rows [B, heads, R, d])."""
     from oracle import attention as OA
-    N = q.shape[2]
+    N, d = q.shape[2], q.shape[3]
     live_keys_per_block = (bm * np.array([min(N, (b + 1) * BLOCK) - b * BLOCK
                                           for b in range(bm.shape[0])])[None, :]).sum(1)
-    flops = 4.0 * D * float(live_keys_per_block[rows // BLOCK].sum()) * BATCH * wl["heads"]
+    flops = 4.0 * d * float(live_keys_per_block[rows // BLOCK].sum()) * BATCH * wl["heads"]
     t0 = time.perf_counter()
-    o, _ = OA.block_sparse_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(D), rows=rows)
+    o, _ = OA.block_sparse_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(d), rows=rows)
     return time.perf_counter() - t0, flops, o
 
 
@@ -302,7 +306,7 @@ def run_ours(args, world, rank, local):
     out = torch.empty_like(qt)
     kind = {"radial": va.RADIAL, "lvsa": va.LVSA, "dense": va.DENSE}[wl["kind"]]
     mask = va.mask_build(kind, T, H, W, block=BLOCK, step=wl["step"], **wl["params"])
-    flops = 4.0 * D * mask.live_pairs * BATCH * heads
+    flops = 4.0 * wl.get("d", D) * mask.live_pairs * BATCH * heads
     stream = torch.cuda.current_stream()
 
     def call():
@@ -362,7 +366,7 @@ def run_ours(args, world, rank, local):
                      "flops_per_launch": flops, "launch_ms_mean": round(float(np.mean(launch_ms)), 4),
                      "launch_ms_min": round(float(np.min(launch_ms)), 4),
                      "traffic": profiled_traffic() if name == "wan_radial" else None,
-                     "kernel": "va::attn_tc_kernel"},
+                     "kernel": "va::attn_tc_kernel<%d>" % wl.get("d", D)},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }

@@ -186,8 +186,9 @@ int va_mask_build_static(int kind, int T, int H, int W, const va_mask_params* pa
  * q, k, v, out: [B, heads, N, d] device arrays of `dtype`; lse: NULL or a
  * [B, heads, N] float32 device array. Softmax and accumulation are float32;
  * VA_BF16 inputs give a bf16 output, VA_F32 inputs a float32 output.
- * Supported: VA_BF16 with d = 128 and block 128 (tcgen05 tensor-core kernel);
- * VA_F32 with d in {64, 128} and block in {64, 128} (float32 FMA kernel).
+ * Supported: VA_BF16 with d in {64, 128} and block 128 (tcgen05 tensor-core
+ * kernel); VA_F32 with d in {64, 128} and block in {64, 128} (float32 FMA
+ * kernel).
  * Errors: VA_ERR_INVALID (null pointers, N != T*H*W of the mask, B or heads
  * < 1, misaligned pointers, a mask built on another device), VA_ERR_UNSUPPORTED
  * (other dtype/d/block), VA_ERR_CUDA (launch failure).

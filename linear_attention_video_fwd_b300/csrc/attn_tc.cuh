@@ -1,5 +1,7 @@
 // Block-sparse flash-attention forward on the 5th-generation tensor cores
-// (tcgen05 + TMEM + TMA), bf16 inputs, head_dim 128, 128-token blocks.
+// (tcgen05 + TMEM + TMA), bf16 inputs, head_dim D in {64, 128}, 128-token
+// blocks. A D = 128 tile is two 64-dim halves (one 128B swizzle atom wide
+// each); a D = 64 tile is one.
 //
 // Work unit: one CTA per (batch*head, query-block pair {2P, 2P+1}). The two
 // query tiles share one stream of K/V tiles: the union of the two CSR rows,
@@ -23,7 +25,7 @@
 //
 // TMEM (512 columns): tile t uses columns [256t, 256t + 128) for S_t (fp32;
 // P_t is written back over its first 64 columns as packed bf16 pairs) and
-// [256t + 128, 256t + 256) for the O_t accumulator.
+// [256t + 128, 256t + 128 + D) for the O_t accumulator.
 //
 // Online softmax in the log2 domain: the running max used for exponentiation
 // is only raised when a block's max exceeds it by more than TAU (so P <= 2^TAU
@@ -59,6 +61,15 @@ constexpr int TC_REGS_INC = 216;
 static_assert(128 * TC_REGS_DEC + 256 * TC_REGS_INC <= TC_THREADS * TC_LAUNCH_REGS,
               "register split exceeds the launch allocation");
 static_assert(TC_NV >= 2 && TC_NV <= 4, "V stage bookkeeping assumes 2..4 stages");
+
+// Sizes that depend on the head dimension D of the forward kernel.
+template <int D>
+struct TcDim {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kTileBytes = TC_BLK * D * 2;   // one 128 x D bf16 tile
+  static constexpr int kHalves = D / 64;              // 64-dim TMA boxes per tile
+  static constexpr int kSmemBytes = 1024 + kTileBytes * (2 + TC_NK + TC_NV);
+};
 
 struct TcArgs {
   const int* row_ptr;  // [nqb + 1] CSR rows
@@ -120,7 +131,34 @@ __device__ __forceinline__ void tc_issue_pv(uint32_t o_tmem, uint32_t p_tmem, ui
 
 // S = Q K^T: A and B are K-major tiles, steps 16 elements (32 B) apart
 // within a 64-wide half and TC_HALF_BYTES between the halves.
-__device__ __forceinline__ void tc_qk_group(uint32_t d, uint32_t alo, uint32_t blo, uint32_t hi) {
+template <int D>
+__device__ __forceinline__ void tc_qk_group(uint32_t d, uint32_t alo, uint32_t blo, uint32_t hi);
+
+// D = 64: four steps within the one 64-dim atom.
+template <>
+__device__ __forceinline__ void tc_qk_group<64>(uint32_t d, uint32_t alo, uint32_t blo,
+                                                uint32_t hi) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 pf, %3, %3;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+      "mov.b64 a, {%4, %2};\n\tmov.b64 b, {%5, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pf;\n\t"
+      "mov.b64 a, {%6, %2};\n\tmov.b64 b, {%7, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t"
+      "mov.b64 a, {%8, %2};\n\tmov.b64 b, {%9, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t"
+      "mov.b64 a, {%10, %2};\n\tmov.b64 b, {%11, %2};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %1, pt;\n\t}"
+      ::"r"(d), "r"(idesc), "r"(hi), "r"(0u), "r"(alo), "r"(blo), "r"(alo + 2u), "r"(blo + 2u),
+      "r"(alo + 4u), "r"(blo + 4u), "r"(alo + 6u), "r"(blo + 6u)
+      : "memory");
+}
+
+// D = 128: four steps per 64-dim half.
+template <>
+__device__ __forceinline__ void tc_qk_group<128>(uint32_t d, uint32_t alo, uint32_t blo,
+                                                 uint32_t hi) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #define TC_QK_OFS(k) ((((k) >> 2) * TC_HALF_BYTES + ((k) & 3) * 32) >> 4)
   asm volatile(
@@ -154,11 +192,13 @@ __device__ __forceinline__ void tc_qk_group(uint32_t d, uint32_t alo, uint32_t b
 }
 
 // O (+)= P V: A (P, bf16 pairs) from TMEM columns p + 8k, B (V) an MN-major
-// tile whose start advances 16 rows (2048 B) per step. The first step
+// tile of D columns whose start advances 16 rows (2048 B) per step (the
+// 64-dim halves of a D = 128 tile lie TC_HALF_BYTES apart). The first step
 // accumulates only if `accumulate`.
+template <int D>
 __device__ __forceinline__ void tc_pv_group(uint32_t d, uint32_t p, uint32_t blo, uint32_t hi,
                                             bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
   asm volatile(
       "{\n\t.reg .pred pf, pt;\n\t.reg .b64 b;\n\t"
       "setp.ne.b32 pf, %3, 0;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
@@ -229,6 +269,7 @@ __device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float 
 }
 
 // Softmax of one tile: its CSR row, its TMEM columns and its barriers.
+template <int D>
 __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I, int bh,
                                                 uint32_t tmem, uint64_t* bars,
                                                 volatile int* abort_p) {
@@ -311,7 +352,7 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tO + c * 32, v);
         tmem_wait_ld();
@@ -352,14 +393,14 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
     mbar_arrive(bP);
   }
   // epilogue
-  const long long obase = (static_cast<long long>(bh) * a.N + row) * TC_D;
+  const long long obase = (static_cast<long long>(bh) * a.N + row) * D;
   if (n > 0 && ok)
     ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (n - 1) & 1, lim, abort_p));
   if (n > 0 && ok) {
     tc_fence_after();
     const float inv = 1.f / l;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
       uint32_t v[32];
       tmem_ld32(tO + c * 32, v);
       tmem_wait_ld();
@@ -381,11 +422,12 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
   } else if (n == 0 && row < a.N) {
     uint4* dst = reinterpret_cast<uint4*>(a.out + obase);
 #pragma unroll
-    for (int q4 = 0; q4 < 16; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
+    for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
     if (a.lse != nullptr) a.lse[static_cast<long long>(bh) * a.N + row] = -INFINITY;
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
@@ -398,8 +440,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sQ0 = smem_u32(smem);
-  const uint32_t sK0 = sQ0 + 2 * TC_TILE_BYTES;
-  const uint32_t sV0 = sK0 + TC_NK * TC_TILE_BYTES;
+  constexpr int kTile = TcDim<D>::kTileBytes;
+  const uint32_t sK0 = sQ0 + 2 * kTile;
+  const uint32_t sV0 = sK0 + TC_NK * kTile;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int bh = blockIdx.x / a.npairs;
@@ -444,7 +487,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ------------------------------------------- softmax / correction / out --
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(TC_REGS_INC));
     const int tile = (warp - 4) >> 2;
-    if (tile == 0 || has1) tc_softmax_tile(a, tile, tile == 0 ? I0 : I1, bh, tmem, bars, abort_p);
+    if (tile == 0 || has1)
+      tc_softmax_tile<D>(a, tile, tile == 0 ? I0 : I1, bh, tmem, bars, abort_p);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(TC_REGS_DEC));
   if (warp == 0) {
@@ -453,33 +497,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      mbar_arrive_expect_tx(bar(B_Q_FULL + 0), TC_TILE_BYTES);
-      tma_load_3d(sQ0, &map_q, bar(B_Q_FULL + 0), 0, I0 * TC_BLK, bh);
-      tma_load_3d(sQ0 + TC_HALF_BYTES, &map_q, bar(B_Q_FULL + 0), 64, I0 * TC_BLK, bh);
-      if (has1) {
-        const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
-        mbar_arrive_expect_tx(bar(B_Q_FULL + 1), TC_TILE_BYTES);
-        tma_load_3d(sQ1, &map_q, bar(B_Q_FULL + 1), 0, I1 * TC_BLK, bh);
-        tma_load_3d(sQ1 + TC_HALF_BYTES, &map_q, bar(B_Q_FULL + 1), 64, I1 * TC_BLK, bh);
-      }
+      // a tile is kHalves boxes of 64 dims x 128 rows, TC_HALF_BYTES apart
+      auto load_tile = [&](uint32_t dst, const CUtensorMap* map, uint32_t b, int row0) {
+        mbar_arrive_expect_tx(b, kTile);
+#pragma unroll
+        for (int h = 0; h < TcDim<D>::kHalves; ++h)
+          tma_load_3d(dst + h * TC_HALF_BYTES, map, b, 64 * h, row0, bh);
+      };
+      load_tile(sQ0, &map_q, bar(B_Q_FULL + 0), I0 * TC_BLK);
+      if (has1) load_tile(sQ0 + kTile, &map_q, bar(B_Q_FULL + 1), I1 * TC_BLK);
       int issued_k = 0, issued_v = 0;
       for (int u = 0; u < nu; ++u) {
         const int J = a.pcol[pbeg + u] >> 2;
         const int sk = u % TC_NK, sv = u % TC_NV;
-        const uint32_t sK = sK0 + sk * TC_TILE_BYTES, sV = sV0 + sv * TC_TILE_BYTES;
+        const uint32_t sK = sK0 + sk * kTile, sV = sV0 + sv * kTile;
         if (u >= TC_NK &&
             !mbar_wait_bounded(bar(B_K_EMPTY + sk), ((u / TC_NK) & 1) ^ 1, lim, abort_p))
           break;
-        mbar_arrive_expect_tx(bar(B_K_FULL + sk), TC_TILE_BYTES);
-        tma_load_3d(sK, &map_k, bar(B_K_FULL + sk), 0, J * TC_BLK, bh);
-        tma_load_3d(sK + TC_HALF_BYTES, &map_k, bar(B_K_FULL + sk), 64, J * TC_BLK, bh);
+        load_tile(sK, &map_k, bar(B_K_FULL + sk), J * TC_BLK);
         issued_k = u + 1;
         if (u >= TC_NV &&
             !mbar_wait_bounded(bar(B_V_EMPTY + sv), ((u / TC_NV) & 1) ^ 1, lim, abort_p))
           break;
-        mbar_arrive_expect_tx(bar(B_V_FULL + sv), TC_TILE_BYTES);
-        tma_load_3d(sV, &map_v, bar(B_V_FULL + sv), 0, J * TC_BLK, bh);
-        tma_load_3d(sV + TC_HALF_BYTES, &map_v, bar(B_V_FULL + sv), 64, J * TC_BLK, bh);
+        load_tile(sV, &map_v, bar(B_V_FULL + sv), J * TC_BLK);
         issued_v = u + 1;
       }
       if (*abort_p) {
@@ -505,7 +545,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA --
     if (lane == 0 && nu > 0) {
-      const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
+      const uint32_t sQ1 = sQ0 + kTile;
       bool ok = mbar_wait_bounded(bar(B_Q_FULL + 0), 0, lim, abort_p);
       if (ok && has1) ok = mbar_wait_bounded(bar(B_Q_FULL + 1), 0, lim, abort_p);
       // Descriptor halves of the Q tiles and of stage 0 of the K and V rings;
@@ -527,8 +567,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int sv = pu % TC_NV;
         if (!mbar_wait_bounded(bar(B_V_FULL + sv), (pu / TC_NV) & 1, lim, abort_p)) return false;
         tc_fence_after();
-        tc_pv_group(tmem + t * 256 + 128, tmem + t * 256, v_lo + sv * (TC_TILE_BYTES >> 4), v_hi,
-                    jj > 0);
+        tc_pv_group<D>(tmem + t * 256 + 128, tmem + t * 256, v_lo + sv * (kTile >> 4), v_hi,
+                       jj > 0);
         umma_commit(bar(B_O_DONE + t));
         outst &= ~(1u << (2 * sv + t));
         if (((outst >> (2 * sv)) & 3u) == 0) umma_commit(bar(B_V_EMPTY + sv));
@@ -545,7 +585,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int t = 0; t < 2; ++t) {
           if (pend[t] >= 0 && !(ok = issue_pv(t))) break;
           if ((f >> t) & 1u) {
-            tc_qk_group(tmem + t * 256, q_lo[t], k_lo + sk * (TC_TILE_BYTES >> 4), k_hi);
+            tc_qk_group<D>(tmem + t * 256, q_lo[t], k_lo + sk * (kTile >> 4), k_hi);
             umma_commit(bar(B_S_FULL + t));
             pend[t] = u;
             ++cnt[t];

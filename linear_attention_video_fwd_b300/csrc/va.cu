@@ -454,6 +454,7 @@ int launch_simt(const void* q, const void* k, const void* v, const va_mask* m, v
   return launch_status();
 }
 
+template <int D>
 int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, void* out, float* lse,
               int BH, int N, float scale, cudaStream_t s) {
   static DeviceOnce once;
@@ -464,16 +465,17 @@ int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, voi
     // The kernel's setmaxnreg split assumes this exact per-thread register
     // count at launch; anything else could leave the increase waiting.
     cudaFuncAttributes fa;
-    int r = cuda_status(cudaFuncGetAttributes(&fa, va::attn_tc_kernel));
+    int r = cuda_status(cudaFuncGetAttributes(&fa, va::attn_tc_kernel<D>));
     if (r) return r;
     if (fa.numRegs != va::TC_LAUNCH_REGS) return VA_ERR_UNSUPPORTED;
-    return cuda_status(cudaFuncSetAttribute(
-        va::attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, va::TC_SMEM_BYTES));
+    return cuda_status(cudaFuncSetAttribute(va::attn_tc_kernel<D>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            va::TcDim<D>::kSmemBytes));
   });
   if (st) return st;
   CUtensorMap mq, mk, mv;
-  if ((st = encode_bf16_rows(&mq, q, BH, N, 128)) || (st = encode_bf16_rows(&mk, k, BH, N, 128)) ||
-      (st = encode_bf16_rows(&mv, v, BH, N, 128)))
+  if ((st = encode_bf16_rows(&mq, q, BH, N, D)) || (st = encode_bf16_rows(&mk, k, BH, N, D)) ||
+      (st = encode_bf16_rows(&mv, v, BH, N, D)))
     return st;
   va::TcArgs a;
   a.row_ptr = m->row_ptr;
@@ -490,8 +492,8 @@ int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, voi
   a.wait_limit = g_wait_limit;
   const long long grid = static_cast<long long>(m->npairs) * BH;
   if (grid > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
-  va::attn_tc_kernel<<<static_cast<unsigned>(grid), va::TC_THREADS, va::TC_SMEM_BYTES, s>>>(
-      mq, mk, mv, a);
+  va::attn_tc_kernel<D><<<static_cast<unsigned>(grid), va::TC_THREADS, va::TcDim<D>::kSmemBytes,
+                          s>>>(mq, mk, mv, a);
   return launch_status();
 }
 
@@ -521,7 +523,8 @@ VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, co
     return VA_ERR_UNSUPPORTED;
   }
   if (dtype == VA_BF16) {
-    if (d == 128 && blk == 128) return launch_tc(q, k, v, m, out, lse, BH, N, scale, s);
+    if (d == 128 && blk == 128) return launch_tc<128>(q, k, v, m, out, lse, BH, N, scale, s);
+    if (d == 64 && blk == 128) return launch_tc<64>(q, k, v, m, out, lse, BH, N, scale, s);
     return VA_ERR_UNSUPPORTED;
   }
   return VA_ERR_UNSUPPORTED;

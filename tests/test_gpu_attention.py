@@ -71,10 +71,11 @@ SMALL_BF16 = [
 ]
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("case", SMALL_BF16)
-def test_bf16_small_all_rows(va, dev, case):
+def test_bf16_small_all_rows(va, dev, case, d):
     kind, T, H, W, p, step = case
-    q, k, v = synth.video_qkv(2, 3, T, H, W, 128, seed=11)
+    q, k, v = synth.video_qkv(2, 3, T, H, W, d, seed=11)
     got, want, gl, wl = _run(va, dev, q, k, v, kind, T, H, W, p, step, "bf16")
     assert_bf16_close(got, want)
     assert np.abs(gl - wl).max() <= 2e-2
@@ -89,11 +90,12 @@ def test_bf16_single_live_key_block_extremes(va, dev):
     assert_bf16_close(got, want)
 
 
-def test_wan_radial_full_size_sampled_rows(va, dev):
+@pytest.mark.parametrize("d", [128, 64])
+def test_wan_radial_full_size_sampled_rows(va, dev, d):
     # The benchmarked workload: B=1, 12 heads, 21x30x52 = 32,760 tokens, d=128,
-    # bf16, radial mask with block 128 (W0 = H*W).
+    # bf16, radial mask with block 128 (W0 = H*W); and the same grid with d=64.
     T, H, W = 21, 30, 52
-    q, k, v = cached_video_qkv(1, 12, T, H, W, 128, seed=1235)
+    q, k, v = cached_video_qkv(1, 12, T, H, W, d, seed=1235)
     rows = OA.sample_rows(T * H * W, 128, 512, seed=5)
     got, want, gl, wl = _run(va, dev, q, k, v, OM.RADIAL, T, H, W, OM.MaskParams(block=128),
                              0, "bf16", rows=rows)
@@ -116,16 +118,22 @@ def test_attention_rejects_bad_arguments(va, dev):
     with pytest.raises(va.VAError) as e:                 # bf16 needs block 128
         va.sparse_attn_fwd(q, q, q, m64)
     assert e.value.status == va.ERR_UNSUPPORTED
+    q64 = torch.zeros((1, 1, 240, 64), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(va.VAError) as e:                 # d = 64 with block 64: not on bf16
+        va.sparse_attn_fwd(q64, q64, q64, m64)
+    assert e.value.status == va.ERR_UNSUPPORTED
     assert va.device_error() == va.OK
 
 
-@pytest.mark.parametrize("pinned,with_lse,dtype", [(True, True, "bf16"), (False, False, "bf16"),
-                                                   (True, True, "f32")])
-def test_host_buffers_match_device_call(va, dev, pinned, with_lse, dtype):
+@pytest.mark.parametrize("pinned,with_lse,dtype,d", [(True, True, "bf16", 128),
+                                                     (False, False, "bf16", 128),
+                                                     (True, True, "f32", 128),
+                                                     (True, True, "bf16", 64)])
+def test_host_buffers_match_device_call(va, dev, pinned, with_lse, dtype, d):
     # va_sparse_attn_fwd_host (host q/k/v/out, pipelined chunks) must give the
     # device call's result bit for bit: every (batch, head) runs the same kernel.
     T, H, W = 5, 6, 11                                    # N = 330: ragged last block
-    B, Hh, d = 3, 5, 128                                  # 15 slices: chunks of one slice
+    B, Hh = 3, 5                                          # 15 slices: chunks of one slice
     q, k, v = synth.iid_qkv(B, Hh, T * H * W, d, seed=17)
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     qh, kh, vh = (torch.from_numpy(x).to(tdt) for x in (q, k, v))
