@@ -257,17 +257,6 @@ __device__ __forceinline__ void ffma2_bc(float& d0, float& d1, float a0, float a
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
 
-// (s0, s1) += (a0, a1) as one packed f32x2 add.
-__device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float a1) {
-  asm("{\n\t.reg .b64 ra, rs;\n\t"
-      "mov.b64 ra, {%2, %3};\n\t"
-      "mov.b64 rs, {%0, %1};\n\t"
-      "add.rn.f32x2 rs, rs, ra;\n\t"
-      "mov.b64 {%0, %1}, rs;\n\t}"
-      : "+f"(s0), "+f"(s1)
-      : "f"(a0), "f"(a1));
-}
-
 // Softmax of one tile: its CSR row, its TMEM columns and its barriers.
 template <int D>
 __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I, int bh,

@@ -475,6 +475,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // by the runtime tile number would live in local memory.
         int pend0 = -1, pend1 = -1;  // entry whose PV is still to issue
         int cnt0 = 0, cnt1 = 0;      // QKs issued
+        // descriptor low words of the Q tiles and of stage 0 of the K and V
+        // rings (a stage adds stage * (tile bytes >> 4); one asm block issues
+        // a product's eight steps)
+        const uint64_t dq0 = sw128_desc(sQ0, 16, 1024), dq1 = sw128_desc(sQ1, 16, 1024);
+        const uint64_t dk = sw128_desc(sK0, 16, 1024);
+        const uint64_t dv = sw128_desc(sV0, TC_HALF_BYTES, 1024);
+        const uint32_t k_lo = static_cast<uint32_t>(dk), k_hi = static_cast<uint32_t>(dk >> 32);
+        const uint32_t v_lo = static_cast<uint32_t>(dv), v_hi = static_cast<uint32_t>(dv >> 32);
         using Tile0 = std::integral_constant<int, 0>;
         using Tile1 = std::integral_constant<int, 1>;
         auto issue_pv = [&](auto tile) -> bool {
@@ -486,7 +494,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const int sv = pu % CT_NV;
           if (!mbar_wait_bounded(bar(CB_V_FULL + sv), (pu / CT_NV) & 1, lim, abort_p)) return false;
           tc_fence_after();
-          tc_issue_pv(tmem + t * 256 + 128, tmem + t * 256, sV0 + sv * TC_TILE_BYTES, jj > 0);
+          tc_pv_group<128>(tmem + t * 256 + 128, tmem + t * 256,
+                           v_lo + sv * (TC_TILE_BYTES >> 4), v_hi, jj > 0);
           umma_commit(bar(CB_O_DONE + t));
           umma_commit(bar(CB_V_EMPTY + sv));  // every entry is read by one tile only
           pend = -1;
@@ -498,7 +507,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (!mbar_wait_bounded(bar(CB_K_FULL + sk), (u / CT_NK) & 1, lim, abort_p)) return false;
           if ((t == 0 ? pend0 : pend1) >= 0 && !issue_pv(tile)) return false;
           tc_fence_after();
-          tc_issue_qk(tmem + t * 256, t == 0 ? sQ0 : sQ1, sK0 + sk * TC_TILE_BYTES);
+          tc_qk_group<128>(tmem + t * 256,
+                           static_cast<uint32_t>(t == 0 ? dq0 : dq1),
+                           k_lo + sk * (TC_TILE_BYTES >> 4), k_hi);
           umma_commit(bar(CB_S_FULL + t));
           umma_commit(bar(CB_K_EMPTY + sk));
           (t == 0 ? pend0 : pend1) = u;
