@@ -277,6 +277,7 @@ def timed_region(args, world, local, call, stream):
             for _ in range(4):
                 call()
             torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("va:timed %d steps" % args.steps)
         t_begin.record(stream)
         for i in range(args.steps):
             starts[i].record(stream)
@@ -284,6 +285,7 @@ def timed_region(args, world, local, call, stream):
             ends[i].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_pop()
         time.sleep(0.25)
     barrier(world)
     total_ms = max_over_ranks(t_begin.elapsed_time(t_end), world, torch.device("cuda", local))

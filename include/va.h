@@ -407,6 +407,22 @@ int va_set_wait_limit(int64_t cycles);
  */
 int va_selftest_wait_timeout(int64_t cycles, va_stream_t stream);
 
+/*
+ * Host-side validation of a block CSR (an interface for checks and tests; the
+ * paper has no counterpart): row_ptr[nqb + 1] and col_idx[nnz] in HOST
+ * memory. Valid means row_ptr[0] == 0, row_ptr[nqb] == nnz, rows
+ * non-decreasing, and every row's columns strictly ascending in [0, nqb); with
+ * require_diagonal, every row I also holds column I (the radial, LVSA and
+ * dense rules always keep the diagonal block). Returns VA_OK, VA_ERR_DEVICE
+ * for a list that breaks a rule, or VA_ERR_INVALID for null pointers or bad
+ * sizes. When the environment variable VA_CHECKED is set (and not "0"),
+ * va_mask_build validates its rows and transposed lists this way, and the
+ * transposed lists as the exact transpose of the rows, before returning; a
+ * failure frees the mask and returns VA_ERR_DEVICE.
+ */
+int va_csr_validate(const int32_t* row_ptr, const int32_t* col_idx, int nqb, int64_t nnz,
+                    int require_diagonal);
+
 /* Static text for a status code. */
 const char* va_status_string(int status);
 

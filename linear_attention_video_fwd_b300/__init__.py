@@ -66,6 +66,7 @@ def _load():
         "va_device_error": [vp],
         "va_set_wait_limit": [i64],
         "va_selftest_wait_timeout": [i64, vp],
+        "va_csr_validate": [i32p, i32p, i32, i64, i32],
         "va_status_string": [i32],
         "va_version": [],
     }
@@ -376,6 +377,15 @@ def compensate_route(q, k, v, qassign, Cq: int, kassign, Ck: int, density: float
                                     _dtype_code(q), _ptr(out), _ptr(err), _ptr(sel),
                                     _stream(stream)), "va_compensate_route")
     return out, err, sel
+
+
+def csr_validate(row_ptr, col_idx, require_diagonal: bool = True) -> int:
+    """va_csr_validate on host int32 arrays: VA_OK, ERR_DEVICE or ERR_INVALID."""
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    col = np.ascontiguousarray(col_idx, dtype=np.int32)
+    p32 = ctypes.POINTER(ctypes.c_int32)
+    return _lib.va_csr_validate(rp.ctypes.data_as(p32), col.ctypes.data_as(p32), len(rp) - 1,
+                                len(col), 1 if require_diagonal else 0)
 
 
 def device_error(stream=None) -> int:

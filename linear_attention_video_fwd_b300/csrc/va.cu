@@ -11,6 +11,7 @@
 #include <atomic>
 #include <mutex>
 #include <type_traits>
+#include <vector>
 
 #include "va.h"
 #include "common.cuh"
@@ -221,6 +222,68 @@ constexpr int64_t kMaxMaskNnz = 0x7fffffffLL;
 
 VA_EXPORT int va_version(void) { return 100; }
 
+VA_EXPORT int va_csr_validate(const int32_t* row_ptr, const int32_t* col_idx, int nqb, int64_t nnz,
+                              int require_diagonal) {
+  if (row_ptr == nullptr || nqb < 1 || nnz < 0 || (nnz > 0 && col_idx == nullptr))
+    return VA_ERR_INVALID;
+  if (row_ptr[0] != 0 || static_cast<int64_t>(row_ptr[nqb]) != nnz) return VA_ERR_DEVICE;
+  for (int i = 0; i < nqb; ++i) {
+    const int32_t b = row_ptr[i], e = row_ptr[i + 1];
+    if (e < b || static_cast<int64_t>(e) > nnz) return VA_ERR_DEVICE;
+    bool diag = false;
+    for (int32_t p = b; p < e; ++p) {
+      const int32_t c = col_idx[p];
+      if (c < 0 || c >= nqb || (p > b && c <= col_idx[p - 1])) return VA_ERR_DEVICE;
+      diag = diag || c == i;
+    }
+    if (require_diagonal && !diag) return VA_ERR_DEVICE;
+  }
+  return VA_OK;
+}
+
+namespace {
+
+// VA_CHECKED=1 makes every mask build copy its lists back and validate them
+// on the host: the rows and the transposed lists as CSR (with the diagonal,
+// which every rule of the library keeps), and the transposed lists as the
+// exact transpose of the rows.
+bool checked_mode() {
+  const char* f = std::getenv("VA_CHECKED");
+  return f != nullptr && f[0] != '\0' && f[0] != '0';
+}
+
+int validate_mask(const va_mask* m) {
+  const int nb = m->nqb;
+  const int64_t nnz = m->nnz;
+  std::vector<int32_t> rp(nb + 1), col(nnz > 0 ? nnz : 1), tp(nb + 1), tr(nnz > 0 ? nnz : 1);
+  int st;
+  if ((st = cuda_status(cudaMemcpy(rp.data(), m->row_ptr, sizeof(int32_t) * (nb + 1),
+                                   cudaMemcpyDeviceToHost))) ||
+      (st = cuda_status(cudaMemcpy(tp.data(), m->t_ptr, sizeof(int32_t) * (nb + 1),
+                                   cudaMemcpyDeviceToHost))))
+    return st;
+  if (nnz > 0 &&
+      ((st = cuda_status(cudaMemcpy(col.data(), m->col, sizeof(int32_t) * nnz,
+                                    cudaMemcpyDeviceToHost))) ||
+       (st = cuda_status(cudaMemcpy(tr.data(), m->t_row, sizeof(int32_t) * nnz,
+                                    cudaMemcpyDeviceToHost)))))
+    return st;
+  if ((st = va_csr_validate(rp.data(), col.data(), nb, nnz, 1)) ||
+      (st = va_csr_validate(tp.data(), tr.data(), nb, nnz, 1)))
+    return st;
+  // transpose check: count of (i, j) in rows == count of (j, i) in columns
+  std::vector<int32_t> fill(tp.begin(), tp.end() - 1);
+  for (int i = 0; i < nb; ++i)
+    for (int32_t p = rp[i]; p < rp[i + 1]; ++p) {
+      const int32_t j = col[p];
+      if (fill[j] >= tp[j + 1] || tr[fill[j]] != i) return VA_ERR_DEVICE;
+      ++fill[j];
+    }
+  return VA_OK;
+}
+
+}  // namespace
+
 VA_EXPORT const char* va_status_string(int status) {
   switch (status) {
     case VA_OK: return "ok";
@@ -388,6 +451,10 @@ VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params*
     }
   }
   if ((st = cuda_status(cudaStreamSynchronize(s)))) {
+    va_mask_free(m);
+    return st;
+  }
+  if (checked_mode() && (st = validate_mask(m))) {
     va_mask_free(m);
     return st;
   }

@@ -113,3 +113,33 @@ def test_mask_size_limits_are_checked_on_the_host(lib):
               ctypes.byref(nnz), None) == -2
     assert fn(1, 1 << 10, 1 << 10, 1 << 10, ctypes.byref(p1), 0, fake, fake, 0,
               ctypes.byref(nnz), None) == -1
+
+
+def test_csr_validator_on_host_arrays():
+    # va_csr_validate works on host arrays alone (no device call): the hand-
+    # derived tiny LVSA CSR passes, and each way a list can break is rejected.
+    import numpy as np
+    import linear_attention_video_fwd_b300 as va
+    from conftest import read_golden
+    g = read_golden("lvsa_tiny_csr.txt")
+    rp = np.array([int(x) for x in g[3]], dtype=np.int32)
+    col = np.array([int(x) for x in g[5]], dtype=np.int32)
+    assert va.csr_validate(rp, col) == va.OK
+    bad_rows = rp.copy()
+    bad_rows[2] = bad_rows[1] - 1                          # rows run backwards
+    assert va.csr_validate(bad_rows, col) == va.ERR_DEVICE
+    bad_nnz = rp.copy()
+    bad_nnz[-1] -= 1                                       # last offset is not nnz
+    assert va.csr_validate(bad_nnz, col) == va.ERR_DEVICE
+    out_of_range = col.copy()
+    out_of_range[0] = len(rp) - 1                          # column == nqb
+    assert va.csr_validate(rp, out_of_range) == va.ERR_DEVICE
+    unsorted = col.copy()
+    unsorted[[0, 1]] = unsorted[[1, 0]]                    # not ascending within a row
+    assert va.csr_validate(rp, unsorted) == va.ERR_DEVICE
+    # a row without its diagonal block: fine as a CSR, not for a mask rule
+    nodiag_rp = np.array([0, 1, 2], dtype=np.int32)
+    nodiag_col = np.array([1, 0], dtype=np.int32)
+    assert va.csr_validate(nodiag_rp, nodiag_col, require_diagonal=False) == va.OK
+    assert va.csr_validate(nodiag_rp, nodiag_col) == va.ERR_DEVICE
+    assert va.csr_validate(np.zeros(1, dtype=np.int32), col) == va.ERR_INVALID   # nqb = 0

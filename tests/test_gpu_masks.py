@@ -96,3 +96,16 @@ def test_mask_limits_on_blocks_and_live_pairs(va):
     assert m.nnz == 4096 * 4096
     m.free()
     assert va.device_error() == va.OK
+
+
+@pytest.mark.parametrize("case", SMALL[:6] + FULL)
+def test_checked_mode_validates_built_masks(va, case, monkeypatch):
+    # With VA_CHECKED set, va_mask_build copies its rows and transposed lists
+    # back and validates them (CSR rules, diagonal, exact transpose).
+    monkeypatch.setenv("VA_CHECKED", "1")
+    kind, T, H, W, p, step = case
+    m = _build(va, kind, T, H, W, p, step)
+    rp, col = m.csr()
+    assert va.csr_validate(rp, col) == va.OK
+    m.free()
+    assert va.device_error() == va.OK
