@@ -215,8 +215,9 @@ int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mas
  * order (no atomics): results are deterministic. Uses the mask's transposed
  * block lists (built by va_mask_build) for dk and dv, and 8 * B * heads *
  * ceil(N / block) * block bytes of stream-ordered scratch.
- * Supported: as the forward (VA_BF16, d = 128, block 128 on tcgen05; VA_F32,
- * d in {64, 128}, block in {64, 128} on the FMA pipes), B * heads <= 65535.
+ * Supported: as the forward (VA_BF16, d in {64, 128}, block 128 on tcgen05;
+ * VA_F32, d in {64, 128}, block in {64, 128} on the FMA pipes),
+ * B * heads <= 65535.
  * Errors: VA_ERR_INVALID (null or misaligned pointers, N != T*H*W of the
  * mask, B or heads < 1, non-finite scale, a mask built on another device),
  * VA_ERR_UNSUPPORTED, VA_ERR_OOM (scratch), VA_ERR_CUDA.

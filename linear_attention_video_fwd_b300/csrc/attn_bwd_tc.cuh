@@ -1,5 +1,6 @@
 // Block-sparse attention backward on the 5th-generation tensor cores (tcgen05
-// + TMEM + TMA), bf16, head_dim 128, 128-token blocks. The gradients are
+// + TMEM + TMA), bf16, head_dim D in {64, 128}, 128-token blocks (a D = 128
+// tile is two 64-dim halves, a D = 64 tile one). The gradients are
 // those of the float32 kernels' header (chain rule of the attention
 // definition); p is recomputed from the forward's lse, in the log2 domain:
 // p = exp2(scale_log2 s + nlse2), nlse2 = -lse log2(e) (-inf on padding rows).
@@ -35,7 +36,24 @@ namespace va {
 constexpr int BW_THREADS = 384;
 constexpr int BW_NS = 2;  // ring stages
 constexpr int BW_ROWVEC = 1024;  // per stage: nlse2 and ndelta of one 128-row block
-constexpr int BW_SMEM_BYTES = 1024 + TC_TILE_BYTES * (2 + 2 * BW_NS) + BW_NS * BW_ROWVEC;
+template <int D>
+struct BwDim {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kTileBytes = TC_BLK * D * 2;
+  static constexpr int kSmemBytes = 1024 + kTileBytes * (2 + 2 * BW_NS) + BW_NS * BW_ROWVEC;
+};
+
+// A (rows x D) B^T over the D dims into TMEM: both operands 128-row K-major
+// tiles of D dims (D / 16 steps), e.g. S = Q K^T.
+template <int D>
+__device__ __forceinline__ void bw_issue_ss(uint32_t d_tmem, uint32_t sA, uint32_t sB) {
+  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const uint32_t off = (k >> 2) * TC_HALF_BYTES + (k & 3) * 32;
+    umma_ss(d_tmem, sw128_desc(sA + off, 16, 1024), sw128_desc(sB + off, 16, 1024), idesc, k > 0);
+  }
+}
 
 struct BwArgs {
   const int* ptr;    // CSR (query side) or transposed CSR (key side) offsets
@@ -57,10 +75,11 @@ __device__ __forceinline__ uint32_t bw_pcol(int k) {
 }
 
 // D (+)= A x B, A = 128 x 128 bf16 packed in TMEM (bw_pcol), B a 128-token
-// tile in shared memory whose 128 dims are the N side (MN-major).
+// tile in shared memory whose D dims are the N side (MN-major).
+template <int D>
 __device__ __forceinline__ void bw_issue_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t sB,
                                             bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 1);
+  constexpr uint32_t idesc = idesc_bf16_f32(128, D, 0, 1);
 #pragma unroll
   for (int k = 0; k < 8; ++k)
     umma_ts(d_tmem, a_tmem + bw_pcol(k), sw128_desc(sB + k * 2048, TC_HALF_BYTES, 1024), idesc,
@@ -134,10 +153,11 @@ __device__ __forceinline__ void bw_bulk_load(uint32_t dst, const void* src, uint
       : "memory");
 }
 
+template <int D>
 __device__ __forceinline__ void bw_load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                              int row, int bh) {
-  tma_load_3d(dst, map, bar, 0, row, bh);
-  tma_load_3d(dst + TC_HALF_BYTES, map, bar, 64, row, bh);
+#pragma unroll
+  for (int h = 0; h < D / 64; ++h) tma_load_3d(dst + h * TC_HALF_BYTES, map, bar, 64 * h, row, bh);
 }
 
 enum : int {
@@ -184,6 +204,7 @@ __device__ __forceinline__ void bw_setup(uint64_t* bars, uint32_t* tmem_base_s, 
 // the streamed pair for every entry of the list. With rv0 != nullptr each
 // entry also brings the 128 floats of rv0 and rv1 at its block (the nlse2 and
 // ndelta rows of a query block) to sX + stage * BW_ROWVEC.
+template <int D>
 __device__ __forceinline__ void bw_produce(const CUtensorMap* r0, const CUtensorMap* r1,
                                            const CUtensorMap* s0, const CUtensorMap* s1,
                                            uint32_t sR, uint32_t sA, uint32_t sB, int own,
@@ -196,18 +217,19 @@ __device__ __forceinline__ void bw_produce(const CUtensorMap* r0, const CUtensor
   tma_prefetch_desc(r1);
   tma_prefetch_desc(s0);
   tma_prefetch_desc(s1);
-  mbar_arrive_expect_tx(bar(KA_RES), 2 * TC_TILE_BYTES);
-  bw_load_tile(sR, r0, bar(KA_RES), own * TC_BLK, bh);
-  bw_load_tile(sR + TC_TILE_BYTES, r1, bar(KA_RES), own * TC_BLK, bh);
+  constexpr int kTile = BwDim<D>::kTileBytes;
+  mbar_arrive_expect_tx(bar(KA_RES), 2 * kTile);
+  bw_load_tile<D>(sR, r0, bar(KA_RES), own * TC_BLK, bh);
+  bw_load_tile<D>(sR + kTile, r1, bar(KA_RES), own * TC_BLK, bh);
   int issued = 0;
   for (int u = 0; u < n; ++u) {
     const int s = u % BW_NS, blk = list[u];
     if (u >= BW_NS &&
         !mbar_wait_bounded(bar(KA_EMPTY + s), ((u / BW_NS) & 1) ^ 1, lim, abort_p))
       break;
-    mbar_arrive_expect_tx(bar(KA_FULL + s), 2 * TC_TILE_BYTES + (rv0 ? BW_ROWVEC : 0));
-    bw_load_tile(sA + s * TC_TILE_BYTES, s0, bar(KA_FULL + s), blk * TC_BLK, bh);
-    bw_load_tile(sB + s * TC_TILE_BYTES, s1, bar(KA_FULL + s), blk * TC_BLK, bh);
+    mbar_arrive_expect_tx(bar(KA_FULL + s), 2 * kTile + (rv0 ? BW_ROWVEC : 0));
+    bw_load_tile<D>(sA + s * kTile, s0, bar(KA_FULL + s), blk * TC_BLK, bh);
+    bw_load_tile<D>(sB + s * kTile, s1, bar(KA_FULL + s), blk * TC_BLK, bh);
     if (rv0 != nullptr) {
       bw_bulk_load(sX + s * BW_ROWVEC, rv0 + blk * TC_BLK, 512, bar(KA_FULL + s));
       bw_bulk_load(sX + s * BW_ROWVEC + 512, rv1 + blk * TC_BLK, 512, bar(KA_FULL + s));
@@ -240,6 +262,7 @@ __device__ __forceinline__ void bw_mma_drain(uint64_t* bars, bool ok, long long 
 // TMEM: S^T [0, 128) (P^T packed over it), dP^T [128, 256) (dS^T packed over
 // it), dV [256, 384), dK [384, 512). Shared memory: K, V, then the Q ring and
 // the G ring.
+template <int D>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -251,9 +274,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   __shared__ int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const uint32_t sK = smem_u32(smem), sV = sK + TC_TILE_BYTES;
-  const uint32_t sQ0 = sV + TC_TILE_BYTES, sG0 = sQ0 + BW_NS * TC_TILE_BYTES;
-  const uint32_t sX = sG0 + BW_NS * TC_TILE_BYTES;  // nlse2 | ndelta per stage
+  constexpr int kTile = BwDim<D>::kTileBytes;
+  const uint32_t sK = smem_u32(smem), sV = sK + kTile;
+  const uint32_t sQ0 = sV + kTile, sG0 = sQ0 + BW_NS * kTile;
+  const uint32_t sX = sG0 + BW_NS * kTile;  // nlse2 | ndelta per stage
   const float* rowvec = reinterpret_cast<const float*>(smem + (sX - sK));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x / a.nb;
@@ -269,38 +293,38 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0 && n > 0)
-      bw_produce(&map_k, &map_v, &map_q, &map_g, sK, sQ0, sG0, J, list, n, bh, bars, lim,
-                 abort_p, a.nlse2 + static_cast<long long>(bh) * a.Np,
-                 a.ndelta + static_cast<long long>(bh) * a.Np, sX);
+      bw_produce<D>(&map_k, &map_v, &map_q, &map_g, sK, sQ0, sG0, J, list, n, bh, bars, lim,
+                    abort_p, a.nlse2 + static_cast<long long>(bh) * a.Np,
+                    a.ndelta + static_cast<long long>(bh) * a.Np, sX);
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       bool ok = mbar_wait_bounded(bar(KA_RES), 0, lim, abort_p) &&
                 mbar_wait_bounded(bar(KA_FULL), 0, lim, abort_p);
       if (ok) {
         tc_fence_after();
-        tc_issue_qk(tS, sK, sQ0);
+        bw_issue_ss<D>(tS, sK, sQ0);
         umma_commit(bar(KA_S));
-        tc_issue_qk(tDP, sV, sG0);
+        bw_issue_ss<D>(tDP, sV, sG0);
         umma_commit(bar(KA_DP));
       }
       for (int u = 0; ok && u < n; ++u) {
         const int s = u % BW_NS, s1 = (u + 1) % BW_NS;
         if (!(ok = mbar_wait_bounded(bar(KA_P), u & 1, lim, abort_p))) break;
         tc_fence_after();
-        bw_issue_ts(tDV, tS, sG0 + s * TC_TILE_BYTES, u > 0);
+        bw_issue_ts<D>(tDV, tS, sG0 + s * kTile, u > 0);
         if (u + 1 < n) {
           if (!(ok = mbar_wait_bounded(bar(KA_FULL + s1), ((u + 1) / BW_NS) & 1, lim, abort_p)))
             break;
           tc_fence_after();
-          tc_issue_qk(tS, sK, sQ0 + s1 * TC_TILE_BYTES);
+          bw_issue_ss<D>(tS, sK, sQ0 + s1 * kTile);
           umma_commit(bar(KA_S));
         }
         if (!(ok = mbar_wait_bounded(bar(KA_DS), u & 1, lim, abort_p))) break;
         tc_fence_after();
-        bw_issue_ts(tDK, tDP, sQ0 + s * TC_TILE_BYTES, u > 0);
+        bw_issue_ts<D>(tDK, tDP, sQ0 + s * kTile, u > 0);
         umma_commit(bar(KA_EMPTY + s));
         if (u + 1 < n) {
-          tc_issue_qk(tDP, sV, sG0 + s1 * TC_TILE_BYTES);
+          bw_issue_ss<D>(tDP, sV, sG0 + s1 * kTile);
           umma_commit(bar(KA_DP));
         }
       }
@@ -357,19 +381,19 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     }
     // epilogue: warpgroup 0 writes dV, warpgroup 1 writes scale * dK
     const int key = J * TC_BLK + r;
-    __nv_bfloat16* dst = (h == 0 ? a.d0 : a.d1) + (static_cast<long long>(bh) * a.N + key) * TC_D;
+    __nv_bfloat16* dst = (h == 0 ? a.d0 : a.d1) + (static_cast<long long>(bh) * a.N + key) * D;
     if (n > 0 && ok)
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(KA_DONE), 0, lim, abort_p));
     if (n > 0 && ok) {
       tc_fence_after();
       const uint32_t src = (h == 0 ? tDV : tDK) + lane_off;
       const float mul = h == 0 ? 1.f : a.scale;
-      bw_store64(src, mul, dst, key < a.N);
-      bw_store64(src + 64, mul, dst + 64, key < a.N);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) bw_store64(src + 64 * c, mul, dst + 64 * c, key < a.N);
     } else if (n == 0 && key < a.N) {
       uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) d[q4] = make_uint4(0, 0, 0, 0);
+      for (int q4 = 0; q4 < D / 8; ++q4) d[q4] = make_uint4(0, 0, 0, 0);
     }
   }
   tc_fence_before();
@@ -381,6 +405,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 // dQ of query block I = order[blockIdx % nb] of head blockIdx / nb.
 // TMEM: S [0, 128), dP [128, 256) (dS packed over it), dQ [256, 384).
 // Shared memory: Q, G, then the K ring and the V ring.
+template <int D>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                      const __grid_constant__ CUtensorMap map_k,
@@ -392,8 +417,9 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   __shared__ int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const uint32_t sQ = smem_u32(smem), sG = sQ + TC_TILE_BYTES;
-  const uint32_t sK0 = sG + TC_TILE_BYTES, sV0 = sK0 + BW_NS * TC_TILE_BYTES;
+  constexpr int kTile = BwDim<D>::kTileBytes;
+  const uint32_t sQ = smem_u32(smem), sG = sQ + kTile;
+  const uint32_t sK0 = sG + kTile, sV0 = sK0 + BW_NS * kTile;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x / a.nb;
   const int I = a.order[blockIdx.x % a.nb];
@@ -408,17 +434,17 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
   if (warp == 0) {
     if (lane == 0 && n > 0)
-      bw_produce(&map_q, &map_g, &map_k, &map_v, sQ, sK0, sV0, I, list, n, bh, bars, lim,
-                 abort_p);
+      bw_produce<D>(&map_q, &map_g, &map_k, &map_v, sQ, sK0, sV0, I, list, n, bh, bars, lim,
+                    abort_p);
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       bool ok = mbar_wait_bounded(bar(KA_RES), 0, lim, abort_p) &&
                 mbar_wait_bounded(bar(KA_FULL), 0, lim, abort_p);
       if (ok) {
         tc_fence_after();
-        tc_issue_qk(tS, sQ, sK0);
+        bw_issue_ss<D>(tS, sQ, sK0);
         umma_commit(bar(KA_S));
-        tc_issue_qk(tDP, sG, sV0);
+        bw_issue_ss<D>(tDP, sG, sV0);
         umma_commit(bar(KA_DP));
       }
       for (int u = 0; ok && u < n; ++u) {
@@ -429,15 +455,15 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
           if (!(ok = mbar_wait_bounded(bar(KA_FULL + s1), ((u + 1) / BW_NS) & 1, lim, abort_p)))
             break;
           tc_fence_after();
-          tc_issue_qk(tS, sQ, sK0 + s1 * TC_TILE_BYTES);
+          bw_issue_ss<D>(tS, sQ, sK0 + s1 * kTile);
           umma_commit(bar(KA_S));
         }
         if (!(ok = mbar_wait_bounded(bar(KA_DS), u & 1, lim, abort_p))) break;
         tc_fence_after();
-        bw_issue_ts(tDQ, tDP, sK0 + s * TC_TILE_BYTES, u > 0);
+        bw_issue_ts<D>(tDQ, tDP, sK0 + s * kTile, u > 0);
         umma_commit(bar(KA_EMPTY + s));
         if (u + 1 < n) {
-          tc_issue_qk(tDP, sG, sV0 + s1 * TC_TILE_BYTES);
+          bw_issue_ss<D>(tDP, sG, sV0 + s1 * kTile);
           umma_commit(bar(KA_DP));
         }
       }
@@ -487,10 +513,13 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(KA_DS));
     }
-    __nv_bfloat16* dst = a.d0 + (static_cast<long long>(bh) * a.N + row) * TC_D + h * 64;
+    // dQ has D columns: warpgroup h writes columns [64 h, 64 h + 64) of them
+    __nv_bfloat16* dst = a.d0 + (static_cast<long long>(bh) * a.N + row) * D + h * 64;
     if (n > 0 && ok)
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(KA_DONE), 0, lim, abort_p));
-    if (n > 0 && ok) {
+    if (h * 64 >= D) {
+      // D = 64: the second key-column half has no dQ columns to write
+    } else if (n > 0 && ok) {
       tc_fence_after();
       bw_store64(tDQ + col, a.scale, dst, row < a.N);
     } else if (n == 0 && row < a.N) {

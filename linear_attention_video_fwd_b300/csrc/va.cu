@@ -618,6 +618,7 @@ int launch_bwd_simt(const void* q, const void* k, const void* v, const void* g, 
   return launch_status();
 }
 
+template <int D>
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, const va_mask* m,
                   const float* ndelta, const float* nlse2, void* dq, void* dk, void* dv, int BH,
                   int N, int Np, float scale, cudaStream_t s) {
@@ -627,19 +628,19 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, co
   if (st) return st;
   st = device_once(once, dev, [] {
     int r;
-    if ((r = cuda_status(cudaFuncSetAttribute(va::bwd_dkdv_tc_kernel,
+    if ((r = cuda_status(cudaFuncSetAttribute(va::bwd_dkdv_tc_kernel<D>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              va::BW_SMEM_BYTES))) ||
-        (r = cuda_status(cudaFuncSetAttribute(va::bwd_dq_tc_kernel,
+                                              va::BwDim<D>::kSmemBytes))) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::bwd_dq_tc_kernel<D>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              va::BW_SMEM_BYTES))))
+                                              va::BwDim<D>::kSmemBytes))))
       return r;
     return VA_OK;
   });
   if (st) return st;
   CUtensorMap mq, mk, mv, mg;
-  if ((st = encode_bf16_rows(&mq, q, BH, N, 128)) || (st = encode_bf16_rows(&mk, k, BH, N, 128)) ||
-      (st = encode_bf16_rows(&mv, v, BH, N, 128)) || (st = encode_bf16_rows(&mg, g, BH, N, 128)))
+  if ((st = encode_bf16_rows(&mq, q, BH, N, D)) || (st = encode_bf16_rows(&mk, k, BH, N, D)) ||
+      (st = encode_bf16_rows(&mv, v, BH, N, D)) || (st = encode_bf16_rows(&mg, g, BH, N, D)))
     return st;
   const long long grid = static_cast<long long>(m->nqb) * BH;
   if (grid > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
@@ -657,15 +658,17 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, co
   a.order = m->t_order;
   a.d0 = static_cast<__nv_bfloat16*>(dv);
   a.d1 = static_cast<__nv_bfloat16*>(dk);
-  va::bwd_dkdv_tc_kernel<<<static_cast<unsigned>(grid), va::BW_THREADS, va::BW_SMEM_BYTES, s>>>(
-      mq, mk, mv, mg, a);
+  va::bwd_dkdv_tc_kernel<D>
+      <<<static_cast<unsigned>(grid), va::BW_THREADS, va::BwDim<D>::kSmemBytes, s>>>(mq, mk, mv,
+                                                                                  mg, a);
   a.ptr = m->row_ptr;
   a.idx = m->col;
   a.order = m->order;
   a.d0 = static_cast<__nv_bfloat16*>(dq);
   a.d1 = nullptr;
-  va::bwd_dq_tc_kernel<<<static_cast<unsigned>(grid), va::BW_THREADS, va::BW_SMEM_BYTES, s>>>(
-      mq, mk, mv, mg, a);
+  va::bwd_dq_tc_kernel<D>
+      <<<static_cast<unsigned>(grid), va::BW_THREADS, va::BwDim<D>::kSmemBytes, s>>>(mq, mk, mv,
+                                                                                mg, a);
   return launch_status();
 }
 
@@ -691,7 +694,7 @@ VA_EXPORT int va_sparse_attn_bwd(const void* q, const void* k, const void* v, co
   const int BH = static_cast<int>(BH64);
   const int blk = m->p.block;
   const int Np = m->nqb * blk;
-  const bool tc = dtype == VA_BF16 && d == 128 && blk == 128;
+  const bool tc = dtype == VA_BF16 && (d == 64 || d == 128) && blk == 128;
   const bool simt = dtype == VA_F32 && (d == 64 || d == 128) && (blk == 64 || blk == 128);
   if (!tc && !simt) return VA_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -707,7 +710,9 @@ VA_EXPORT int va_sparse_attn_bwd(const void* q, const void* k, const void* v, co
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, N,
         Np, d, ndelta, nlse2);
     if ((st = launch_status())) return st;
-    return launch_bwd_tc(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);
+    if (d == 64)
+      return launch_bwd_tc<64>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);
+    return launch_bwd_tc<128>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);
   }
   va::bwd_prep_kernel<float><<<pgrid, 256, 0, s>>>(static_cast<const float*>(out),
                                                    static_cast<const float*>(dout), lse, N, Np,

@@ -94,22 +94,24 @@ SMALL_BF16 = [
 ]
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("case", SMALL_BF16)
-def test_bf16_small_all_rows(va, dev, case):
+def test_bf16_small_all_rows(va, dev, case, d):
     kind, T, H, W, p, step = case
     N = T * H * W
-    q, k, v = synth.video_qkv(2, 3, T, H, W, 128, seed=11)
-    g = synth.upstream_grad(2, 3, N, 128, seed=11)
+    q, k, v = synth.video_qkv(2, 3, T, H, W, d, seed=11)
+    g = synth.upstream_grad(2, 3, N, d, seed=11)
     _check(va, dev, q, k, v, g, kind, T, H, W, p, step, "bf16")
 
 
-def test_bf16_other_scale_and_lvsa_asymmetry(va, dev):
+@pytest.mark.parametrize("d", [128, 64])
+def test_bf16_other_scale_and_lvsa_asymmetry(va, dev, d):
     # LVSA's anchor frames make the block mask asymmetric, so the transposed
     # lists differ from the rows; a non-default scale checks where it enters.
     T, H, W = 10, 8, 16
     p = OM.MaskParams(block=128, local=0, period=3, anchor0=1, rot_stride=1)
-    q, k, v = synth.video_qkv(1, 2, T, H, W, 128, seed=13)
-    g = synth.upstream_grad(1, 2, T * H * W, 128, seed=13)
+    q, k, v = synth.video_qkv(1, 2, T, H, W, d, seed=13)
+    g = synth.upstream_grad(1, 2, T * H * W, d, seed=13)
     bm = OM.block_mask(OM.LVSA, T, H, W, p, 1)
     assert not np.array_equal(bm, bm.T)
     _check(va, dev, q, k, v, g, OM.LVSA, T, H, W, p, 1, "bf16", scale=0.05)
