@@ -316,8 +316,9 @@ def run_ours(args, world, rank, local):
 
     # ---- device-timed region: inputs resident in HBM --------------------------
     total_ms, launch_ms, clocks = timed_region(args, world, local, call, stream)
-    if va.device_error() != va.OK:
-        raise RuntimeError("device error in the timed region")
+    err = va.device_error()
+    if err != va.OK:
+        raise RuntimeError("device error in the timed region: %s" % va.status_string(err))
     ms_per_step = total_ms / args.steps
     value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
 
@@ -454,8 +455,9 @@ def run_svgear(args, world, rank, local):
             stage_ms["compensate_route"].append(ev[2].elapsed_time(ev[3]))
 
     total_ms, launch_ms, clocks = timed_region(args, world, local, call, stream)
-    if va.device_error() != va.OK:
-        raise RuntimeError("device error in the timed region")
+    err = va.device_error()
+    if err != va.OK:
+        raise RuntimeError("device error in the timed region: %s" % va.status_string(err))
     record[0] = True
     for _ in range(3):
         call()
@@ -638,8 +640,9 @@ def run_linear(args, world, rank, local, mixed):
             va.linear_attn_fwd(qt, kt, vt, out=out)
 
     total_ms, launch_ms, clocks = timed_region(args, world, local, call, stream)
-    if va.device_error() != va.OK:
-        raise RuntimeError("device error in the timed region")
+    err = va.device_error()
+    if err != va.OK:
+        raise RuntimeError("device error in the timed region: %s" % va.status_string(err))
     ms_per_step = total_ms / args.steps
     call_ms = float(np.mean(launch_ms))
     tensor_bytes = qt.numel() * qt.element_size()
@@ -751,8 +754,9 @@ def run_bwd(args, world, rank, local):
         va.sparse_attn_bwd(qt, kt, vt, out, gt, lse, mask, dq=dq, dk=dk, dv=dv)
 
     total_ms, launch_ms, clocks = timed_region(args, world, local, call, stream)
-    if va.device_error() != va.OK:
-        raise RuntimeError("device error in the timed region")
+    err = va.device_error()
+    if err != va.OK:
+        raise RuntimeError("device error in the timed region: %s" % va.status_string(err))
     ms_per_step = total_ms / args.steps
     call_ms = float(np.mean(launch_ms))
 

@@ -34,8 +34,8 @@ constexpr int LN_NEXT = 144;             // rows of [S | z]^T (128 + z + padding
 constexpr int LN_PIECE = LN_NEXT * 128 * 2;   // 36 KB: one bf16 piece of [S | z]^T
 constexpr int LN_PIECE_HALF = LN_PIECE / 2;   // 144 rows x 64 dims
 constexpr int LN_ROW = 129;              // partial row: S[dim][0..128) and z[dim]
-constexpr int LN_STATE_THREADS = 384;
-constexpr int LN_OUT_THREADS = 512;
+constexpr int LN_STATE_THREADS = 640;   // producer, MMA, 2 idle warps, 4 phi warpgroups
+constexpr int LN_OUT_THREADS = 768;
 constexpr int LN_NS = 3;                 // ring stages (K and V, or Q)
 constexpr int LN_STATE_SMEM = 1024 + 2 * LN_NS * LN_TILE + 4096;    // K, V rings + ones
 constexpr int LN_OUT_SMEM = 1024 + 2 * LN_PIECE + LN_NS * LN_TILE;  // pieces + Q ring
@@ -83,7 +83,7 @@ __device__ __forceinline__ void lin_range(int ntiles, int nsplit, int split, int
   t_hi = min(ntiles, t_lo + per);
 }
 
-// Grid (nsplit, BH), 256 threads. part[bh][split][dim][0..129) = {S row, z}.
+// Grid (nsplit, BH), 640 threads. part[bh][split][dim][0..129) = {S row, z}.
 __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
     lin_state_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v, int N, float* __restrict__ part,
@@ -189,19 +189,27 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
       }
     }
   } else if (warp >= 4) {
-    const int r = (warp & 3) * 32 + lane, h = (warp - 4) >> 2;
+    // Two pairs of warpgroups take alternate tiles: pair g transforms tiles
+    // u = g, g + 2, ..., warpgroup h of a pair one 64-dim half. Tile u - 3,
+    // the previous user of stage s, belongs to the other pair, so the pair
+    // first waits for that tile's phi: until then the K-full barrier of stage s
+    // may sit two phases behind tile u and its parity would match too early.
+    const int r = (warp & 3) * 32 + lane, h = ((warp - 4) >> 2) & 1, g = (warp - 4) >> 3;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
-    for (int u = 0; u < nt; ++u) {
+    for (int u = g; u < nt; u += 2) {
       const int s = u % LN_NS;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(LS_KF + s), (u / LN_NS) & 1, lim,
-                                                          abort_p))))
+      const uint32_t ph = (u / LN_NS) & 1;
+      if (u >= LN_NS &&
+          !(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(LS_PHI + s), ph ^ 1, lim, abort_p))))
+        break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(LS_KF + s), ph, lim, abort_p))))
         break;
       lin_phi_half(kt + s * LN_TILE, h, r, (t_lo + u) * 128 + r < N);
       fence_proxy_async_smem();
       mbar_arrive(bar(LS_PHI + s));
     }
-    if (h == 0) {  // the epilogue is warps 4..7
+    if (h == 0 && g == 0) {  // the epilogue is warps 4..7
       float* out = part + ((static_cast<long long>(bh) * nsplit + split) * 128 + r) * LN_ROW;
       if (nt == 0) {
         for (int n = 0; n < LN_ROW; ++n) out[n] = 0.f;
@@ -257,9 +265,11 @@ enum : int {
   LO_COUNT = LO_DRAIN + 1
 };
 
-// Grid (nsplit, BH), 512 threads: warp 0 TMA producer, warp 1 MMA issuer,
-// warps 4..7 and 12..15 phi(Q) in place (dims 0..63 and 64..127), warps 8..11
-// epilogue (thread r owns token row r of the tile). out = num / den, or r_mix * out + (1 - r_mix) * num / den when
+// Grid (nsplit, BH), 768 threads: warp 0 TMA producer, warp 1 MMA issuer,
+// warps 8..11 epilogue (thread r owns token row r of the tile), and two pairs
+// of warpgroups that apply phi(Q) in place to alternate tiles: warps 4..7 and
+// 12..15 (dims 0..63 and 64..127) the even tiles, warps 16..19 and 20..23 the
+// odd ones. out = num / den, or r_mix * out + (1 - r_mix) * num / den when
 // mix != 0 (out then holds the attention output on entry).
 __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
     lin_out_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -367,11 +377,18 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
       }
     }
   } else if ((warp >= 4 && warp < 8) || warp >= 12) {
-    const int r = (warp & 3) * 32 + lane, h = warp >= 12 ? 1 : 0;
-    for (int u = 0; u < nt; ++u) {
+    const int r = (warp & 3) * 32 + lane;
+    const int h = (warp >= 12 && warp < 16) || warp >= 20 ? 1 : 0;
+    const int g = warp >= 16 ? 1 : 0;
+    for (int u = g; u < nt; u += 2) {
+      // As in lin_state_kernel: first the other pair's phi of tile u - 3, the
+      // previous user of stage s, so the Q-full parity cannot match too early.
       const int s = u % LN_NS;
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait_bounded(bar(LO_QF + s), (u / LN_NS) & 1, lim, abort_p)))
+      const uint32_t ph = (u / LN_NS) & 1;
+      if (u >= LN_NS &&
+          !__all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_PHI + s), ph ^ 1, lim, abort_p)))
+        break;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_QF + s), ph, lim, abort_p)))
         break;
       lin_phi_half(qt + s * LN_TILE, h, r, true);
       fence_proxy_async_smem();
