@@ -33,14 +33,35 @@ constexpr int LN_HALF = LN_TILE / 2;     // 128 rows x 64 dims
 constexpr int LN_NEXT = 144;             // rows of [S | z]^T (128 + z + padding)
 constexpr int LN_PIECE = LN_NEXT * 128 * 2;   // 36 KB: one bf16 piece of [S | z]^T
 constexpr int LN_PIECE_HALF = LN_PIECE / 2;   // 144 rows x 64 dims
-constexpr int LN_ROW = 129;              // partial row: S[dim][0..128) and z[dim]
+constexpr int LN_ROW = 129;              // partial rows per split: S[.][n], n < 128, and z
 constexpr int LN_STATE_THREADS = 640;   // producer, MMA, 2 idle warps, 4 phi warpgroups
 constexpr int LN_OUT_THREADS = 768;
 constexpr int LN_NS = 3;                 // ring stages (K and V, or Q)
 constexpr int LN_STATE_SMEM = 1024 + 2 * LN_NS * LN_TILE + 4096;    // K, V rings + ones
-constexpr int LN_OUT_SMEM = 1024 + 2 * LN_PIECE + LN_NS * LN_TILE;  // pieces + Q ring
+constexpr int LN_OUT_SMEM = 1024 + 2 * LN_PIECE + (LN_NS + 1) * LN_TILE;  // pieces, Q ring, O tile
 
-__device__ __forceinline__ float lin_phi(float x) { return x > 0.f ? x + 1.f : __expf(x); }
+// phi(x) = elu(x) + 1 = max(x, 0) + exp(n), n = max(min(x, 0), -100), on a
+// pair of bf16 values in bf16x2 arithmetic. max and min are exact; exp(n) =
+// 2^(n log2 e) with the argument formed as fma(n, c_hi, n c_lo) (c_hi + c_lo
+// equals log2 e to 2^-17, so the constant adds no bias), then the hardware 2^x
+// in bf16; the final add rounds once. For x > 0 the result is bf16(x + 1)
+// exactly. For x <= 0 the relative error (measured over every bf16 input) is
+// at most 0.75% on [-1, 0) and 1.5% on [-4, -1) and grows with |x| (the
+// argument keeps 8 bits), while the absolute error stays below 0.008; after the
+// fp32 sums this is below the bf16 rounding of the output. The clamp at -100
+// (where exp is below the smallest bf16 normal) keeps -inf from forming
+// -inf + inf: -inf gives 0, +inf gives +inf, NaN stays NaN.
+__device__ __forceinline__ uint32_t lin_phi_bf16x2(uint32_t x) {
+  uint32_t m, n, t, y, ex, r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(x), "r"(0u));
+  asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(n) : "r"(x), "r"(0u));
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(n) : "r"(n), "r"(0xc2c8c2c8u));              // -100
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(n), "r"(0xbb2cbb2cu));               // c_lo = -0.0026245
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(y) : "r"(n), "r"(0x3fb93fb9u), "r"(t));  // c_hi = 1.4453125
+  asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(ex) : "r"(y));
+  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(ex));
+  return r;
+}
 
 // phi in place on one 64-dim half h of a 128-token bf16 tile (two
 // 128B-swizzled halves); the thread owns token row r of that half, rows with
@@ -57,11 +78,7 @@ __device__ __forceinline__ void lin_phi_half(uint8_t* tile, int h, int r, bool v
   for (int c = 0; c < 8; ++c) {
     uint32_t* e = reinterpret_cast<uint32_t*>(&w[c]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float lo = lin_phi(__uint_as_float(e[i] << 16));
-      const float hi = lin_phi(__uint_as_float(e[i] & 0xffff0000u));
-      e[i] = valid ? pack_bf16x2(lo, hi) : 0u;
-    }
+    for (int i = 0; i < 4; ++i) e[i] = valid ? lin_phi_bf16x2(e[i]) : 0u;
     *reinterpret_cast<uint4*>(tile + h * LN_HALF + r * 128 + ((c + r) & 7) * 16) = w[c];
   }
 }
@@ -83,7 +100,9 @@ __device__ __forceinline__ void lin_range(int ntiles, int nsplit, int split, int
   t_hi = min(ntiles, t_lo + per);
 }
 
-// Grid (nsplit, BH), 640 threads. part[bh][split][dim][0..129) = {S row, z}.
+// Grid (nsplit, BH), 640 threads. part[bh][split][n][dim]: n < 128 S[dim][n],
+// n = 128 z[dim] (dims contiguous, so both the stores here and the loads of
+// lin_prep_kernel are coalesced).
 __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
     lin_state_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v, int N, float* __restrict__ part,
@@ -128,6 +147,7 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;  // S at [0, 128), z at [128, 144)
   volatile int* abort_p = &abort_flag;
+  grid_dep_launch();  // lin_prep_kernel may be scheduled now; it waits for this grid
 
   if (warp == 0) {
     if (lane == 0 && nt > 0) {
@@ -209,10 +229,10 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
       fence_proxy_async_smem();
       mbar_arrive(bar(LS_PHI + s));
     }
-    if (h == 0 && g == 0) {  // the epilogue is warps 4..7
-      float* out = part + ((static_cast<long long>(bh) * nsplit + split) * 128 + r) * LN_ROW;
+    if (h == 0 && g == 0) {  // the epilogue is warps 4..7; thread r stores column r
+      float* out = part + (static_cast<long long>(bh) * nsplit + split) * LN_ROW * 128 + r;
       if (nt == 0) {
-        for (int n = 0; n < LN_ROW; ++n) out[n] = 0.f;
+        for (int n = 0; n < LN_ROW; ++n) out[n * 128] = 0.f;
       } else if (ok && __all_sync(0xffffffffu, mbar_wait_bounded(bar(LS_DONE), 0, lim, abort_p))) {
         tc_fence_after();
 #pragma unroll
@@ -221,12 +241,12 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
           tmem_ld32(tmem + lane_off + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) out[c * 32 + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 32; ++i) out[(c * 32 + i) * 128] = __uint_as_float(v[i]);
         }
         uint32_t zv[16];
         tmem_ld16(tmem + lane_off + 128, zv);
         tmem_wait_ld();
-        out[128] = __uint_as_float(zv[0]);
+        out[128 * 128] = __uint_as_float(zv[0]);
       }
     }
   }
@@ -238,14 +258,18 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
 
 // [S | z]^T of each batch*head from the split partials, as bf16 pieces:
 // piece[bh][p][n][dim], p = 0 hi, 1 lo, n < 128 S[dim][n], n = 128 z[dim],
-// n > 128 zero. Grid (LN_NEXT, BH), 128 threads (one per dim).
+// n > 128 zero. Grid (LN_NEXT, BH), 128 threads (one per dim). Launched as a
+// programmatic dependent of lin_state_kernel: it waits for that grid before
+// reading the partials.
 __global__ void lin_prep_kernel(const float* __restrict__ part, int nsplit,
                                 __nv_bfloat16* __restrict__ piece) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int n = blockIdx.x, bh = blockIdx.y, dim = threadIdx.x;
   float acc = 0.f;
   if (n <= 128) {
-    const float* pp = part + static_cast<long long>(bh) * nsplit * 128 * LN_ROW;
-    for (int s = 0; s < nsplit; ++s) acc += pp[(static_cast<long long>(s) * 128 + dim) * LN_ROW + n];
+    const float* pp = part + static_cast<long long>(bh) * nsplit * LN_ROW * 128 + n * 128 + dim;
+    for (int s = 0; s < nsplit; ++s) acc += pp[static_cast<long long>(s) * LN_ROW * 128];
   }
   const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
   const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
@@ -266,14 +290,16 @@ enum : int {
 };
 
 // Grid (nsplit, BH), 768 threads: warp 0 TMA producer, warp 1 MMA issuer,
-// warps 8..11 epilogue (thread r owns token row r of the tile), and two pairs
+// warps 8..11 epilogue (thread r owns token row r of the tile; the tile goes
+// out through shared memory and a TMA store), and two pairs
 // of warpgroups that apply phi(Q) in place to alternate tiles: warps 4..7 and
 // 12..15 (dims 0..63 and 64..127) the even tiles, warps 16..19 and 20..23 the
 // odd ones. out = num / den, or r_mix * out + (1 - r_mix) * num / den when
 // mix != 0 (out then holds the attention output on entry).
 __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
     lin_out_kernel(const __grid_constant__ CUtensorMap map_q,
-                   const __grid_constant__ CUtensorMap map_p, int N, __nv_bfloat16* __restrict__ out,
+                   const __grid_constant__ CUtensorMap map_p, const __grid_constant__ CUtensorMap map_o,
+                   int N, __nv_bfloat16* __restrict__ out,
                    int mix, float r_mix, long long lim) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[LO_COUNT];
@@ -283,6 +309,7 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* pc = smem;                    // piece p at pc + p PIECE
   uint8_t* qt = smem + 2 * LN_PIECE;     // Q stage s at qt + s TILE
+  uint8_t* ot = qt + LN_NS * LN_TILE;    // output tile staged for the TMA store
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, bh = blockIdx.y;
   const int ntiles = (N + 127) / 128;
@@ -319,21 +346,27 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
     if (lane == 0 && nt > 0) {
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_p);
+      tma_prefetch_desc(&map_o);
+      int issued = 0;
+      auto load_q = [&](int u) {
+        const int s = u % LN_NS, row = (t_lo + u) * 128;
+        mbar_arrive_expect_tx(bar(LO_QF + s), LN_TILE);
+        tma_load_3d(smem_u32(qt + s * LN_TILE), &map_q, bar(LO_QF + s), 0, row, bh);
+        tma_load_3d(smem_u32(qt + s * LN_TILE + LN_HALF), &map_q, bar(LO_QF + s), 64, row, bh);
+        issued = u + 1;
+      };
+      // The first Q tiles need no wait. The pieces are the previous kernel's
+      // output, so under a programmatic dependent launch they load after it.
+      for (int u = 0; u < nt && u < LN_NS; ++u) load_q(u);
+      grid_dep_wait();
       mbar_arrive_expect_tx(bar(LO_PF), 2 * LN_PIECE);
       for (int p = 0; p < 2; ++p)
         for (int h = 0; h < 2; ++h)
           tma_load_3d(smem_u32(pc + p * LN_PIECE + h * LN_PIECE_HALF), &map_p, bar(LO_PF), 64 * h,
                       p * LN_NEXT, bh);
-      int issued = 0;
-      for (int u = 0; u < nt; ++u) {
-        const int s = u % LN_NS, row = (t_lo + u) * 128;
-        if (u >= LN_NS &&
-            !mbar_wait_bounded(bar(LO_QE + s), ((u / LN_NS) & 1) ^ 1, lim, abort_p))
-          break;
-        mbar_arrive_expect_tx(bar(LO_QF + s), LN_TILE);
-        tma_load_3d(smem_u32(qt + s * LN_TILE), &map_q, bar(LO_QF + s), 0, row, bh);
-        tma_load_3d(smem_u32(qt + s * LN_TILE + LN_HALF), &map_q, bar(LO_QF + s), 64, row, bh);
-        issued = u + 1;
+      for (int u = LN_NS; u < nt; ++u) {
+        if (!mbar_wait_bounded(bar(LO_QE + u % LN_NS), ((u / LN_NS) & 1) ^ 1, lim, abort_p)) break;
+        load_q(u);
       }
       if (*abort_p) {
         volatile int no_abort = 0;
@@ -395,12 +428,21 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
       mbar_arrive(bar(LO_PHI + s));
     }
   } else if (warp >= 8) {
+    // Thread r converts token row r of the tile into the staging tile (the
+    // 128B-swizzled layout of the Q tiles, so the 16-byte stores of a warp hit
+    // distinct banks), then one thread writes the tile with two TMA stores
+    // (rows past N are clipped by the tensor map). Before the staging tile is
+    // rewritten, the previous stores must have read it; the four warps decide
+    // together (bar.red) whether to go on, so none is left at the barrier.
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool issuer = warp == 8 && lane == 0;
     for (int u = 0; u < nt; ++u) {
       const int b = u & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_AF + b), (u >> 1) & 1, lim, abort_p)))
-        break;
+      const bool full =
+          __all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_AF + b), (u >> 1) & 1, lim, abort_p));
+      if (issuer) bulk_wait_read_all();
+      if (!named_bar_and(1, 128, full)) break;
       tc_fence_after();
       const uint32_t tA = tmem + b * 256 + lane_off;
       uint32_t dv[16];
@@ -408,7 +450,7 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
       tmem_wait_ld();
       const float inv = 1.f / __uint_as_float(dv[0]);
       const int tok = (t_lo + u) * 128 + r;
-      __nv_bfloat16* orow = out + (static_cast<long long>(bh) * N + tok) * 128;
+      const __nv_bfloat16* arow = out + (static_cast<long long>(bh) * N + tok) * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
@@ -418,33 +460,39 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
           tc_fence_before();
           mbar_arrive(bar(LO_AE + b));
         }
-        if (tok < N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            float o[8];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          float o[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(v[q4 * 8 + e]) * inv;
-            if (mix) {
-              const uint4 a = dst[q4];
-              const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+          for (int e = 0; e < 8; ++e) o[e] = __uint_as_float(v[q4 * 8 + e]) * inv;
+          if (mix && tok < N) {
+            const uint4 a = reinterpret_cast<const uint4*>(arow + c * 32)[q4];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                o[2 * e] = fmaf(r_mix, __uint_as_float(aw[e] << 16) - o[2 * e], o[2 * e]);
-                o[2 * e + 1] =
-                    fmaf(r_mix, __uint_as_float(aw[e] & 0xffff0000u) - o[2 * e + 1], o[2 * e + 1]);
-              }
+            for (int e = 0; e < 4; ++e) {
+              o[2 * e] = fmaf(r_mix, __uint_as_float(aw[e] << 16) - o[2 * e], o[2 * e]);
+              o[2 * e + 1] =
+                  fmaf(r_mix, __uint_as_float(aw[e] & 0xffff0000u) - o[2 * e + 1], o[2 * e + 1]);
             }
-            uint4 w;
-            w.x = pack_bf16x2(o[0], o[1]);
-            w.y = pack_bf16x2(o[2], o[3]);
-            w.z = pack_bf16x2(o[4], o[5]);
-            w.w = pack_bf16x2(o[6], o[7]);
-            dst[q4] = w;
           }
+          uint4 w;
+          w.x = pack_bf16x2(o[0], o[1]);
+          w.y = pack_bf16x2(o[2], o[3]);
+          w.z = pack_bf16x2(o[4], o[5]);
+          w.w = pack_bf16x2(o[6], o[7]);
+          const int j = (c & 1) * 4 + q4;  // 16-byte chunk within the 64-dim half c / 2
+          *reinterpret_cast<uint4*>(ot + (c >> 1) * LN_HALF + r * 128 + ((j ^ (r & 7)) * 16)) = w;
         }
       }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (issuer) {
+        tma_store_3d(&map_o, smem_u32(ot), 0, (t_lo + u) * 128, bh);
+        tma_store_3d(&map_o, smem_u32(ot + LN_HALF), 64, (t_lo + u) * 128, bh);
+        bulk_commit();
+      }
     }
+    if (issuer) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();

@@ -12,6 +12,7 @@
 #include <mutex>
 #include <type_traits>
 #include <vector>
+#include <utility>
 
 #include "va.h"
 #include "common.cuh"
@@ -123,6 +124,25 @@ int cuda_status(cudaError_t e) {
 }
 
 int launch_status() { return cuda_status(cudaGetLastError()); }
+
+// Launch `kernel` as a programmatic dependent of the previous kernel on `s`:
+// it may be scheduled before that kernel completes, and must itself execute
+// griddepcontrol.wait before touching that kernel's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -898,16 +918,21 @@ int run_linear(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat
   if ((st = scratch.alloc(&part, bh * nsplit * 128 * va::LN_ROW)) ||
       (st = scratch.alloc(&piece, bh * 2 * va::LN_NEXT * 128)))
     return st;
-  CUtensorMap mk, mv, mq, mp;
+  CUtensorMap mk, mv, mq, mp, mo;
   if ((st = encode_bf16_rows(&mk, k, BH, N, 128)) || (st = encode_bf16_rows(&mv, v, BH, N, 128)) ||
-      (st = encode_bf16_rows(&mq, q, BH, N, 128)) ||
+      (st = encode_bf16_rows(&mq, q, BH, N, 128)) || (st = encode_bf16_rows(&mo, out, BH, N, 128)) ||
       (st = encode_bf16_rows_box(&mp, piece, BH, 2 * va::LN_NEXT, 128, va::LN_NEXT)))
     return st;
   va::lin_state_kernel<<<dim3(nsplit, BH), va::LN_STATE_THREADS, va::LN_STATE_SMEM, s>>>(
       mk, mv, N, part, g_wait_limit);
-  va::lin_prep_kernel<<<dim3(va::LN_NEXT, BH), 128, 0, s>>>(part, nsplit, piece);
-  va::lin_out_kernel<<<dim3(nsplit, BH), va::LN_OUT_THREADS, va::LN_OUT_SMEM, s>>>(
-      mq, mp, N, out, mix, r, g_wait_limit);
+  // prep and out are programmatic dependents: each starts while its
+  // predecessor drains and waits (griddepcontrol.wait) before reading its output.
+  if ((st = cuda_status(launch_dependent(va::lin_prep_kernel, dim3(va::LN_NEXT, BH), 128, 0, s,
+                                         static_cast<const float*>(part), nsplit, piece))) ||
+      (st = cuda_status(launch_dependent(va::lin_out_kernel, dim3(nsplit, BH), va::LN_OUT_THREADS,
+                                         va::LN_OUT_SMEM, s, mq, mp, mo, N, out, mix, r,
+                                         static_cast<long long>(g_wait_limit)))))
+    return st;
   return launch_status();
 }
 

@@ -46,6 +46,28 @@ def test_linear_identical_keys_give_mean_value(va, dev):
     assert_bf16_close(out.float().cpu().numpy(), want)
 
 
+def test_linear_extreme_feature_inputs(va, dev):
+    # phi(-inf) = 0 and phi of large negative inputs underflows to 0; large
+    # positive inputs give x + 1. Some dims of Q and K take such values (no
+    # row is all -inf, so every denominator stays positive).
+    T, H, W = 3, 7, 13
+    q, k, v = synth.video_qkv(1, 2, T, H, W, 128, seed=47, dtype="bf16")
+    q, k = q.copy(), k.copy()
+    k[:, :, ::3, 5] = -np.inf
+    k[:, :, 1::4, 7] = -300.0
+    k[:, :, 2::5, 9] = -40.0
+    k[:, :, ::7, 11] = 30.0
+    q[:, :, ::2, 3] = -np.inf
+    q[:, :, 1::3, 4] = -90.0
+    q[:, :, ::5, 6] = 20.0
+    out = va.linear_attn_fwd(_dev(q, dev), _dev(k, dev), _dev(v, dev))
+    torch.cuda.synchronize()
+    assert va.device_error() == va.OK
+    got = out.float().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert_bf16_close(got, OL.linear_attention(q, k, v))
+
+
 def test_linear_full_size(va, dev):
     # Wan-shaped inputs: B=1, 12 heads, 21x30x52 = 32,760 tokens, d=128, bf16;
     # the oracle on 512 sampled rows of every head
