@@ -242,15 +242,25 @@ __global__ void km_count_kernel(const int* __restrict__ assign, int N, int C,
     atomicAdd(&count[static_cast<long long>(bh) * C + a], __popc(grp));
 }
 
-// bf16 value as a signed fixed-point integer with 32 fraction bits: exact
-// for |x| >= 2^-25, truncated toward zero (error < 2^-32) below.
+// A bf16 value as a signed fixed-point integer with 32 fraction bits: exact
+// for |x| >= 2^-25, truncated toward zero (error < 2^-32) below, for
+// |x| < 2^31. value = mant * 2^(e - 134), so the magnitude is mant shifted
+// by e - 102; PTX shifts clamp counts past the width, so a tiny value shifts
+// out to 0 and zero / subnormal inputs (e = 0) are masked to 0.
 __device__ __forceinline__ long long bf16_fixed32(uint32_t bits16) {
   const uint32_t e = (bits16 >> 7) & 0xFFu;
-  if (e == 0) return 0;                        // zero and subnormals (|x| < 2^-126)
-  const long long mant = static_cast<long long>((bits16 & 0x7Fu) | 0x80u);
-  const int sh = static_cast<int>(e) - 102;    // value = mant * 2^(e - 134) * 2^32
-  const long long mag = sh >= 0 ? (mant << min(sh, 62)) : (sh > -63 ? (mant >> -sh) : 0);
-  return (bits16 & 0x8000u) ? -mag : mag;
+  const uint32_t mant = ((bits16 & 0x7Fu) | 0x80u) & (e != 0 ? 0xFFu : 0u);
+  const int sh = static_cast<int>(e) - 102;
+  unsigned long long mag;
+  if (sh >= 0) {
+    asm("shl.b64 %0, %1, %2;" : "=l"(mag) : "l"(static_cast<unsigned long long>(mant)), "r"(sh));
+  } else {
+    uint32_t m32;
+    asm("shr.u32 %0, %1, %2;" : "=r"(m32) : "r"(mant), "r"(-sh));
+    mag = m32;
+  }
+  const long long sg = static_cast<long long>(static_cast<int>(bits16 << 16) >> 31);  // 0 or -1
+  return (static_cast<long long>(mag) ^ sg) - sg;
 }
 
 // One warp per cluster: mean of its members, written as fp32 to mean[bh][c];
@@ -366,9 +376,22 @@ __global__ void km_sum_kernel(const __nv_bfloat16* __restrict__ x, int N, int C,
       for (int e = 0; e < PER; ++e) acc[e] = 0;
       cur = c;
     }
-    const uint16_t* row = xb + static_cast<long long>(idx) * D;
+    // the lane's PER consecutive bf16 values in one 4- or 8-byte load
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(xb + static_cast<long long>(idx) * D);
+    uint32_t w[PER / 2];
+    if constexpr (PER == 4) {
+      const uint2 v = *reinterpret_cast<const uint2*>(row);
+      w[0] = v.x;
+      w[1] = v.y;
+    } else {
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] += bf16_fixed32(row[e]);
+      for (int i = 0; i < PER / 2; ++i) w[i] = row[i];
+    }
+#pragma unroll
+    for (int i = 0; i < PER / 2; ++i) {
+      acc[2 * i] += bf16_fixed32(w[i] & 0xffffu);
+      acc[2 * i + 1] += bf16_fixed32(w[i] >> 16);
+    }
   }
   if (cur >= 0 && cur < C) {
     unsigned long long* dst = sums + (static_cast<long long>(bh) * C + cur) * D + lane * PER;
