@@ -615,15 +615,15 @@ def run_reference(args, world, rank):
     }
 
 
-def run_linear(args, world, rank, local, mixed):
+def run_linear(args, world, rank, local, mixed, d=D):
     """Linear attention (or LinVideo's mixed attention, r = 0.5 with the radial
-    mask) on the Wan-shaped inputs."""
+    mask) on the Wan-shaped inputs, head_dim d."""
     import torch
     import linear_attention_video_fwd_b300 as va
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = WORKLOADS["wan_radial"]
+    wl = dict(WORKLOADS["wan_radial"], d=d)
     T, H, W, heads = wl["T"], wl["H"], wl["W"], wl["heads"]
     N = T * H * W
     q, k, v = make_inputs(wl, seed=1235 + rank)
@@ -647,12 +647,13 @@ def run_linear(args, world, rank, local, mixed):
     call_ms = float(np.mean(launch_ms))
     tensor_bytes = qt.numel() * qt.element_size()
     io_bytes = 4 * tensor_bytes                       # read Q, K, V; write O
-    lin_flops = 4.0 * N * D * (D + 1) * BATCH * heads  # phi(K)^T [V | 1] and phi(Q) [S | z]
+    lin_flops = 4.0 * N * d * (d + 1) * BATCH * heads  # phi(K)^T [V | 1] and phi(Q) [S | z]
     pk, src = peaks()
     cfg = {"workload": ("LinVideo mixed attention r=0.5 (radial block-sparse + linear)"
                         if mixed else "linear attention forward, elu+1 feature map"),
-           "B": BATCH, "heads": heads, "grid_THW": [T, H, W], "tokens": N, "head_dim": D,
-           "l2": "inputs larger than L2 (Q+K+V+O = 403 MB per call vs 126 MB L2), no flush",
+           "B": BATCH, "heads": heads, "grid_THW": [T, H, W], "tokens": N, "head_dim": d,
+           "l2": "inputs larger than L2 (Q+K+V+O = %d MB per call vs 126 MB L2), no flush"
+                 % round(4 * N * d * 2 * BATCH * heads / 1e6),
            "parallelism": "replicas: one independent workload per GPU"}
     line = {"n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -665,11 +666,12 @@ def run_linear(args, world, rank, local, mixed):
         sizes = np.minimum(blk, N - np.arange((N + blk - 1) // blk) * blk)
         live = sum(int(sizes[i]) * int(sizes[col[rp[i]:rp[i + 1]]].sum())
                    for i in range(len(rp) - 1))
-        att_flops = 4.0 * D * live * BATCH * heads
+        att_flops = 4.0 * d * live * BATCH * heads
         flops = att_flops + lin_flops
         tf = flops / (call_ms * 1e-3) / 1e12
         line.update({
-            "metric": "LinVideo mixed attention (r=0.5) effective TFLOP/s + ms/call at 32,760 tok",
+            "metric": "LinVideo mixed attention (r=0.5) effective TFLOP/s + ms/call at 32,760 tok"
+                      + ("" if d == D else ", head_dim %d" % d),
             "value": round(world * flops * args.steps / (total_ms * 1e-3) / 1e12, 2),
             "unit": UNIT,
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16_tflops"],
@@ -680,7 +682,8 @@ def run_linear(args, world, rank, local, mixed):
     else:
         gbs = io_bytes / (call_ms * 1e-3) / 1e9
         line.update({
-            "metric": "linear attention forward achieved GB/s + ms/call at 32,760 tok",
+            "metric": "linear attention forward achieved GB/s + ms/call at 32,760 tok"
+                      + ("" if d == D else ", head_dim %d" % d),
             "value": round(world * io_bytes * args.steps / (total_ms * 1e-3) / 1e9, 1),
             "unit": "GB/s",
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"],
@@ -696,7 +699,7 @@ def run_linear(args, world, rank, local, mixed):
         t0 = time.perf_counter()
         if mixed:
             bm = oracle_block_mask(wl)
-            want = OL.mixed_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(D), r, rows=rows)
+            want = OL.mixed_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(d), r, rows=rows)
         else:
             want = OL.linear_attention(q, k, v, rows=rows)
         secs = time.perf_counter() - t0
@@ -705,8 +708,8 @@ def run_linear(args, world, rank, local, mixed):
         if world == 1 and not args.no_cpu_baseline:
             if mixed:
                 live_keys = (bm * np.minimum(BLOCK, N - np.arange(bm.shape[0]) * BLOCK)[None, :]).sum(1)
-                oflops = (4.0 * D * float(live_keys[rows // BLOCK].sum())
-                          + 4.0 * N * D * len(rows)) * BATCH * heads
+                oflops = (4.0 * d * float(live_keys[rows // BLOCK].sum())
+                          + 4.0 * N * d * len(rows)) * BATCH * heads
                 base = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT}
             else:
                 # the oracle's time for R rows, scaled to a whole call's rows,
@@ -847,7 +850,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload",
-                    choices=sorted(WORKLOADS) + ["svgear", "linear", "mixed", "backward"],
+                    choices=sorted(WORKLOADS) + ["svgear", "linear", "linear_d64", "mixed",
+                                                 "mixed_d64", "backward"],
                     default="wan_radial")
     ap.add_argument("--oracle-rows", type=int, default=512,
                     help="query rows per head in the CPU-oracle baseline sample")
@@ -864,8 +868,9 @@ def main():
         line = run_reference(args, world, rank)
     elif args.workload == "svgear":
         line = run_svgear(args, world, rank, local)
-    elif args.workload in ("linear", "mixed"):
-        line = run_linear(args, world, rank, local, args.workload == "mixed")
+    elif args.workload in ("linear", "mixed", "linear_d64", "mixed_d64"):
+        line = run_linear(args, world, rank, local, args.workload.startswith("mixed"),
+                          64 if args.workload.endswith("_d64") else D)
     elif args.workload == "backward":
         line = run_bwd(args, world, rank, local)
     else:

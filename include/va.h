@@ -255,8 +255,8 @@ int va_sparse_attn_fwd_host(const void* q, const void* k, const void* v, const v
  *   out_i = sum_j (phi(q_i) . phi(k_j)) v_j / sum_j (phi(q_i) . phi(k_j))
  * computed as phi(q_i)^T S / phi(q_i)^T z with S = sum_j phi(k_j) v_j^T and
  * z = sum_j phi(k_j) (one read of K and V, one of Q). q, k, v, out:
- * [B, heads, N, d] device arrays. Supported: VA_BF16 with d = 128 (fp32
- * accumulation, bf16 output). Errors: VA_ERR_INVALID (null or misaligned
+ * [B, heads, N, d] device arrays. Supported: VA_BF16 with d = 64 or 128
+ * (fp32 accumulation, bf16 output). Errors: VA_ERR_INVALID (null or misaligned
  * pointers, B, heads or N < 1), VA_ERR_UNSUPPORTED (other dtype or d),
  * VA_ERR_OOM, VA_ERR_CUDA.
  */
@@ -272,7 +272,7 @@ int va_linear_attn_fwd(const void* q, const void* k, const void* v, void* out, i
  * `mask` (the dense mask gives full attention) and lin that of
  * va_linear_attn_fwd. r = 1 runs the attention only, r = 0 the linear
  * attention only. The attention part is rounded to bf16 before the blend.
- * Supported: VA_BF16, d = 128, mask block 128. Errors: as the two calls, and
+ * Supported: VA_BF16, d = 64 or 128, mask block 128. Errors: as the two calls, and
  * VA_ERR_INVALID for r outside [0, 1], N != the mask's N or a mask built on
  * another device.
  */

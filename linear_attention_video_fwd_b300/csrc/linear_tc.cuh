@@ -1,7 +1,7 @@
 // Linear attention and LinVideo's mixed attention (LinVideo, gist.science
 // 2510.08318, technical summary sec. 1: O(n) linear attention; sec. 2 A: per
 // layer a scalar r mixes quadratic (r = 1) and linear (r = 0) attention) on
-// the 5th-generation tensor cores, bf16, head_dim 128. Feature map
+// the 5th-generation tensor cores, bf16, head_dim D = 64 or 128. Feature map
 // phi(x) = elu(x) + 1; non-causal:
 //   lin_i = phi(q_i)^T S / phi(q_i)^T z,  S = sum_j phi(k_j) v_j^T,  z = sum_j phi(k_j)
 //   mix_i = r att_i + (1 - r) lin_i
@@ -13,8 +13,8 @@
 //                     (tokens >= N get 0), then S += phi(K)^T V and
 //                     z += phi(K)^T 1 on the tensor cores (TMEM), and the
 //                     split's partial {S, z} goes to global memory;
-//   lin_prep_kernel   sums the partials and writes [S | z]^T (144 x 128, rows
-//                     past 128 zero) as bf16 pieces hi + lo (16 significant
+//   lin_prep_kernel   sums the partials and writes [S | z]^T ((D + 16) x D,
+//                     rows past D zero) as bf16 pieces hi + lo (16 significant
 //                     bits, so the product keeps fp32-level accuracy);
 //   lin_out_kernel    persistent CTAs keep the pieces resident and stream
 //                     128-token tiles of Q; num | den = phi(Q) [S | z] on the
@@ -28,17 +28,27 @@
 
 namespace va {
 
-constexpr int LN_TILE = 128 * 128 * 2;   // 32 KB: 128 tokens x 128 dims bf16
-constexpr int LN_HALF = LN_TILE / 2;     // 128 rows x 64 dims
-constexpr int LN_NEXT = 144;             // rows of [S | z]^T (128 + z + padding)
-constexpr int LN_PIECE = LN_NEXT * 128 * 2;   // 36 KB: one bf16 piece of [S | z]^T
-constexpr int LN_PIECE_HALF = LN_PIECE / 2;   // 144 rows x 64 dims
-constexpr int LN_ROW = 129;              // partial rows per split: S[.][n], n < 128, and z
-constexpr int LN_STATE_THREADS = 640;   // producer, MMA, 2 idle warps, 4 phi warpgroups
+constexpr int LN_HALF = 128 * 64 * 2;    // 16 KB: 128 tokens x 64 dims bf16 (one TMA box)
+constexpr int LN_KSTAGE = 2 * LN_HALF;   // a K stage: phi(K) is the M = 128 MMA operand
+constexpr int LN_STATE_THREADS = 640;    // producer, MMA, 2 idle warps, 4 phi warpgroups
 constexpr int LN_OUT_THREADS = 768;
 constexpr int LN_NS = 3;                 // ring stages (K and V, or Q)
-constexpr int LN_STATE_SMEM = 1024 + 2 * LN_NS * LN_TILE + 4096;    // K, V rings + ones
-constexpr int LN_OUT_SMEM = 1024 + 2 * LN_PIECE + (LN_NS + 1) * LN_TILE;  // pieces, Q ring, O tile
+
+// Sizes that depend on the head dimension D.
+template <int D>
+struct LnDim {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kHalves = D / 64;           // 64-dim TMA boxes per tile
+  static constexpr int kTile = 128 * D * 2;        // 128 tokens x D dims bf16
+  static constexpr int kNext = D + 16;             // rows of [S | z]^T (D + z + padding)
+  static constexpr int kPieceHalf = kNext * 128;   // kNext rows x 64 dims bf16
+  static constexpr int kPiece = kNext * D * 2;     // one bf16 piece of [S | z]^T
+  static constexpr int kRow = D + 1;               // partial rows per split: S[.][n], n < D, z
+  // K and V rings and the ones tile. With D = 64 the upper half of each K stage
+  // stays zero, so phi(K)^T keeps M = 128 and S's rows past D come out zero.
+  static constexpr int kStateSmem = 1024 + LN_NS * (LN_KSTAGE + kTile) + 4096;
+  static constexpr int kOutSmem = 1024 + 2 * kPiece + (LN_NS + 1) * kTile;  // pieces, Q ring, O
+};
 
 // phi(x) = elu(x) + 1 = max(x, 0) + exp(n), n = max(min(x, 0), -100), on a
 // pair of bf16 values in bf16x2 arithmetic. max and min are exact; exp(n) =
@@ -63,23 +73,38 @@ __device__ __forceinline__ uint32_t lin_phi_bf16x2(uint32_t x) {
   return r;
 }
 
-// phi in place on one 64-dim half h of a 128-token bf16 tile (two
-// 128B-swizzled halves); the thread owns token row r of that half, rows with
-// token >= N become 0. Two warpgroups (h = 0, 1) cover a tile. The 16-byte
-// chunks of a row are visited in a rotated order so the warp's accesses fall
-// on distinct banks (the swizzle only permutes chunks within a row, and phi is
-// elementwise); all eight loads are issued before the stores.
-__device__ __forceinline__ void lin_phi_half(uint8_t* tile, int h, int r, bool valid) {
-  uint4 w[8];
+// phi in place on NC 16-byte chunks (c0 .. c0 + NC - 1) of token row `row` of
+// a 128-row x 64-dim 128B-swizzled half tile; rows with token >= N become 0.
+// The chunks are visited in an order rotated by the row, so the warp's
+// 16-byte accesses fall on distinct banks (the swizzle only permutes chunks
+// within a row, and phi is elementwise); all loads are issued before the
+// stores.
+template <int NC>
+__device__ __forceinline__ void lin_phi_chunks(uint8_t* half, int row, int c0, bool valid) {
+  uint4 w[NC];
 #pragma unroll
-  for (int c = 0; c < 8; ++c)
-    w[c] = *reinterpret_cast<const uint4*>(tile + h * LN_HALF + r * 128 + ((c + r) & 7) * 16);
+  for (int c = 0; c < NC; ++c)
+    w[c] = *reinterpret_cast<const uint4*>(half + row * 128 + ((c0 + c + row) & 7) * 16);
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < NC; ++c) {
     uint32_t* e = reinterpret_cast<uint32_t*>(&w[c]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) e[i] = valid ? lin_phi_bf16x2(e[i]) : 0u;
-    *reinterpret_cast<uint4*>(tile + h * LN_HALF + r * 128 + ((c + r) & 7) * 16) = w[c];
+    *reinterpret_cast<uint4*>(half + row * 128 + ((c0 + c + row) & 7) * 16) = w[c];
+  }
+}
+
+// phi on a 128-token tile of D dims by the two warpgroups (h = 0, 1) of a
+// pair, thread r of each: with D = 128 warpgroup h takes 64-dim half h, one
+// row per thread; with D = 64 the 256 threads take half a row each. Rows
+// >= nvalid become 0.
+template <int D>
+__device__ __forceinline__ void lin_phi_tile(uint8_t* tile, int h, int r, int nvalid) {
+  if constexpr (D == 128) {
+    lin_phi_chunks<8>(tile + h * LN_HALF, r, 0, r < nvalid);
+  } else {
+    const int t = h * 128 + r, row = t >> 1;
+    lin_phi_chunks<4>(tile, row, (t & 1) * 4, row < nvalid);
   }
 }
 
@@ -100,9 +125,10 @@ __device__ __forceinline__ void lin_range(int ntiles, int nsplit, int split, int
   t_hi = min(ntiles, t_lo + per);
 }
 
-// Grid (nsplit, BH), 640 threads. part[bh][split][n][dim]: n < 128 S[dim][n],
-// n = 128 z[dim] (dims contiguous, so both the stores here and the loads of
+// Grid (nsplit, BH), 640 threads. part[bh][split][n][dim]: n < D S[dim][n],
+// n = D z[dim] (dims contiguous, so both the stores here and the loads of
 // lin_prep_kernel are coalesced).
+template <int D>
 __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
     lin_state_kernel(const __grid_constant__ CUtensorMap map_k,
                      const __grid_constant__ CUtensorMap map_v, int N, float* __restrict__ part,
@@ -113,9 +139,10 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
   __shared__ int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* kt = smem;                    // stage s at kt + s TILE
-  uint8_t* vt = smem + LN_NS * LN_TILE;
-  uint8_t* ones = smem + 2 * LN_NS * LN_TILE;  // 16 rows x 128 tokens of 1.0 (K-major halves)
+  using Dm = LnDim<D>;
+  uint8_t* kt = smem;                    // stage s at kt + s KSTAGE
+  uint8_t* vt = smem + LN_NS * LN_KSTAGE;  // stage s at vt + s Dm::kTile
+  uint8_t* ones = vt + LN_NS * Dm::kTile;  // 16 rows x 128 tokens of 1.0 (K-major halves)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, bh = blockIdx.y, nsplit = gridDim.x;
   const int ntiles = (N + 127) / 128;
@@ -137,6 +164,12 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
   }
   for (int i = tid; i < 4096 / 4; i += LN_STATE_THREADS)
     reinterpret_cast<uint32_t*>(ones)[i] = 0x3f803f80u;  // bf16 1.0 pairs
+  if constexpr (D == 64) {  // the upper 64 dims of phi(K), never loaded, stay zero
+    for (int i = tid; i < LN_NS * LN_HALF / 16; i += LN_STATE_THREADS) {
+      const int s = i / (LN_HALF / 16), o = i % (LN_HALF / 16);
+      reinterpret_cast<uint4*>(kt + s * LN_KSTAGE + LN_HALF)[o] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_base_s), 256);
@@ -159,12 +192,14 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
         if (u >= LN_NS &&
             !mbar_wait_bounded(bar(LS_EMPTY + s), ((u / LN_NS) & 1) ^ 1, lim, abort_p))
           break;
-        mbar_arrive_expect_tx(bar(LS_KF + s), LN_TILE);
-        tma_load_3d(smem_u32(kt + s * LN_TILE), &map_k, bar(LS_KF + s), 0, row, bh);
-        tma_load_3d(smem_u32(kt + s * LN_TILE + LN_HALF), &map_k, bar(LS_KF + s), 64, row, bh);
-        mbar_arrive_expect_tx(bar(LS_VF + s), LN_TILE);
-        tma_load_3d(smem_u32(vt + s * LN_TILE), &map_v, bar(LS_VF + s), 0, row, bh);
-        tma_load_3d(smem_u32(vt + s * LN_TILE + LN_HALF), &map_v, bar(LS_VF + s), 64, row, bh);
+        mbar_arrive_expect_tx(bar(LS_KF + s), Dm::kTile);
+        for (int hh = 0; hh < Dm::kHalves; ++hh)
+          tma_load_3d(smem_u32(kt + s * LN_KSTAGE + hh * LN_HALF), &map_k, bar(LS_KF + s), 64 * hh,
+                      row, bh);
+        mbar_arrive_expect_tx(bar(LS_VF + s), Dm::kTile);
+        for (int hh = 0; hh < Dm::kHalves; ++hh)
+          tma_load_3d(smem_u32(vt + s * Dm::kTile + hh * LN_HALF), &map_v, bar(LS_VF + s),
+                      64 * hh, row, bh);
         issued = u + 1;
       }
       if (*abort_p) {
@@ -179,9 +214,10 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && nt > 0) {
-      // S (+)= phi(K)^T V: A = phi(K) and B = V, both MN-major (dims contiguous),
-      // K = 16 tokens per MMA; z (+)= phi(K)^T 1 with a K-major ones tile, N = 16.
-      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, 1, 1);
+      // S (+)= phi(K)^T V: A = phi(K) (M = 128 dims) and B = V (N = D), both
+      // MN-major (dims contiguous), K = 16 tokens per MMA; z (+)= phi(K)^T 1
+      // with a K-major ones tile, N = 16.
+      constexpr uint32_t id_s = idesc_bf16_f32(128, D, 1, 1);
       constexpr uint32_t id_z = idesc_bf16_f32(128, 16, 1, 0);
       const uint32_t sOnes = smem_u32(ones);
       bool ok = true;
@@ -191,7 +227,7 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
         if (!(ok = mbar_wait_bounded(bar(LS_PHI + s), ph, lim, abort_p))) break;
         if (!(ok = mbar_wait_bounded(bar(LS_VF + s), ph, lim, abort_p))) break;
         tc_fence_after();
-        const uint32_t sK = smem_u32(kt + s * LN_TILE), sV = smem_u32(vt + s * LN_TILE);
+        const uint32_t sK = smem_u32(kt + s * LN_KSTAGE), sV = smem_u32(vt + s * Dm::kTile);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint64_t a = sw128_desc(sK + k * 2048, LN_HALF, 1024);
@@ -210,7 +246,7 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
     }
   } else if (warp >= 4) {
     // Two pairs of warpgroups take alternate tiles: pair g transforms tiles
-    // u = g, g + 2, ..., warpgroup h of a pair one 64-dim half. Tile u - 3,
+    // u = g, g + 2, ... (lin_phi_tile splits a tile between the pair). Tile u - 3,
     // the previous user of stage s, belongs to the other pair, so the pair
     // first waits for that tile's phi: until then the K-full barrier of stage s
     // may sit two phases behind tile u and its parity would match too early.
@@ -225,28 +261,30 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
         break;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(LS_KF + s), ph, lim, abort_p))))
         break;
-      lin_phi_half(kt + s * LN_TILE, h, r, (t_lo + u) * 128 + r < N);
+      lin_phi_tile<D>(kt + s * LN_KSTAGE, h, r, N - (t_lo + u) * 128);
       fence_proxy_async_smem();
       mbar_arrive(bar(LS_PHI + s));
     }
-    if (h == 0 && g == 0) {  // the epilogue is warps 4..7; thread r stores column r
-      float* out = part + (static_cast<long long>(bh) * nsplit + split) * LN_ROW * 128 + r;
+    // The epilogue is the warps of 4..7 whose TMEM lanes hold dims (r < D);
+    // thread r stores column r.
+    if (h == 0 && g == 0 && (warp & 3) * 32 < D) {
+      float* out = part + (static_cast<long long>(bh) * nsplit + split) * Dm::kRow * D + r;
       if (nt == 0) {
-        for (int n = 0; n < LN_ROW; ++n) out[n * 128] = 0.f;
+        for (int n = 0; n < Dm::kRow; ++n) out[n * D] = 0.f;
       } else if (ok && __all_sync(0xffffffffu, mbar_wait_bounded(bar(LS_DONE), 0, lim, abort_p))) {
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) out[(c * 32 + i) * 128] = __uint_as_float(v[i]);
+          for (int i = 0; i < 32; ++i) out[(c * 32 + i) * D] = __uint_as_float(v[i]);
         }
         uint32_t zv[16];
         tmem_ld16(tmem + lane_off + 128, zv);
         tmem_wait_ld();
-        out[128 * 128] = __uint_as_float(zv[0]);
+        out[D * D] = __uint_as_float(zv[0]);
       }
     }
   }
@@ -257,25 +295,27 @@ __global__ void __launch_bounds__(LN_STATE_THREADS, 1)
 }
 
 // [S | z]^T of each batch*head from the split partials, as bf16 pieces:
-// piece[bh][p][n][dim], p = 0 hi, 1 lo, n < 128 S[dim][n], n = 128 z[dim],
-// n > 128 zero. Grid (LN_NEXT, BH), 128 threads (one per dim). Launched as a
+// piece[bh][p][n][dim], p = 0 hi, 1 lo, n < D S[dim][n], n = D z[dim],
+// n > D zero. Grid (D + 16, BH), D threads (one per dim). Launched as a
 // programmatic dependent of lin_state_kernel: it waits for that grid before
 // reading the partials.
+template <int D>
 __global__ void lin_prep_kernel(const float* __restrict__ part, int nsplit,
                                 __nv_bfloat16* __restrict__ piece) {
+  constexpr int kRow = LnDim<D>::kRow, kNext = LnDim<D>::kNext;
   grid_dep_launch();
   grid_dep_wait();
   const int n = blockIdx.x, bh = blockIdx.y, dim = threadIdx.x;
   float acc = 0.f;
-  if (n <= 128) {
-    const float* pp = part + static_cast<long long>(bh) * nsplit * LN_ROW * 128 + n * 128 + dim;
-    for (int s = 0; s < nsplit; ++s) acc += pp[static_cast<long long>(s) * LN_ROW * 128];
+  if (n <= D) {
+    const float* pp = part + static_cast<long long>(bh) * nsplit * kRow * D + n * D + dim;
+    for (int s = 0; s < nsplit; ++s) acc += pp[static_cast<long long>(s) * kRow * D];
   }
   const __nv_bfloat16 hi = __float2bfloat16_rn(acc);
   const __nv_bfloat16 lo = __float2bfloat16_rn(acc - __bfloat162float(hi));
-  const long long o = ((static_cast<long long>(bh) * 2) * LN_NEXT + n) * 128 + dim;
+  const long long o = ((static_cast<long long>(bh) * 2) * kNext + n) * D + dim;
   piece[o] = hi;
-  piece[o + static_cast<long long>(LN_NEXT) * 128] = lo;
+  piece[o + static_cast<long long>(kNext) * D] = lo;
 }
 
 enum : int {
@@ -291,11 +331,12 @@ enum : int {
 
 // Grid (nsplit, BH), 768 threads: warp 0 TMA producer, warp 1 MMA issuer,
 // warps 8..11 epilogue (thread r owns token row r of the tile; the tile goes
-// out through shared memory and a TMA store), and two pairs
-// of warpgroups that apply phi(Q) in place to alternate tiles: warps 4..7 and
-// 12..15 (dims 0..63 and 64..127) the even tiles, warps 16..19 and 20..23 the
-// odd ones. out = num / den, or r_mix * out + (1 - r_mix) * num / den when
-// mix != 0 (out then holds the attention output on entry).
+// out through shared memory and a TMA store), and two pairs of warpgroups
+// that apply phi(Q) in place to alternate tiles: warps 4..7 and 12..15 the
+// even tiles, warps 16..19 and 20..23 the odd ones. out = num / den, or
+// r_mix * out + (1 - r_mix) * num / den when mix != 0 (out then holds the
+// attention output on entry).
+template <int D>
 __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
     lin_out_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_p, const __grid_constant__ CUtensorMap map_o,
@@ -307,9 +348,10 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
   __shared__ int abort_flag;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* pc = smem;                    // piece p at pc + p PIECE
-  uint8_t* qt = smem + 2 * LN_PIECE;     // Q stage s at qt + s TILE
-  uint8_t* ot = qt + LN_NS * LN_TILE;    // output tile staged for the TMA store
+  using Dm = LnDim<D>;
+  uint8_t* pc = smem;                    // piece p at pc + p kPiece
+  uint8_t* qt = smem + 2 * Dm::kPiece;   // Q stage s at qt + s kTile
+  uint8_t* ot = qt + LN_NS * Dm::kTile;  // output tile staged for the TMA store
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, bh = blockIdx.y;
   const int ntiles = (N + 127) / 128;
@@ -350,20 +392,21 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
       int issued = 0;
       auto load_q = [&](int u) {
         const int s = u % LN_NS, row = (t_lo + u) * 128;
-        mbar_arrive_expect_tx(bar(LO_QF + s), LN_TILE);
-        tma_load_3d(smem_u32(qt + s * LN_TILE), &map_q, bar(LO_QF + s), 0, row, bh);
-        tma_load_3d(smem_u32(qt + s * LN_TILE + LN_HALF), &map_q, bar(LO_QF + s), 64, row, bh);
+        mbar_arrive_expect_tx(bar(LO_QF + s), Dm::kTile);
+        for (int hh = 0; hh < Dm::kHalves; ++hh)
+          tma_load_3d(smem_u32(qt + s * Dm::kTile + hh * LN_HALF), &map_q, bar(LO_QF + s), 64 * hh,
+                      row, bh);
         issued = u + 1;
       };
       // The first Q tiles need no wait. The pieces are the previous kernel's
       // output, so under a programmatic dependent launch they load after it.
       for (int u = 0; u < nt && u < LN_NS; ++u) load_q(u);
       grid_dep_wait();
-      mbar_arrive_expect_tx(bar(LO_PF), 2 * LN_PIECE);
+      mbar_arrive_expect_tx(bar(LO_PF), 2 * Dm::kPiece);
       for (int p = 0; p < 2; ++p)
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(smem_u32(pc + p * LN_PIECE + h * LN_PIECE_HALF), &map_p, bar(LO_PF), 64 * h,
-                      p * LN_NEXT, bh);
+        for (int h = 0; h < Dm::kHalves; ++h)
+          tma_load_3d(smem_u32(pc + p * Dm::kPiece + h * Dm::kPieceHalf), &map_p, bar(LO_PF),
+                      64 * h, p * Dm::kNext, bh);
       for (int u = LN_NS; u < nt; ++u) {
         if (!mbar_wait_bounded(bar(LO_QE + u % LN_NS), ((u / LN_NS) & 1) ^ 1, lim, abort_p)) break;
         load_q(u);
@@ -380,8 +423,8 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
   } else if (warp == 1) {
     if (lane == 0 && nt > 0) {
       // num | den = phi(Q) [S | z]: A = phi(Q) K-major, B = [S | z]^T K-major
-      // (144 rows), two pieces accumulated in fp32.
-      constexpr uint32_t id = idesc_bf16_f32(128, LN_NEXT, 0, 0);
+      // (D + 16 rows), two pieces accumulated in fp32.
+      constexpr uint32_t id = idesc_bf16_f32(128, Dm::kNext, 0, 0);
       const uint32_t sP = smem_u32(pc);
       bool ok = mbar_wait_bounded(bar(LO_PF), 0, lim, abort_p);
       for (int u = 0; ok && u < nt; ++u) {
@@ -391,14 +434,15 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
             !(ok = mbar_wait_bounded(bar(LO_AE + b), ((u >> 1) & 1) ^ 1, lim, abort_p)))
           break;
         tc_fence_after();
-        const uint32_t sQ = smem_u32(qt + s * LN_TILE);
+        const uint32_t sQ = smem_u32(qt + s * Dm::kTile);
 #pragma unroll
         for (int p = 0; p < 2; ++p)
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+          for (int k = 0; k < D / 16; ++k)
             umma_ss(tmem + b * 256,
                     sw128_desc(sQ + (k >> 2) * LN_HALF + (k & 3) * 32, 16, 1024),
-                    sw128_desc(sP + p * LN_PIECE + (k >> 2) * LN_PIECE_HALF + (k & 3) * 32, 16, 1024),
+                    sw128_desc(sP + p * Dm::kPiece + (k >> 2) * Dm::kPieceHalf + (k & 3) * 32, 16,
+                               1024),
                     id, (p | k) ? 1u : 0u);
         umma_commit(bar(LO_QE + s));
         umma_commit(bar(LO_AF + b));
@@ -423,7 +467,7 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
         break;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_QF + s), ph, lim, abort_p)))
         break;
-      lin_phi_half(qt + s * LN_TILE, h, r, true);
+      lin_phi_tile<D>(qt + s * Dm::kTile, h, r, 128);
       fence_proxy_async_smem();
       mbar_arrive(bar(LO_PHI + s));
     }
@@ -446,17 +490,17 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
       tc_fence_after();
       const uint32_t tA = tmem + b * 256 + lane_off;
       uint32_t dv[16];
-      tmem_ld16(tA + 128, dv);
+      tmem_ld16(tA + D, dv);
       tmem_wait_ld();
       const float inv = 1.f / __uint_as_float(dv[0]);
       const int tok = (t_lo + u) * 128 + r;
-      const __nv_bfloat16* arow = out + (static_cast<long long>(bh) * N + tok) * 128;
+      const __nv_bfloat16* arow = out + (static_cast<long long>(bh) * N + tok) * D;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tA + c * 32, v);
         tmem_wait_ld();
-        if (c == 3) {
+        if (c == D / 32 - 1) {
           tc_fence_before();
           mbar_arrive(bar(LO_AE + b));
         }
@@ -487,8 +531,8 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (issuer) {
-        tma_store_3d(&map_o, smem_u32(ot), 0, (t_lo + u) * 128, bh);
-        tma_store_3d(&map_o, smem_u32(ot + LN_HALF), 64, (t_lo + u) * 128, bh);
+        for (int hh = 0; hh < Dm::kHalves; ++hh)
+          tma_store_3d(&map_o, smem_u32(ot + hh * LN_HALF), 64 * hh, (t_lo + u) * 128, bh);
         bulk_commit();
       }
     }

@@ -884,12 +884,14 @@ VA_EXPORT int va_sparse_attn_fwd_host(const void* q, const void* k, const void* 
 
 namespace {
 
-// Linear attention (bf16, d = 128) of every (batch, head): split state sums,
+// Linear attention (bf16, d = D) of every (batch, head): split state sums,
 // their merge into bf16 pieces of [S | z]^T, then the output; with mix != 0
 // the output kernel blends r * out (the attention already there) with the
 // linear result.
+template <int D>
 int run_linear(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
                __nv_bfloat16* out, int BH, int N, int mix, float r, cudaStream_t s) {
+  using Dm = va::LnDim<D>;
   static DeviceOnce once;
   static int num_sms[64] = {0};
   int dev = 0;
@@ -897,12 +899,12 @@ int run_linear(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat
   if (st) return st;
   st = device_once(once, dev, [dev] {
     int r;
-    if ((r = cuda_status(cudaFuncSetAttribute(va::lin_state_kernel,
+    if ((r = cuda_status(cudaFuncSetAttribute(va::lin_state_kernel<D>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              va::LN_STATE_SMEM))) ||
-        (r = cuda_status(cudaFuncSetAttribute(va::lin_out_kernel,
+                                              Dm::kStateSmem))) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::lin_out_kernel<D>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              va::LN_OUT_SMEM))) ||
+                                              Dm::kOutSmem))) ||
         (r = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
                                                 dev))))
       return r;
@@ -915,25 +917,31 @@ int run_linear(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat
   float* part;
   __nv_bfloat16* piece;
   const size_t bh = static_cast<size_t>(BH);
-  if ((st = scratch.alloc(&part, bh * nsplit * 128 * va::LN_ROW)) ||
-      (st = scratch.alloc(&piece, bh * 2 * va::LN_NEXT * 128)))
+  if ((st = scratch.alloc(&part, bh * nsplit * D * Dm::kRow)) ||
+      (st = scratch.alloc(&piece, bh * 2 * Dm::kNext * D)))
     return st;
   CUtensorMap mk, mv, mq, mp, mo;
-  if ((st = encode_bf16_rows(&mk, k, BH, N, 128)) || (st = encode_bf16_rows(&mv, v, BH, N, 128)) ||
-      (st = encode_bf16_rows(&mq, q, BH, N, 128)) || (st = encode_bf16_rows(&mo, out, BH, N, 128)) ||
-      (st = encode_bf16_rows_box(&mp, piece, BH, 2 * va::LN_NEXT, 128, va::LN_NEXT)))
+  if ((st = encode_bf16_rows(&mk, k, BH, N, D)) || (st = encode_bf16_rows(&mv, v, BH, N, D)) ||
+      (st = encode_bf16_rows(&mq, q, BH, N, D)) || (st = encode_bf16_rows(&mo, out, BH, N, D)) ||
+      (st = encode_bf16_rows_box(&mp, piece, BH, 2 * Dm::kNext, D, Dm::kNext)))
     return st;
-  va::lin_state_kernel<<<dim3(nsplit, BH), va::LN_STATE_THREADS, va::LN_STATE_SMEM, s>>>(
+  va::lin_state_kernel<D><<<dim3(nsplit, BH), va::LN_STATE_THREADS, Dm::kStateSmem, s>>>(
       mk, mv, N, part, g_wait_limit);
   // prep and out are programmatic dependents: each starts while its
   // predecessor drains and waits (griddepcontrol.wait) before reading its output.
-  if ((st = cuda_status(launch_dependent(va::lin_prep_kernel, dim3(va::LN_NEXT, BH), 128, 0, s,
+  if ((st = cuda_status(launch_dependent(va::lin_prep_kernel<D>, dim3(Dm::kNext, BH), D, 0, s,
                                          static_cast<const float*>(part), nsplit, piece))) ||
-      (st = cuda_status(launch_dependent(va::lin_out_kernel, dim3(nsplit, BH), va::LN_OUT_THREADS,
-                                         va::LN_OUT_SMEM, s, mq, mp, mo, N, out, mix, r,
-                                         static_cast<long long>(g_wait_limit)))))
+      (st = cuda_status(launch_dependent(va::lin_out_kernel<D>, dim3(nsplit, BH),
+                                         va::LN_OUT_THREADS, Dm::kOutSmem, s, mq, mp, mo, N, out,
+                                         mix, r, static_cast<long long>(g_wait_limit)))))
     return st;
   return launch_status();
+}
+
+int run_linear_d(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                 __nv_bfloat16* out, int BH, int N, int d, int mix, float r, cudaStream_t s) {
+  return d == 64 ? run_linear<64>(q, k, v, out, BH, N, mix, r, s)
+                 : run_linear<128>(q, k, v, out, BH, N, mix, r, s);
 }
 
 int check_linear_args(const void* q, const void* k, const void* v, const void* out, int B,
@@ -941,7 +949,7 @@ int check_linear_args(const void* q, const void* k, const void* v, const void* o
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return VA_ERR_INVALID;
   if (B < 1 || heads < 1 || N < 1) return VA_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return VA_ERR_INVALID;
-  if (dtype != VA_BF16 || d != 128) return VA_ERR_UNSUPPORTED;
+  if (dtype != VA_BF16 || (d != 64 && d != 128)) return VA_ERR_UNSUPPORTED;
   const int64_t BH64 = static_cast<int64_t>(B) * heads;
   if (BH64 > 65535 || BH64 * N >= (1LL << 31)) return VA_ERR_UNSUPPORTED;
   *BH = static_cast<int>(BH64);
@@ -956,8 +964,8 @@ VA_EXPORT int va_linear_attn_fwd(const void* q, const void* k, const void* v, vo
   const int st = check_linear_args(q, k, v, out, B, heads, N, d, dtype, &BH);
   if (st) return st;
   using T = __nv_bfloat16;
-  return run_linear(static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
-                    static_cast<T*>(out), BH, N, 0, 0.f, reinterpret_cast<cudaStream_t>(stream));
+  return run_linear_d(static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+                      static_cast<T*>(out), BH, N, d, 0, 0.f, reinterpret_cast<cudaStream_t>(stream));
 }
 
 VA_EXPORT int va_mixed_attn_fwd(const void* q, const void* k, const void* v, const va_mask* m,
@@ -975,8 +983,8 @@ VA_EXPORT int va_mixed_attn_fwd(const void* q, const void* k, const void* v, con
       (st = va_sparse_attn_fwd(q, k, v, m, out, nullptr, B, heads, N, d, scale, dtype, stream)))
     return st;
   if (r == 1.f) return VA_OK;
-  return run_linear(static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
-                    static_cast<T*>(out), BH, N, r > 0.f ? 1 : 0, r, s);
+  return run_linear_d(static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v),
+                      static_cast<T*>(out), BH, N, d, r > 0.f ? 1 : 0, r, s);
 }
 
 // ------------------------------------------------------------------ LIPAR --

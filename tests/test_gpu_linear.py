@@ -21,13 +21,14 @@ def _dev(x, dev):
     return torch.from_numpy(np.ascontiguousarray(x)).to(dev, torch.bfloat16)
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("B,Hh,T,H,W", [(2, 2, 5, 6, 11),     # N = 330: ragged tail tile
                                         (1, 3, 1, 7, 13),     # N = 91 < one tile
                                         (1, 1, 3, 43, 1),     # N = 129: one token past a tile
                                         (2, 80, 2, 8, 8)])    # 160 slices: one split each
-def test_linear_small(va, dev, B, Hh, T, H, W):
+def test_linear_small(va, dev, B, Hh, T, H, W, d):
     N = T * H * W
-    q, k, v = synth.video_qkv(B, Hh, T, H, W, 128, seed=41, dtype="bf16")
+    q, k, v = synth.video_qkv(B, Hh, T, H, W, d, seed=41, dtype="bf16")
     out = va.linear_attn_fwd(_dev(q, dev), _dev(k, dev), _dev(v, dev))
     torch.cuda.synchronize()
     assert va.device_error() == va.OK
@@ -46,12 +47,13 @@ def test_linear_identical_keys_give_mean_value(va, dev):
     assert_bf16_close(out.float().cpu().numpy(), want)
 
 
-def test_linear_extreme_feature_inputs(va, dev):
+@pytest.mark.parametrize("d", [128, 64])
+def test_linear_extreme_feature_inputs(va, dev, d):
     # phi(-inf) = 0 and phi of large negative inputs underflows to 0; large
     # positive inputs give x + 1. Some dims of Q and K take such values (no
     # row is all -inf, so every denominator stays positive).
     T, H, W = 3, 7, 13
-    q, k, v = synth.video_qkv(1, 2, T, H, W, 128, seed=47, dtype="bf16")
+    q, k, v = synth.video_qkv(1, 2, T, H, W, d, seed=47, dtype="bf16")
     q, k = q.copy(), k.copy()
     k[:, :, ::3, 5] = -np.inf
     k[:, :, 1::4, 7] = -300.0
@@ -68,12 +70,13 @@ def test_linear_extreme_feature_inputs(va, dev):
     assert_bf16_close(got, OL.linear_attention(q, k, v))
 
 
-def test_linear_full_size(va, dev):
-    # Wan-shaped inputs: B=1, 12 heads, 21x30x52 = 32,760 tokens, d=128, bf16;
-    # the oracle on 512 sampled rows of every head
+@pytest.mark.parametrize("d", [128, 64])
+def test_linear_full_size(va, dev, d):
+    # Wan-shaped inputs: B=1, 12 heads, 21x30x52 = 32,760 tokens, bf16, with
+    # head_dim 128 and 64; the oracle on 512 sampled rows of every head
     T, H, W = 21, 30, 52
     N = T * H * W
-    q, k, v = cached_video_qkv(1, 12, T, H, W, 128, seed=1235)
+    q, k, v = cached_video_qkv(1, 12, T, H, W, d, seed=1235)
     out = va.linear_attn_fwd(_dev(q, dev), _dev(k, dev), _dev(v, dev))
     torch.cuda.synchronize()
     assert va.device_error() == va.OK
@@ -82,11 +85,11 @@ def test_linear_full_size(va, dev):
     assert_bf16_close(got, OL.linear_attention(q, k, v, rows=rows))
 
 
-@pytest.mark.parametrize("r", [0.0, 0.3, 1.0])
-def test_mixed(va, dev, r):
+@pytest.mark.parametrize("r,d", [(0.0, 128), (0.3, 128), (1.0, 128), (0.0, 64), (0.3, 64)])
+def test_mixed(va, dev, r, d):
     T, H, W = 5, 6, 11
     N = T * H * W
-    q, k, v = synth.video_qkv(1, 3, T, H, W, 128, seed=47, dtype="bf16")
+    q, k, v = synth.video_qkv(1, 3, T, H, W, d, seed=47, dtype="bf16")
     p = OM.MaskParams(block=128, w0=9)
     m = va.mask_build(OM.RADIAL, T, H, W, block=128, w0=9)
     qt, kt, vt = _dev(q, dev), _dev(k, dev), _dev(v, dev)
@@ -94,7 +97,7 @@ def test_mixed(va, dev, r):
     torch.cuda.synchronize()
     assert va.device_error() == va.OK
     bm = OM.block_mask(OM.RADIAL, T, H, W, p, 0)
-    want = OL.mixed_attention(q, k, v, bm, 128, 1.0 / np.sqrt(128), r)
+    want = OL.mixed_attention(q, k, v, bm, 128, 1.0 / np.sqrt(d), r)
     assert_bf16_close(out.float().cpu().numpy(), want)
     if r == 1.0:   # the attention alone, bit for bit
         att, _ = va.sparse_attn_fwd(qt, kt, vt, m)
@@ -112,4 +115,8 @@ def test_mixed_rejects_bad_arguments(va, dev):
             va.mixed_attn_fwd(q, q, q, m, r)
     with pytest.raises(va.VAError):
         va.linear_attn_fwd(q.float(), q.float(), q.float())
+    q32 = torch.zeros((1, 1, 64, 32), dtype=torch.bfloat16, device=dev)
+    with pytest.raises(va.VAError) as e:       # head_dim 64 and 128 only
+        va.linear_attn_fwd(q32, q32, q32)
+    assert e.value.status == va.ERR_UNSUPPORTED
     m.free()
