@@ -1,16 +1,16 @@
 // k-means assignment on the 5th-generation tensor cores (tcgen05 + TMEM +
-// TMA) for bf16 points with d = 128: the distance cross term x . c of the
+// TMA) for bf16 points with d = D (64 or 128): the distance cross term x . c of the
 // Lloyd assign step (SVG-EAR, gist.science 2603.08982, technical summary
 // sec. 2, idea 1: semantic clustering of queries and keys).
 //
 // The float32 centroid is split as c = c_hi + c_lo with both parts bf16
 // (|c - c_hi - c_lo| <= 2^-17 |c|), so x . c = x . c_hi + x . c_lo is two
-// exact-product bf16 MMAs accumulated in one fp32 TMEM accumulator (K = 256).
+// exact-product bf16 MMAs accumulated in one fp32 TMEM accumulator (K = 2 D).
 // dist(i, c) = |c|^2 - 2 x_i . c; the argmin takes the lowest c on ties.
 //
 // Persistent CTAs with resident centroids: CTA (split, chunk, batch*head)
-// holds the hi and lo halves of one chunk of 256 clusters in shared memory
-// (128 KB) and streams its share of the 128-point tiles through a two-stage
+// holds the hi and lo parts of one chunk of 256 clusters in shared memory
+// (128 KB at D = 128) and streams its share of the 128-point tiles through a two-stage
 // TMA ring; the accumulators of consecutive point tiles alternate between two
 // TMEM halves, so the argmin of one tile overlaps the MMAs of the next. With
 // several chunks the per-chunk (distance, index) results are merged by
@@ -31,10 +31,17 @@ namespace va {
 
 constexpr int KA_THREADS = 256;
 constexpr int KA_CHUNK = 256;            // clusters resident per CTA
-constexpr int KA_TILE = 128 * 128 * 2;   // 32 KB: 128 rows x 128 bf16
-constexpr int KA_HALF = KA_TILE / 2;
+constexpr int KA_HALF = 128 * 64 * 2;    // 16 KB: 128 rows x 64 bf16 (one TMA box)
 constexpr int KA_NX = 2;                 // point-tile ring stages
-constexpr int KA_SMEM_BYTES = 1024 + KA_TILE * (4 + KA_NX);
+
+// Sizes that depend on the head dimension D.
+template <int D>
+struct KaDim {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTile = 128 * D * 2;   // 128 rows x D bf16
+  static constexpr int kSmemBytes = 1024 + kTile * (4 + KA_NX);
+};
 
 enum : int {
   KB_C_FULL = 0,
@@ -52,12 +59,13 @@ __device__ __forceinline__ float ka_min3(float a, float b, float c) {
   return d;
 }
 
-// D (+)= A[128 x 128] . B[128 x 128]^T, both K-major 128B-swizzled halves.
+// Acc (+)= A[128 x D] . B[128 x D]^T, both K-major 128B-swizzled halves.
+template <int D>
 __device__ __forceinline__ void ka_issue(uint32_t d_tmem, uint32_t sA, uint32_t sB,
                                          bool accumulate) {
   constexpr uint32_t idesc = idesc_bf16_f32(128, 128, 0, 0);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
+  for (int k = 0; k < D / 16; ++k) {
     const uint32_t off = (k >> 2) * KA_HALF + (k & 3) * 32;
     umma_ss(d_tmem, sw128_desc(sA + off, 16, 1024), sw128_desc(sB + off, 16, 1024), idesc,
             (accumulate || k > 0) ? 1u : 0u);
@@ -73,6 +81,7 @@ __device__ __forceinline__ void ka_range(int ntiles, int nsplit, int split, int&
 
 // Grid (nsplit, nchunks, BH). With one chunk the result is the assignment
 // (assign, count += 1); with several, (pdist, pidx)[bh][chunk][i] for the merge.
+template <int D>
 __global__ void __launch_bounds__(KA_THREADS, 1)
     km_assign_tc_kernel(const __grid_constant__ CUtensorMap map_x,
                         const __grid_constant__ CUtensorMap map_hi,
@@ -87,9 +96,10 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
   __shared__ __align__(8) float cn_s[KA_CHUNK];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  const uint32_t sHi = smem_u32(smem);          // cluster tile t: hi at sHi + t TILE
-  const uint32_t sLo = sHi + 2 * KA_TILE;       // lo at sLo + t TILE
-  const uint32_t sX0 = sLo + 2 * KA_TILE;       // point-tile stage s at sX0 + s TILE
+  constexpr int kTile = KaDim<D>::kTile, kHalves = KaDim<D>::kHalves;
+  const uint32_t sHi = smem_u32(smem);          // cluster tile t: hi at sHi + t kTile
+  const uint32_t sLo = sHi + 2 * kTile;         // lo at sLo + t kTile
+  const uint32_t sX0 = sLo + 2 * kTile;         // point-tile stage s at sX0 + s kTile
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, chunk = blockIdx.y, bh = blockIdx.z;
   const int nchunks = gridDim.y;
@@ -132,13 +142,14 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
       tma_prefetch_desc(&map_x);
       tma_prefetch_desc(&map_hi);
       tma_prefetch_desc(&map_lo);
-      mbar_arrive_expect_tx(bar(KB_C_FULL), 4 * KA_TILE);
-      for (int t = 0; t < 2; ++t) {
-        tma_load_3d(sHi + t * KA_TILE, &map_hi, bar(KB_C_FULL), 0, c0 + 128 * t, bh);
-        tma_load_3d(sHi + t * KA_TILE + KA_HALF, &map_hi, bar(KB_C_FULL), 64, c0 + 128 * t, bh);
-        tma_load_3d(sLo + t * KA_TILE, &map_lo, bar(KB_C_FULL), 0, c0 + 128 * t, bh);
-        tma_load_3d(sLo + t * KA_TILE + KA_HALF, &map_lo, bar(KB_C_FULL), 64, c0 + 128 * t, bh);
-      }
+      mbar_arrive_expect_tx(bar(KB_C_FULL), 4 * kTile);
+      for (int t = 0; t < 2; ++t)
+        for (int h = 0; h < kHalves; ++h) {
+          tma_load_3d(sHi + t * kTile + h * KA_HALF, &map_hi, bar(KB_C_FULL), 64 * h,
+                      c0 + 128 * t, bh);
+          tma_load_3d(sLo + t * kTile + h * KA_HALF, &map_lo, bar(KB_C_FULL), 64 * h,
+                      c0 + 128 * t, bh);
+        }
       int issued = 0;
       for (int i = 0; i < nt; ++i) {
         const int s = i % KA_NX;
@@ -146,9 +157,9 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
             !mbar_wait_bounded(bar(KB_X_EMPTY + s), ((i / KA_NX) & 1) ^ 1, lim, abort_p))
           break;
         const int row = (t_lo + i) * 128;
-        mbar_arrive_expect_tx(bar(KB_X_FULL + s), KA_TILE);
-        tma_load_3d(sX0 + s * KA_TILE, &map_x, bar(KB_X_FULL + s), 0, row, bh);
-        tma_load_3d(sX0 + s * KA_TILE + KA_HALF, &map_x, bar(KB_X_FULL + s), 64, row, bh);
+        mbar_arrive_expect_tx(bar(KB_X_FULL + s), kTile);
+        for (int h = 0; h < kHalves; ++h)
+          tma_load_3d(sX0 + s * kTile + h * KA_HALF, &map_x, bar(KB_X_FULL + s), 64 * h, row, bh);
         issued = i + 1;
       }
       if (*abort_p) {
@@ -170,11 +181,11 @@ __global__ void __launch_bounds__(KA_THREADS, 1)
             !(ok = mbar_wait_bounded(bar(KB_ACC_EMPTY + b), ((i >> 1) & 1) ^ 1, lim, abort_p)))
           break;
         tc_fence_after();
-        const uint32_t sX = sX0 + s * KA_TILE;
+        const uint32_t sX = sX0 + s * kTile;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          ka_issue(tmem + b * 256 + t * 128, sX, sHi + t * KA_TILE, false);
-          ka_issue(tmem + b * 256 + t * 128, sX, sLo + t * KA_TILE, true);
+          ka_issue<D>(tmem + b * 256 + t * 128, sX, sHi + t * kTile, false);
+          ka_issue<D>(tmem + b * 256 + t * 128, sX, sLo + t * kTile, true);
         }
         umma_commit(bar(KB_X_EMPTY + s));
         umma_commit(bar(KB_ACC_FULL + b));
@@ -282,7 +293,7 @@ __global__ void ka_merge_kernel(const float* __restrict__ pdist, const int* __re
   }
 }
 
-// c = hi + lo with hi = bf16(c) and lo = bf16(c - hi), for [rows, 128] fp32.
+// c = hi + lo with hi = bf16(c) and lo = bf16(c - hi), elementwise over n fp32.
 __global__ void km_split_kernel(const float* __restrict__ cent, long long n,
                                 __nv_bfloat16* __restrict__ hi, __nv_bfloat16* __restrict__ lo) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;

@@ -1111,7 +1111,8 @@ int cluster_lists(const int* assign, int BH, int N, int C, int* count, int* off,
   return launch_status();
 }
 
-// bf16, d = 128: distances on the tensor cores (split-bf16 centroids).
+// bf16, d = D: distances on the tensor cores (split-bf16 centroids).
+template <int D>
 int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int BH, int N, int C,
                    int iters, int* assign, float* cent, int* count, cudaStream_t s) {
   static DeviceOnce once;
@@ -1121,10 +1122,10 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int
   if (st) return st;
   st = device_once(once, dev, [dev] {
     int r;
-    if ((r = set_smem_attrs<__nv_bfloat16, 128>()) ||
-        (r = cuda_status(cudaFuncSetAttribute(va::km_assign_tc_kernel,
+    if ((r = set_smem_attrs<__nv_bfloat16, D>()) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::km_assign_tc_kernel<D>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              va::KA_SMEM_BYTES))) ||
+                                              va::KaDim<D>::kSmemBytes))) ||
         (r = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
                                                 dev))))
       return r;
@@ -1144,7 +1145,7 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int
   int *off = nullptr, *fill = nullptr, *perm = nullptr;
   __nv_bfloat16 *hi = nullptr, *lo = nullptr;
   unsigned long long* sums = nullptr;
-  const size_t nc = static_cast<size_t>(BH) * C * 128;
+  const size_t nc = static_cast<size_t>(BH) * C * D;
   if ((st = scratch.alloc(&cnorm, static_cast<size_t>(BH) * C)) ||
       (st = scratch.alloc(&off, static_cast<size_t>(BH) * (C + 1))) ||
       (st = scratch.alloc(&fill, static_cast<size_t>(BH) * C)) ||
@@ -1159,22 +1160,22 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int
     if ((st = scratch.alloc(&pdist, np)) || (st = scratch.alloc(&pidx, np))) return st;
   }
   CUtensorMap mx, mh, ml;
-  if ((st = encode_bf16_rows(&mx, x, BH, N, 128)) || (st = encode_bf16_rows(&mh, hi, BH, C, 128)) ||
-      (st = encode_bf16_rows(&ml, lo, BH, C, 128)))
+  if ((st = encode_bf16_rows(&mx, x, BH, N, D)) || (st = encode_bf16_rows(&mh, hi, BH, C, D)) ||
+      (st = encode_bf16_rows(&ml, lo, BH, C, D)))
     return st;
   const dim3 gc((C + 7) / 8, BH);
   const dim3 ga(nsplit, nchunks, BH);
   const dim3 gn((N + 255) / 256, BH);
   const unsigned gs = static_cast<unsigned>((nc + 255) / 256);
   if (c0 != nullptr)
-    va::km_warm_kernel<128><<<gc, 256, 0, s>>>(c0, C, cent, cnorm);
+    va::km_warm_kernel<D><<<gc, 256, 0, s>>>(c0, C, cent, cnorm);
   else
-    va::km_init_kernel<__nv_bfloat16, 128><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
+    va::km_init_kernel<__nv_bfloat16, D><<<gc, 256, 0, s>>>(x, init, N, C, cent, cnorm);
   va::km_split_kernel<<<gs, 256, 0, s>>>(cent, static_cast<long long>(nc), hi, lo);
   const int rounds = iters > 0 ? iters : 1;
   for (int it = 0; it < rounds; ++it) {
     if ((st = cuda_status(cudaMemsetAsync(count, 0, sizeof(int) * BH * C, s)))) return st;
-    va::km_assign_tc_kernel<<<ga, va::KA_THREADS, va::KA_SMEM_BYTES, s>>>(
+    va::km_assign_tc_kernel<D><<<ga, va::KA_THREADS, va::KaDim<D>::kSmemBytes, s>>>(
         mx, mh, ml, cnorm, N, C, assign, count, pdist, pidx, g_wait_limit);
     if (nchunks > 1)
       va::ka_merge_kernel<<<dim3((N + 255) / 256, BH), 256, 0, s>>>(pdist, pidx, N, C, nchunks,
@@ -1183,8 +1184,8 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int
     va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
     va::km_scatter_kernel<<<gn, 256, 0, s>>>(assign, N, C, off, fill, perm);
     if ((st = cuda_status(cudaMemsetAsync(sums, 0, sizeof(unsigned long long) * nc, s)))) return st;
-    va::km_sum_kernel<128><<<gn, 256, 0, s>>>(x, N, C, perm, assign, sums);
-    va::km_finalize_kernel<128><<<gc, 256, 0, s>>>(sums, count, C, cent, cnorm, hi, lo, 1);
+    va::km_sum_kernel<D><<<gn, 256, 0, s>>>(x, N, C, perm, assign, sums);
+    va::km_finalize_kernel<D><<<gc, 256, 0, s>>>(sums, count, C, cent, cnorm, hi, lo, 1);
   }
   return launch_status();
 }
@@ -1245,9 +1246,8 @@ int cluster_entry(const void* x, const int32_t* init_idx, const float* c0, int B
   const int* ii = init_idx;
   if (dtype == VA_BF16) {
     const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-    return d == 128 ? run_cluster_tc(xb, ii, c0, BH, N, C, iters, assign, centroid, count, s)
-                    : run_cluster<__nv_bfloat16, 64>(xb, ii, c0, BH, N, C, iters, assign,
-                                                     centroid, count, s);
+    return d == 128 ? run_cluster_tc<128>(xb, ii, c0, BH, N, C, iters, assign, centroid, count, s)
+                    : run_cluster_tc<64>(xb, ii, c0, BH, N, C, iters, assign, centroid, count, s);
   }
   if (dtype == VA_F32) {
     const float* xf = static_cast<const float*>(x);

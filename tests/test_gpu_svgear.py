@@ -62,6 +62,7 @@ KM_CASES = [
     (2, 1, 300, 128, 33, "f32"),
     (1, 3, 1000, 128, 100, "bf16"),
     (1, 2, 1500, 128, 300, "bf16"),          # tensor-core path, ragged cluster tile
+    (2, 1, 1300, 64, 300, "bf16"),           # the same at head_dim 64: two cluster chunks
 ]
 
 
