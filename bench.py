@@ -395,25 +395,25 @@ def run_ours(args, world, rank, local):
 SVG = dict(T=21, H=30, W=52, heads=12, Cq=256, Ck=1024, iters=10, density=0.15, seed=1238)
 
 
-def svgear_flops(qa, ka, sel, Cq, Ck, N, iters):
+def svgear_flops(qa, ka, sel, Cq, Ck, N, iters, d=D):
     """Algorithmic FLOPs of one SVG-EAR step per stage (all heads), from the
     step's own clusters and selection."""
     heads = qa.shape[1]
-    out = {"cluster_q": 2.0 * N * Cq * D * iters * heads,
-           "cluster_k": 2.0 * N * Ck * D * iters * heads, "probe": 0.0, "exact": 0.0,
+    out = {"cluster_q": 2.0 * N * Cq * d * iters * heads,
+           "cluster_k": 2.0 * N * Ck * d * iters * heads, "probe": 0.0, "exact": 0.0,
            "virtual": 0.0}
     for h in range(heads):
         nq = np.bincount(qa[0, h], minlength=Cq).astype(np.float64)
         nk = np.bincount(ka[0, h], minlength=Ck).astype(np.float64)
         s = sel[0, h]
-        out["probe"] += 8.0 * (nq > 0).sum() * N * D          # 2 passes x (logits + values)
-        out["exact"] += 4.0 * D * float((nq[:, None] * nk[None, :])[s].sum())
+        out["probe"] += 8.0 * (nq > 0).sum() * N * d          # 2 passes x (logits + values)
+        out["exact"] += 4.0 * d * float((nq[:, None] * nk[None, :])[s].sum())
         virt = (~s) & (nk[None, :] > 0)
-        out["virtual"] += 4.0 * D * float((nq[:, None] * virt).sum())
+        out["virtual"] += 4.0 * d * float((nq[:, None] * virt).sum())
     return out
 
 
-def run_svgear(args, world, rank, local):
+def run_svgear(args, world, rank, local, d=D):
     import torch
     import linear_attention_video_fwd_b300 as va
     import synth
@@ -422,15 +422,15 @@ def run_svgear(args, world, rank, local):
     dev = torch.device("cuda", local)
     T, H, W, heads, Cq, Ck = SVG["T"], SVG["H"], SVG["W"], SVG["heads"], SVG["Cq"], SVG["Ck"]
     N = T * H * W
-    q, k, v = synth.video_qkv(BATCH, heads, T, H, W, D, seed=SVG["seed"] + rank, dtype="bf16")
+    q, k, v = synth.video_qkv(BATCH, heads, T, H, W, d, seed=SVG["seed"] + rank, dtype="bf16")
     qt, kt, vt = (torch.from_numpy(x).to(dev, torch.bfloat16) for x in (q, k, v))
     qinit = torch.from_numpy(synth.init_indices(BATCH, heads, N, Cq, seed=SVG["seed"])).to(dev)
     kinit = torch.from_numpy(synth.init_indices(BATCH, heads, N, Ck, seed=SVG["seed"],
                                                 tensor=synth.INIT + 1)).to(dev)
     qa = torch.empty((BATCH, heads, N), dtype=torch.int32, device=dev)
     ka = torch.empty_like(qa)
-    qc = torch.empty((BATCH, heads, Cq, D), dtype=torch.float32, device=dev)
-    kc = torch.empty((BATCH, heads, Ck, D), dtype=torch.float32, device=dev)
+    qc = torch.empty((BATCH, heads, Cq, d), dtype=torch.float32, device=dev)
+    kc = torch.empty((BATCH, heads, Ck, d), dtype=torch.float32, device=dev)
     qn = torch.empty((BATCH, heads, Cq), dtype=torch.int32, device=dev)
     kn = torch.empty((BATCH, heads, Ck), dtype=torch.int32, device=dev)
     out = torch.empty_like(qt)
@@ -462,7 +462,7 @@ def run_svgear(args, world, rank, local):
     for _ in range(3):
         call()
     fl = svgear_flops(qa.cpu().numpy(), ka.cpu().numpy(), sel.cpu().numpy().astype(bool), Cq, Ck,
-                      N, SVG["iters"])
+                      N, SVG["iters"], d)
     step_flops = sum(fl.values())
     ms_per_step = total_ms / args.steps
     st = {k2: float(np.median(v2)) for k2, v2 in stage_ms.items()}
@@ -474,7 +474,7 @@ def run_svgear(args, world, rank, local):
     step_tf = step_flops / (ms_per_step * 1e-3) / 1e12
     line = {
         "metric": "SVG-EAR step (k-means Q/K + probe + routing + compensated attention) "
-                  "effective TFLOP/s + ms/step at 32,760 tok",
+                  "effective TFLOP/s + ms/step at 32,760 tok" + ("" if d == D else ", head_dim %d" % d),
         "value": round(world * step_flops * args.steps / (total_ms * 1e-3) / 1e12, 3),
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 3), "higher_is_better": True, "scaling": "weak",
@@ -482,7 +482,7 @@ def run_svgear(args, world, rank, local):
         "data": "synthetic (seeded Fourier-mode Q/K + N(0,0.5^2), V~N(0,1))",
         "config": {"workload": "SVG-EAR-style compensated sparse attention, Wan shape",
                    "B": BATCH, "heads": heads, "grid_THW": [T, H, W], "tokens": N,
-                   "head_dim": D, "Cq": Cq, "Ck": Ck, "kmeans_iters": SVG["iters"],
+                   "head_dim": d, "Cq": Cq, "Ck": Ck, "kmeans_iters": SVG["iters"],
                    "density": SVG["density"],
                    "parallelism": "replicas: one independent workload per GPU"},
         "stages_ms": {k2: round(v2, 3) for k2, v2 in st.items()},
@@ -502,12 +502,12 @@ def run_svgear(args, world, rank, local):
     }
     if rank == 0:
         line.update(svgear_checks(args, world, va, q, k, v, qt, kt, vt, qa, ka, qinit, kinit,
-                                  out, sel, Cq, Ck, N))
+                                  out, sel, Cq, Ck, N, d))
     return line
 
 
 def svgear_checks(args, world, va, q, k, v, qt, kt, vt, qa, ka, qinit, kinit, out, sel, Cq, Ck,
-                  N):
+                  N, d=D):
     """Outside the timed region: the step's output and routing against the
     float64 oracle (given the step's own clusters), the last k-means step
     against the oracle's argmin, and the oracle's compensated attention timed
@@ -517,13 +517,13 @@ def svgear_checks(args, world, va, q, k, v, qt, kt, vt, qa, ka, qinit, kinit, ou
     from oracle import kmeans as KM
     from oracle import svgear as S
     heads = q.shape[1]
-    scale = 1.0 / np.sqrt(D)
+    scale = 1.0 / np.sqrt(d)
     dev = qt.device
     err = torch.empty((BATCH, heads, Cq, Ck), dtype=torch.float32, device=dev)
     sel2 = torch.empty_like(sel)
     out2, _, _ = va.compensate_route(qt, kt, vt, qa, Cq, ka, Ck, SVG["density"], err=err, sel=sel2)
     qa9 = torch.empty_like(qa)
-    qc9 = torch.empty((BATCH, heads, Cq, D), dtype=torch.float32, device=dev)
+    qc9 = torch.empty((BATCH, heads, Cq, d), dtype=torch.float32, device=dev)
     qn9 = torch.empty((BATCH, heads, Cq), dtype=torch.int32, device=dev)
     va.cluster(qt, Cq, SVG["iters"] - 1, qinit, qa9, qc9, qn9)
     if va.device_error() != va.OK:
@@ -552,7 +552,7 @@ def svgear_checks(args, world, va, q, k, v, qt, kt, vt, qa, ka, qinit, kinit, ou
         secs += time.perf_counter() - t0
         for i in rows:
             s_row = sel_h[0, h][qa_h[0, h, i]]
-            oflops += 4.0 * D * (float(s_row[ka_h[0, h]].sum()) + float((~s_row & (nk > 0)).sum()))
+            oflops += 4.0 * d * (float(s_row[ka_h[0, h]].sum()) + float((~s_row & (nk > 0)).sum()))
     rec = parity_record(got, want, "compensated output rows %d x %d heads vs the float64 oracle "
                         "on the step's clusters and selection" % (len(rows), heads))
     near = 0
@@ -850,7 +850,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload",
-                    choices=sorted(WORKLOADS) + ["svgear", "linear", "linear_d64", "mixed",
+                    choices=sorted(WORKLOADS) + ["svgear", "svgear_d64", "linear", "linear_d64", "mixed",
                                                  "mixed_d64", "backward"],
                     default="wan_radial")
     ap.add_argument("--oracle-rows", type=int, default=512,
@@ -866,8 +866,8 @@ def main():
         print("warning: --gpus %d but WORLD_SIZE %d" % (args.gpus, world), file=sys.stderr)
     if args.impl == "reference":
         line = run_reference(args, world, rank)
-    elif args.workload == "svgear":
-        line = run_svgear(args, world, rank, local)
+    elif args.workload in ("svgear", "svgear_d64"):
+        line = run_svgear(args, world, rank, local, 64 if args.workload == "svgear_d64" else D)
     elif args.workload in ("linear", "mixed", "linear_d64", "mixed_d64"):
         line = run_linear(args, world, rank, local, args.workload.startswith("mixed"),
                           64 if args.workload.endswith("_d64") else D)

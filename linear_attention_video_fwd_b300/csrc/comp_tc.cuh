@@ -1,5 +1,5 @@
 // SVG-EAR compensated attention on the 5th-generation tensor cores (bf16,
-// d = 128): one softmax per query over (1) virtual centroid keys kc_c with
+// d = D, 64 or 128): one softmax per query over (1) virtual centroid keys kc_c with
 // logit bias ln n_c and values vc_c for every non-empty key cluster that is
 // not selected for the query's cluster, and (2) the exact keys of the
 // selected key clusters (SVG-EAR, gist.science 2603.08982, technical summary
@@ -35,7 +35,9 @@ constexpr int CT_NM = 4;  // validity-mask ring entries
 // K and V ring depths (two stages each, as in the attention kernel).
 constexpr int CT_NK = 2;
 constexpr int CT_NV = 2;
-constexpr int CT_SMEM_BYTES = 1024 + TC_TILE_BYTES * (2 + CT_NK + CT_NV);
+// Two Q tiles plus the K and V rings, tiles of 128 rows x D dims.
+template <int D>
+constexpr int ct_smem_bytes() { return 1024 + TcDim<D>::kTileBytes * (2 + CT_NK + CT_NV); }
 // Register split of this kernel (launched at TC_LAUNCH_REGS per thread): the
 // producer's slot search needs more than the attention kernel's producer.
 constexpr int CT_REGS_DEC = 72;
@@ -106,7 +108,8 @@ __device__ __forceinline__ int ct_index(int t, int j, int n0, int n1) {
   return j < nmin ? 2 * j + t : 2 * nmin + (j - nmin);
 }
 
-// Softmax of one tile (thread r owns row r of the tile).
+// Softmax of one tile (thread r owns row r of the tile); O has D columns.
+template <int D>
 __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const CompTile& T,
                                            int n0, int n1, int bh, uint32_t tmem,
                                            uint64_t* bars, const float4* bias_ring,
@@ -175,7 +178,7 @@ __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const Co
       if (!ok) break;
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tO + c * 32, v);
         tmem_wait_ld();
@@ -217,9 +220,9 @@ __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const Co
     const float inv = l > 0.f ? 1.f / l : 0.f;
     const bool live = r < T.nrows;
     const int tok = live ? a.qperm[static_cast<long long>(bh) * a.N + T.r0 + r] : 0;
-    __nv_bfloat16* orow = a.out + (static_cast<long long>(bh) * a.N + tok) * 128;
+    __nv_bfloat16* orow = a.out + (static_cast<long long>(bh) * a.N + tok) * D;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
       uint32_t v[32];
       tmem_ld32(tO + c * 32, v);
       tmem_wait_ld();
@@ -257,6 +260,7 @@ __device__ __forceinline__ void ct_locate(const CompArgs& a, int bh, int chunk, 
   T.n = a.nv + (T.nslots + 15) / 16;
 }
 
+template <int D>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     comp_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_kc,
@@ -277,9 +281,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  constexpr int kTile = TcDim<D>::kTileBytes, kHalves = TcDim<D>::kHalves;
   const uint32_t sQ0 = smem_u32(smem);
-  const uint32_t sK0 = sQ0 + 2 * TC_TILE_BYTES;
-  const uint32_t sV0 = sK0 + CT_NK * TC_TILE_BYTES;
+  const uint32_t sK0 = sQ0 + 2 * kTile;
+  const uint32_t sV0 = sK0 + CT_NK * kTile;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(CT_REGS_INC));
     const int tile = (warp - 4) >> 2;
     if (tile == 0 || has1)
-      ct_softmax(a, tile, tile == 0 ? T0 : T1, n0, n1, bh, tmem, bars, bias_ring, abort_p);
+      ct_softmax<D>(a, tile, tile == 0 ? T0 : T1, n0, n1, bh, tmem, bars, bias_ring, abort_p);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(CT_REGS_DEC));
     if (warp == 0 || warp == 2) {
@@ -343,14 +348,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tma_prefetch_desc(&map_q);
           tma_prefetch_desc(&map_kc);
           for (int i = 0; i < CT_NBOX; ++i) tma_prefetch_desc(&maps.k[i]);
-          mbar_arrive_expect_tx(bar(CB_Q_FULL + 0), TC_TILE_BYTES);
-          tma_load_3d(sQ0, &map_q, bar(CB_Q_FULL + 0), 0, T0.r0, bh);
-          tma_load_3d(sQ0 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 0), 64, T0.r0, bh);
+          mbar_arrive_expect_tx(bar(CB_Q_FULL + 0), kTile);
+          for (int h = 0; h < kHalves; ++h)
+            tma_load_3d(sQ0 + h * TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 0), 64 * h, T0.r0, bh);
           if (has1) {
-            const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
-            mbar_arrive_expect_tx(bar(CB_Q_FULL + 1), TC_TILE_BYTES);
-            tma_load_3d(sQ1, &map_q, bar(CB_Q_FULL + 1), 0, T1.r0, bh);
-            tma_load_3d(sQ1 + TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 1), 64, T1.r0, bh);
+            const uint32_t sQ1 = sQ0 + kTile;
+            mbar_arrive_expect_tx(bar(CB_Q_FULL + 1), kTile);
+            for (int h = 0; h < kHalves; ++h)
+              tma_load_3d(sQ1 + h * TC_HALF_BYTES, &map_q, bar(CB_Q_FULL + 1), 64 * h, T1.r0, bh);
           }
         } else {
           tma_prefetch_desc(&map_vc);
@@ -381,7 +386,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         int t, j;
         ct_entry(u, n0, n1, t, j);
         const int st = u % nst;
-        const uint32_t dst = s0 + st * TC_TILE_BYTES;
+        const uint32_t dst = s0 + st * kTile;
         // slot of this lane (exact tiles): source row and valid row count,
         // from the slot table (16 slots per exact tile, padding slots valid 0)
         const int sd = sd_next;
@@ -391,13 +396,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (lane == 0) {
           if (u >= nst)
             ok = mbar_wait_bounded(bar(b_empty + st), ((u / nst) & 1) ^ 1, lim, abort_p);
-          if (ok) mbar_arrive_expect_tx(bar(b_full + st), TC_TILE_BYTES);
+          if (ok) mbar_arrive_expect_tx(bar(b_full + st), kTile);
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         if (j < a.nv) {
           if (lane == 0) {
-            tma_load_3d(dst, map_c, bar(b_full + st), 0, j * 128, bh);
-            tma_load_3d(dst + TC_HALF_BYTES, map_c, bar(b_full + st), 64, j * 128, bh);
+            for (int h = 0; h < kHalves; ++h)
+              tma_load_3d(dst + h * TC_HALF_BYTES, map_c, bar(b_full + st), 64 * h, j * 128, bh);
           }
         } else {
           // Runs of slots with contiguous source rows (slot l continues slot
@@ -420,9 +425,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               at += 1 << l2;
             }
             if (lg >= 0) {
-              tma_load_3d(dst + lane * 1024, map_slots + lg, bar(b_full + st), 0, src, bh);
-              tma_load_3d(dst + TC_HALF_BYTES + lane * 1024, map_slots + lg, bar(b_full + st), 64,
-                          src, bh);
+              for (int h = 0; h < kHalves; ++h)
+                tma_load_3d(dst + h * TC_HALF_BYTES + lane * 1024, map_slots + lg,
+                            bar(b_full + st), 64 * h, src, bh);
             }
           }
         }
@@ -468,7 +473,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp == 1) {
       // --------------------------------------------------------------- MMA --
       if (lane == 0) {
-        const uint32_t sQ1 = sQ0 + TC_TILE_BYTES;
+        const uint32_t sQ1 = sQ0 + kTile;
         bool ok = mbar_wait_bounded(bar(CB_Q_FULL + 0), 0, lim, abort_p);
         if (ok && has1) ok = mbar_wait_bounded(bar(CB_Q_FULL + 1), 0, lim, abort_p);
         // Per-tile state in scalars selected at compile time: an array indexed
@@ -494,8 +499,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const int sv = pu % CT_NV;
           if (!mbar_wait_bounded(bar(CB_V_FULL + sv), (pu / CT_NV) & 1, lim, abort_p)) return false;
           tc_fence_after();
-          tc_pv_group<128>(tmem + t * 256 + 128, tmem + t * 256,
-                           v_lo + sv * (TC_TILE_BYTES >> 4), v_hi, jj > 0);
+          tc_pv_group<D>(tmem + t * 256 + 128, tmem + t * 256, v_lo + sv * (kTile >> 4), v_hi,
+                         jj > 0);
           umma_commit(bar(CB_O_DONE + t));
           umma_commit(bar(CB_V_EMPTY + sv));  // every entry is read by one tile only
           pend = -1;
@@ -507,9 +512,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (!mbar_wait_bounded(bar(CB_K_FULL + sk), (u / CT_NK) & 1, lim, abort_p)) return false;
           if ((t == 0 ? pend0 : pend1) >= 0 && !issue_pv(tile)) return false;
           tc_fence_after();
-          tc_qk_group<128>(tmem + t * 256,
-                           static_cast<uint32_t>(t == 0 ? dq0 : dq1),
-                           k_lo + sk * (TC_TILE_BYTES >> 4), k_hi);
+          tc_qk_group<D>(tmem + t * 256, static_cast<uint32_t>(t == 0 ? dq0 : dq1),
+                         k_lo + sk * (kTile >> 4), k_hi);
           umma_commit(bar(CB_S_FULL + t));
           umma_commit(bar(CB_K_EMPTY + sk));
           (t == 0 ? pend0 : pend1) = u;
@@ -543,18 +547,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 // ------------------------------------------------------------ preparation --
 
-// dst[bh][t] = src[bh][perm[bh][t]] for bf16 rows of 128 (one half-warp per row).
+// dst[bh][t] = src[bh][perm[bh][t]] for bf16 rows of D (D / 8 lanes per row,
+// 16 bytes each). Grid (ceil(N / GR_ROWS<D>), BH), 128 threads.
+template <int D>
+constexpr int GR_ROWS = 128 / (D / 8);
+template <int D>
 __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ src,
                                    const int* __restrict__ perm, int N,
                                    __nv_bfloat16* __restrict__ dst) {
+  constexpr int kLanes = D / 8, kRows = GR_ROWS<D>;
   const int bh = blockIdx.y;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 4);
-  const int c = threadIdx.x & 15;
+  const int t = blockIdx.x * kRows + threadIdx.x / kLanes;
+  const int c = threadIdx.x % kLanes;
   if (t >= N) return;
   const long long base = static_cast<long long>(bh) * N;
   const int row = perm[base + t];
-  const uint4* s = reinterpret_cast<const uint4*>(src + (base + row) * 128);
-  uint4* d = reinterpret_cast<uint4*>(dst + (base + t) * 128);
+  const uint4* s = reinterpret_cast<const uint4*>(src + (base + row) * D);
+  uint4* d = reinterpret_cast<uint4*>(dst + (base + t) * D);
   d[c] = s[c];
 }
 

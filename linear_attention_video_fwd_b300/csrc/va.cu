@@ -1280,9 +1280,10 @@ VA_EXPORT int va_cluster_from(const void* x, const float* centroid_init, int B, 
 
 namespace {
 
-// Compensated attention on the tensor cores (bf16, d = 128): cluster-ordered
+// Compensated attention on the tensor cores (bf16, d = D): cluster-ordered
 // copies of Q, K, V, bf16 centroids, per-cluster slot prefixes and virtual
 // biases, then comp_tc_kernel over pairs of 128-row query chunks.
+template <int D>
 int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
                       int Cq, int Ck, int BH, int N, const int* nq, const int* qoff,
                       const int* qperm, const int* nk, const int* koff, const int* kperm,
@@ -1295,11 +1296,12 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   if (st) return st;
   st = device_once(once, dev, [] {
     cudaFuncAttributes fa;
-    int r = cuda_status(cudaFuncGetAttributes(&fa, va::comp_tc_kernel));
+    int r = cuda_status(cudaFuncGetAttributes(&fa, va::comp_tc_kernel<D>));
     if (r) return r;
     if (fa.numRegs != va::TC_LAUNCH_REGS) return VA_ERR_UNSUPPORTED;
-    return cuda_status(cudaFuncSetAttribute(
-        va::comp_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, va::CT_SMEM_BYTES));
+    return cuda_status(cudaFuncSetAttribute(va::comp_tc_kernel<D>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            va::ct_smem_bytes<D>()));
   });
   if (st) return st;
   const size_t bh = static_cast<size_t>(BH);
@@ -1307,18 +1309,18 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   __nv_bfloat16 *qs, *ks, *vs, *kcb, *vcb;
   int *selbox, *nch, *choff, *chfill;
   float* vbias;
-  if ((st = scratch.alloc(&qs, bh * N * 128)) || (st = scratch.alloc(&ks, bh * N * 128)) ||
-      (st = scratch.alloc(&vs, bh * N * 128)) || (st = scratch.alloc(&kcb, bh * Ck * 128)) ||
-      (st = scratch.alloc(&vcb, bh * Ck * 128)) ||
+  if ((st = scratch.alloc(&qs, bh * N * D)) || (st = scratch.alloc(&ks, bh * N * D)) ||
+      (st = scratch.alloc(&vs, bh * N * D)) || (st = scratch.alloc(&kcb, bh * Ck * D)) ||
+      (st = scratch.alloc(&vcb, bh * Ck * D)) ||
       (st = scratch.alloc(&selbox, bh * Cq * (Ck + 1))) ||
       (st = scratch.alloc(&vbias, bh * Cq * nv * 128)) || (st = scratch.alloc(&nch, bh * Cq)) ||
       (st = scratch.alloc(&choff, bh * (Cq + 1))) || (st = scratch.alloc(&chfill, bh * Cq)))
     return st;
-  const dim3 gg((N + 7) / 8, BH);
-  va::gather_rows_kernel<<<gg, 128, 0, s>>>(q, qperm, N, qs);
-  va::gather_rows_kernel<<<gg, 128, 0, s>>>(k, kperm, N, ks);
-  va::gather_rows_kernel<<<gg, 128, 0, s>>>(v, kperm, N, vs);
-  const long long ncen = static_cast<long long>(bh) * Ck * 128;
+  const dim3 gg((N + va::GR_ROWS<D> - 1) / va::GR_ROWS<D>, BH);
+  va::gather_rows_kernel<D><<<gg, 128, 0, s>>>(q, qperm, N, qs);
+  va::gather_rows_kernel<D><<<gg, 128, 0, s>>>(k, kperm, N, ks);
+  va::gather_rows_kernel<D><<<gg, 128, 0, s>>>(v, kperm, N, vs);
+  const long long ncen = static_cast<long long>(bh) * Ck * D;
   va::f32_to_bf16_kernel<<<static_cast<unsigned>((ncen + 255) / 256), 256, 0, s>>>(kc, ncen, kcb);
   va::f32_to_bf16_kernel<<<static_cast<unsigned>((ncen + 255) / 256), 256, 0, s>>>(vc, ncen, vcb);
   va::comp_prep_kernel<<<dim3((Cq + 7) / 8, BH), 256, 0, s>>>(nk, seln, selc, sel, Cq, Ck, nv,
@@ -1346,13 +1348,13 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   if ((st = launch_status())) return st;
   CUtensorMap mq, mkc, mvc;
   va::CompSlotMaps slot_maps;
-  if ((st = encode_bf16_rows_box(&mq, qs, BH, N, 128, 128)) ||
-      (st = encode_bf16_rows_box(&mkc, kcb, BH, Ck, 128, 128)) ||
-      (st = encode_bf16_rows_box(&mvc, vcb, BH, Ck, 128, 128)))
+  if ((st = encode_bf16_rows_box(&mq, qs, BH, N, D, 128)) ||
+      (st = encode_bf16_rows_box(&mkc, kcb, BH, Ck, D, 128)) ||
+      (st = encode_bf16_rows_box(&mvc, vcb, BH, Ck, D, 128)))
     return st;
   for (int i = 0; i < va::CT_NBOX; ++i)
-    if ((st = encode_bf16_rows_box(&slot_maps.k[i], ks, BH, N, 128, 8 << i)) ||
-        (st = encode_bf16_rows_box(&slot_maps.v[i], vs, BH, N, 128, 8 << i)))
+    if ((st = encode_bf16_rows_box(&slot_maps.k[i], ks, BH, N, D, 8 << i)) ||
+        (st = encode_bf16_rows_box(&slot_maps.v[i], vs, BH, N, D, 8 << i)))
       return st;
   va::CompArgs a;
   a.choff = choff;
@@ -1375,8 +1377,8 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit = g_wait_limit;
   const int max_chunks = (N + 127) / 128 + Cq;
-  va::comp_tc_kernel<<<dim3((max_chunks + 1) / 2, BH), va::TC_THREADS, va::CT_SMEM_BYTES, s>>>(
-      mq, mkc, mvc, slot_maps, a);
+  va::comp_tc_kernel<D><<<dim3((max_chunks + 1) / 2, BH), va::TC_THREADS, va::ct_smem_bytes<D>(),
+                          s>>>(mq, mkc, mvc, slot_maps, a);
   return launch_status();
 }
 
@@ -1525,7 +1527,7 @@ int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int C
   if ((st = cluster_lists(qassign, BH, N, Cq, nq, qoff, qfill, qperm, s)) ||
       (st = cluster_lists(kassign, BH, N, Ck, nk, koff, kfill, kperm, s)))
     return st;
-  if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
     // balanced exact sums over the cluster-ordered members, then the means
     unsigned long long* sums;
     const size_t cmax = static_cast<size_t>(Cq > Ck ? Cq : Ck);
@@ -1585,8 +1587,8 @@ int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int C
   va::route_mark_kernel<<<dim3(Cq, BH), 256, 0, s>>>(err, nq, nk, Cq, Ck, cut, sel, seln, selc);
   if ((st = launch_status())) return st;
 
-  if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128) {
-    return comp_tensor_cores(q, k, v, Cq, Ck, BH, N, nq, qoff, qperm, nk, koff, kperm, kc, vc,
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    return comp_tensor_cores<D>(q, k, v, Cq, Ck, BH, N, nq, qoff, qperm, nk, koff, kperm, kc, vc,
                              seln, selc, sel, scale, out, scratch, s);
   }
 

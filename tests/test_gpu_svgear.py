@@ -156,6 +156,10 @@ ROUTE_CASES = [
     (2500, 128, 130, 150, 0.1, "bf16", True),
     # clusters longer than a 64-key tile
     (1500, 128, 3, 7, 0.3, "bf16", False),
+    # head_dim 64 on the tensor-core compensated attention
+    (331, 64, 5, 17, 0.2, "bf16", True),
+    (2500, 64, 130, 150, 0.1, "bf16", True),
+    (1500, 64, 3, 7, 0.3, "bf16", False),
 ]
 
 
