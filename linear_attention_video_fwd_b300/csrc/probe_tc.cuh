@@ -1,6 +1,7 @@
 // Error probe of SVG-EAR (gist.science 2603.08982, technical summary sec. 2,
 // idea 2: query-cluster centroids as proxies, streamed over the keys without
-// storing logits) on the 5th-generation tensor cores, bf16 K/V, head_dim 128.
+// storing logits) on the 5th-generation tensor cores, bf16 K/V, head_dim D
+// (64 or 128).
 //
 // Per (batch*head, proxy tile of 128 query clusters, key split):
 //   pass 1  sweep A: l = qc . k for every key of the split, row max m2 (log2
@@ -42,6 +43,8 @@
 // VA_ERR_TIMEOUT, drains its copies and MMAs and frees its TMEM.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace va {
@@ -50,12 +53,19 @@ constexpr int PT_KT = 64;    // keys per tile (4 groups of 16)
 constexpr int PT_NK = 3;     // K ring stages
 constexpr int PT_NV = 3;     // V ring stages
 constexpr int PT_THREADS = 384;
-constexpr int PT_QP_BYTES = 128 * 128 * 2;   // one bf16 piece of a 128-proxy tile
-constexpr int PT_QP_HALF = PT_QP_BYTES / 2;  // 128 rows x 64 dims
-constexpr int PT_KV_BYTES = PT_KT * 128 * 2;  // one 64-key tile of K or V
-constexpr int PT_KV_HALF = PT_KV_BYTES / 2;   // 64 rows x 64 dims
-constexpr int PT_SMEM_BYTES = 1024 + 3 * PT_QP_BYTES + (PT_NK + PT_NV) * PT_KV_BYTES;
-constexpr int PT_ROW = 130;  // {m2, Z, O[128]} per proxy
+constexpr int PT_QP_HALF = 128 * 64 * 2;    // 128 proxy rows x 64 dims (one TMA box)
+constexpr int PT_KV_HALF = PT_KT * 64 * 2;   // 64 key rows x 64 dims
+
+// Sizes that depend on the head dimension D.
+template <int D>
+struct PtDim {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQP = 128 * D * 2;     // one bf16 piece of a 128-proxy tile
+  static constexpr int kKV = PT_KT * D * 2;   // one 64-key tile of K or V
+  static constexpr int kSmem = 1024 + 3 * kQP + (PT_NK + PT_NV) * kKV;
+  static constexpr int kRow = 2 + D;          // {m2, Z, O[D]} per proxy
+};
 constexpr int PT_G_FIRST = 1 << 5;
 constexpr int PT_G_LAST = 1 << 6;
 constexpr uint32_t PT_STAGE_COLS = 128;  // S of the hi piece, S of mid + lo, then P
@@ -73,9 +83,9 @@ struct ProbeArgs {
                       // cluster << 8
   const int* kpoff;   // [BH][Ck + 1] first padded row of each key cluster
   const int* nq;      // [BH][Cq] query-cluster sizes
-  const float* mzo;   // pass 2: [BH][Cq][PT_ROW] merged {m2, Z, O / Z}
-  const float* vc;    // pass 2: [BH][Ck][128] value means
-  float* part;        // pass 1: [BH][Cq][NS][PT_ROW] split partials {m2, Z, O}
+  const float* mzo;   // pass 2: [BH][Cq][D + 2] merged {m2, Z, O / Z}
+  const float* vc;    // pass 2: [BH][Ck][D] value means
+  float* part;        // pass 1: [BH][Cq][NS][D + 2] split partials {m2, Z, O}
   float* err;         // pass 2: [BH][Cq][Ck]
   int Cq, Ck, Cqp, G, NS;
   float sl2;          // scale * log2(e)
@@ -123,7 +133,7 @@ __device__ __forceinline__ void pt_split3(float x0, float x1, uint32_t& hi, uint
 }
 
 // Softmax warpgroup: thread r owns proxy row r of the tile.
-template <int PASS>
+template <int PASS, int D>
 __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, int split,
                                            int g_lo, int g_hi, int nt, uint32_t tmem,
                                            uint64_t* bars, float (*zc_s)[128],
@@ -141,7 +151,7 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
   float m2 = -INFINITY, Z = 0.f, zc = 0.f, ls = 0.f, vc_pre = 0.f;
   int nv = 0, cur_c = 0;
   if constexpr (PASS == 2)
-    m2 = a.mzo[(static_cast<long long>(bh) * a.Cq + min(p, a.Cq - 1)) * PT_ROW];
+    m2 = a.mzo[(static_cast<long long>(bh) * a.Cq + min(p, a.Cq - 1)) * PtDim<D>::kRow];
   int ci = -1;
   bool ok = true;
   int mn[4] = {0, 0, 0, 0};  // group metadata, read one tile ahead
@@ -222,8 +232,9 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
           ls = 0.f;
           nv = 0;
           cur_c = mg >> 8;
-          // value mean of the cluster, read now and published at its end
-          vc_pre = a.vc[(static_cast<long long>(bh) * a.Ck + cur_c) * 128 + r];
+          // value mean of the cluster (thread r holds dim r < D), read now and
+          // published at its end
+          vc_pre = r < D ? a.vc[(static_cast<long long>(bh) * a.Ck + cur_c) * D + r] : 0.f;
         }
         float gs = 0.f;
 #pragma unroll
@@ -268,14 +279,14 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
     // split partial {m2, Z, O} of this row (O unnormalised); a split without
     // keys reports m2 = -inf, Z = 0
     float* out = a.part + ((static_cast<long long>(bh) * a.Cq + min(p, a.Cq - 1)) * a.NS + split) *
-                              PT_ROW;
+                              PtDim<D>::kRow;
     const bool mine = p < a.Cq;
     if (nt > 0 && ok)
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&bars[PB_OD]), 0, lim, abort_p));
     if (nt > 0 && ok) {
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tmem + PT_T_ACC + c * 32 + lane_off, v);
         tmem_wait_ld();
@@ -293,7 +304,7 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
     } else if (nt == 0 && mine) {
       out[0] = -INFINITY;
       out[1] = 0.f;
-      for (int i = 0; i < 128; i += 2) *reinterpret_cast<float2*>(out + 2 + i) = make_float2(0.f, 0.f);
+      for (int i = 0; i < D; i += 2) *reinterpret_cast<float2*>(out + 2 + i) = make_float2(0.f, 0.f);
     }
   }
 }
@@ -302,6 +313,7 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
 // publishes each finished cluster through a slot of shared memory (its id,
 // Zc and w_c per row, and its value mean), then a sentinel id -1 after the
 // last one.
+template <int D>
 __device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, uint32_t tmem,
                                             uint64_t* bars, const float (*zc_s)[128],
                                             const float (*w_s)[128], const float (*vc_s)[128],
@@ -312,11 +324,11 @@ __device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, 
   const int pr = min(p, a.Cq - 1);
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const long long lim = a.wait_limit;
-  const float* mz = a.mzo + (static_cast<long long>(bh) * a.Cq + pr) * PT_ROW;
+  const float* mz = a.mzo + (static_cast<long long>(bh) * a.Cq + pr) * PtDim<D>::kRow;
   const float invZ = 1.f / mz[1];
-  float O[128];
+  float O[D];
 #pragma unroll
-  for (int i = 0; i < 128; i += 2) {
+  for (int i = 0; i < D; i += 2) {
     const float2 t = *reinterpret_cast<const float2*>(mz + 2 + i);
     O[i] = t.x;
     O[i + 1] = t.y;
@@ -341,7 +353,7 @@ __device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, 
     const uint32_t tE = tmem + PT_T_ACC + slot * 128 + lane_off;
     float n2 = 0.f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < D / 32; ++q) {
       uint32_t v[32];
       tmem_ld32(tE + q * 32, v);
       tmem_wait_ld();
@@ -363,7 +375,7 @@ __device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, 
   }
 }
 
-template <int PASS>
+template <int PASS, int D>
 __global__ void __launch_bounds__(PT_THREADS, 1)
     probe_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
@@ -379,9 +391,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
+  using Pd = PtDim<D>;
   const uint32_t sQ = smem_u32(smem);
-  const uint32_t sK0 = sQ + 3 * PT_QP_BYTES;
-  const uint32_t sV0 = sK0 + PT_NK * PT_KV_BYTES;
+  const uint32_t sK0 = sQ + 3 * Pd::kQP;
+  const uint32_t sV0 = sK0 + PT_NK * Pd::kKV;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, pt = blockIdx.y, bh = blockIdx.z;
   const int* kp = a.kpoff + static_cast<long long>(bh) * (a.Ck + 1);
@@ -429,10 +442,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   if (warp >= 4) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(PT_REGS_INC));
     if (warp < 8) {
-      pt_softmax<PASS>(a, bh, pt, split, g_lo, g_hi, nt, tmem, bars, zc_s, w_s, vc_s, cid_s,
-                       abort_p);
+      pt_softmax<PASS, D>(a, bh, pt, split, g_lo, g_hi, nt, tmem, bars, zc_s, w_s, vc_s, cid_s,
+                          abort_p);
     } else if constexpr (PASS == 2) {
-      pt_residual(a, bh, pt, tmem, bars, zc_s, w_s, vc_s, cid_s, abort_p);
+      pt_residual<D>(a, bh, pt, tmem, bars, zc_s, w_s, vc_s, cid_s, abort_p);
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(PT_REGS_DEC));
@@ -442,10 +455,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
       tma_prefetch_desc(&map_q);
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
-      mbar_arrive_expect_tx(bar(PB_Q), 3 * PT_QP_BYTES);
+      mbar_arrive_expect_tx(bar(PB_Q), 3 * Pd::kQP);
       for (int i = 0; i < 3; ++i)
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sQ + i * PT_QP_BYTES + h * PT_QP_HALF, &map_q, bar(PB_Q), 64 * h,
+        for (int h = 0; h < Pd::kHalves; ++h)
+          tma_load_3d(sQ + i * Pd::kQP + h * PT_QP_HALF, &map_q, bar(PB_Q), 64 * h,
                       i * a.Cqp + pt * 128, bh);
       const int row0 = 16 * g_lo;
       int issued_k = 0, issued_v = 0;
@@ -455,20 +468,20 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         if (u >= PT_NK &&
             !mbar_wait_bounded(bar(PB_KE + sk), ((u / PT_NK) & 1) ^ 1, lim, abort_p))
           break;
-        mbar_arrive_expect_tx(bar(PB_KF + sk), PT_KV_BYTES);
-        tma_load_3d(sK0 + sk * PT_KV_BYTES, &map_k, bar(PB_KF + sk), 0, row0 + PT_KT * t, bh);
-        tma_load_3d(sK0 + sk * PT_KV_BYTES + PT_KV_HALF, &map_k, bar(PB_KF + sk), 64,
-                    row0 + PT_KT * t, bh);
+        mbar_arrive_expect_tx(bar(PB_KF + sk), Pd::kKV);
+        for (int h = 0; h < Pd::kHalves; ++h)
+          tma_load_3d(sK0 + sk * Pd::kKV + h * PT_KV_HALF, &map_k, bar(PB_KF + sk), 64 * h,
+                      row0 + PT_KT * t, bh);
         issued_k = u + 1;
         if (u >= nval0) {
           const int vu = u - nval0, sv = vu % PT_NV;
           if (vu >= PT_NV &&
               !mbar_wait_bounded(bar(PB_VE + sv), ((vu / PT_NV) & 1) ^ 1, lim, abort_p))
             break;
-          mbar_arrive_expect_tx(bar(PB_VF + sv), PT_KV_BYTES);
-          tma_load_3d(sV0 + sv * PT_KV_BYTES, &map_v, bar(PB_VF + sv), 0, row0 + PT_KT * t, bh);
-          tma_load_3d(sV0 + sv * PT_KV_BYTES + PT_KV_HALF, &map_v, bar(PB_VF + sv), 64,
-                      row0 + PT_KT * t, bh);
+          mbar_arrive_expect_tx(bar(PB_VF + sv), Pd::kKV);
+          for (int h = 0; h < Pd::kHalves; ++h)
+            tma_load_3d(sV0 + sv * Pd::kKV + h * PT_KV_HALF, &map_v, bar(PB_VF + sv), 64 * h,
+                        row0 + PT_KT * t, bh);
           issued_v = vu + 1;
         }
       }
@@ -490,7 +503,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
     // ----------------------------------------------------------------- MMA --
     if (lane == 0 && ne > 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(128, PT_KT, 0, 0);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, 128, 0, 1);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, 0, 1);
       const int* gm = a.gmeta + static_cast<long long>(bh) * a.G;
       bool ok = mbar_wait_bounded(bar(PB_Q), 0, lim, abort_p);
       int ci = -1;
@@ -503,7 +516,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         if (!mbar_wait_bounded(bar(PB_VF + sv), (vu / PT_NV) & 1, lim, abort_p)) return false;
         tc_fence_after();
         const uint32_t tP = tmem + b * PT_STAGE_COLS;
-        const uint32_t sV = sV0 + sv * PT_KV_BYTES;
+        const uint32_t sV = sV0 + sv * Pd::kKV;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const int mg = m4[g];
@@ -546,13 +559,13 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
         const int sk = u % PT_NK, b = u & 1;
         if (!(ok = mbar_wait_bounded(bar(PB_KF + sk), (u / PT_NK) & 1, lim, abort_p))) break;
         tc_fence_after();
-        const uint32_t sK = sK0 + sk * PT_KV_BYTES;
+        const uint32_t sK = sK0 + sk * Pd::kKV;
 #pragma unroll
         for (int i = 0; i < 3; ++i)
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
+          for (int k = 0; k < D / 16; ++k)
             umma_ss(tmem + b * PT_STAGE_COLS + (i > 0 ? 64 : 0),
-                    sw128_desc(sQ + i * PT_QP_BYTES + (k >> 2) * PT_QP_HALF + (k & 3) * 32, 16, 1024),
+                    sw128_desc(sQ + i * Pd::kQP + (k >> 2) * PT_QP_HALF + (k & 3) * 32, 16, 1024),
                     sw128_desc(sK + (k >> 2) * PT_KV_HALF + (k & 3) * 32, 16, 1024), id_qk,
                     (i == 2 || k > 0) ? 1u : 0u);
         umma_commit(bar(PB_SF + b));
@@ -578,23 +591,25 @@ __global__ void __launch_bounds__(PT_THREADS, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// mzo[bh][p] = {m2, Z, O / Z} from the NS split partials. Grid (Cq, BH), 128
+// mzo[bh][p] = {m2, Z, O / Z} from the NS split partials. Grid (Cq, BH), D
 // threads (one per dim).
+template <int D>
 __global__ void probe_tc_combine_kernel(const float* __restrict__ part, int Cq, int NS,
                                         float* __restrict__ mzo) {
+  constexpr int kRow = PtDim<D>::kRow;
   const int bh = blockIdx.y, p = blockIdx.x, d = threadIdx.x;
-  const float* pp = part + (static_cast<long long>(bh) * Cq + p) * NS * PT_ROW;
+  const float* pp = part + (static_cast<long long>(bh) * Cq + p) * NS * kRow;
   float m = -INFINITY;
-  for (int s = 0; s < NS; ++s) m = fmaxf(m, pp[s * PT_ROW]);
+  for (int s = 0; s < NS; ++s) m = fmaxf(m, pp[s * kRow]);
   float Z = 0.f, O = 0.f;
   for (int s = 0; s < NS; ++s) {
-    const float ms = pp[s * PT_ROW];
+    const float ms = pp[s * kRow];
     if (ms == -INFINITY) continue;
     const float wgt = exp2f(ms - m);
-    Z = fmaf(pp[s * PT_ROW + 1], wgt, Z);
-    O = fmaf(pp[s * PT_ROW + 2 + d], wgt, O);
+    Z = fmaf(pp[s * kRow + 1], wgt, Z);
+    O = fmaf(pp[s * kRow + 2 + d], wgt, O);
   }
-  float* out = mzo + (static_cast<long long>(bh) * Cq + p) * PT_ROW;
+  float* out = mzo + (static_cast<long long>(bh) * Cq + p) * kRow;
   if (d == 0) {
     out[0] = m;
     out[1] = Z;
@@ -610,10 +625,12 @@ __global__ void pad16_count_kernel(const int* __restrict__ nk, int n, int* __res
   if (i < n) cnt16[i] = (nk[i] + 15) & ~15;
 }
 
-// Padded cluster-ordered copies of K and V ([BH][Npad][128]) and the group
+// Padded cluster-ordered copies of K and V ([BH][Npad][D]) and the group
 // metadata; block (c, bh) copies cluster c (its members, then zero rows up to
 // a multiple of 16); block (Ck, bh) zeroes the 64 rows after the last cluster,
-// which a tile may read past its split. 128 threads, one warp per row.
+// which a tile may read past its split. 128 threads, one warp per row (D / 32
+// values per lane).
+template <int D>
 __global__ void pad_gather_kernel(const __nv_bfloat16* __restrict__ k,
                                   const __nv_bfloat16* __restrict__ v, int N, int Ck,
                                   const int* __restrict__ nk, const int* __restrict__ koff,
@@ -632,15 +649,16 @@ __global__ void pad_gather_kernel(const __nv_bfloat16* __restrict__ k,
   const int src0 = c < Ck ? koff[static_cast<long long>(bh) * (Ck + 1) + c] : 0;
   for (int row = warp; row < rows; row += 4) {
     const int j = row < n ? kperm[static_cast<long long>(bh) * N + src0 + row] : -1;
-    uint2 kv = make_uint2(0, 0), vv = make_uint2(0, 0);
+    using W = typename std::conditional<D == 128, uint2, uint32_t>::type;  // D / 32 bf16
+    W kv{}, vv{};
     if (j >= 0) {
-      const long long src = (static_cast<long long>(bh) * N + j) * 128 + lane * 4;
-      kv = *reinterpret_cast<const uint2*>(k + src);
-      vv = *reinterpret_cast<const uint2*>(v + src);
+      const long long src = (static_cast<long long>(bh) * N + j) * D + lane * (D / 32);
+      kv = *reinterpret_cast<const W*>(k + src);
+      vv = *reinterpret_cast<const W*>(v + src);
     }
-    const long long dst = (base + row) * 128 + lane * 4;
-    *reinterpret_cast<uint2*>(kpad + dst) = kv;
-    *reinterpret_cast<uint2*>(vpad + dst) = vv;
+    const long long dst = (base + row) * D + lane * (D / 32);
+    *reinterpret_cast<W*>(kpad + dst) = kv;
+    *reinterpret_cast<W*>(vpad + dst) = vv;
   }
   if (c < Ck) {
     const int ng = rows >> 4;
@@ -653,17 +671,18 @@ __global__ void pad_gather_kernel(const __nv_bfloat16* __restrict__ k,
 }
 
 // Three bf16 pieces of the proxies: qp[bh][i][p][d], p < Cqp (rows >= Cq
-// zero). Grid (Cqp, BH), 128 threads.
+// zero). Grid (Cqp, BH), D threads.
+template <int D>
 __global__ void proxy_pieces_kernel(const float* __restrict__ qc, int Cq, int Cqp,
                                     __nv_bfloat16* __restrict__ qp) {
   const int p = blockIdx.x, bh = blockIdx.y, d = threadIdx.x;
-  const float x = p < Cq ? qc[(static_cast<long long>(bh) * Cq + p) * 128 + d] : 0.f;
+  const float x = p < Cq ? qc[(static_cast<long long>(bh) * Cq + p) * D + d] : 0.f;
   const __nv_bfloat16 hi = __float2bfloat16_rn(x);
   const float r1 = x - __bfloat162float(hi);
   const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
   const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
-  const long long o = (static_cast<long long>(bh) * 3 * Cqp + p) * 128 + d;
-  const long long piece = static_cast<long long>(Cqp) * 128;
+  const long long o = (static_cast<long long>(bh) * 3 * Cqp + p) * D + d;
+  const long long piece = static_cast<long long>(Cqp) * D;
   qp[o] = hi;
   qp[o + piece] = mid;
   qp[o + 2 * piece] = lo;

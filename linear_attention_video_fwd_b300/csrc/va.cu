@@ -1382,9 +1382,10 @@ int comp_tensor_cores(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv
   return launch_status();
 }
 
-// Error probe on the tensor cores (bf16, d = 128): padded cluster-ordered
+// Error probe on the tensor cores (bf16, d = D): padded cluster-ordered
 // K/V with group metadata, three bf16 pieces of the proxies, then pass 1
 // (split partials of m2, Z, O), their merge and pass 2 (err).
+template <int D>
 int probe_tensor_cores(const __nv_bfloat16* k, const __nv_bfloat16* v, int Cq, int Ck, int BH,
                        int N, const int* nq, const int* nk, const int* koff, const int* kperm,
                        const float* qc, const float* vc, float scale, float* err,
@@ -1397,17 +1398,17 @@ int probe_tensor_cores(const __nv_bfloat16* k, const __nv_bfloat16* v, int Cq, i
   st = device_once(once, dev, [dev] {
     cudaFuncAttributes fa1, fa2;
     int r;
-    if ((r = cuda_status(cudaFuncGetAttributes(&fa1, va::probe_tc_kernel<1>))) ||
-        (r = cuda_status(cudaFuncGetAttributes(&fa2, va::probe_tc_kernel<2>))))
+    if ((r = cuda_status(cudaFuncGetAttributes(&fa1, va::probe_tc_kernel<1, D>))) ||
+        (r = cuda_status(cudaFuncGetAttributes(&fa2, va::probe_tc_kernel<2, D>))))
       return r;
     if (fa1.numRegs != va::PT_LAUNCH_REGS || fa2.numRegs != va::PT_LAUNCH_REGS)
       return VA_ERR_UNSUPPORTED;
-    if ((r = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<1>,
+    if ((r = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<1, D>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              va::PT_SMEM_BYTES))) ||
-        (r = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<2>,
+                                              va::PtDim<D>::kSmem))) ||
+        (r = cuda_status(cudaFuncSetAttribute(va::probe_tc_kernel<2, D>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              va::PT_SMEM_BYTES))) ||
+                                              va::PtDim<D>::kSmem))) ||
         (r = cuda_status(cudaDeviceGetAttribute(&num_sms[dev], cudaDevAttrMultiProcessorCount,
                                                 dev))))
       return r;
@@ -1431,24 +1432,24 @@ int probe_tensor_cores(const __nv_bfloat16* k, const __nv_bfloat16* v, int Cq, i
   if ((st = scratch.alloc(&cnt16, bh * Ck)) || (st = scratch.alloc(&kpoff, bh * (Ck + 1))) ||
       (st = scratch.alloc(&kpfill, bh * Ck)) ||
       (st = scratch.alloc(&gmeta, bh * static_cast<size_t>(G))) ||
-      (st = scratch.alloc(&kpad, bh * static_cast<size_t>(Npad) * 128)) ||
-      (st = scratch.alloc(&vpad, bh * static_cast<size_t>(Npad) * 128)) ||
-      (st = scratch.alloc(&qp, bh * 3 * Cqp * 128)) ||
-      (st = scratch.alloc(&part, bh * Cq * NS * va::PT_ROW)) ||
-      (st = scratch.alloc(&mzo, bh * Cq * va::PT_ROW)))
+      (st = scratch.alloc(&kpad, bh * static_cast<size_t>(Npad) * D)) ||
+      (st = scratch.alloc(&vpad, bh * static_cast<size_t>(Npad) * D)) ||
+      (st = scratch.alloc(&qp, bh * 3 * Cqp * D)) ||
+      (st = scratch.alloc(&part, bh * Cq * NS * va::PtDim<D>::kRow)) ||
+      (st = scratch.alloc(&mzo, bh * Cq * va::PtDim<D>::kRow)))
     return st;
   const long long nbk = static_cast<long long>(bh) * Ck;
   va::pad16_count_kernel<<<static_cast<unsigned>((nbk + 255) / 256), 256, 0, s>>>(
       nk, static_cast<int>(nbk), cnt16);
   va::km_offsets_kernel<<<BH, 1024, 0, s>>>(cnt16, Ck, kpoff, kpfill);
-  va::pad_gather_kernel<<<dim3(Ck + 1, BH), 128, 0, s>>>(k, v, N, Ck, nk, koff, kperm, kpoff,
-                                                        Npad, G, kpad, vpad, gmeta);
-  va::proxy_pieces_kernel<<<dim3(Cqp, BH), 128, 0, s>>>(qc, Cq, Cqp, qp);
+  va::pad_gather_kernel<D><<<dim3(Ck + 1, BH), 128, 0, s>>>(k, v, N, Ck, nk, koff, kperm, kpoff,
+                                                           Npad, G, kpad, vpad, gmeta);
+  va::proxy_pieces_kernel<D><<<dim3(Cqp, BH), D, 0, s>>>(qc, Cq, Cqp, qp);
   if ((st = launch_status())) return st;
   CUtensorMap mq, mk, mv;
-  if ((st = encode_bf16_rows_box(&mq, qp, BH, 3 * Cqp, 128, 128)) ||
-      (st = encode_bf16_rows_box(&mk, kpad, BH, static_cast<int>(Npad), 128, va::PT_KT)) ||
-      (st = encode_bf16_rows_box(&mv, vpad, BH, static_cast<int>(Npad), 128, va::PT_KT)))
+  if ((st = encode_bf16_rows_box(&mq, qp, BH, 3 * Cqp, D, 128)) ||
+      (st = encode_bf16_rows_box(&mk, kpad, BH, static_cast<int>(Npad), D, va::PT_KT)) ||
+      (st = encode_bf16_rows_box(&mv, vpad, BH, static_cast<int>(Npad), D, va::PT_KT)))
     return st;
   va::ProbeArgs a;
   a.gmeta = gmeta;
@@ -1466,9 +1467,9 @@ int probe_tensor_cores(const __nv_bfloat16* k, const __nv_bfloat16* v, int Cq, i
   a.sl2 = scale * 1.4426950408889634f;
   a.wait_limit = g_wait_limit;
   const dim3 grid(NS, ntiles, BH);
-  va::probe_tc_kernel<1><<<grid, va::PT_THREADS, va::PT_SMEM_BYTES, s>>>(mq, mk, mv, a);
-  va::probe_tc_combine_kernel<<<dim3(Cq, BH), 128, 0, s>>>(part, Cq, NS, mzo);
-  va::probe_tc_kernel<2><<<grid, va::PT_THREADS, va::PT_SMEM_BYTES, s>>>(mq, mk, mv, a);
+  va::probe_tc_kernel<1, D><<<grid, va::PT_THREADS, va::PtDim<D>::kSmem, s>>>(mq, mk, mv, a);
+  va::probe_tc_combine_kernel<D><<<dim3(Cq, BH), D, 0, s>>>(part, Cq, NS, mzo);
+  va::probe_tc_kernel<2, D><<<grid, va::PT_THREADS, va::PtDim<D>::kSmem, s>>>(mq, mk, mv, a);
   return launch_status();
 }
 
@@ -1557,9 +1558,9 @@ int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int C
 
   // probe: err = NaN where a cluster is empty, else the proxy error
   if ((st = cuda_status(cudaMemsetAsync(err, 0xFF, sizeof(float) * bh * Cq * Ck, s)))) return st;
-  if constexpr (std::is_same<T, __nv_bfloat16>::value && D == 128)
-    st = probe_tensor_cores(k, v, Cq, Ck, BH, N, nq, nk, koff, kperm, qc, vc, scale, err, scratch,
-                            s);
+  if constexpr (std::is_same<T, __nv_bfloat16>::value)
+    st = probe_tensor_cores<D>(k, v, Cq, Ck, BH, N, nq, nk, koff, kperm, qc, vc, scale, err,
+                               scratch, s);
   else
     st = probe_simt<T, D>(k, v, Cq, Ck, BH, N, nq, nk, koff, kperm, kassign, qc, kc, vc, scale,
                           err, scratch, s);
