@@ -400,6 +400,54 @@ __global__ void km_sum_kernel(const __nv_bfloat16* __restrict__ x, int N, int C,
   }
 }
 
+// Incremental member sums: for every point whose cluster changed from prev to
+// assign, its 64-bit fixed-point row (bf16_fixed32) is added to the new
+// cluster's sum and subtracted from the old one, and prev takes the new
+// cluster. Integer arithmetic keeps the sums exactly equal to a full
+// recomputation, in any order. Warp g handles points 32g .. 32g + 31 of its
+// (batch, head) in token order. Grid (ceil(N / 256), BH), 256 threads.
+template <int D>
+__global__ void km_delta_kernel(const __nv_bfloat16* __restrict__ x, int N, int C,
+                                int* __restrict__ prev, const int* __restrict__ assign,
+                                unsigned long long* __restrict__ sums) {
+  constexpr int PER = D / 32;
+  const int bh = blockIdx.y;
+  const int t0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * 32;
+  const int lane = threadIdx.x & 31;
+  if (t0 >= N) return;
+  const long long nb = static_cast<long long>(bh) * N;
+  const int i = t0 + lane;
+  int an = 0, ao = 0;
+  bool moved = false;
+  if (i < N) {
+    an = assign[nb + i];
+    ao = prev[nb + i];
+    moved = an != ao;
+    if (moved && (an < 0 || an >= C || ao < 0 || ao >= C)) {
+      raise_error(VA_ERR_DEVICE);
+      moved = false;
+    }
+    if (moved) prev[nb + i] = an;
+  }
+  const uint16_t* xb = reinterpret_cast<const uint16_t*>(x) + nb * D + lane * PER;
+  for (unsigned m = __ballot_sync(0xffffffffu, moved); m; m &= m - 1) {
+    const int q = __ffs(m) - 1;
+    const int cn = __shfl_sync(0xffffffffu, an, q), co = __shfl_sync(0xffffffffu, ao, q);
+    const uint32_t* row = reinterpret_cast<const uint32_t*>(xb + static_cast<long long>(t0 + q) * D);
+    unsigned long long* dn = sums + (static_cast<long long>(bh) * C + cn) * D + lane * PER;
+    unsigned long long* dold = sums + (static_cast<long long>(bh) * C + co) * D + lane * PER;
+#pragma unroll
+    for (int w = 0; w < PER / 2; ++w) {
+      const uint32_t v = row[w];
+      const long long lo = bf16_fixed32(v & 0xffffu), hi = bf16_fixed32(v >> 16);
+      atomicAdd(dn + 2 * w, static_cast<unsigned long long>(lo));
+      atomicAdd(dn + 2 * w + 1, static_cast<unsigned long long>(hi));
+      atomicAdd(dold + 2 * w, static_cast<unsigned long long>(-lo));
+      atomicAdd(dold + 2 * w + 1, static_cast<unsigned long long>(-hi));
+    }
+  }
+}
+
 // mean[bh][c] = sums / count (fp32), |mean|^2 to norm (if non-null), and the
 // bf16 split hi = bf16(mean), lo = bf16(mean - hi) (if non-null). An empty
 // cluster keeps mean (and its split) when keep_empty, else gets zeros.

@@ -1142,7 +1142,7 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int
   if (nchunks > 65535) return VA_ERR_UNSUPPORTED;
   Scoped scratch(s);
   float* cnorm = nullptr;
-  int *off = nullptr, *fill = nullptr, *perm = nullptr;
+  int *off = nullptr, *fill = nullptr, *perm = nullptr, *prev = nullptr;
   __nv_bfloat16 *hi = nullptr, *lo = nullptr;
   unsigned long long* sums = nullptr;
   const size_t nc = static_cast<size_t>(BH) * C * D;
@@ -1150,6 +1150,7 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int
       (st = scratch.alloc(&off, static_cast<size_t>(BH) * (C + 1))) ||
       (st = scratch.alloc(&fill, static_cast<size_t>(BH) * C)) ||
       (st = scratch.alloc(&perm, static_cast<size_t>(BH) * N)) ||
+      (st = scratch.alloc(&prev, static_cast<size_t>(BH) * N)) ||
       (st = scratch.alloc(&hi, nc)) || (st = scratch.alloc(&lo, nc)) ||
       (st = scratch.alloc(&sums, nc)))
     return st;
@@ -1181,10 +1182,20 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int
       va::ka_merge_kernel<<<dim3((N + 255) / 256, BH), 256, 0, s>>>(pdist, pidx, N, C, nchunks,
                                                                    assign, count);
     if (iters == 0) break;
-    va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
-    va::km_scatter_kernel<<<gn, 256, 0, s>>>(assign, N, C, off, fill, perm);
-    if ((st = cuda_status(cudaMemsetAsync(sums, 0, sizeof(unsigned long long) * nc, s)))) return st;
-    va::km_sum_kernel<D><<<gn, 256, 0, s>>>(x, N, C, perm, assign, sums);
+    if (it == 0) {
+      // member sums from scratch: cluster-ordered runs of the first assignment
+      va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
+      va::km_scatter_kernel<<<gn, 256, 0, s>>>(assign, N, C, off, fill, perm);
+      if ((st = cuda_status(cudaMemsetAsync(sums, 0, sizeof(unsigned long long) * nc, s))) ||
+          (st = cuda_status(cudaMemcpyAsync(prev, assign, sizeof(int) * BH * N,
+                                            cudaMemcpyDeviceToDevice, s))))
+        return st;
+      va::km_sum_kernel<D><<<gn, 256, 0, s>>>(x, N, C, perm, assign, sums);
+    } else {
+      // later iterations move the points that changed cluster (few, as the
+      // clustering settles); the sums stay exact
+      va::km_delta_kernel<D><<<gn, 256, 0, s>>>(x, N, C, prev, assign, sums);
+    }
     va::km_finalize_kernel<D><<<gc, 256, 0, s>>>(sums, count, C, cent, cnorm, hi, lo, 1);
   }
   return launch_status();
