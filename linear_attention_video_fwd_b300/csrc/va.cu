@@ -1182,8 +1182,10 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int
       va::ka_merge_kernel<<<dim3((N + 255) / 256, BH), 256, 0, s>>>(pdist, pidx, N, C, nchunks,
                                                                    assign, count);
     if (iters == 0) break;
-    if (it == 0) {
-      // member sums from scratch: cluster-ordered runs of the first assignment
+    if (it <= 1) {
+      // member sums from scratch (cluster-ordered runs) while many points still
+      // move: at the Wan shape a third of them do after the first update, where
+      // the moves alone cost more than the full sum
       va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
       va::km_scatter_kernel<<<gn, 256, 0, s>>>(assign, N, C, off, fill, perm);
       if ((st = cuda_status(cudaMemsetAsync(sums, 0, sizeof(unsigned long long) * nc, s))) ||
@@ -1192,8 +1194,8 @@ int run_cluster_tc(const __nv_bfloat16* x, const int* init, const float* c0, int
         return st;
       va::km_sum_kernel<D><<<gn, 256, 0, s>>>(x, N, C, perm, assign, sums);
     } else {
-      // later iterations move the points that changed cluster (few, as the
-      // clustering settles); the sums stay exact
+      // later iterations move the points that changed cluster (a few percent,
+      // as the clustering settles); the sums stay exact
       va::km_delta_kernel<D><<<gn, 256, 0, s>>>(x, N, C, prev, assign, sums);
     }
     va::km_finalize_kernel<D><<<gc, 256, 0, s>>>(sums, count, C, cent, cnorm, hi, lo, 1);
