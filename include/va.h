@@ -186,9 +186,10 @@ int va_mask_build_static(int kind, int T, int H, int W, const va_mask_params* pa
  * q, k, v, out: [B, heads, N, d] device arrays of `dtype`; lse: NULL or a
  * [B, heads, N] float32 device array. Softmax and accumulation are float32;
  * VA_BF16 inputs give a bf16 output, VA_F32 inputs a float32 output.
- * Supported: VA_BF16 with d in {64, 128} and block 128 (tcgen05 tensor-core
- * kernel); VA_F32 with d in {64, 128} and block in {64, 128} (float32 FMA
- * kernel).
+ * Supported: VA_BF16 with d in {64, 128} and block 128 or 64 (tcgen05
+ * tensor-core kernel; with block 64 it runs 128-row tiles over pairs of
+ * blocks and masks the dead 64 x 64 quarters); VA_F32 with d in {64, 128} and
+ * block in {64, 128} (float32 FMA kernel).
  * Errors: VA_ERR_INVALID (null pointers, N != T*H*W of the mask, B or heads
  * < 1, misaligned pointers, a mask built on another device), VA_ERR_UNSUPPORTED
  * (other dtype/d/block), VA_ERR_CUDA (launch failure).
@@ -215,8 +216,8 @@ int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mas
  * order (no atomics): results are deterministic. Uses the mask's transposed
  * block lists (built by va_mask_build) for dk and dv, and 8 * B * heads *
  * ceil(N / block) * block bytes of stream-ordered scratch.
- * Supported: as the forward (VA_BF16, d in {64, 128}, block 128 on tcgen05;
- * VA_F32, d in {64, 128}, block in {64, 128} on the FMA pipes),
+ * Supported: VA_BF16, d in {64, 128}, block 128 on tcgen05 (block 64 gives
+ * VA_ERR_UNSUPPORTED); VA_F32, d in {64, 128}, block in {64, 128} on the FMA pipes,
  * B * heads <= 65535.
  * Errors: VA_ERR_INVALID (null or misaligned pointers, N != T*H*W of the
  * mask, B or heads < 1, non-finite scale, a mask built on another device),
@@ -272,7 +273,7 @@ int va_linear_attn_fwd(const void* q, const void* k, const void* v, void* out, i
  * `mask` (the dense mask gives full attention) and lin that of
  * va_linear_attn_fwd. r = 1 runs the attention only, r = 0 the linear
  * attention only. The attention part is rounded to bf16 before the blend.
- * Supported: VA_BF16, d = 64 or 128, mask block 128. Errors: as the two calls, and
+ * Supported: VA_BF16, d = 64 or 128, mask block 64 or 128. Errors: as the two calls, and
  * VA_ERR_INVALID for r outside [0, 1], N != the mask's N or a mask built on
  * another device.
  */

@@ -257,11 +257,16 @@ __device__ __forceinline__ void ffma2_bc(float& d0, float& d1, float a0, float a
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
 
-// Softmax of one tile: its CSR row, its TMEM columns and its barriers.
-template <int D>
+// Softmax of one tile: its CSR row, its TMEM columns and its barriers. With
+// SUB (64-token mask blocks) the tile is two query blocks and an entry two key
+// blocks: the tile walks the CTA's union stream (entries pbeg .. pbeg + nu)
+// for those with its tile bit, and a 64-key half that is not live for this
+// row's query block takes part in neither the max nor the sum.
+template <int D, bool SUB = false>
 __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I, int bh,
                                                 uint32_t tmem, uint64_t* bars,
-                                                volatile int* abort_p) {
+                                                volatile int* abort_p, int pbeg = 0,
+                                                int nu = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wq = warp & 3;               // TMEM lane quarter of this warp
   const int r = wq * 32 + lane;          // query row within the tile
@@ -274,15 +279,31 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
   const uint32_t bO = smem_u32(&bars[B_O_DONE + tile]);
   const long long lim = a.wait_limit;
   const float sl2 = a.scale_log2;
-  const int beg = a.row_ptr[I];
-  const int n = a.row_ptr[I + 1] - beg;
-  // Only the last live block of a row can be the ragged tail block.
-  const int tail_valid =
-      (n > 0 && a.col[beg + n - 1] == a.nqb - 1) ? a.N - (a.nqb - 1) * TC_BLK : TC_BLK;
+  int n = nu, tail_valid = TC_BLK;
+  if constexpr (!SUB) {
+    const int beg = a.row_ptr[I];
+    n = a.row_ptr[I + 1] - beg;
+    // Only the last live block of a row can be the ragged tail block.
+    if (n > 0 && a.col[beg + n - 1] == a.nqb - 1) tail_valid = a.N - (a.nqb - 1) * TC_BLK;
+  }
 
   float m_used = -INFINITY, l = 0.f;
   bool ok = true;
-  for (int j = 0; j < n; ++j) {
+  int nl = 0;  // entries of this tile so far (SUB: the union entries with its bit)
+  for (int it = 0; it < n; ++it) {
+    int valid = TC_BLK, lo_end = 64, hi_end = 128;  // live key columns [0, lo_end), [64, hi_end)
+    if constexpr (SUB) {
+      const int e = a.pcol[pbeg + it];
+      if (!((e >> tile) & 1)) continue;
+      const int jc = e >> 10;
+      const int sb = (e >> (2 + 4 * tile + 2 * (r >> 6))) & 3;  // this row's block, both key halves
+      valid = jc == a.nqb - 1 ? a.N - jc * TC_BLK : TC_BLK;
+      lo_end = (sb & 1) ? min(valid, 64) : 0;
+      hi_end = (sb & 2) ? valid : 64;
+    } else {
+      valid = it == n - 1 ? tail_valid : TC_BLK;
+    }
+    const int j = nl++;
     ok = __all_sync(0xffffffffu, mbar_wait_bounded(bS, j & 1, lim, abort_p));
     if (!ok) break;
     tc_fence_after();
@@ -295,8 +316,19 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
       for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
     }
     tmem_wait_ld();
-    const int valid = (j == n - 1) ? tail_valid : TC_BLK;
-    if (valid < TC_BLK) {
+    // SUB: the entry may hold no live key of this row (a row of the other query
+    // block of the tile is live): it then adds nothing (warp-uniform, as a
+    // warp's 32 rows lie in one block)
+    const bool row_live = !SUB || lo_end > 0 || hi_end > 64;
+    if constexpr (SUB) {
+      if (row_live && (lo_end < 64 || hi_end < 128)) {
+        // dead columns take a live value of the block for the max, and a zero
+        // weight below
+        const float rep = lo_end > 0 ? s[0] : s[64];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = (i < lo_end || (i >= 64 && i < hi_end)) ? s[i] : rep;
+      }
+    } else if (valid < TC_BLK) {
       // Key columns >= valid hold zero-filled rows: give them a real value of
       // the block for the max, and a zero weight below.
 #pragma unroll
@@ -328,7 +360,7 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
       mx = fmin3(fmin3(m0, m1, s[124]), fmin3(m2, m3, s[125]), fminf(s[126], s[127]));
     }
     const float m_cand = mx * sl2;
-    const bool need = m_cand > m_used + TC_TAU;
+    const bool need = row_live && m_cand > m_used + TC_TAU;
     float alpha = 1.f;
     if (need) {
       alpha = ex2_approx(m_used - m_cand);
@@ -357,7 +389,15 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
       s[i] = ex2_approx(s[i]);
       s[i + 1] = ex2_approx(s[i + 1]);
     }
-    if (valid < TC_BLK) {
+    if constexpr (SUB) {
+      if (!row_live) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = 0.f;
+      } else if (lo_end < 64 || hi_end < 128) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = (i < lo_end || (i >= 64 && i < hi_end)) ? s[i] : 0.f;
+      }
+    } else if (valid < TC_BLK) {
 #pragma unroll
       for (int i = 1; i < 128; ++i) s[i] = (i < valid) ? s[i] : 0.f;
     }
@@ -381,11 +421,13 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
     tc_fence_before();
     mbar_arrive(bP);
   }
-  // epilogue
+  // epilogue (SUB: a row that no entry made live ends with l = 0 and is
+  // written as a row without live blocks)
   const long long obase = (static_cast<long long>(bh) * a.N + row) * D;
-  if (n > 0 && ok)
-    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (n - 1) & 1, lim, abort_p));
-  if (n > 0 && ok) {
+  if (nl > 0 && ok)
+    ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (nl - 1) & 1, lim, abort_p));
+  const bool empty_row = SUB && l == 0.f;
+  if (nl > 0 && ok && !empty_row) {
     tc_fence_after();
     const float inv = 1.f / l;
 #pragma unroll
@@ -408,7 +450,7 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
     }
     if (row < a.N && a.lse != nullptr)
       a.lse[static_cast<long long>(bh) * a.N + row] = (m_used + log2f(l)) * 0.69314718055994530942f;
-  } else if (n == 0 && row < a.N) {
+  } else if ((nl == 0 || (empty_row && ok)) && row < a.N) {
     uint4* dst = reinterpret_cast<uint4*>(a.out + obase);
 #pragma unroll
     for (int q4 = 0; q4 < D / 8; ++q4) dst[q4] = make_uint4(0, 0, 0, 0);
@@ -416,7 +458,7 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
   }
 }
 
-template <int D>
+template <int D, bool SUB = false>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
@@ -438,7 +480,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const int P = a.porder[blockIdx.x % a.npairs];
   const int I0 = 2 * P, I1 = 2 * P + 1;
   const bool has1 = I1 < a.nqb;
-  const int pbeg = a.row_ptr[I0];
+  // SUB: the CTA's union starts at the offset of its first 64-token query row
+  const int pbeg = a.row_ptr[SUB ? 2 * I0 : I0];
   const int nu = a.plen[P];
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -477,7 +520,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(TC_REGS_INC));
     const int tile = (warp - 4) >> 2;
     if (tile == 0 || has1)
-      tc_softmax_tile<D>(a, tile, tile == 0 ? I0 : I1, bh, tmem, bars, abort_p);
+      tc_softmax_tile<D, SUB>(a, tile, tile == 0 ? I0 : I1, bh, tmem, bars, abort_p, pbeg, nu);
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(TC_REGS_DEC));
   if (warp == 0) {
@@ -497,7 +540,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (has1) load_tile(sQ0 + kTile, &map_q, bar(B_Q_FULL + 1), I1 * TC_BLK);
       int issued_k = 0, issued_v = 0;
       for (int u = 0; u < nu; ++u) {
-        const int J = a.pcol[pbeg + u] >> 2;
+        const int J = a.pcol[pbeg + u] >> (SUB ? 10 : 2);
         const int sk = u % TC_NK, sv = u % TC_NV;
         const uint32_t sK = sK0 + sk * kTile, sV = sV0 + sv * kTile;
         if (u >= TC_NK &&

@@ -212,6 +212,75 @@ __global__ void pair_merge_kernel(int nb, const int* __restrict__ row_ptr,
   plen[P] = k;
 }
 
+// Quads for the two-tile kernel on 64-token blocks: tile t of quad Q covers
+// the 128 query rows of blocks 4Q + 2t and 4Q + 2t + 1, and an entry covers
+// the 128 keys of blocks 2J' and 2J' + 1. The union over the four rows is
+// keyed by J'; entry = J' << 10 | sub << 2 | tile bits, where sub bit
+// 4t + 2a + b says that block 4Q + 2t + a sees block 2J' + b, and tile bit t
+// that any of tile t's four sub bits is set. Quad Q's entries start at
+// row_ptr[4Q] (the union is never longer than the four rows together). One
+// thread per quad.
+__global__ void quad_merge_kernel(int nb, const int* __restrict__ row_ptr,
+                                  const int* __restrict__ col, int* __restrict__ qcol,
+                                  int* __restrict__ qlen) {
+  const int Q = blockIdx.x * blockDim.x + threadIdx.x;
+  const int nquads = (nb + 3) / 4;
+  if (Q >= nquads) return;
+  int cur[4], end[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = 4 * Q + i;
+    cur[i] = row < nb ? row_ptr[row] : 0;
+    end[i] = row < nb ? row_ptr[row + 1] : 0;
+  }
+  const int out = row_ptr[4 * Q];
+  int k = 0;
+  while (true) {
+    int jc = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (cur[i] < end[i]) jc = min(jc, col[cur[i]] >> 1);
+    if (jc == 0x7fffffff) break;
+    int sub = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      // row i = 2t + a holds bit 4t + 2a + b = 2i + b for key block 2jc + b
+      while (cur[i] < end[i] && (col[cur[i]] >> 1) == jc) {
+        sub |= 1 << (2 * i + (col[cur[i]] & 1));
+        ++cur[i];
+      }
+    }
+    const int tiles = ((sub & 0x0f) ? 1 : 0) | ((sub & 0xf0) ? 2 : 0);
+    qcol[out + k] = (jc << 10) | (sub << 2) | tiles;
+    ++k;
+  }
+  qlen[Q] = k;
+}
+
+// Single thread: quads ordered by descending summed length of their four rows
+// (stable counting sort; lengths are 0..4*nb). hist must hold 4*nb + 2 ints.
+__global__ void quad_order_kernel(int nb, const int* __restrict__ row_ptr,
+                                  int* __restrict__ qorder, int* __restrict__ hist) {
+  if (blockIdx.x != 0 || threadIdx.x != 0) return;
+  const int nquads = (nb + 3) / 4;
+  const int top = 4 * nb + 1;
+  for (int i = 0; i <= top; ++i) hist[i] = 0;
+  for (int Q = 0; Q < nquads; ++Q) {
+    const int e = min(4 * Q + 4, nb);
+    hist[top - (row_ptr[e] - row_ptr[4 * Q])]++;
+  }
+  int acc = 0;
+  for (int i = 0; i <= top; ++i) {
+    const int v = hist[i];
+    hist[i] = acc;
+    acc += v;
+  }
+  for (int Q = 0; Q < nquads; ++Q) {
+    const int e = min(4 * Q + 4, nb);
+    qorder[hist[top - (row_ptr[e] - row_ptr[4 * Q])]++] = Q;
+  }
+}
+
 // Single thread: pairs ordered by descending summed row length (stable
 // counting sort; lengths are 0..2*nb). hist must hold 2*nb + 2 ints.
 __global__ void pair_order_kernel(int nb, const int* __restrict__ row_ptr,

@@ -214,6 +214,12 @@ struct va_mask {
   int32_t* pcol = nullptr;     // device [nnz]: merged rows, entry J << 2 | live bits
   int32_t* plen = nullptr;     // device [npairs]: merged length per pair
   int32_t* porder = nullptr;   // device [npairs]: pairs by descending work
+  // 64-token blocks only: quads of query blocks {4Q .. 4Q + 3} over pairs of
+  // key blocks for the two-tile tensor-core kernel (quad_merge_kernel)
+  int nquads = 0;
+  int32_t* qcol = nullptr;     // device [nnz]: entry J' << 10 | sub bits << 2 | tile bits
+  int32_t* qlen = nullptr;     // device [nquads]
+  int32_t* qorder = nullptr;   // device [nquads]: quads by descending work
   // transposed lists for the backward: for key block J, the query blocks
   // that see it (ascending), and key blocks by descending list length
   int32_t* t_ptr = nullptr;    // device [nqb + 1]
@@ -451,6 +457,24 @@ VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params*
       va_mask_free(m);
       return st;
     }
+    if (m->p.block == 64) {
+      m->nquads = (md.nb + 3) / 4;
+      int* qhist = nullptr;
+      if ((st = scratch.alloc(&qhist, 4 * static_cast<size_t>(md.nb) + 2)) ||
+          (st = cuda_status(cudaMalloc(&m->qcol, sizeof(int32_t) * (m->nnz > 0 ? m->nnz : 1)))) ||
+          (st = cuda_status(cudaMalloc(&m->qlen, sizeof(int32_t) * m->nquads))) ||
+          (st = cuda_status(cudaMalloc(&m->qorder, sizeof(int32_t) * m->nquads)))) {
+        va_mask_free(m);
+        return st;
+      }
+      va::quad_merge_kernel<<<(m->nquads + 127) / 128, 128, 0, s>>>(md.nb, m->row_ptr, m->col,
+                                                                     m->qcol, m->qlen);
+      va::quad_order_kernel<<<1, 1, 0, s>>>(md.nb, m->row_ptr, m->qorder, qhist);
+      if ((st = launch_status())) {
+        va_mask_free(m);
+        return st;
+      }
+    }
     // The transposed lists reuse the count / scan / fill kernels with the
     // roles of query and key blocks swapped; the live pairs are the same, so
     // their number is already known.
@@ -520,6 +544,9 @@ VA_EXPORT int va_mask_free(va_mask* m) {
   if (m->pcol) cudaFree(m->pcol);
   if (m->plen) cudaFree(m->plen);
   if (m->porder) cudaFree(m->porder);
+  if (m->qcol) cudaFree(m->qcol);
+  if (m->qlen) cudaFree(m->qlen);
+  if (m->qorder) cudaFree(m->qorder);
   if (m->t_ptr) cudaFree(m->t_ptr);
   if (m->t_row) cudaFree(m->t_row);
   if (m->t_order) cudaFree(m->t_order);
@@ -541,7 +568,8 @@ int launch_simt(const void* q, const void* k, const void* v, const va_mask* m, v
   return launch_status();
 }
 
-template <int D>
+// SUB: a mask of 64-token blocks, run as 128-row tiles over the mask's quads.
+template <int D, bool SUB = false>
 int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, void* out, float* lse,
               int BH, int N, float scale, cudaStream_t s) {
   static DeviceOnce once;
@@ -552,10 +580,10 @@ int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, voi
     // The kernel's setmaxnreg split assumes this exact per-thread register
     // count at launch; anything else could leave the increase waiting.
     cudaFuncAttributes fa;
-    int r = cuda_status(cudaFuncGetAttributes(&fa, va::attn_tc_kernel<D>));
+    int r = cuda_status(cudaFuncGetAttributes(&fa, va::attn_tc_kernel<D, SUB>));
     if (r) return r;
     if (fa.numRegs != va::TC_LAUNCH_REGS) return VA_ERR_UNSUPPORTED;
-    return cuda_status(cudaFuncSetAttribute(va::attn_tc_kernel<D>,
+    return cuda_status(cudaFuncSetAttribute(va::attn_tc_kernel<D, SUB>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             va::TcDim<D>::kSmemBytes));
   });
@@ -567,20 +595,21 @@ int launch_tc(const void* q, const void* k, const void* v, const va_mask* m, voi
   va::TcArgs a;
   a.row_ptr = m->row_ptr;
   a.col = m->col;
-  a.pcol = m->pcol;
-  a.plen = m->plen;
-  a.porder = m->porder;
+  a.pcol = SUB ? m->qcol : m->pcol;
+  a.plen = SUB ? m->qlen : m->plen;
+  a.porder = SUB ? m->qorder : m->porder;
   a.out = static_cast<__nv_bfloat16*>(out);
   a.lse = lse;
   a.N = N;
-  a.nqb = m->nqb;
-  a.npairs = m->npairs;
+  a.nqb = SUB ? (m->nqb + 1) / 2 : m->nqb;   // 128-row tiles
+  a.npairs = SUB ? m->nquads : m->npairs;
+  if (SUB && a.pcol == nullptr) return VA_ERR_UNSUPPORTED;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit = g_wait_limit;
-  const long long grid = static_cast<long long>(m->npairs) * BH;
+  const long long grid = static_cast<long long>(a.npairs) * BH;
   if (grid > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
-  va::attn_tc_kernel<D><<<static_cast<unsigned>(grid), va::TC_THREADS, va::TcDim<D>::kSmemBytes,
-                          s>>>(mq, mk, mv, a);
+  va::attn_tc_kernel<D, SUB><<<static_cast<unsigned>(grid), va::TC_THREADS,
+                               va::TcDim<D>::kSmemBytes, s>>>(mq, mk, mv, a);
   return launch_status();
 }
 
@@ -612,6 +641,8 @@ VA_EXPORT int va_sparse_attn_fwd(const void* q, const void* k, const void* v, co
   if (dtype == VA_BF16) {
     if (d == 128 && blk == 128) return launch_tc<128>(q, k, v, m, out, lse, BH, N, scale, s);
     if (d == 64 && blk == 128) return launch_tc<64>(q, k, v, m, out, lse, BH, N, scale, s);
+    if (d == 128 && blk == 64) return launch_tc<128, true>(q, k, v, m, out, lse, BH, N, scale, s);
+    if (d == 64 && blk == 64) return launch_tc<64, true>(q, k, v, m, out, lse, BH, N, scale, s);
     return VA_ERR_UNSUPPORTED;
   }
   return VA_ERR_UNSUPPORTED;

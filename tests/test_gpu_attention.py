@@ -81,6 +81,41 @@ def test_bf16_small_all_rows(va, dev, case, d):
     assert np.abs(gl - wl).max() <= 2e-2
 
 
+# 64-token mask blocks on the tensor-core kernel: 128-row tiles over pairs of
+# query blocks, entries over pairs of key blocks, dead 64 x 64 quarters masked
+SMALL_BF16_B64 = [
+    (OM.RADIAL, 5, 6, 20, OM.MaskParams(block=64, w0=10), 0),           # 10 blocks, tail 24
+    (OM.RADIAL, 9, 8, 16, OM.MaskParams(block=64), 0),                  # 18 blocks, no tail
+    (OM.LVSA, 12, 7, 9, OM.MaskParams(block=64, local=1, period=4, anchor0=2, rot_stride=3), 2),
+    (OM.LVSA, 16, 4, 8, OM.MaskParams(block=64, local=0, period=5, anchor0=1, rot_stride=2), 1),
+    (OM.DENSE, 3, 7, 13, OM.MaskParams(block=64), 0),                  # 5 blocks, tail 17
+    (OM.RADIAL, 3, 4, 20, OM.MaskParams(block=64, w0=7), 0),            # 4 blocks, tail 48
+    (OM.RADIAL, 1, 3, 5, OM.MaskParams(block=64), 0),                   # N=15 < block
+]
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("case", SMALL_BF16_B64)
+def test_bf16_block64_small_all_rows(va, dev, case, d):
+    kind, T, H, W, p, step = case
+    q, k, v = synth.video_qkv(2, 3, T, H, W, d, seed=13)
+    got, want, gl, wl = _run(va, dev, q, k, v, kind, T, H, W, p, step, "bf16")
+    assert_bf16_close(got, want)
+    assert np.abs(gl - wl).max() <= 2e-2
+
+
+def test_bf16_block64_wan_sampled_rows(va, dev):
+    # The Wan grid (32,760 tokens, 12 heads, d=128) under the radial mask with
+    # 64-token blocks (512 blocks; W0 = H*W)
+    T, H, W = 21, 30, 52
+    q, k, v = cached_video_qkv(1, 12, T, H, W, 128, seed=1235)
+    rows = OA.sample_rows(T * H * W, 64, 512, seed=6)
+    got, want, gl, wl = _run(va, dev, q, k, v, OM.RADIAL, T, H, W, OM.MaskParams(block=64),
+                             0, "bf16", rows=rows)
+    assert_bf16_close(got, want)
+    assert np.abs(gl - wl).max() <= 2e-2
+
+
 def test_bf16_single_live_key_block_extremes(va, dev):
     # Large-magnitude logits (scale 1): the online softmax must stay finite.
     T, H, W = 4, 8, 16
@@ -113,14 +148,6 @@ def test_attention_rejects_bad_arguments(va, dev):
     q96 = torch.zeros((1, 1, 240, 96), dtype=torch.bfloat16, device=dev)
     with pytest.raises(va.VAError) as e:                 # head_dim 96
         va.sparse_attn_fwd(q96, q96, q96, m)
-    assert e.value.status == va.ERR_UNSUPPORTED
-    m64 = va.mask_build(va.RADIAL, 3, 4, 20, block=64)
-    with pytest.raises(va.VAError) as e:                 # bf16 needs block 128
-        va.sparse_attn_fwd(q, q, q, m64)
-    assert e.value.status == va.ERR_UNSUPPORTED
-    q64 = torch.zeros((1, 1, 240, 64), dtype=torch.bfloat16, device=dev)
-    with pytest.raises(va.VAError) as e:                 # d = 64 with block 64: not on bf16
-        va.sparse_attn_fwd(q64, q64, q64, m64)
     assert e.value.status == va.ERR_UNSUPPORTED
     assert va.device_error() == va.OK
 

@@ -183,4 +183,8 @@ def test_backward_rejects_bad_arguments(va, dev):
     with pytest.raises(va.VAError) as e:
         va.sparse_attn_bwd(q, q, q, q, q, lse, m2)
     assert e.value.status == va.ERR_INVALID
+    m64 = va.mask_build(va.RADIAL, 3, 4, 20, block=64)   # bf16 gradients need block 128
+    with pytest.raises(va.VAError) as e:
+        va.sparse_attn_bwd(q, q, q, q, q, lse, m64)
+    assert e.value.status == va.ERR_UNSUPPORTED
     assert va.device_error() == va.OK
