@@ -69,6 +69,9 @@ WORKLOADS = {
     "wan_radial_d64": dict(T=21, H=30, W=52, heads=12, kind="radial", params={}, step=0,
                            seed=1235, d=64, desc="Wan-shaped radial block-sparse attention "
                            "forward with head_dim 64", mask="radial, W0=H*W"),
+    "wan_radial_b64": dict(T=21, H=30, W=52, heads=12, kind="radial", params={}, step=0,
+                           seed=1235, block=64, desc="Wan-shaped radial block-sparse attention "
+                           "forward with 64-token mask blocks", mask="radial, W0=H*W, block 64"),
 }
 METRIC = "block-sparse attn effective TFLOP/s + ms/call at 32,760 tok; % of B300 BF16 peak"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "attn_tc_wan_radial_traffic.json")
@@ -91,7 +94,7 @@ def workload_config(name, wl):
     d = wl.get("d", D)
     return {"workload": wl["desc"], "B": BATCH, "heads": wl["heads"],
             "grid_THW": [wl["T"], wl["H"], wl["W"]], "tokens": N, "head_dim": d,
-            "block": BLOCK, "mask": wl["mask"],
+            "block": wl.get("block", BLOCK), "mask": wl["mask"],
             "l2": "inputs larger than L2 (Q+K+V+O = %d MB per call vs 126 MB L2), no flush"
                   % round(4 * BATCH * wl["heads"] * N * d * 2 / 1e6)}
 
@@ -223,7 +226,7 @@ def oracle_block_mask(wl):
     from oracle import masks as OM
     kind = {"radial": OM.RADIAL, "lvsa": OM.LVSA, "dense": OM.DENSE}[wl["kind"]]
     return OM.block_mask(kind, wl["T"], wl["H"], wl["W"],
-                         OM.MaskParams(block=BLOCK, **wl["params"]), wl["step"])
+                         OM.MaskParams(block=wl.get("block", BLOCK), **wl["params"]), wl["step"])
 
 
 def oracle_sample(wl, q, k, v, bm, rows):
@@ -231,11 +234,12 @@ def oracle_sample(wl, q, k, v, bm, rows):
     FLOPs done, output rows [B, heads, R, d])."""
     from oracle import attention as OA
     N, d = q.shape[2], q.shape[3]
-    live_keys_per_block = (bm * np.array([min(N, (b + 1) * BLOCK) - b * BLOCK
+    blk = wl.get("block", BLOCK)
+    live_keys_per_block = (bm * np.array([min(N, (b + 1) * blk) - b * blk
                                           for b in range(bm.shape[0])])[None, :]).sum(1)
-    flops = 4.0 * d * float(live_keys_per_block[rows // BLOCK].sum()) * BATCH * wl["heads"]
+    flops = 4.0 * d * float(live_keys_per_block[rows // blk].sum()) * BATCH * wl["heads"]
     t0 = time.perf_counter()
-    o, _ = OA.block_sparse_attention(q, k, v, bm, BLOCK, 1.0 / np.sqrt(d), rows=rows)
+    o, _ = OA.block_sparse_attention(q, k, v, bm, blk, 1.0 / np.sqrt(d), rows=rows)
     return time.perf_counter() - t0, flops, o
 
 
@@ -307,7 +311,7 @@ def run_ours(args, world, rank, local):
     qt, kt, vt = (torch.from_numpy(x).to(dev, torch.bfloat16) for x in (q, k, v))
     out = torch.empty_like(qt)
     kind = {"radial": va.RADIAL, "lvsa": va.LVSA, "dense": va.DENSE}[wl["kind"]]
-    mask = va.mask_build(kind, T, H, W, block=BLOCK, step=wl["step"], **wl["params"])
+    mask = va.mask_build(kind, T, H, W, block=wl.get("block", BLOCK), step=wl["step"], **wl["params"])
     flops = 4.0 * wl.get("d", D) * mask.live_pairs * BATCH * heads
     stream = torch.cuda.current_stream()
 
@@ -369,14 +373,15 @@ def run_ours(args, world, rank, local):
                      "flops_per_launch": flops, "launch_ms_mean": round(float(np.mean(launch_ms)), 4),
                      "launch_ms_min": round(float(np.min(launch_ms)), 4),
                      "traffic": profiled_traffic() if name == "wan_radial" else None,
-                     "kernel": "va::attn_tc_kernel<%d>" % wl.get("d", D)},
+                     "kernel": "va::attn_tc_kernel<%d%s>" % (
+                         wl.get("d", D), ", true" if wl.get("block", BLOCK) == 64 else "")},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
     if rank == 0:
         bm = oracle_block_mask(wl)
         full = world == 1 and not args.no_cpu_baseline
-        rows = OA.sample_rows(N, BLOCK, args.oracle_rows if full else 64, seed=7)
+        rows = OA.sample_rows(N, wl.get("block", BLOCK), args.oracle_rows if full else 64, seed=7)
         secs, oflops, want = oracle_sample(wl, q, k, v, bm, rows)
         got = out[:, :, torch.from_numpy(rows).to(dev)].float().cpu().numpy()
         line["parity"] = parity_record(got, want, "output rows %d x %d heads vs the float64 "
@@ -593,10 +598,12 @@ def run_reference(args, world, rank):
     bm = oracle_block_mask(wl)
     per_step = args.reference_rows
     for i in range(args.warmup):
-        oracle_sample(wl, q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=1000 + i))
+        oracle_sample(wl, q, k, v, bm, OA.sample_rows(N, wl.get("block", BLOCK), per_step,
+                                                       seed=1000 + i))
     secs, fl = 0.0, 0.0
     for i in range(args.steps):
-        s, f, _ = oracle_sample(wl, q, k, v, bm, OA.sample_rows(N, BLOCK, per_step, seed=2000 + i))
+        s, f, _ = oracle_sample(wl, q, k, v, bm, OA.sample_rows(N, wl.get("block", BLOCK),
+                                                                per_step, seed=2000 + i))
         secs += s
         fl += f
     value = fl / secs / 1e12

@@ -321,12 +321,18 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
     // warp's 32 rows lie in one block)
     const bool row_live = !SUB || lo_end > 0 || hi_end > 64;
     if constexpr (SUB) {
-      if (row_live && (lo_end < 64 || hi_end < 128)) {
+      if (row_live) {
         // dead columns take a live value of the block for the max, and a zero
         // weight below
         const float rep = lo_end > 0 ? s[0] : s[64];
+        if (lo_end < 64) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = (i < lo_end || (i >= 64 && i < hi_end)) ? s[i] : rep;
+          for (int i = 0; i < 64; ++i) s[i] = i < lo_end ? s[i] : rep;
+        }
+        if (hi_end < 128) {
+#pragma unroll
+          for (int i = 64; i < 128; ++i) s[i] = i < hi_end ? s[i] : rep;
+        }
       }
     } else if (valid < TC_BLK) {
       // Key columns >= valid hold zero-filled rows: give them a real value of
@@ -390,12 +396,13 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
       s[i + 1] = ex2_approx(s[i + 1]);
     }
     if constexpr (SUB) {
-      if (!row_live) {
+      if (lo_end < 64) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = 0.f;
-      } else if (lo_end < 64 || hi_end < 128) {
+        for (int i = 0; i < 64; ++i) s[i] = i < lo_end ? s[i] : 0.f;
+      }
+      if (hi_end < 128) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = (i < lo_end || (i >= 64 && i < hi_end)) ? s[i] : 0.f;
+        for (int i = 64; i < 128; ++i) s[i] = i < hi_end ? s[i] : 0.f;
       }
     } else if (valid < TC_BLK) {
 #pragma unroll
