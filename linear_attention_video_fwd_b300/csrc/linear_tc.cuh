@@ -321,19 +321,28 @@ __global__ void lin_prep_kernel(const float* __restrict__ part, int nsplit,
 enum : int {
   LO_PF = 0,                 // pieces loaded
   LO_QF = 1,                 // LN_NS: Q tile loaded
-  LO_PHI = LO_QF + LN_NS,    // LN_NS: phi(Q) written (256 arrivals)
-  LO_QE = LO_PHI + LN_NS,    // LN_NS: Q tile consumed by the MMAs
-  LO_AF = LO_QE + LN_NS,     // 2: accumulator full
+  LO_QE = LO_QF + LN_NS,     // LN_NS: Q tile read into registers by its phi pair (256 arrivals)
+  LO_PHI = LO_QE + LN_NS,    // 2: phi(Q) written to TMEM operand buffer a (256 arrivals)
+  LO_ABE = LO_PHI + 2,       // 2: operand buffer a read by the MMAs
+  LO_AF = LO_ABE + 2,        // 2: accumulator full
   LO_AE = LO_AF + 2,         // 2: accumulator read (128 arrivals)
   LO_DRAIN = LO_AE + 2,
   LO_COUNT = LO_DRAIN + 1
 };
 
+// TMEM columns of the output kernel: accumulator b at [256 b, 256 b + D + 16);
+// phi(Q) operand buffer a (128 rows x D bf16, two per 32-bit column) at
+// column 160 + 256 a, past the accumulator of its half.
+__device__ __forceinline__ uint32_t ln_opd(int a) { return 160u + 256u * static_cast<uint32_t>(a); }
+
 // Grid (nsplit, BH), 768 threads: warp 0 TMA producer, warp 1 MMA issuer,
 // warps 8..11 epilogue (thread r owns token row r of the tile; the tile goes
 // out through shared memory and a TMA store), and two pairs of warpgroups
-// that apply phi(Q) in place to alternate tiles: warps 4..7 and 12..15 the
-// even tiles, warps 16..19 and 20..23 the odd ones. out = num / den, or
+// that take alternate tiles: warps 4..7 and 12..15 the even tiles (TMEM
+// operand buffer 0), warps 16..19 and 20..23 the odd ones (buffer 1). A pair
+// reads its Q tile into registers, releases the ring stage at once, and writes
+// phi(Q) as the MMA's A operand into its TMEM buffer; the MMA is then
+// TMEM x shared memory (the [S | z]^T pieces). out = num / den, or
 // r_mix * out + (1 - r_mix) * num / den when mix != 0 (out then holds the
 // attention output on entry).
 template <int D>
@@ -364,10 +373,11 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
     mbar_init(bar(LO_PF), 1);
     for (int s = 0; s < LN_NS; ++s) {
       mbar_init(bar(LO_QF + s), 1);
-      mbar_init(bar(LO_PHI + s), 256);
-      mbar_init(bar(LO_QE + s), 1);
+      mbar_init(bar(LO_QE + s), 256);
     }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(LO_PHI + b), 256);
+      mbar_init(bar(LO_ABE + b), 1);
       mbar_init(bar(LO_AF + b), 1);
       mbar_init(bar(LO_AE + b), 128);
     }
@@ -422,29 +432,28 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && nt > 0) {
-      // num | den = phi(Q) [S | z]: A = phi(Q) K-major, B = [S | z]^T K-major
-      // (D + 16 rows), two pieces accumulated in fp32.
+      // num | den = phi(Q) [S | z]: A = phi(Q) from TMEM (K-major), B = [S | z]^T
+      // K-major in shared memory (D + 16 rows), two pieces accumulated in fp32.
       constexpr uint32_t id = idesc_bf16_f32(128, Dm::kNext, 0, 0);
       const uint32_t sP = smem_u32(pc);
       bool ok = mbar_wait_bounded(bar(LO_PF), 0, lim, abort_p);
       for (int u = 0; ok && u < nt; ++u) {
-        const int s = u % LN_NS, b = u & 1;
-        if (!(ok = mbar_wait_bounded(bar(LO_PHI + s), (u / LN_NS) & 1, lim, abort_p))) break;
+        const int b = u & 1;  // operand buffer and accumulator of the tile
+        if (!(ok = mbar_wait_bounded(bar(LO_PHI + b), (u >> 1) & 1, lim, abort_p))) break;
         if (u >= 2 &&
             !(ok = mbar_wait_bounded(bar(LO_AE + b), ((u >> 1) & 1) ^ 1, lim, abort_p)))
           break;
         tc_fence_after();
-        const uint32_t sQ = smem_u32(qt + s * Dm::kTile);
+        const uint32_t tA = tmem + ln_opd(b);
 #pragma unroll
         for (int p = 0; p < 2; ++p)
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
-            umma_ss(tmem + b * 256,
-                    sw128_desc(sQ + (k >> 2) * LN_HALF + (k & 3) * 32, 16, 1024),
+            umma_ts(tmem + b * 256, tA + k * 8,
                     sw128_desc(sP + p * Dm::kPiece + (k >> 2) * Dm::kPieceHalf + (k & 3) * 32, 16,
                                1024),
                     id, (p | k) ? 1u : 0u);
-        umma_commit(bar(LO_QE + s));
+        umma_commit(bar(LO_ABE + b));
         umma_commit(bar(LO_AF + b));
       }
       if (!ok) {
@@ -457,19 +466,48 @@ __global__ void __launch_bounds__(LN_OUT_THREADS, 1)
     const int r = (warp & 3) * 32 + lane;
     const int h = (warp >= 12 && warp < 16) || warp >= 20 ? 1 : 0;
     const int g = warp >= 16 ? 1 : 0;
+    // Thread r of warpgroup h: chunks [c0, c0 + NC) of token row r (TMEM lane
+    // r, in this warp's lane quarter), i.e. dims 8 c0 .. 8 (c0 + NC) - 1.
+    constexpr int NC = D / 16;                       // 16-byte chunks per thread
+    uint8_t* const half0 = qt + (D == 128 ? h * LN_HALF : 0);
+    const int c0 = D == 128 ? 0 : 4 * h;
+    const uint32_t tOpd = tmem + ln_opd(g) + (static_cast<uint32_t>((warp & 3) * 32) << 16) +
+                          static_cast<uint32_t>(h * NC * 4);
     for (int u = g; u < nt; u += 2) {
-      // As in lin_state_kernel: first the other pair's phi of tile u - 3, the
-      // previous user of stage s, so the Q-full parity cannot match too early.
+      // As in lin_state_kernel: first the other pair's release of tile u - 3,
+      // the previous user of stage s, so the Q-full parity cannot match too
+      // early; then this pair's operand buffer, read by the MMAs of tile u - 2.
       const int s = u % LN_NS;
       const uint32_t ph = (u / LN_NS) & 1;
       if (u >= LN_NS &&
-          !__all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_PHI + s), ph ^ 1, lim, abort_p)))
+          !__all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_QE + s), ph ^ 1, lim, abort_p)))
         break;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_QF + s), ph, lim, abort_p)))
         break;
-      lin_phi_tile<D>(qt + s * Dm::kTile, h, r, 128);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(LO_PHI + s));
+      if (u >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded(bar(LO_ABE + g),
+                                                               ((u >> 1) - 1) & 1, lim, abort_p)))
+        break;
+      // chunk j of row r sits at 16-byte position j ^ (r & 7) (128-byte
+      // swizzle); in logical order the warp's loads still hit distinct banks
+      const uint8_t* rowp = half0 + s * Dm::kTile + r * 128;
+      uint4 w[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c)
+        w[c] = *reinterpret_cast<const uint4*>(rowp + (((c0 + c) ^ (r & 7)) * 16));
+      mbar_arrive(bar(LO_QE + s));  // the stage may be reloaded (release: loads done)
+      uint32_t e[NC * 4];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) {
+        e[4 * c + 0] = lin_phi_bf16x2(w[c].x);
+        e[4 * c + 1] = lin_phi_bf16x2(w[c].y);
+        e[4 * c + 2] = lin_phi_bf16x2(w[c].z);
+        e[4 * c + 3] = lin_phi_bf16x2(w[c].w);
+      }
+      if constexpr (NC * 4 == 32) tmem_st32(tOpd, e);
+      else tmem_st16(tOpd, e);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(LO_PHI + g));
     }
   } else if (warp >= 8) {
     // Thread r converts token row r of the tile into the staging tile (the
