@@ -215,9 +215,11 @@ int va_sparse_attn_fwd(const void* q, const void* k, const void* v, const va_mas
  * and must not overlap the inputs. Each gradient row is reduced in a fixed
  * order (no atomics): results are deterministic. Uses the mask's transposed
  * block lists (built by va_mask_build) for dk and dv, and 8 * B * heads *
- * ceil(N / block) * block bytes of stream-ordered scratch.
- * Supported: VA_BF16, d in {64, 128}, block 128 on tcgen05 (block 64 gives
- * VA_ERR_UNSUPPORTED); VA_F32, d in {64, 128}, block in {64, 128} on the FMA pipes,
+ * ceil(N / block) * block bytes of stream-ordered scratch (ceil(N / 128) * 128 for
+ * bf16 with block 64).
+ * Supported: VA_BF16, d in {64, 128}, block 128 or 64 on tcgen05 (block 64 as
+ * 128-token tiles over pairs of blocks); VA_F32, d in {64, 128}, block in
+ * {64, 128} on the FMA pipes,
  * B * heads <= 65535.
  * Errors: VA_ERR_INVALID (null or misaligned pointers, N != T*H*W of the
  * mask, B or heads < 1, non-finite scale, a mask built on another device),

@@ -59,6 +59,7 @@ struct BwArgs {
   const int* ptr;    // CSR (query side) or transposed CSR (key side) offsets
   const int* idx;    // the blocks of each list
   const int* order;  // blocks by descending list length
+  const int* len;    // 64-token blocks: coarse list lengths (entries c << 4 | 2 x 2 live bits)
   const float* ndelta;  // [BH, Np]: -(dO . O)
   const float* nlse2;   // [BH, Np]: -lse log2(e)
   __nv_bfloat16* d0;   // dq (query side) or dv (key side)
@@ -201,9 +202,10 @@ __device__ __forceinline__ void bw_setup(uint64_t* bars, uint32_t* tmem_base_s, 
 }
 
 // Producer of both kernels: the resident pair of tiles at block `own`, then
-// the streamed pair for every entry of the list. With rv0 != nullptr each
-// entry also brings the 128 floats of rv0 and rv1 at its block (the nlse2 and
-// ndelta rows of a query block) to sX + stage * BW_ROWVEC.
+// the streamed pair for every entry of the list (block list[u] >> shift).
+// With rv0 != nullptr each entry also brings the 128 floats of rv0 and rv1 at
+// its block (the nlse2 and ndelta rows of a query block) to sX + stage *
+// BW_ROWVEC.
 template <int D>
 __device__ __forceinline__ void bw_produce(const CUtensorMap* r0, const CUtensorMap* r1,
                                            const CUtensorMap* s0, const CUtensorMap* s1,
@@ -211,7 +213,8 @@ __device__ __forceinline__ void bw_produce(const CUtensorMap* r0, const CUtensor
                                            const int* list, int n, int bh, uint64_t* bars,
                                            long long lim, volatile int* abort_p,
                                            const float* rv0 = nullptr,
-                                           const float* rv1 = nullptr, uint32_t sX = 0) {
+                                           const float* rv1 = nullptr, uint32_t sX = 0,
+                                           int shift = 0) {
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   tma_prefetch_desc(r0);
   tma_prefetch_desc(r1);
@@ -223,7 +226,7 @@ __device__ __forceinline__ void bw_produce(const CUtensorMap* r0, const CUtensor
   bw_load_tile<D>(sR + kTile, r1, bar(KA_RES), own * TC_BLK, bh);
   int issued = 0;
   for (int u = 0; u < n; ++u) {
-    const int s = u % BW_NS, blk = list[u];
+    const int s = u % BW_NS, blk = list[u] >> shift;
     if (u >= BW_NS &&
         !mbar_wait_bounded(bar(KA_EMPTY + s), ((u / BW_NS) & 1) ^ 1, lim, abort_p))
       break;
@@ -261,8 +264,10 @@ __device__ __forceinline__ void bw_mma_drain(uint64_t* bars, bool ok, long long 
 // dK and dV of key block J = order[blockIdx % nb] of head blockIdx / nb.
 // TMEM: S^T [0, 128) (P^T packed over it), dP^T [128, 256) (dS^T packed over
 // it), dV [256, 384), dK [384, 512). Shared memory: K, V, then the Q ring and
-// the G ring.
-template <int D>
+// the G ring. SUB (64-token mask blocks): J is a pair of key blocks and each
+// entry a pair of query blocks; p is zero in the 64 x 64 quarters whose key
+// block does not see the query block.
+template <int D, bool SUB = false>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -282,7 +287,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x / a.nb;
   const int J = a.order[blockIdx.x % a.nb];
-  const int beg = a.ptr[J], n = a.ptr[J + 1] - beg;
+  const int beg = a.ptr[SUB ? 2 * J : J];
+  const int n = SUB ? a.len[J] : a.ptr[J + 1] - beg;
   const int* list = a.idx + beg;
   bw_setup(bars, &tmem_base_s, &abort_flag);
   const uint32_t tmem = tmem_base_s;
@@ -295,7 +301,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     if (lane == 0 && n > 0)
       bw_produce<D>(&map_k, &map_v, &map_q, &map_g, sK, sQ0, sG0, J, list, n, bh, bars, lim,
                     abort_p, a.nlse2 + static_cast<long long>(bh) * a.Np,
-                    a.ndelta + static_cast<long long>(bh) * a.Np, sX);
+                    a.ndelta + static_cast<long long>(bh) * a.Np, sX, SUB ? 4 : 0);
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       bool ok = mbar_wait_bounded(bar(KA_RES), 0, lim, abort_p) &&
@@ -351,13 +357,20 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
       tc_fence_after();
       float p[64];
       bw_ld64(tS + col, p);
+      // SUB: does this key row's block see this half's query block (warp-uniform)
+      const bool live = !SUB || ((list[u] >> (2 * (r >> 6) + h)) & 1);
+      if (live) {
 #pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        const float4 l = *reinterpret_cast<const float4*>(l2b + c);
-        ffma2_v(p[c], p[c + 1], p[c], p[c + 1], sl2, l.x, l.y);
-        ffma2_v(p[c + 2], p[c + 3], p[c + 2], p[c + 3], sl2, l.z, l.w);
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l = *reinterpret_cast<const float4*>(l2b + c);
+          ffma2_v(p[c], p[c + 1], p[c], p[c + 1], sl2, l.x, l.y);
+          ffma2_v(p[c + 2], p[c + 3], p[c + 2], p[c + 3], sl2, l.z, l.w);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) p[c + i] = ex2_approx(p[c + i]);
+          for (int i = 0; i < 4; ++i) p[c + i] = ex2_approx(p[c + i]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) p[c] = 0.f;
       }
       bw_st_packed(tS + col, p);
       tc_fence_before();
@@ -404,8 +417,10 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
 
 // dQ of query block I = order[blockIdx % nb] of head blockIdx / nb.
 // TMEM: S [0, 128), dP [128, 256) (dS packed over it), dQ [256, 384).
-// Shared memory: Q, G, then the K ring and the V ring.
-template <int D>
+// Shared memory: Q, G, then the K ring and the V ring. SUB (64-token mask
+// blocks): I is a pair of query blocks and each entry a pair of key blocks;
+// p is zero in the 64 x 64 quarters that are not live.
+template <int D, bool SUB = false>
 __global__ void __launch_bounds__(BW_THREADS, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap map_q,
                      const __grid_constant__ CUtensorMap map_k,
@@ -423,7 +438,8 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x / a.nb;
   const int I = a.order[blockIdx.x % a.nb];
-  const int beg = a.ptr[I], n = a.ptr[I + 1] - beg;
+  const int beg = a.ptr[SUB ? 2 * I : I];
+  const int n = SUB ? a.len[I] : a.ptr[I + 1] - beg;
   const int* list = a.idx + beg;
   bw_setup(bars, &tmem_base_s, &abort_flag);
   const uint32_t tmem = tmem_base_s;
@@ -435,7 +451,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
   if (warp == 0) {
     if (lane == 0 && n > 0)
       bw_produce<D>(&map_q, &map_g, &map_k, &map_v, sQ, sK0, sV0, I, list, n, bh, bars, lim,
-                    abort_p);
+                    abort_p, nullptr, nullptr, 0, SUB ? 4 : 0);
   } else if (warp == 1) {
     if (lane == 0 && n > 0) {
       bool ok = mbar_wait_bounded(bar(KA_RES), 0, lim, abort_p) &&
@@ -480,8 +496,12 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int u = 0; u < n; ++u) {
-      // key columns of this half that are real tokens (the last block is ragged)
-      const int kvalid = a.N - list[u] * TC_BLK - h * 64;
+      // key columns of this half that are real tokens (the last block is ragged);
+      // SUB: none if this row's query block does not see this half's key block
+      const int e = list[u];
+      const int kvalid = (!SUB || ((e >> (2 * (r >> 6) + h)) & 1))
+                             ? a.N - (e >> (SUB ? 4 : 0)) * TC_BLK - h * 64
+                             : 0;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar(KA_S), u & 1, lim, abort_p))))
         break;
       tc_fence_after();
@@ -495,7 +515,7 @@ __global__ void __launch_bounds__(BW_THREADS, 1)
         p[c] = ex2_approx(p[c]);
         p[c + 1] = ex2_approx(p[c + 1]);
       }
-      if (kvalid < 64) {  // warp-uniform: only the ragged last key block
+      if (kvalid < 64) {  // warp-uniform: the ragged last key block (SUB: or a dead quarter)
 #pragma unroll
         for (int c = 0; c < 64; ++c) p[c] = c < kvalid ? p[c] : 0.f;
       }

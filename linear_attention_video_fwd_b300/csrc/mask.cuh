@@ -257,6 +257,46 @@ __global__ void quad_merge_kernel(int nb, const int* __restrict__ row_ptr,
   qlen[Q] = k;
 }
 
+// Coarse pairs for the backward on 64-token blocks: row R of the coarse list
+// merges rows 2R and 2R + 1 of a block list (the CSR, or the transposed lists)
+// by coarse index c = idx >> 1; entry = c << 4 | sub, sub bit 2a + b meaning
+// that row 2R + a lists block 2c + b. Row R's entries start at ptr[2R]. One
+// thread per coarse row.
+__global__ void coarse_pair_merge_kernel(int nb, const int* __restrict__ ptr,
+                                         const int* __restrict__ idx, int* __restrict__ ccol,
+                                         int* __restrict__ clen) {
+  const int R = blockIdx.x * blockDim.x + threadIdx.x;
+  const int ncoarse = (nb + 1) / 2;
+  if (R >= ncoarse) return;
+  int cur[2], end[2];
+#pragma unroll
+  for (int a = 0; a < 2; ++a) {
+    const int row = 2 * R + a;
+    cur[a] = row < nb ? ptr[row] : 0;
+    end[a] = row < nb ? ptr[row + 1] : 0;
+  }
+  const int out = ptr[2 * R];
+  int k = 0;
+  while (true) {
+    int c = 0x7fffffff;
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+      if (cur[a] < end[a]) c = min(c, idx[cur[a]] >> 1);
+    if (c == 0x7fffffff) break;
+    int sub = 0;
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      while (cur[a] < end[a] && (idx[cur[a]] >> 1) == c) {
+        sub |= 1 << (2 * a + (idx[cur[a]] & 1));
+        ++cur[a];
+      }
+    }
+    ccol[out + k] = (c << 4) | sub;
+    ++k;
+  }
+  clen[R] = k;
+}
+
 // Single thread: quads ordered by descending summed length of their four rows
 // (stable counting sort; lengths are 0..4*nb). hist must hold 4*nb + 2 ints.
 __global__ void quad_order_kernel(int nb, const int* __restrict__ row_ptr,

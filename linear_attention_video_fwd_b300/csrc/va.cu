@@ -225,6 +225,15 @@ struct va_mask {
   int32_t* t_ptr = nullptr;    // device [nqb + 1]
   int32_t* t_row = nullptr;    // device [nnz]
   int32_t* t_order = nullptr;  // device [nqb]
+  // 64-token blocks only: coarse pairs for the tensor-core backward
+  // (coarse_pair_merge_kernel): query-block pairs over key-block pairs (dq)
+  // and key-block pairs over query-block pairs (dk, dv); entry c << 4 | sub
+  int32_t* cq_col = nullptr;   // device [nnz], rows start at row_ptr[2R]
+  int32_t* cq_len = nullptr;   // device [ceil(nqb / 2)]
+  int32_t* cq_order = nullptr;
+  int32_t* ck_col = nullptr;   // device [nnz], rows start at t_ptr[2R]
+  int32_t* ck_len = nullptr;
+  int32_t* ck_order = nullptr;
   int device = 0;
 };
 
@@ -493,6 +502,32 @@ VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params*
       va_mask_free(m);
       return st;
     }
+    if (m->p.block == 64) {
+      // coarse pairs of both lists for the tensor-core backward
+      const int nc = (md.nb + 1) / 2;
+      const size_t nn = static_cast<size_t>(m->nnz > 0 ? m->nnz : 1);
+      int* chist = nullptr;
+      if ((st = scratch.alloc(&chist, 2 * static_cast<size_t>(md.nb) + 2)) ||
+          (st = cuda_status(cudaMalloc(&m->cq_col, sizeof(int32_t) * nn))) ||
+          (st = cuda_status(cudaMalloc(&m->cq_len, sizeof(int32_t) * nc))) ||
+          (st = cuda_status(cudaMalloc(&m->cq_order, sizeof(int32_t) * nc))) ||
+          (st = cuda_status(cudaMalloc(&m->ck_col, sizeof(int32_t) * nn))) ||
+          (st = cuda_status(cudaMalloc(&m->ck_len, sizeof(int32_t) * nc))) ||
+          (st = cuda_status(cudaMalloc(&m->ck_order, sizeof(int32_t) * nc)))) {
+        va_mask_free(m);
+        return st;
+      }
+      va::coarse_pair_merge_kernel<<<(nc + 127) / 128, 128, 0, s>>>(md.nb, m->row_ptr, m->col,
+                                                                     m->cq_col, m->cq_len);
+      va::coarse_pair_merge_kernel<<<(nc + 127) / 128, 128, 0, s>>>(md.nb, m->t_ptr, m->t_row,
+                                                                     m->ck_col, m->ck_len);
+      va::pair_order_kernel<<<1, 1, 0, s>>>(md.nb, m->row_ptr, m->cq_order, chist);
+      va::pair_order_kernel<<<1, 1, 0, s>>>(md.nb, m->t_ptr, m->ck_order, chist);
+      if ((st = launch_status())) {
+        va_mask_free(m);
+        return st;
+      }
+    }
   }
   if ((st = cuda_status(cudaStreamSynchronize(s)))) {
     va_mask_free(m);
@@ -547,6 +582,8 @@ VA_EXPORT int va_mask_free(va_mask* m) {
   if (m->qcol) cudaFree(m->qcol);
   if (m->qlen) cudaFree(m->qlen);
   if (m->qorder) cudaFree(m->qorder);
+  for (int32_t* pp : {m->cq_col, m->cq_len, m->cq_order, m->ck_col, m->ck_len, m->ck_order})
+    if (pp) cudaFree(pp);
   if (m->t_ptr) cudaFree(m->t_ptr);
   if (m->t_row) cudaFree(m->t_row);
   if (m->t_order) cudaFree(m->t_order);
@@ -669,7 +706,8 @@ int launch_bwd_simt(const void* q, const void* k, const void* v, const void* g, 
   return launch_status();
 }
 
-template <int D>
+// SUB: a mask of 64-token blocks, run on its coarse pairs (128-token tiles).
+template <int D, bool SUB = false>
 int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, const va_mask* m,
                   const float* ndelta, const float* nlse2, void* dq, void* dk, void* dv, int BH,
                   int N, int Np, float scale, cudaStream_t s) {
@@ -679,10 +717,10 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, co
   if (st) return st;
   st = device_once(once, dev, [] {
     int r;
-    if ((r = cuda_status(cudaFuncSetAttribute(va::bwd_dkdv_tc_kernel<D>,
+    if ((r = cuda_status(cudaFuncSetAttribute(va::bwd_dkdv_tc_kernel<D, SUB>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               va::BwDim<D>::kSmemBytes))) ||
-        (r = cuda_status(cudaFuncSetAttribute(va::bwd_dq_tc_kernel<D>,
+        (r = cuda_status(cudaFuncSetAttribute(va::bwd_dq_tc_kernel<D, SUB>,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               va::BwDim<D>::kSmemBytes))))
       return r;
@@ -693,31 +731,35 @@ int launch_bwd_tc(const void* q, const void* k, const void* v, const void* g, co
   if ((st = encode_bf16_rows(&mq, q, BH, N, D)) || (st = encode_bf16_rows(&mk, k, BH, N, D)) ||
       (st = encode_bf16_rows(&mv, v, BH, N, D)) || (st = encode_bf16_rows(&mg, g, BH, N, D)))
     return st;
-  const long long grid = static_cast<long long>(m->nqb) * BH;
+  if (SUB && (m->cq_col == nullptr || m->ck_col == nullptr)) return VA_ERR_UNSUPPORTED;
+  const int nb = SUB ? (m->nqb + 1) / 2 : m->nqb;  // 128-token tiles
+  const long long grid = static_cast<long long>(nb) * BH;
   if (grid > 0x7fffffffLL) return VA_ERR_UNSUPPORTED;
   va::BwArgs a;
   a.ndelta = ndelta;
   a.nlse2 = nlse2;
   a.N = N;
   a.Np = Np;
-  a.nb = m->nqb;
+  a.nb = nb;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit = g_wait_limit;
   a.ptr = m->t_ptr;
-  a.idx = m->t_row;
-  a.order = m->t_order;
+  a.idx = SUB ? m->ck_col : m->t_row;
+  a.order = SUB ? m->ck_order : m->t_order;
+  a.len = SUB ? m->ck_len : nullptr;
   a.d0 = static_cast<__nv_bfloat16*>(dv);
   a.d1 = static_cast<__nv_bfloat16*>(dk);
-  va::bwd_dkdv_tc_kernel<D>
+  va::bwd_dkdv_tc_kernel<D, SUB>
       <<<static_cast<unsigned>(grid), va::BW_THREADS, va::BwDim<D>::kSmemBytes, s>>>(mq, mk, mv,
                                                                                   mg, a);
   a.ptr = m->row_ptr;
-  a.idx = m->col;
-  a.order = m->order;
+  a.idx = SUB ? m->cq_col : m->col;
+  a.order = SUB ? m->cq_order : m->order;
+  a.len = SUB ? m->cq_len : nullptr;
   a.d0 = static_cast<__nv_bfloat16*>(dq);
   a.d1 = nullptr;
-  va::bwd_dq_tc_kernel<D>
+  va::bwd_dq_tc_kernel<D, SUB>
       <<<static_cast<unsigned>(grid), va::BW_THREADS, va::BwDim<D>::kSmemBytes, s>>>(mq, mk, mv,
                                                                                 mg, a);
   return launch_status();
@@ -744,8 +786,10 @@ VA_EXPORT int va_sparse_attn_bwd(const void* q, const void* k, const void* v, co
   if (BH64 * N >= (1LL << 31)) return VA_ERR_UNSUPPORTED;
   const int BH = static_cast<int>(BH64);
   const int blk = m->p.block;
-  const int Np = m->nqb * blk;
-  const bool tc = dtype == VA_BF16 && (d == 64 || d == 128) && blk == 128;
+  const bool tc = dtype == VA_BF16 && (d == 64 || d == 128) && (blk == 64 || blk == 128);
+  // rows of the per-row scratch, whole blocks (whole 128-token tiles on the
+  // tensor-core path with 64-token blocks)
+  const int Np = tc && blk == 64 ? (m->nqb + 1) / 2 * 128 : m->nqb * blk;
   const bool simt = dtype == VA_F32 && (d == 64 || d == 128) && (blk == 64 || blk == 128);
   if (!tc && !simt) return VA_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -761,6 +805,11 @@ VA_EXPORT int va_sparse_attn_bwd(const void* q, const void* k, const void* v, co
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, N,
         Np, d, ndelta, nlse2);
     if ((st = launch_status())) return st;
+    if (blk == 64)
+      return d == 64 ? launch_bwd_tc<64, true>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH,
+                                               N, Np, scale, s)
+                     : launch_bwd_tc<128, true>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH,
+                                                N, Np, scale, s);
     if (d == 64)
       return launch_bwd_tc<64>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);
     return launch_bwd_tc<128>(q, k, v, dout, m, ndelta, nlse2, dq, dk, dv, BH, N, Np, scale, s);

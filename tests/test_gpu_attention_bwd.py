@@ -104,6 +104,28 @@ def test_bf16_small_all_rows(va, dev, case, d):
     _check(va, dev, q, k, v, g, kind, T, H, W, p, step, "bf16")
 
 
+# 64-token mask blocks on the tensor-core kernels: 128-token tiles over pairs
+# of blocks with the dead 64 x 64 quarters zeroed; odd block counts and ragged
+# tails, and an LVSA mask whose transposed lists differ from its rows
+SMALL_BF16_B64 = [
+    (OM.RADIAL, 5, 6, 20, OM.MaskParams(block=64, w0=10), 0),           # 10 blocks, tail 24
+    (OM.LVSA, 12, 7, 9, OM.MaskParams(block=64, local=1, period=4, anchor0=2, rot_stride=3), 2),
+    (OM.LVSA, 10, 8, 16, OM.MaskParams(block=64, local=0, period=3, anchor0=1, rot_stride=1), 1),
+    (OM.DENSE, 3, 7, 13, OM.MaskParams(block=64), 0),                  # 5 blocks, tail 17
+    (OM.RADIAL, 1, 3, 5, OM.MaskParams(block=64), 0),                   # N=15 < block
+]
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("case", SMALL_BF16_B64)
+def test_bf16_block64_small_all_rows(va, dev, case, d):
+    kind, T, H, W, p, step = case
+    N = T * H * W
+    q, k, v = synth.video_qkv(1, 2, T, H, W, d, seed=17)
+    g = synth.upstream_grad(1, 2, N, d, seed=17)
+    _check(va, dev, q, k, v, g, kind, T, H, W, p, step, "bf16")
+
+
 @pytest.mark.parametrize("d", [128, 64])
 def test_bf16_other_scale_and_lvsa_asymmetry(va, dev, d):
     # LVSA's anchor frames make the block mask asymmetric, so the transposed
@@ -183,8 +205,4 @@ def test_backward_rejects_bad_arguments(va, dev):
     with pytest.raises(va.VAError) as e:
         va.sparse_attn_bwd(q, q, q, q, q, lse, m2)
     assert e.value.status == va.ERR_INVALID
-    m64 = va.mask_build(va.RADIAL, 3, 4, 20, block=64)   # bf16 gradients need block 128
-    with pytest.raises(va.VAError) as e:
-        va.sparse_attn_bwd(q, q, q, q, q, lse, m64)
-    assert e.value.status == va.ERR_UNSUPPORTED
     assert va.device_error() == va.OK
