@@ -226,11 +226,6 @@ __device__ __forceinline__ void tc_pv_group(uint32_t d, uint32_t p, uint32_t blo
       : "memory");
 }
 
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

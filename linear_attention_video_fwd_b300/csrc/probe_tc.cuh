@@ -199,7 +199,7 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
     for (int j = 0; j < 64; ++j) {
       const bool valid = (j & 15) < (m4[j >> 4] & 31);
       if (PASS == 2 && valid) lsum[j >> 4] += s[j];
-      s[j] = valid ? exp2f(fmaf(s[j], sl2, -m2)) : 0.f;
+      s[j] = valid ? ex2_approx(fmaf(s[j], sl2, -m2)) : 0.f;
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -253,7 +253,7 @@ __device__ __forceinline__ void pt_softmax(const ProbeArgs& a, int bh, int pt, i
           // compensated weight n_c 2^(lbar sl2 - m2) of the centroid
           const float nf = static_cast<float>(nv);
           zc_s[slot][r] = zc;
-          w_s[slot][r] = nf * exp2f(fmaf(ls / nf, sl2, -m2));
+          w_s[slot][r] = nf * ex2_approx(fmaf(ls / nf, sl2, -m2));
           vc_s[slot][r] = vc_pre;
           if (r == 0) cid_s[slot] = cur_c;
           mbar_arrive(smem_u32(&bars[PB_ZF + slot]));

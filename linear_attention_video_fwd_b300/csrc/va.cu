@@ -1674,9 +1674,17 @@ int run_compensate(const T* q, const T* k, const T* v, const int* qassign, int C
     return st;
   va::route_init_kernel<<<(BH * 256 + 255) / 256, 256, 0, s>>>(budget, BH, rstate, rhist, rcount);
   const dim3 gsel((Cq * Ck + va::RS_PER_CTA - 1) / va::RS_PER_CTA, BH);
-  for (int shift = 56; shift >= 0; shift -= 8)
+  // The low 32 bits of a key are the block index p * Ck + c: digits above its
+  // bit length are 0 in every valid key, so those passes would only append
+  // zero digits to the prefix (the mass under the prefix always exceeds the
+  // remaining budget after the first pass) and are skipped.
+  int idx_bits = 0;
+  while (idx_bits < 32 && (static_cast<long long>(Cq) * Ck - 1) >> idx_bits) ++idx_bits;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    if (shift < 32 && shift >= idx_bits) continue;
     va::route_pass_kernel<<<gsel, va::RS_THREADS, 0, s>>>(rkeys, rcosts, Cq * Ck, shift, rstate,
                                                            rhist, rcount);
+  }
   va::route_cut_kernel<<<(BH + 255) / 256, 256, 0, s>>>(rstate, BH, cut);
   va::route_mark_kernel<<<dim3(Cq, BH), 256, 0, s>>>(err, nq, nk, Cq, Ck, cut, sel, seln, selc);
   if ((st = launch_status())) return st;
