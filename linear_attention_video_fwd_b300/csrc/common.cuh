@@ -330,6 +330,17 @@ __device__ __forceinline__ void ffma2_v(float& d0, float& d1, float a0, float a1
       : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
 }
 
+// (s0, s1) += (a0 * a0, a1 * a1) as one packed f32x2 FMA.
+__device__ __forceinline__ void fsq2_acc(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rs;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rs, {%0, %1};\n\t"
+      "fma.rn.f32x2 rs, ra, ra, rs;\n\t"
+      "mov.b64 {%0, %1}, rs;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
 // (s0, s1) += (a0, a1) as one packed f32x2 add.
 __device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float a1) {
   asm("{\n\t.reg .b64 ra, rs;\n\t"

@@ -351,7 +351,10 @@ __device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, 
     const float w = w_s[slot][r];
     const float4* vc4 = reinterpret_cast<const float4*>(vc_s[slot]);
     const uint32_t tE = tmem + PT_T_ACC + slot * 128 + lane_off;
-    float n2 = 0.f;
+    // r = E_c - Zc O - w (vc - O) = (E_c + (w - Zc) O) - w vc, two packed
+    // FMAs per pair of dims, and |r|^2 accumulated by a third.
+    const float al = w - zc, nw = -w;
+    float n2a = 0.f, n2b = 0.f;
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) {
       uint32_t v[32];
@@ -360,18 +363,20 @@ __device__ __forceinline__ void pt_residual(const ProbeArgs& a, int bh, int pt, 
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         const float4 vv = vc4[(q * 32 + i) / 4];
-        const float vcv[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float o = O[q * 32 + i + k];
-          const float re = fmaf(-w, vcv[k] - o, fmaf(-zc, o, __uint_as_float(v[i + k])));
-          n2 = fmaf(re, re, n2);
-        }
+        const int o = q * 32 + i;
+        float t0, t1, t2, t3;
+        ffma2_v(t0, t1, O[o], O[o + 1], al, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+        ffma2_v(t2, t3, O[o + 2], O[o + 3], al, __uint_as_float(v[i + 2]),
+                __uint_as_float(v[i + 3]));
+        ffma2_v(t0, t1, vv.x, vv.y, nw, t0, t1);
+        ffma2_v(t2, t3, vv.z, vv.w, nw, t2, t3);
+        fsq2_acc(n2a, n2b, t0, t1);
+        fsq2_acc(n2a, n2b, t2, t3);
       }
     }
     tc_fence_before();
     mbar_arrive(smem_u32(&bars[PB_EE + slot]));
-    if (write) errr[c] = sqrtf(n2) * invZ;
+    if (write) errr[c] = sqrtf(n2a + n2b) * invZ;
   }
 }
 
