@@ -171,6 +171,56 @@ int va_mask_build_static(int kind, int T, int H, int W, const va_mask_params* pa
                          va_stream_t stream);
 
 /*
+ * Mask cache: reuse of block masks across denoising steps (LVSA review,
+ * secrett2633 blog, sec. 3: the anchors rotate with the denoising step, so a
+ * step's mask repeats once the rotation comes round; Radial Attention news
+ * page, hyper.ai: the radial mask is static, one for every step).
+ *
+ * va_mask_cache_get returns the library-owned mask for (kind, grid, params,
+ * step) on the current device, building it with va_mask_build on the first
+ * request and returning the same handle afterwards. Requests that differ only
+ * in what the CSR does not depend on share one entry: a radial or dense mask
+ * ignores `step` (and the LVSA fields); an LVSA mask with period > 0 depends
+ * on the step only through the phase (anchor0 + rot_stride * step) mod
+ * period, so period distinct phases cover every step. The returned handle's
+ * recorded step is the one it was built for; its CSR is bit-identical to
+ * va_mask_build at the requested step.
+ *
+ * Ownership: the cache owns its masks. Do not pass them to va_mask_free. A
+ * handle stays valid until va_mask_cache_clear or va_mask_cache_destroy on
+ * its cache; the cache never evicts by itself. A miss with `capacity` entries
+ * already held returns VA_ERR_UNSUPPORTED and builds nothing.
+ * Calls on one cache are serialised by a mutex. A hit does no device work and
+ * does not touch `stream`; a miss synchronises `stream` once (as
+ * va_mask_build). Clearing frees each mask on its own device; free its masks
+ * only after the kernels that read them have completed.
+ * Errors: VA_ERR_INVALID (null pointers, capacity outside
+ * 1..VA_MASK_CACHE_MAX, and the argument errors of va_mask_build),
+ * VA_ERR_UNSUPPORTED (cache full, or as va_mask_build), VA_ERR_OOM,
+ * VA_ERR_CUDA.
+ */
+#define VA_MASK_CACHE_MAX 4096
+typedef struct va_mask_cache va_mask_cache; /* opaque, library-owned */
+int va_mask_cache_create(int capacity, va_mask_cache** out);
+int va_mask_cache_get(va_mask_cache* cache, int kind, int T, int H, int W,
+                      const va_mask_params* params, int step, const va_mask** out,
+                      va_stream_t stream);
+/* Counters of a cache: requests served from it, masks built, entries held.
+ * Any output pointer may be NULL. Errors: VA_ERR_INVALID for a NULL cache. */
+int va_mask_cache_stats(va_mask_cache* cache, int64_t* hits, int64_t* misses, int* entries);
+/* Frees every mask of the cache (their handles become invalid) and keeps the
+ * cache. Errors: VA_ERR_INVALID for a NULL cache. */
+int va_mask_cache_clear(va_mask_cache* cache);
+/* Clears and frees the cache. NULL is a no-op. */
+int va_mask_cache_destroy(va_mask_cache* cache);
+/* Host only: *same = 1 when the cache serves (kind, grid, params) at steps
+ * step_a and step_b from one entry (their CSRs are identical), else 0.
+ * Errors: the argument errors of va_mask_build (VA_ERR_INVALID,
+ * VA_ERR_UNSUPPORTED); *same is 0 then. */
+int va_mask_same(int kind, int T, int H, int W, const va_mask_params* params, int step_a,
+                 int step_b, int* same);
+
+/*
  * Block-sparse attention forward (LVSA review, secrett2633 blog, sec. 1:
  * attention computed only on the live blocks of a block-sparse mask; Radial
  * Attention news page, hyper.ai: the same computation under the static
@@ -335,6 +385,8 @@ int va_lipar_restore(const void* y, const int32_t* src, int B, int heads, int N,
  * seeded random draw, supplied by the caller). Outputs (device, caller-owned):
  * assign int32 [B, heads, N], centroid float32 [B, heads, C, d] (means of the
  * returned assignment), count int32 [B, heads, C]. Distances are float32.
+ * Deterministic: member sums are exact (bf16) or taken over member lists in
+ * ascending token order (float32), so repeated calls are bit-identical.
  * Scratch: allocated and released on `stream` (stream-ordered allocator).
  * Supported: dtype VA_BF16 or VA_F32, d in {64, 128}, 1 <= C <= min(N, 4096).
  * Errors: VA_ERR_INVALID, VA_ERR_UNSUPPORTED, VA_ERR_OOM, VA_ERR_CUDA.
@@ -377,6 +429,9 @@ int va_cluster_from(const void* x, const float* centroid_init, int B, int heads,
  * out: [B, heads, N, d] of dtype (bf16 for VA_BF16, float32 for VA_F32).
  * err_out: NULL or device float32 [B, heads, Cq, Ck] (the probe errors).
  * sel_out: NULL or device uint8 [B, heads, Cq, Ck] (1 = computed exactly).
+ * Deterministic: the member lists hold each cluster's tokens in ascending
+ * order, so repeated calls on the same inputs return bit-identical out,
+ * err_out and sel_out.
  * Scratch: allocated and released on `stream` (stream-ordered allocator).
  * Supported: d in {64, 128}, 1 <= Cq, Ck <= 4096, 0 <= density <= 1.
  * Errors: VA_ERR_INVALID, VA_ERR_UNSUPPORTED, VA_ERR_OOM, VA_ERR_CUDA;

@@ -50,6 +50,15 @@ def _load():
         "va_mask_info": [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i64)],
         "va_mask_to_host": [vp, i32p, i32p],
         "va_mask_free": [vp],
+        "va_mask_cache_create": [i32, ctypes.POINTER(vp)],
+        "va_mask_cache_get": [vp, i32, i32, i32, i32, ctypes.POINTER(_MaskParams), i32,
+                              ctypes.POINTER(vp), vp],
+        "va_mask_cache_stats": [vp, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                ctypes.POINTER(i32)],
+        "va_mask_cache_clear": [vp],
+        "va_mask_cache_destroy": [vp],
+        "va_mask_same": [i32, i32, i32, i32, ctypes.POINTER(_MaskParams), i32, i32,
+                         ctypes.POINTER(i32)],
         "va_sparse_attn_fwd": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp],
         "va_sparse_attn_fwd_host": [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, vp],
         "va_sparse_attn_bwd": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, f32,
@@ -121,10 +130,13 @@ def _require_cuda(*ts):
 
 
 class Mask:
-    """A library-owned block mask (device CSR). Free with .free() or on GC."""
+    """A library-owned block mask (device CSR). Free with .free() or on GC;
+    a mask from a MaskCache belongs to the cache and is freed by it."""
 
-    def __init__(self, handle, kind, T, H, W, params, step):
+    def __init__(self, handle, kind, T, H, W, params, step, cache=None):
         self._h = handle
+        self._cache = cache
+        self._gen = cache._gen if cache is not None else 0
         self.kind, self.T, self.H, self.W, self.step = kind, T, H, W, step
         self.params = params
         nqb, nnz = ctypes.c_int(), ctypes.c_int64()
@@ -138,6 +150,9 @@ class Mask:
 
     @property
     def handle(self):
+        c = self._cache
+        if c is not None and (c._h is None or c._gen != self._gen):
+            raise VAError(ERR_INVALID, "mask of a cleared or closed MaskCache")
         return self._h
 
     def csr(self):
@@ -150,9 +165,9 @@ class Mask:
         return rp, col[: self.nnz]
 
     def free(self):
-        if self._h:
+        if self._h and self._cache is None:
             _lib.va_mask_free(self._h)
-            self._h = None
+        self._h = None
 
     def __del__(self):
         try:
@@ -170,6 +185,69 @@ def mask_build(kind: int, T: int, H: int, W: int, block: int = 128, w0: int = 0,
     _check(_lib.va_mask_build(kind, T, H, W, ctypes.byref(p), step, ctypes.byref(h),
                               _stream(stream)), "va_mask_build")
     return Mask(h, kind, T, H, W, p, step)
+
+
+def _mask_params(block, w0, local, period, anchor0, rot_stride):
+    return _MaskParams(block, w0, local, period, anchor0, rot_stride)
+
+
+class MaskCache:
+    """va_mask_cache: block masks reused across denoising steps. get() builds a
+    mask on its first request and returns the cached one afterwards; requests
+    that differ only in what the CSR does not depend on (the step of a radial
+    mask, the LVSA rotation phase) share one entry."""
+
+    def __init__(self, capacity: int = 64):
+        h = ctypes.c_void_p()
+        _check(_lib.va_mask_cache_create(capacity, ctypes.byref(h)), "va_mask_cache_create")
+        self._h = h
+        self._gen = 0
+
+    def get(self, kind: int, T: int, H: int, W: int, block: int = 128, w0: int = 0,
+            local: int = 1, period: int = 0, anchor0: int = 0, rot_stride: int = 1,
+            step: int = 0, stream=None) -> Mask:
+        if self._h is None:
+            raise VAError(ERR_INVALID, "closed MaskCache")
+        p = _mask_params(block, w0, local, period, anchor0, rot_stride)
+        m = ctypes.c_void_p()
+        _check(_lib.va_mask_cache_get(self._h, kind, T, H, W, ctypes.byref(p), step,
+                                      ctypes.byref(m), _stream(stream)), "va_mask_cache_get")
+        return Mask(m, kind, T, H, W, p, step, cache=self)
+
+    def stats(self):
+        """(hits, misses, entries)."""
+        hits, misses, entries = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int()
+        _check(_lib.va_mask_cache_stats(self._h, ctypes.byref(hits), ctypes.byref(misses),
+                                        ctypes.byref(entries)), "va_mask_cache_stats")
+        return hits.value, misses.value, entries.value
+
+    def clear(self):
+        """Free every cached mask; masks returned earlier become invalid."""
+        self._gen += 1
+        _check(_lib.va_mask_cache_clear(self._h), "va_mask_cache_clear")
+
+    def close(self):
+        if self._h is not None:
+            _lib.va_mask_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def mask_same(kind: int, T: int, H: int, W: int, step_a: int, step_b: int, block: int = 128,
+              w0: int = 0, local: int = 1, period: int = 0, anchor0: int = 0,
+              rot_stride: int = 1) -> bool:
+    """va_mask_same (host only): whether a MaskCache serves the two steps from
+    one entry."""
+    p = _mask_params(block, w0, local, period, anchor0, rot_stride)
+    same = ctypes.c_int()
+    _check(_lib.va_mask_same(kind, T, H, W, ctypes.byref(p), step_a, step_b,
+                             ctypes.byref(same)), "va_mask_same")
+    return bool(same.value)
 
 
 def sparse_attn_fwd(q, k, v, mask: Mask, scale: float | None = None, out=None, lse=None,

@@ -227,6 +227,85 @@ __global__ void km_scatter_kernel(const int* __restrict__ assign, int N, int C,
   perm[static_cast<long long>(bh) * N + pos] = i;
 }
 
+// Stable member lists: perm[off[a] + k] = the k-th member of cluster a in
+// ascending token order, so that everything summed over a member list (fp32
+// means, probe and attention accumulations) is the same on every call. Tiles
+// of KS_TILE tokens: per-tile member counts, a scan of those counts down the
+// tiles of each cluster, then one warp per tile placing its tokens in order.
+// base is [BH][ntiles][C]. Assignment values outside [0, C) are reported as
+// VA_ERR_DEVICE and skipped.
+constexpr int KS_TILE = 1024;
+
+__global__ void __launch_bounds__(256) km_tile_count_kernel(const int* __restrict__ assign, int N,
+                                                            int C, int* __restrict__ base) {
+  extern __shared__ int hist[];  // [C]
+  const int bh = blockIdx.y, tile = blockIdx.x, ntiles = gridDim.x;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) hist[c] = 0;
+  __syncthreads();
+  const int i0 = tile * KS_TILE, i1 = min(N, i0 + KS_TILE);
+  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
+    const int a = assign[static_cast<long long>(bh) * N + i];
+    if (a >= 0 && a < C) {
+      atomicAdd(&hist[a], 1);
+    } else {
+      raise_error(VA_ERR_DEVICE);
+    }
+  }
+  __syncthreads();
+  int* row = base + (static_cast<long long>(bh) * ntiles + tile) * C;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) row[c] = hist[c];
+}
+
+// In place: base[t][c] <- off[c] + sum over tiles t' < t of count[t'][c].
+__global__ void km_tile_scan_kernel(const int* __restrict__ off, int C, int ntiles,
+                                    int* __restrict__ base) {
+  const int bh = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  int run = off[static_cast<long long>(bh) * (C + 1) + c];
+  int* col = base + static_cast<long long>(bh) * ntiles * C + c;
+  for (int t0 = 0; t0 < ntiles; t0 += 8) {
+    int v[8];  // eight loads in flight before the stores
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      v[j] = t0 + j < ntiles ? col[static_cast<long long>(t0 + j) * C] : 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (t0 + j < ntiles) col[static_cast<long long>(t0 + j) * C] = run;
+      run += v[j];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(128) km_tile_place_kernel(const int* __restrict__ assign, int N,
+                                                            int C,
+                                                            const int* __restrict__ base,
+                                                            int* __restrict__ perm) {
+  extern __shared__ int next[];  // [C]: next free slot of each cluster
+  const int bh = blockIdx.y, tile = blockIdx.x, ntiles = gridDim.x;
+  const int* row = base + (static_cast<long long>(bh) * ntiles + tile) * C;
+  for (int c = threadIdx.x; c < C; c += blockDim.x) next[c] = row[c];
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int i0 = tile * KS_TILE, i1 = min(N, i0 + KS_TILE);
+  for (int i = i0 + lane; i - lane < i1; i += 32) {
+    const bool inr = i < i1;
+    const int a = inr ? assign[static_cast<long long>(bh) * N + i] : -1;
+    const bool valid = inr && a >= 0 && a < C;
+    const unsigned grp = __match_any_sync(0xffffffffu, valid ? a : -1);
+    const int leader = __ffs(grp) - 1;
+    int pos = 0;
+    if (valid) {
+      pos = next[a] + __popc(grp & ((1u << lane) - 1u));
+      perm[static_cast<long long>(bh) * N + pos] = i;
+    }
+    __syncwarp();
+    if (valid && lane == leader) next[a] += __popc(grp);
+    __syncwarp();
+  }
+}
+
 // Histogram of an externally supplied assignment (range-checked).
 __global__ void km_count_kernel(const int* __restrict__ assign, int N, int C,
                                 int* __restrict__ count) {

@@ -10,6 +10,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <new>
 #include <type_traits>
 #include <vector>
 #include <utility>
@@ -357,20 +358,35 @@ VA_EXPORT int va_selftest_wait_timeout(int64_t cycles, va_stream_t stream) {
 
 // ------------------------------------------------------------------ masks --
 
+namespace {
+
+// Host checks shared by the mask entries: kind, grid and parameters. Sets the
+// token count N and the block count nb; the callers apply their block limits.
+int mask_grid_args(int kind, int T, int H, int W, const va_mask_params& p, int64_t* N64,
+                   int64_t* nb64) {
+  if (kind != VA_MASK_DENSE && kind != VA_MASK_RADIAL && kind != VA_MASK_LVSA)
+    return VA_ERR_INVALID;
+  if (T < 1 || H < 1 || W < 1) return VA_ERR_INVALID;
+  const int64_t n = static_cast<int64_t>(H) * W * T;
+  if (n >= (1LL << 30)) return VA_ERR_INVALID;
+  if (p.block < 1 || p.block > 4096) return VA_ERR_INVALID;
+  if (p.w0 < 0 || p.local < 0 || p.period < 0) return VA_ERR_INVALID;
+  *N64 = n;
+  *nb64 = (n + p.block - 1) / p.block;
+  return VA_OK;
+}
+
+}  // namespace
+
 VA_EXPORT int va_mask_build(int kind, int T, int H, int W, const va_mask_params* params,
                             int step, va_mask** out, va_stream_t stream) {
   if (out == nullptr || params == nullptr) return VA_ERR_INVALID;
   *out = nullptr;
-  if (kind != VA_MASK_DENSE && kind != VA_MASK_RADIAL && kind != VA_MASK_LVSA)
-    return VA_ERR_INVALID;
-  if (T < 1 || H < 1 || W < 1) return VA_ERR_INVALID;
-  const int64_t F64 = static_cast<int64_t>(H) * W;
-  const int64_t N64 = F64 * T;
-  if (N64 >= (1LL << 30)) return VA_ERR_INVALID;
   const va_mask_params p = *params;
-  if (p.block < 1 || p.block > 4096) return VA_ERR_INVALID;
-  if (p.w0 < 0 || p.local < 0 || p.period < 0) return VA_ERR_INVALID;
-  if ((N64 + p.block - 1) / p.block > VA_MASK_MAX_BLOCKS) return VA_ERR_UNSUPPORTED;
+  int64_t N64 = 0, nb64 = 0;
+  if (int st0 = mask_grid_args(kind, T, H, W, p, &N64, &nb64)) return st0;
+  const int64_t F64 = static_cast<int64_t>(H) * W;
+  if (nb64 > VA_MASK_MAX_BLOCKS) return VA_ERR_UNSUPPORTED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   va::MaskDesc md;
@@ -588,6 +604,145 @@ VA_EXPORT int va_mask_free(va_mask* m) {
   if (m->t_row) cudaFree(m->t_row);
   if (m->t_order) cudaFree(m->t_order);
   delete m;
+  return VA_OK;
+}
+
+// ------------------------------------------------------------ mask cache --
+// Masks are reused across the denoising steps of one video (the radial mask
+// is static; LVSA's anchors rotate with the step, so its mask repeats with the
+// rotation's period): the cache keys a mask by what its CSR depends on.
+
+namespace {
+
+// Everything a mask's CSR depends on. For a radial mask that is the grid, the
+// block and the effective w0 (0 means the frame size); for LVSA the grid, the
+// block, the local window and the anchor rule, where with period > 0 only the
+// phase (anchor0 + rot_stride * step) mod period matters; a dense mask
+// depends on the grid and the block alone.
+struct MaskKey {
+  int dev, kind, T, H, W, block, w0, local, period, anchor;
+  bool operator==(const MaskKey& o) const {
+    return dev == o.dev && kind == o.kind && T == o.T && H == o.H && W == o.W &&
+           block == o.block && w0 == o.w0 && local == o.local && period == o.period &&
+           anchor == o.anchor;
+  }
+};
+
+int mask_key(int kind, int T, int H, int W, const va_mask_params& p, int step, int dev,
+             MaskKey* k) {
+  int64_t N64 = 0, nb64 = 0;
+  if (int st = mask_grid_args(kind, T, H, W, p, &N64, &nb64)) return st;
+  if (nb64 > VA_MASK_MAX_BLOCKS) return VA_ERR_UNSUPPORTED;
+  *k = MaskKey{dev, kind, T, H, W, p.block, 0, 0, 0, 0};
+  if (kind == VA_MASK_RADIAL) {
+    k->w0 = p.w0 == 0 ? H * W : p.w0;
+  } else if (kind == VA_MASK_LVSA) {
+    k->local = p.local;
+    k->period = p.period;
+    if (p.period > 0) {
+      int64_t r = (static_cast<int64_t>(p.anchor0) +
+                   static_cast<int64_t>(p.rot_stride) * step) % p.period;
+      if (r < 0) r += p.period;
+      k->anchor = static_cast<int>(r);
+    } else {
+      k->anchor = p.anchor0;
+    }
+  }
+  return VA_OK;
+}
+
+// Frees a mask with its own device current (a cache may hold masks of
+// several devices).
+void free_on_device(va_mask* m) {
+  const int dev = m->device;
+  int cur = 0;
+  const bool have = cudaGetDevice(&cur) == cudaSuccess;
+  if (have && cur != dev) cudaSetDevice(dev);
+  va_mask_free(m);
+  if (have && cur != dev) cudaSetDevice(cur);
+}
+
+}  // namespace
+
+struct va_mask_cache {
+  std::mutex mu;
+  int capacity = 0;
+  std::vector<std::pair<MaskKey, va_mask*>> entries;
+  int64_t hits = 0, misses = 0;
+};
+
+VA_EXPORT int va_mask_cache_create(int capacity, va_mask_cache** out) {
+  if (out == nullptr) return VA_ERR_INVALID;
+  *out = nullptr;
+  if (capacity < 1 || capacity > VA_MASK_CACHE_MAX) return VA_ERR_INVALID;
+  va_mask_cache* c = new (std::nothrow) va_mask_cache();
+  if (c == nullptr) return VA_ERR_OOM;
+  c->capacity = capacity;
+  c->entries.reserve(static_cast<size_t>(capacity));
+  *out = c;
+  return VA_OK;
+}
+
+VA_EXPORT int va_mask_cache_get(va_mask_cache* cache, int kind, int T, int H, int W,
+                                const va_mask_params* params, int step, const va_mask** out,
+                                va_stream_t stream) {
+  if (out == nullptr) return VA_ERR_INVALID;
+  *out = nullptr;
+  if (cache == nullptr || params == nullptr) return VA_ERR_INVALID;
+  int dev = 0;
+  if (int st = cuda_status(cudaGetDevice(&dev))) return st;
+  MaskKey key;
+  if (int st = mask_key(kind, T, H, W, *params, step, dev, &key)) return st;
+  std::lock_guard<std::mutex> lock(cache->mu);
+  for (auto& e : cache->entries) {
+    if (e.first == key) {
+      ++cache->hits;
+      *out = e.second;
+      return VA_OK;
+    }
+  }
+  if (static_cast<int>(cache->entries.size()) >= cache->capacity) return VA_ERR_UNSUPPORTED;
+  va_mask* m = nullptr;
+  if (int st = va_mask_build(kind, T, H, W, params, step, &m, stream)) return st;
+  cache->entries.emplace_back(key, m);
+  ++cache->misses;
+  *out = m;
+  return VA_OK;
+}
+
+VA_EXPORT int va_mask_cache_stats(va_mask_cache* cache, int64_t* hits, int64_t* misses,
+                                  int* entries) {
+  if (cache == nullptr) return VA_ERR_INVALID;
+  std::lock_guard<std::mutex> lock(cache->mu);
+  if (hits) *hits = cache->hits;
+  if (misses) *misses = cache->misses;
+  if (entries) *entries = static_cast<int>(cache->entries.size());
+  return VA_OK;
+}
+
+VA_EXPORT int va_mask_cache_clear(va_mask_cache* cache) {
+  if (cache == nullptr) return VA_ERR_INVALID;
+  std::lock_guard<std::mutex> lock(cache->mu);
+  for (auto& e : cache->entries) free_on_device(e.second);
+  cache->entries.clear();
+  return VA_OK;
+}
+
+VA_EXPORT int va_mask_cache_destroy(va_mask_cache* cache) {
+  if (cache == nullptr) return VA_OK;
+  va_mask_cache_clear(cache);
+  delete cache;
+  return VA_OK;
+}
+
+VA_EXPORT int va_mask_same(int kind, int T, int H, int W, const va_mask_params* params,
+                           int step_a, int step_b, int* same) {
+  if (params == nullptr || same == nullptr) return VA_ERR_INVALID;
+  *same = 0;
+  MaskKey ka, kb;
+  if (int st = mask_key(kind, T, H, W, *params, step_a, 0, &ka)) return st;
+  if (int st = mask_key(kind, T, H, W, *params, step_b, 0, &kb)) return st;
+  *same = ka == kb ? 1 : 0;
   return VA_OK;
 }
 
@@ -1180,15 +1335,30 @@ int set_smem_attrs() {
   });
 }
 
-// Member lists of an assignment: count -> offsets -> perm (order within a
-// cluster unspecified). count must be zeroed by the caller.
+// Member lists in ascending token order from counts and offsets: per-tile
+// counts, their scan down the tiles, then the placement (deterministic).
+int stable_lists(const int* assign, int BH, int N, int C, const int* off, int* perm,
+                 cudaStream_t s) {
+  const int ntiles = (N + va::KS_TILE - 1) / va::KS_TILE;
+  Scoped scratch(s);
+  int* tbase = nullptr;
+  if (int st = scratch.alloc(&tbase, static_cast<size_t>(BH) * ntiles * C)) return st;
+  const size_t hist = sizeof(int) * static_cast<size_t>(C);
+  va::km_tile_count_kernel<<<dim3(ntiles, BH), 256, hist, s>>>(assign, N, C, tbase);
+  va::km_tile_scan_kernel<<<dim3((C + 255) / 256, BH), 256, 0, s>>>(off, C, ntiles, tbase);
+  va::km_tile_place_kernel<<<dim3(ntiles, BH), 128, hist, s>>>(assign, N, C, tbase, perm);
+  return launch_status();
+}
+
+// Member lists of an assignment: count -> offsets -> perm, each cluster's
+// members in ascending token order. count must be zeroed by the caller.
 int cluster_lists(const int* assign, int BH, int N, int C, int* count, int* off, int* fill,
                   int* perm, cudaStream_t s) {
   const dim3 g((N + 255) / 256, BH);
   va::km_count_kernel<<<g, 256, 0, s>>>(assign, N, C, count);
   va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
-  va::km_scatter_kernel<<<g, 256, 0, s>>>(assign, N, C, off, fill, perm);
-  return launch_status();
+  if (int st = launch_status()) return st;
+  return stable_lists(assign, BH, N, C, off, perm, s);
 }
 
 // bf16, d = D: distances on the tensor cores (split-bf16 centroids).
@@ -1310,7 +1480,7 @@ int run_cluster(const T* x, const int* init, const float* c0, int BH, int N, int
         x, cent, cnorm, N, C, assign, count);
     if (iters == 0) break;
     va::km_offsets_kernel<<<BH, 1024, 0, s>>>(count, C, off, fill);
-    va::km_scatter_kernel<<<gn, 256, 0, s>>>(assign, N, C, off, fill, perm);
+    if ((st = stable_lists(assign, BH, N, C, off, perm, s))) return st;
     va::km_means_kernel<T, D><<<gc, 256, 0, s>>>(x, N, C, off, perm, cent, cnorm, 1);
   }
   return launch_status();
@@ -1804,16 +1974,10 @@ VA_EXPORT int va_mask_build_static(int kind, int T, int H, int W, const va_mask_
                                    int64_t col_capacity, int64_t* nnz, va_stream_t stream) {
   if (params == nullptr || row_ptr == nullptr || nnz == nullptr) return VA_ERR_INVALID;
   if (col_capacity < 0 || (col_idx == nullptr && col_capacity > 0)) return VA_ERR_INVALID;
-  if (kind != VA_MASK_DENSE && kind != VA_MASK_RADIAL && kind != VA_MASK_LVSA)
-    return VA_ERR_INVALID;
-  if (T < 1 || H < 1 || W < 1) return VA_ERR_INVALID;
-  const int64_t F64 = static_cast<int64_t>(H) * W;
-  const int64_t N64 = F64 * T;
-  if (N64 >= (1LL << 30)) return VA_ERR_INVALID;
   const va_mask_params p = *params;
-  if (p.block < 1 || p.block > 4096) return VA_ERR_INVALID;
-  if (p.w0 < 0 || p.local < 0 || p.period < 0) return VA_ERR_INVALID;
-  const int64_t nb64 = (N64 + p.block - 1) / p.block;
+  int64_t N64 = 0, nb64 = 0;
+  if (int st0 = mask_grid_args(kind, T, H, W, p, &N64, &nb64)) return st0;
+  const int64_t F64 = static_cast<int64_t>(H) * W;
   if (nb64 > static_cast<int64_t>(kStaticMaxBlocks)) return VA_ERR_UNSUPPORTED;
   *nnz = 0;
 

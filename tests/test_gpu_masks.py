@@ -109,3 +109,69 @@ def test_checked_mode_validates_built_masks(va, case, monkeypatch):
     assert va.csr_validate(rp, col) == va.OK
     m.free()
     assert va.device_error() == va.OK
+
+
+def _cache_get(cache, kind, T, H, W, p, step):
+    return cache.get(kind, T, H, W, block=p.block, w0=p.w0, local=p.local, period=p.period,
+                     anchor0=p.anchor0, rot_stride=p.rot_stride, step=step)
+
+
+def test_mask_cache_reuse_is_bit_exact(va):
+    """Cached masks across denoising steps: one entry per LVSA rotation phase,
+    one radial mask for every step, each CSR equal to the oracle's at the
+    requested step."""
+    import torch
+    cache = va.MaskCache(capacity=8)
+    T, H, W = 11, 4, 5
+    p = OM.MaskParams(block=16, local=1, period=3, anchor0=1, rot_stride=1)
+    handles = {}
+    for step in range(8):
+        m = _cache_get(cache, L, T, H, W, p, step)
+        rp, col = m.csr()
+        want_rp, want_col = OM.to_csr(OM.block_mask(L, T, H, W, p, step))
+        assert np.array_equal(rp, want_rp) and np.array_equal(col, want_col), step
+        handles[step] = m.handle.value
+    assert handles[0] == handles[3] == handles[6]
+    assert len({handles[0], handles[1], handles[2]}) == 3
+    assert cache.stats() == (5, 3, 3)
+    pr = OM.MaskParams(block=64)
+    r0 = _cache_get(cache, R, 4, 8, 8, pr, 0)
+    r1 = _cache_get(cache, R, 4, 8, 8, pr, 9)
+    assert r0.handle.value == r1.handle.value
+    assert cache.stats() == (6, 4, 4)
+    # a cached mask drives attention exactly as a freshly built one
+    g = torch.Generator(device="cuda").manual_seed(5)
+    q, k, v = (torch.randn(1, 2, 256, 128, device="cuda", generator=g).to(torch.bfloat16)
+               for _ in range(3))
+    fresh = _build(va, R, 4, 8, 8, pr, 3)
+    oa, _ = va.sparse_attn_fwd(q, k, v, r1)
+    ob, _ = va.sparse_attn_fwd(q, k, v, fresh)
+    torch.cuda.synchronize()
+    assert torch.equal(oa, ob)
+    fresh.free()
+    r1.free()  # a cached mask's free() leaves the mask to the cache
+    oc, _ = va.sparse_attn_fwd(q, k, v, r0)
+    torch.cuda.synchronize()
+    assert torch.equal(oc, oa)
+    cache.clear()
+    with pytest.raises(va.VAError):
+        r0.handle
+    assert cache.stats()[2] == 0
+    again = _cache_get(cache, L, T, H, W, p, 4)
+    assert np.array_equal(again.csr()[1], OM.to_csr(OM.block_mask(L, T, H, W, p, 4))[1])
+    cache.close()
+    with pytest.raises(va.VAError):
+        again.handle
+    assert va.device_error() == va.OK
+
+
+def test_mask_cache_full_builds_nothing(va):
+    cache = va.MaskCache(capacity=2)
+    for w0 in (1, 2):
+        _cache_get(cache, R, 4, 2, 2, OM.MaskParams(block=4, w0=w0), 0)
+    with pytest.raises(va.VAError) as e:
+        _cache_get(cache, R, 4, 2, 2, OM.MaskParams(block=4, w0=3), 0)
+    assert e.value.status == va.ERR_UNSUPPORTED
+    _cache_get(cache, R, 4, 2, 2, OM.MaskParams(block=4, w0=1), 5)  # a hit still works
+    assert cache.stats() == (1, 2, 2)
+    cache.close()

@@ -375,3 +375,37 @@ def test_kmeans_warm_start_continues_the_iteration(va, dev):
     torch.cuda.synchronize()
     assert va.device_error() == va.OK
     assert torch.equal(a, a10) and torch.equal(c, c10) and torch.equal(n, n10)
+
+
+@pytest.mark.parametrize("d,dt", [(128, "bf16"), (64, "bf16"), (128, "f32")])
+def test_repeated_calls_are_bit_identical(va, dev, d, dt):
+    """Member lists hold each cluster's tokens in ascending order (no atomic
+    slot order), so every sum over them, and with them the errors, the
+    routing, the output and the fp32 k-means, repeats bit for bit."""
+    B, Hh, N, Cq, Ck = 1, 3, 3000, 40, 150
+    q, k, v = synth.video_qkv(B, Hh, 1, 1, N, d, seed=41, dtype=dt)
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    qt, kt, vt = (_dev_tensor(x, dev, tdt) for x in (q, k, v))
+    rng = np.random.default_rng(42)
+    qa = _dev_tensor(rng.integers(0, Cq, (B, Hh, N)).astype(np.int32), dev, torch.int32)
+    ka = _dev_tensor(rng.integers(0, Ck, (B, Hh, N)).astype(np.int32), dev, torch.int32)
+    runs = []
+    for _ in range(3):
+        err = torch.empty((B, Hh, Cq, Ck), dtype=torch.float32, device=dev)
+        sel = torch.empty((B, Hh, Cq, Ck), dtype=torch.uint8, device=dev)
+        out, _, _ = va.compensate_route(qt, kt, vt, qa, Cq, ka, Ck, 0.15, err=err, sel=sel)
+        runs.append((out.clone(), err.clone(), sel.clone()))
+    assert va.device_error() == va.OK
+    for o, e, s in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(e, runs[0][1])
+        assert torch.equal(s, runs[0][2])
+    init = _dev_tensor(synth.init_indices(B, Hh, N, Cq, seed=43), dev, torch.int32)
+    res = []
+    for _ in range(2):
+        a = torch.empty((B, Hh, N), dtype=torch.int32, device=dev)
+        c = torch.empty((B, Hh, Cq, d), dtype=torch.float32, device=dev)
+        n = torch.empty((B, Hh, Cq), dtype=torch.int32, device=dev)
+        va.cluster(qt, Cq, 4, init, a, c, n)
+        res.append((a, c, n))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+    assert torch.equal(res[0][2], res[1][2])
