@@ -825,7 +825,7 @@ def run_bwd(args, world, rank, local):
         "gpu_launches": args.steps * 3,
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0:
         bm = oracle_block_mask(wl)
         rows = OA.sample_rows(N, BLOCK, 64, seed=8)
         live_keys = (bm * np.minimum(BLOCK, N - np.arange(bm.shape[0]) * BLOCK)[None, :]).sum(1)
@@ -839,12 +839,13 @@ def run_bwd(args, world, rank, local):
         line["parity"] = parity_record(got_dq, want_dq, "dq rows %d x %d heads vs the float64 "
                                        "gradient oracle (last timed call)" % (len(rows), heads),
                                        max_abs=3e-2, mean_abs=1e-2, relative=True)
-        line["cpu_baseline"] = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT,
-                                "cores": threads_used(), "kind": "oracle",
-                                "seconds": round(secs, 2),
-                                "sample": "dq of %d seeded query rows x %d heads (float64 "
-                                          "oracle: logits, dP and dQ products, 6*d FLOPs per "
-                                          "live pair)" % (len(rows), heads)}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = {"value": round(oflops / secs / 1e12, 6), "unit": UNIT,
+                                    "cores": threads_used(), "kind": "oracle",
+                                    "seconds": round(secs, 2),
+                                    "sample": "dq of %d seeded query rows x %d heads (float64 "
+                                              "oracle: logits, dP and dQ products, 6*d FLOPs "
+                                              "per live pair)" % (len(rows), heads)}
     mask.free()
     return line
 
