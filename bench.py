@@ -260,6 +260,58 @@ def parity_record(got, want, what, max_abs=2e-2, mean_abs=2e-3, relative=False):
             "pass": bool(np.isfinite(got).all() and mx <= bar_max and mn <= bar_mean)}
 
 
+def e2e_leg(world, dev, stream, dev_in, dev_out, call, steps):
+    """The same call end to end: each step copies its inputs in from pinned
+    host memory and its result back out (non-blocking copies on the call's
+    stream) around the call, timed with CUDA events, max over ranks.
+    Returns (ms per step, host-to-device bytes, device-to-host bytes)."""
+    import torch
+    host_in = [x.to("cpu").pin_memory() for x in dev_in]
+    host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in dev_out]
+
+    def step():
+        for d_, h_ in zip(dev_in, host_in):
+            d_.copy_(h_, non_blocking=True)
+        call()
+        for h_, d_ in zip(host_out, dev_out):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(3, min(steps, 10))
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / n
+    return (ms, sum(x.numel() * x.element_size() for x in host_in),
+            sum(x.numel() * x.element_size() for x in host_out))
+
+
+def count_launches(call):
+    """This library's kernels (namespace va) launched by one call, counted from
+    the profiler's CUDA activity outside the timed region; None where the
+    profiler records no kernels."""
+    import torch
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            call()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events()
+                 if e.device_type == torch.autograd.DeviceType.CUDA]
+    except Exception:
+        return None
+    n = sum(1 for name in names if "va::" in name)
+    return n if n > 0 else None
+
+
 def timed_region(args, world, local, call, stream):
     """Warm-up, a >= 0.6 s pre-roll under the clock sampler, then K timed calls.
 
@@ -463,6 +515,10 @@ def run_svgear(args, world, rank, local, d=D):
     err = va.device_error()
     if err != va.OK:
         raise RuntimeError("device error in the timed region: %s" % va.status_string(err))
+    # end to end: host q, k, v and the initial indices in, host output out
+    e2e_ms, h2d, d2h = e2e_leg(world, dev, stream, [qt, kt, vt, qinit, kinit], [out], call,
+                               args.steps)
+    per_call = count_launches(call)
     record[0] = True
     for _ in range(3):
         call()
@@ -493,16 +549,19 @@ def run_svgear(args, world, rank, local, d=D):
         "stages_ms": {k2: round(v2, 3) for k2, v2 in st.items()},
         "stages_tflops": {n: round(f / (t * 1e-3) / 1e12, 2) for n, (f, t) in stages.items()},
         "flops_per_step": {k2: float(v2) for k2, v2 in fl.items()},
-        # The step mixes tensor-core kernels (k-means distances, compensated
-        # attention) with FP32 ones (probe): its roofline is the whole step's
-        # algorithmic FLOPs against the bf16 dense peak; the per-kernel split
-        # is in the ncu launch list.
+        # The step mixes tensor-core kernels (k-means distances, probe,
+        # compensated attention) with memory-bound ones (member sums, routing,
+        # gathers): its roofline is the whole step's algorithmic FLOPs against
+        # the bf16 dense peak; the per-kernel split is in the ncu launch list.
         "roofline": {"bound": "tensor", "achieved": round(step_tf, 2),
                      "peak": pk["bf16_tflops"], "unit": UNIT,
                      "frac": round(step_tf / pk["bf16_tflops"], 4),
                      "peak_source": "%s bf16 dense burst" % src, "kernel": "whole SVG-EAR step",
                      "traffic": None},
-        "gpu_launches": None,
+        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * per_call if per_call else None,
         "clocks": clocks,
     }
     if rank == 0:
@@ -651,6 +710,8 @@ def run_linear(args, world, rank, local, mixed, d=D):
         raise RuntimeError("device error in the timed region: %s" % va.status_string(err))
     ms_per_step = total_ms / args.steps
     call_ms = float(np.mean(launch_ms))
+    e2e_ms, h2d, d2h = e2e_leg(world, dev, stream, [qt, kt, vt], [out], call, args.steps)
+    per_call = count_launches(call)
     tensor_bytes = qt.numel() * qt.element_size()
     io_bytes = 4 * tensor_bytes                       # read Q, K, V; write O
     lin_flops = 4.0 * N * d * (d + 1) * BATCH * heads  # phi(K)^T [V | 1] and phi(Q) [S | z]
@@ -665,7 +726,8 @@ def run_linear(args, world, rank, local, mixed, d=D):
             "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded Fourier-mode Q/K + N(0,0.5^2), V~N(0,1))",
-            "config": cfg, "gpu_launches": args.steps * (4 if mixed else 3), "clocks": clocks}
+            "config": cfg, "gpu_launches": args.steps * per_call if per_call else None,
+            "clocks": clocks}
     if mixed:
         rp, col = mask.csr()
         blk = 128
@@ -683,7 +745,10 @@ def run_linear(args, world, rank, local, mixed, d=D):
             "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": pk["bf16_tflops"],
                          "unit": UNIT, "frac": round(tf / pk["bf16_tflops"], 4),
                          "peak_source": "%s bf16 dense burst" % src,
-                         "kernel": "whole call (attention + linear attention)", "traffic": None}})
+                         "kernel": "whole call (attention + linear attention)", "traffic": None},
+            "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h}})
         mask.free()
     else:
         gbs = io_bytes / (call_ms * 1e-3) / 1e9
@@ -696,7 +761,10 @@ def run_linear(args, world, rank, local, mixed, d=D):
                          "unit": "GB/s", "frac": round(gbs / pk["hbm_gbs"], 4),
                          "peak_source": "%s copy bandwidth" % src,
                          "kernel": "whole call (lin_state + lin_prep + lin_out)",
-                         "algorithmic_bytes": io_bytes, "flops": lin_flops, "traffic": None}})
+                         "algorithmic_bytes": io_bytes, "flops": lin_flops, "traffic": None},
+            "e2e": {"value": round(world * io_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                    "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h}})
     if rank == 0:
         from oracle import attention as OA
         from oracle import linear as OL
@@ -770,32 +838,9 @@ def run_bwd(args, world, rank, local):
     call_ms = float(np.mean(launch_ms))
 
     # end to end: host q, k, v, out, dout, lse in; host dq, dk, dv out
-    host_in = [x.to("cpu").pin_memory() for x in (qt, kt, vt, out, gt, lse)]
-    host_out = [torch.empty(qt.shape, dtype=torch.bfloat16).pin_memory() for _ in range(3)]
-    dev_in = [qt, kt, vt, out, gt, lse]
-
-    def e2e_call():
-        for d_, h_ in zip(dev_in, host_in):
-            d_.copy_(h_, non_blocking=True)
-        call()
-        for h_, d_ in zip(host_out, (dq, dk, dv)):
-            h_.copy_(d_, non_blocking=True)
-
-    for _ in range(2):
-        e2e_call()
-    torch.cuda.synchronize()
-    barrier(world)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(3, min(args.steps, 10))
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_call()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / e2e_steps
-    h2d = sum(x.numel() * x.element_size() for x in host_in)
-    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    e2e_ms, h2d, d2h = e2e_leg(world, dev, stream, [qt, kt, vt, out, gt, lse], [dq, dk, dv],
+                               call, args.steps)
+    per_call = count_launches(call)
 
     pk, src = peaks()
     tf = flops / (call_ms * 1e-3) / 1e12
@@ -822,7 +867,7 @@ def run_bwd(args, world, rank, local):
                      "flops_per_launch": flops, "launch_ms_mean": round(call_ms, 4),
                      "kernel": "whole call (bwd_prep + bwd_dkdv_tc + bwd_dq_tc)",
                      "traffic": None},
-        "gpu_launches": args.steps * 3,
+        "gpu_launches": args.steps * per_call if per_call else None,
         "clocks": clocks,
     }
     if rank == 0:
