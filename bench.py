@@ -425,8 +425,8 @@ def run_ours(args, world, rank, local):
                      "flops_per_launch": flops, "launch_ms_mean": round(float(np.mean(launch_ms)), 4),
                      "launch_ms_min": round(float(np.min(launch_ms)), 4),
                      "traffic": profiled_traffic() if name == "wan_radial" else None,
-                     "kernel": "va::attn_tc_kernel<%d%s>" % (
-                         wl.get("d", D), ", true" if wl.get("block", BLOCK) == 64 else "")},
+                     "kernel": "va::attn_tc_kernel<%d, %s>" % (
+                         wl.get("d", D), "true" if wl.get("block", BLOCK) == 64 else "false")},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
