@@ -28,9 +28,13 @@
 // [256t + 128, 256t + 128 + D) for the O_t accumulator.
 //
 // Online softmax in the log2 domain: the running max used for exponentiation
-// is only raised when a block's max exceeds it by more than TAU (so P <= 2^TAU
-// and fp32 O and l stay exact to rounding); raising it rescales O_t in TMEM
-// after waiting for the previous PV_t to complete.
+// is only raised when a block's max exceeds it by more than TAU_FWD = 16 (so
+// P <= 2^16, far inside bf16 and fp32 range, and O and l stay exact to
+// rounding); raising it rescales O_t in TMEM after waiting for the previous
+// PV_t to complete. A block is first exponentiated against the running max
+// with no max pass; only when its weights sum above 2^(TAU_FWD - 1) (or m_used
+// is still -inf) does the warp take the max, maybe rescale, and exponentiate
+// again, so the weights are those of the max-first order either way.
 //
 // Every mbarrier wait is bounded (clock64 limit): on a timeout the CTA records
 // VA_ERR_TIMEOUT in the device error word, drains its own copies and MMAs
@@ -49,7 +53,11 @@ constexpr int TC_THREADS = 384;
 constexpr int TC_TILE_BYTES = TC_BLK * TC_D * 2;  // 32 KB: one 128 x 128 bf16 tile
 constexpr int TC_HALF_BYTES = TC_TILE_BYTES / 2;  // 16 KB: 128 rows x 64 dims
 constexpr int TC_SMEM_BYTES = 1024 + TC_TILE_BYTES * (2 + TC_NK + TC_NV);
-constexpr float TC_TAU = 8.0f;
+constexpr float TC_TAU = 8.0f;  // compensated attention's rescale threshold
+// The forward's threshold, and the block sum below which a block needs no max
+// pass (every weight is then below 2^(TAU_FWD - 1)).
+constexpr float TC_TAU_FWD = 16.0f;
+constexpr float TC_FAST_SUM = 32768.0f;
 // Register split (setmaxnreg): the kernel is compiled to TC_LAUNCH_REGS per
 // thread; warpgroup 0 (producer, MMA, idle warps) gives registers back and the
 // two softmax warpgroups take them. 128 * DEC + 256 * INC must not exceed
@@ -303,115 +311,143 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
     if (!ok) break;
     tc_fence_after();
     float s[128];
+    auto load_s = [&]() {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tmem_ld32(tS + c * 32, v);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + c * 32, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
-    }
-    tmem_wait_ld();
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+      }
+      tmem_wait_ld();
+    };
+    // P = 2^(s * sl2 - m_used), dead key columns zeroed
+    auto exponentiate = [&]() {
+      const float neg_m = -m_used;
+#pragma unroll
+      for (int i = 0; i < 128; i += 2) {
+        ffma2_bc(s[i], s[i + 1], s[i], s[i + 1], sl2, neg_m);
+        s[i] = ex2_approx(s[i]);
+        s[i + 1] = ex2_approx(s[i + 1]);
+      }
+      if constexpr (SUB) {
+        if (lo_end < 64) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) s[i] = i < lo_end ? s[i] : 0.f;
+        }
+        if (hi_end < 128) {
+#pragma unroll
+          for (int i = 64; i < 128; ++i) s[i] = i < hi_end ? s[i] : 0.f;
+        }
+      } else if (valid < TC_BLK) {
+#pragma unroll
+        for (int i = 1; i < 128; ++i) s[i] = (i < valid) ? s[i] : 0.f;
+      }
+    };
+    float r0, r1, r2, r3;
+    uint32_t pk[64];
+    auto sum_pack = [&]() {
+      r0 = r1 = r2 = r3 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; i += 4) {
+        fadd2_acc(r0, r1, s[i], s[i + 1]);
+        fadd2_acc(r2, r3, s[i + 2], s[i + 3]);
+        pk[i / 2] = pack_bf16x2(s[i], s[i + 1]);
+        pk[i / 2 + 1] = pack_bf16x2(s[i + 2], s[i + 3]);
+      }
+    };
+    load_s();
     // SUB: the entry may hold no live key of this row (a row of the other query
     // block of the tile is live): it then adds nothing (warp-uniform, as a
     // warp's 32 rows lie in one block)
     const bool row_live = !SUB || lo_end > 0 || hi_end > 64;
-    if constexpr (SUB) {
-      if (row_live) {
-        // dead columns take a live value of the block for the max, and a zero
-        // weight below
-        const float rep = lo_end > 0 ? s[0] : s[64];
-        if (lo_end < 64) {
+    // Pass 0 tries the block against the running max, with no max pass. A
+    // block sum of at most 2^(TAU - 1) bounds every weight by it, so the block
+    // max lies more than one below m_used + TAU and the rescale test of pass 1
+    // would keep m_used: the weights are exactly those of pass 1. Any larger
+    // sum, an infinite one (no max yet) or NaN sends the whole warp to pass 1,
+    // which reloads S (P is not written over it yet), takes the max and maybe
+    // rescales before exponentiating.
+#pragma unroll 1
+    for (int pass = 0;; ++pass) {
+      if (pass == 1) {
+        load_s();
+        if constexpr (SUB) {
+          if (row_live) {
+            // dead columns take a live value of the block for the max, and a
+            // zero weight in exponentiate()
+            const float rep = lo_end > 0 ? s[0] : s[64];
+            if (lo_end < 64) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) s[i] = i < lo_end ? s[i] : rep;
+              for (int i = 0; i < 64; ++i) s[i] = i < lo_end ? s[i] : rep;
+            }
+            if (hi_end < 128) {
+#pragma unroll
+              for (int i = 64; i < 128; ++i) s[i] = i < hi_end ? s[i] : rep;
+            }
+          }
+        } else if (valid < TC_BLK) {
+          // Key columns >= valid hold zero-filled rows: give them a real value
+          // of the block for the max, and a zero weight in exponentiate().
+#pragma unroll
+          for (int i = 1; i < 128; ++i) s[i] = (i < valid) ? s[i] : s[0];
         }
-        if (hi_end < 128) {
+        // Largest scaled logit of the block (sl2 may be negative).
+        float mx;
+        if (sl2 >= 0.f) {
+          float m0 = fmax3(s[0], s[1], s[2]), m1 = fmax3(s[3], s[4], s[5]);
+          float m2 = fmax3(s[6], s[7], s[8]), m3 = fmax3(s[9], s[10], s[11]);
 #pragma unroll
-          for (int i = 64; i < 128; ++i) s[i] = i < hi_end ? s[i] : rep;
+          for (int i = 12; i < 124; i += 8) {
+            m0 = fmax3(m0, s[i], s[i + 1]);
+            m1 = fmax3(m1, s[i + 2], s[i + 3]);
+            m2 = fmax3(m2, s[i + 4], s[i + 5]);
+            m3 = fmax3(m3, s[i + 6], s[i + 7]);
+          }
+          mx = fmax3(fmax3(m0, m1, s[124]), fmax3(m2, m3, s[125]), fmaxf(s[126], s[127]));
+        } else {
+          float m0 = fmin3(s[0], s[1], s[2]), m1 = fmin3(s[3], s[4], s[5]);
+          float m2 = fmin3(s[6], s[7], s[8]), m3 = fmin3(s[9], s[10], s[11]);
+#pragma unroll
+          for (int i = 12; i < 124; i += 8) {
+            m0 = fmin3(m0, s[i], s[i + 1]);
+            m1 = fmin3(m1, s[i + 2], s[i + 3]);
+            m2 = fmin3(m2, s[i + 4], s[i + 5]);
+            m3 = fmin3(m3, s[i + 6], s[i + 7]);
+          }
+          mx = fmin3(fmin3(m0, m1, s[124]), fmin3(m2, m3, s[125]), fminf(s[126], s[127]));
+        }
+        const float m_cand = mx * sl2;
+        const bool need = row_live && m_cand > m_used + TC_TAU_FWD;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m_used - m_cand);
+          m_used = m_cand;
+          l *= alpha;
+        }
+        if (__any_sync(0xffffffffu, need && j > 0)) {
+          // O_t holds the sum up to PV_t(j-1): wait for it, then rescale in TMEM.
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (j - 1) & 1, lim, abort_p));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tO + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(tO + c * 32, v);
+          }
         }
       }
-    } else if (valid < TC_BLK) {
-      // Key columns >= valid hold zero-filled rows: give them a real value of
-      // the block for the max, and a zero weight below.
-#pragma unroll
-      for (int i = 1; i < 128; ++i) s[i] = (i < valid) ? s[i] : s[0];
+      exponentiate();
+      sum_pack();
+      if (pass == 1 ||
+          !__any_sync(0xffffffffu, !((r0 + r1) + (r2 + r3) <= TC_FAST_SUM)))
+        break;
     }
-    // Largest scaled logit of the block (sl2 may be negative).
-    float mx;
-    if (sl2 >= 0.f) {
-      float m0 = fmax3(s[0], s[1], s[2]), m1 = fmax3(s[3], s[4], s[5]);
-      float m2 = fmax3(s[6], s[7], s[8]), m3 = fmax3(s[9], s[10], s[11]);
-#pragma unroll
-      for (int i = 12; i < 124; i += 8) {
-        m0 = fmax3(m0, s[i], s[i + 1]);
-        m1 = fmax3(m1, s[i + 2], s[i + 3]);
-        m2 = fmax3(m2, s[i + 4], s[i + 5]);
-        m3 = fmax3(m3, s[i + 6], s[i + 7]);
-      }
-      mx = fmax3(fmax3(m0, m1, s[124]), fmax3(m2, m3, s[125]), fmaxf(s[126], s[127]));
-    } else {
-      float m0 = fmin3(s[0], s[1], s[2]), m1 = fmin3(s[3], s[4], s[5]);
-      float m2 = fmin3(s[6], s[7], s[8]), m3 = fmin3(s[9], s[10], s[11]);
-#pragma unroll
-      for (int i = 12; i < 124; i += 8) {
-        m0 = fmin3(m0, s[i], s[i + 1]);
-        m1 = fmin3(m1, s[i + 2], s[i + 3]);
-        m2 = fmin3(m2, s[i + 4], s[i + 5]);
-        m3 = fmin3(m3, s[i + 6], s[i + 7]);
-      }
-      mx = fmin3(fmin3(m0, m1, s[124]), fmin3(m2, m3, s[125]), fminf(s[126], s[127]));
-    }
-    const float m_cand = mx * sl2;
-    const bool need = row_live && m_cand > m_used + TC_TAU;
-    float alpha = 1.f;
-    if (need) {
-      alpha = ex2_approx(m_used - m_cand);
-      m_used = m_cand;
-      l *= alpha;
-    }
-    if (__any_sync(0xffffffffu, need && j > 0)) {
-      // O_t holds the sum up to PV_t(j-1): wait for it, then rescale in TMEM.
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (j - 1) & 1, lim, abort_p));
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + c * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        tmem_st32(tO + c * 32, v);
-      }
-    }
-    const float neg_m = -m_used;
-#pragma unroll
-    for (int i = 0; i < 128; i += 2) {
-      ffma2_bc(s[i], s[i + 1], s[i], s[i + 1], sl2, neg_m);
-      s[i] = ex2_approx(s[i]);
-      s[i + 1] = ex2_approx(s[i + 1]);
-    }
-    if constexpr (SUB) {
-      if (lo_end < 64) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) s[i] = i < lo_end ? s[i] : 0.f;
-      }
-      if (hi_end < 128) {
-#pragma unroll
-        for (int i = 64; i < 128; ++i) s[i] = i < hi_end ? s[i] : 0.f;
-      }
-    } else if (valid < TC_BLK) {
-#pragma unroll
-      for (int i = 1; i < 128; ++i) s[i] = (i < valid) ? s[i] : 0.f;
-    }
-    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
-    uint32_t pk[64];
-#pragma unroll
-    for (int i = 0; i < 128; i += 4) {
-      fadd2_acc(r0, r1, s[i], s[i + 1]);
-      fadd2_acc(r2, r3, s[i + 2], s[i + 3]);
-      pk[i / 2] = pack_bf16x2(s[i], s[i + 1]);
-      pk[i / 2 + 1] = pack_bf16x2(s[i + 2], s[i + 3]);
-    }
+    if (!ok) break;
     l += (r0 + r1) + (r2 + r3);
     {
       uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&pk[0]);
