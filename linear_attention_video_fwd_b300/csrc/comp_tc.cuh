@@ -137,72 +137,105 @@ __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const Co
     if (!ok) break;
     tc_fence_after();
     float s[128];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t v[32];
-      tmem_ld32(tS + c * 32, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
-    }
-    tmem_wait_ld();
     // scaled logit plus the entry's column bias (log2 units): log2 n_c of a
     // virtual key (-inf for a selected or empty cluster), 0 / -inf for a
     // valid / padding row of an exact tile
     const float4* brow = bias_ring + ms * 32;
+    auto load_biased = [&]() {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float4 bb = brow[i];
-      ffma2_v(s[4 * i], s[4 * i + 1], s[4 * i], s[4 * i + 1], sl2, bb.x, bb.y);
-      ffma2_v(s[4 * i + 2], s[4 * i + 3], s[4 * i + 2], s[4 * i + 3], sl2, bb.z, bb.w);
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        // volatile: each pass loads its own biases (held across the passes
+        // they would take 128 registers)
+        float4 bb;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(bb.x), "=f"(bb.y), "=f"(bb.z), "=f"(bb.w)
+                     : "r"(smem_u32(brow + i)));
+        ffma2_v(s[4 * i], s[4 * i + 1], s[4 * i], s[4 * i + 1], sl2, bb.x, bb.y);
+        ffma2_v(s[4 * i + 2], s[4 * i + 3], s[4 * i + 2], s[4 * i + 3], sl2, bb.z, bb.w);
+      }
+    };
+    float r0, r1, r2, r3;
+    // P = 2^(logit - m_used) in s, row sums in r0..r3
+    auto exp_sum = [&]() {
+      const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
+#pragma unroll
+      for (int i = 0; i < 128; i += 2) {
+        ffma2_bc(s[i], s[i + 1], s[i], s[i + 1], 1.f, neg_m);
+        s[i] = ex2_approx(s[i]);
+        s[i + 1] = ex2_approx(s[i + 1]);
+      }
+      r0 = r1 = r2 = r3 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 128; i += 4) {
+        fadd2_acc(r0, r1, s[i], s[i + 1]);
+        fadd2_acc(r2, r3, s[i + 2], s[i + 3]);
+      }
+    };
+    load_biased();
+    // Pass 0 tries the entry against the running max with no max pass: a sum
+    // of at most 2^(TAU_FWD - 1) bounds every weight by it, so pass 1 would
+    // keep m_used and give exactly these weights. A larger sum, NaN, or a row
+    // with no running max yet sends the warp to pass 1 (S reloaded, the bias
+    // slot still held), which takes the max and maybe rescales.
+#pragma unroll 1
+    for (int pass = 0;; ++pass) {
+      if (pass == 1) {
+        load_biased();
+        float m0 = fmax3(s[0], s[1], s[2]), m1 = fmax3(s[3], s[4], s[5]);
+        float m2 = fmax3(s[6], s[7], s[8]), m3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+        for (int i = 12; i < 124; i += 8) {
+          m0 = fmax3(m0, s[i], s[i + 1]);
+          m1 = fmax3(m1, s[i + 2], s[i + 3]);
+          m2 = fmax3(m2, s[i + 4], s[i + 5]);
+          m3 = fmax3(m3, s[i + 6], s[i + 7]);
+        }
+        const float m_cand =
+            fmax3(fmax3(m0, m1, s[124]), fmax3(m2, m3, s[125]), fmaxf(s[126], s[127]));
+        const bool need = m_cand > m_used + TC_TAU_FWD;  // false while the block is all -inf
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2_approx(m_used - m_cand);
+          m_used = m_cand;
+          l *= alpha;
+        }
+        if (__any_sync(0xffffffffu, need && j > 0)) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (j - 1) & 1, lim, abort_p));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tO + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(tO + c * 32, v);
+          }
+        }
+      }
+      exp_sum();
+      if (pass == 1 ||
+          !__any_sync(0xffffffffu, m_used == -INFINITY ||
+                                       !((r0 + r1) + (r2 + r3) <= TC_FAST_SUM)))
+        break;
     }
     mbar_arrive(smem_u32(&bars[CB_M_EMPTY + ms]));
-    float m0 = fmax3(s[0], s[1], s[2]), m1 = fmax3(s[3], s[4], s[5]);
-    float m2 = fmax3(s[6], s[7], s[8]), m3 = fmax3(s[9], s[10], s[11]);
-#pragma unroll
-    for (int i = 12; i < 124; i += 8) {
-      m0 = fmax3(m0, s[i], s[i + 1]);
-      m1 = fmax3(m1, s[i + 2], s[i + 3]);
-      m2 = fmax3(m2, s[i + 4], s[i + 5]);
-      m3 = fmax3(m3, s[i + 6], s[i + 7]);
-    }
-    const float m_cand = fmax3(fmax3(m0, m1, s[124]), fmax3(m2, m3, s[125]), fmaxf(s[126], s[127]));
-    const bool need = m_cand > m_used + TC_TAU;  // false while the block is all -inf
-    float alpha = 1.f;
-    if (need) {
-      alpha = ex2_approx(m_used - m_cand);
-      m_used = m_cand;
-      l *= alpha;
-    }
-    if (__any_sync(0xffffffffu, need && j > 0)) {
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(bO, (j - 1) & 1, lim, abort_p));
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + c * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        tmem_st32(tO + c * 32, v);
-      }
-    }
-    const float neg_m = m_used == -INFINITY ? 0.f : -m_used;
-#pragma unroll
-    for (int i = 0; i < 128; i += 2) {
-      ffma2_bc(s[i], s[i + 1], s[i], s[i + 1], 1.f, neg_m);
-      s[i] = ex2_approx(s[i]);
-      s[i + 1] = ex2_approx(s[i + 1]);
-    }
-    float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+    if (!ok) break;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {  // pack and store P in two halves of 64 keys
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 64; i += 4) {
         const int c = h * 64 + i;
-        fadd2_acc(r0, r1, s[c], s[c + 1]);
-        fadd2_acc(r2, r3, s[c + 2], s[c + 3]);
         pk[i / 2] = pack_bf16x2(s[c], s[c + 1]);
         pk[i / 2 + 1] = pack_bf16x2(s[c + 2], s[c + 3]);
       }
