@@ -28,11 +28,11 @@
 // [256t + 128, 256t + 128 + D) for the O_t accumulator.
 //
 // Online softmax in the log2 domain: the running max used for exponentiation
-// is only raised when a block's max exceeds it by more than TAU_FWD = 16 (so
+// is only raised when a block's max exceeds it by more than TAU = 16 (so
 // P <= 2^16, far inside bf16 and fp32 range, and O and l stay exact to
 // rounding); raising it rescales O_t in TMEM after waiting for the previous
 // PV_t to complete. A block is first exponentiated against the running max
-// with no max pass; only when its weights sum above 2^(TAU_FWD - 1) (or m_used
+// with no max pass; only when its weights sum above 2^(TAU - 1) (or m_used
 // is still -inf) does the warp take the max, maybe rescale, and exponentiate
 // again, so the weights are those of the max-first order either way.
 //
@@ -53,10 +53,10 @@ constexpr int TC_THREADS = 384;
 constexpr int TC_TILE_BYTES = TC_BLK * TC_D * 2;  // 32 KB: one 128 x 128 bf16 tile
 constexpr int TC_HALF_BYTES = TC_TILE_BYTES / 2;  // 16 KB: 128 rows x 64 dims
 constexpr int TC_SMEM_BYTES = 1024 + TC_TILE_BYTES * (2 + TC_NK + TC_NV);
-constexpr float TC_TAU = 8.0f;  // compensated attention's rescale threshold
-// The forward's threshold, and the block sum below which a block needs no max
-// pass (every weight is then below 2^(TAU_FWD - 1)).
-constexpr float TC_TAU_FWD = 16.0f;
+// Rescale threshold of the online softmax (log2 units), and the block sum
+// below which a block needs no max pass (every weight is then below
+// 2^(TAU - 1)); the compensated attention uses both as well.
+constexpr float TC_TAU = 16.0f;
 constexpr float TC_FAST_SUM = 32768.0f;
 // Register split (setmaxnreg): the kernel is compiled to TC_LAUNCH_REGS per
 // thread; warpgroup 0 (producer, MMA, idle warps) gives registers back and the
@@ -418,7 +418,7 @@ __device__ __forceinline__ void tc_softmax_tile(const TcArgs& a, int tile, int I
           mx = fmin3(fmin3(m0, m1, s[124]), fmin3(m2, m3, s[125]), fminf(s[126], s[127]));
         }
         const float m_cand = mx * sl2;
-        const bool need = row_live && m_cand > m_used + TC_TAU_FWD;
+        const bool need = row_live && m_cand > m_used + TC_TAU;
         float alpha = 1.f;
         if (need) {
           alpha = ex2_approx(m_used - m_cand);

@@ -181,7 +181,7 @@ __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const Co
     };
     load_biased();
     // Pass 0 tries the entry against the running max with no max pass: a sum
-    // of at most 2^(TAU_FWD - 1) bounds every weight by it, so pass 1 would
+    // of at most 2^(TAU - 1) bounds every weight by it, so pass 1 would
     // keep m_used and give exactly these weights. A larger sum, NaN, or a row
     // with no running max yet sends the warp to pass 1 (S reloaded, the bias
     // slot still held), which takes the max and maybe rescales.
@@ -200,7 +200,7 @@ __device__ __forceinline__ void ct_softmax(const CompArgs& a, int tile, const Co
         }
         const float m_cand =
             fmax3(fmax3(m0, m1, s[124]), fmax3(m2, m3, s[125]), fmaxf(s[126], s[127]));
-        const bool need = m_cand > m_used + TC_TAU_FWD;  // false while the block is all -inf
+        const bool need = m_cand > m_used + TC_TAU;  // false while the block is all -inf
         float alpha = 1.f;
         if (need) {
           alpha = ex2_approx(m_used - m_cand);
