@@ -125,6 +125,42 @@ def test_bf16_single_live_key_block_extremes(va, dev):
     assert_bf16_close(got, want)
 
 
+def _bf16_exact(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).bfloat16().float().numpy()
+
+
+@pytest.mark.parametrize("d,block", [(128, 128), (64, 128), (128, 64), (64, 64)])
+def test_bf16_negative_scale(va, dev, d, block):
+    # sl2 < 0: the max pass takes the smallest raw logit
+    T, H, W = 3, 5, 20
+    q, k, v = synth.video_qkv(1, 2, T, H, W, d, seed=14)
+    got, want, gl, wl = _run(va, dev, q, k, v, OM.RADIAL, T, H, W, OM.MaskParams(block=block),
+                             0, "bf16", scale=-1.0 / np.sqrt(d))
+    assert_bf16_close(got, want)
+    assert np.abs(gl - wl).max() <= 2e-2
+
+
+@pytest.mark.parametrize("d,block", [(128, 128), (64, 128), (128, 64), (64, 64)])
+def test_bf16_running_max_rises_every_block(va, dev, d, block):
+    # Every query points along u and key j's component along u grows with j,
+    # so each key block raises the row max by about 25 (log2 units): past the
+    # rescale threshold, every block takes the max pass and rescales O.
+    T, H, W = 4, 16, 16
+    N = T * H * W
+    rng = np.random.default_rng(15)
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    q = 8.0 * u[None, :] + 0.05 * rng.standard_normal((N, d))
+    k = (200.0 * np.arange(N) / N)[:, None] * u[None, :] + 0.05 * rng.standard_normal((N, d))
+    v = rng.standard_normal((N, d))
+    q, k, v = (_bf16_exact(x.reshape(1, 1, N, d)) for x in (q, k, v))
+    got, want, gl, wl = _run(va, dev, q, k, v, OM.DENSE, T, H, W, OM.MaskParams(block=block),
+                             0, "bf16")
+    assert np.isfinite(got).all()
+    assert_bf16_close(got, want)
+    assert np.abs(gl - wl).max() <= 2e-2
+
+
 @pytest.mark.parametrize("d", [128, 64])
 def test_wan_radial_full_size_sampled_rows(va, dev, d):
     # The benchmarked workload: B=1, 12 heads, 21x30x52 = 32,760 tokens, d=128,
