@@ -208,6 +208,35 @@ def test_compensate_route_extremes_match_closed_forms(va, dev):
     assert np.nanmax(err) < 1e-5
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_compensate_route_running_max_rises_every_tile(va, dev, d):
+    # Keys' logits grow with their index and key clusters are index ranges, so
+    # each of the four centroid tiles (128 clusters) raises the row max by
+    # about 51 (log2 units), past the rescale threshold: the bf16 softmax takes
+    # its max pass and rescales O on those entries, then meets exact tiles
+    # below the max it has reached.
+    N, Cq, Ck = 2048, 4, 512
+    rng = np.random.default_rng(44)
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    q = 8.0 * u[None, :] + 0.05 * rng.standard_normal((N, d))
+    k = (200.0 * np.arange(N) / N)[:, None] * u[None, :] + 0.05 * rng.standard_normal((N, d))
+    v = rng.standard_normal((N, d))
+    q, k, v = (torch.from_numpy(x.reshape(1, 1, N, d).astype(np.float32)).bfloat16().float()
+               .numpy() for x in (q, k, v))
+    qa = rng.integers(0, Cq, (1, 1, N)).astype(np.int32)
+    ka = (np.arange(N) * Ck // N).astype(np.int32).reshape(1, 1, N)
+    scale = 1.0 / np.sqrt(d)
+    out, err, sel = _route_case(va, dev, q, k, v, qa, ka, Cq, Ck, 0.3, scale, "bf16")
+    assert np.isfinite(out).all()
+    nq = np.bincount(qa[0, 0], minlength=Cq)
+    nk = np.bincount(ka[0, 0], minlength=Ck)
+    assert np.array_equal(sel[0, 0], S.route(err[0, 0], nq, nk, N, 0.3))
+    want = S.compensated_attention(q[0, 0], k[0, 0], v[0, 0], qa[0, 0], ka[0, 0], Ck, sel[0, 0],
+                                   scale)
+    assert_bf16_close(out[0, 0], want)
+
+
 def _near_cut_agreement(sel_gpu, err_oracle, nq, nk, N, density, rel=1e-3):
     """Routing reading (iii): the GPU's selected set against the oracle's
     selection on its own float64 errors. Blocks whose oracle ratio lies within
