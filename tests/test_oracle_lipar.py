@@ -7,6 +7,7 @@ clip that changes once stays pruned afterwards and restores from the frame
 of the change; restoration of kept tokens is the identity.
 """
 import numpy as np
+import pytest
 
 from oracle import lipar as OL
 
@@ -68,3 +69,44 @@ def test_restore_is_identity_on_kept_tokens():
     full = OL.restore(y, src)
     assert np.array_equal(full[order], y)
     assert not keep[H * W:2 * H * W].any()  # the repeated frame is pruned
+
+
+@pytest.mark.parametrize("T,H,W,tau", [(5, 6, 7, 0.5), (4, 1, 9, 0.3), (6, 5, 1, 0.8),
+                                       (3, 8, 8, 2.0)])
+def test_keep_is_a_3x3_dilation_of_changed(T, H, W, tau):
+    # the motion check as a library routine: keep = 3x3 binary dilation of the
+    # per-frame changed map, frame 0 always kept
+    from scipy.ndimage import binary_dilation
+    rng = np.random.default_rng(T * 100 + H * 10 + W)
+    x = rng.standard_normal((T, H, W, 4)).astype(np.float32)
+    x[1:] = x[:-1] + (rng.random((T - 1, H, W, 1)) < 0.3) * rng.standard_normal(
+        (T - 1, H, W, 4)).astype(np.float32)
+    keep, order, src, n = OL.prune(x.reshape(T * H * W, 4), T, H, W, tau)
+    changed = np.ones((T, H, W), dtype=bool)
+    changed[1:] = np.abs(x[1:] - x[:-1]).max(axis=3) >= np.float32(tau)
+    want = np.stack([binary_dilation(changed[t], structure=np.ones((3, 3), dtype=bool))
+                     for t in range(T)])
+    want[0] = True
+    assert np.array_equal(keep.reshape(T, H, W), want)
+    assert n == int(want.sum()) and np.array_equal(order, np.flatnonzero(want.reshape(-1)))
+
+
+def test_src_points_to_the_latest_kept_token_at_the_same_position():
+    T, H, W = 6, 4, 5
+    rng = np.random.default_rng(77)
+    x = rng.standard_normal((T, H, W, 3)).astype(np.float32)
+    # sparse changes, so tokens stay pruned over several frames
+    x = np.repeat(x[:1], T, axis=0)
+    for t in range(1, T):
+        x[t] = x[t - 1] + (rng.random((H, W, 1)) < 0.04) * 3.0
+    keep, order, src, n = OL.prune(x.reshape(T * H * W, 3), T, H, W, 1.0)
+    F = H * W
+    runs = sum(1 for t in range(2, T) for s in range(F)
+               if not keep[t * F + s] and not keep[(t - 1) * F + s])
+    assert runs > 0 and 0 < n < T * F  # the case covers pruned runs
+    for t in range(T):
+        for s in range(F):
+            tt = t
+            while not keep[tt * F + s]:      # walk back to the latest kept frame
+                tt -= 1
+            assert order[src[t * F + s]] == tt * F + s
