@@ -50,6 +50,8 @@ def _load():
         "va_mask_info": [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i64)],
         "va_mask_to_host": [vp, i32p, i32p],
         "va_mask_free": [vp],
+        "va_mask_build_static": [i32, i32, i32, i32, ctypes.POINTER(_MaskParams), i32, vp, vp,
+                                 i64, ctypes.POINTER(i64), vp],
         "va_mask_cache_create": [i32, ctypes.POINTER(vp)],
         "va_mask_cache_get": [vp, i32, i32, i32, i32, ctypes.POINTER(_MaskParams), i32,
                               ctypes.POINTER(vp), vp],
@@ -185,6 +187,38 @@ def mask_build(kind: int, T: int, H: int, W: int, block: int = 128, w0: int = 0,
     _check(_lib.va_mask_build(kind, T, H, W, ctypes.byref(p), step, ctypes.byref(h),
                               _stream(stream)), "va_mask_build")
     return Mask(h, kind, T, H, W, p, step)
+
+
+def mask_build_static(kind: int, T: int, H: int, W: int, row_ptr, col_idx, block: int = 128,
+                      w0: int = 0, local: int = 1, period: int = 0, anchor0: int = 0,
+                      rot_stride: int = 1, step: int = 0, stream=None) -> int:
+    """va_mask_build_static: the mask's CSR written into caller-owned int32 CUDA
+    tensors row_ptr [nqb + 1] and col_idx [capacity], with no device allocation.
+    Returns nnz. If col_idx is too small, raises VAError with .nnz set to the
+    length needed (col_idx untouched)."""
+    import torch
+    _require_cuda(row_ptr, col_idx)
+    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32:
+        raise VAError(ERR_INVALID, "row_ptr / col_idx dtype (needs int32)")
+    nqb = -(-(T * H * W) // block) if block > 0 else 0
+    if row_ptr.numel() < nqb + 1:
+        raise VAError(ERR_INVALID, "row_ptr length (needs nqb + 1 = %d)" % (nqb + 1))
+    p = _MaskParams(block, w0, local, period, anchor0, rot_stride)
+    nnz = ctypes.c_int64(-1)
+    cap = col_idx.numel()
+    st = _lib.va_mask_build_static(kind, T, H, W, ctypes.byref(p), step, _ptr(row_ptr),
+                                   _ptr(col_idx if cap > 0 else None), cap, ctypes.byref(nnz),
+                                   _stream(stream))
+    if st != OK:
+        e = VAError(st, "va_mask_build_static")
+        e.nnz = nnz.value
+        raise e
+    return nnz.value
+
+
+def version() -> int:
+    """va_version: the library's version number."""
+    return _lib.va_version()
 
 
 def _mask_params(block, w0, local, period, anchor0, rot_stride):

@@ -136,3 +136,28 @@ def test_static_build_rejects_more_live_pairs_than_int32_offsets(va):
     assert st == va.ERR_UNSUPPORTED and nnz == 1 << 32
     assert (col == -7).all()
     assert va.device_error() == va.OK
+
+
+def test_python_wrapper_two_phase(va):
+    # size query with an empty col_idx, then the build into an exact array
+    kind, T, H, W, block, w0, local, period, a0, rho, step = CASES[2]
+    kw = dict(block=block, w0=w0, local=local, period=period, anchor0=a0, rot_stride=rho,
+              step=step)
+    nqb = -(-(T * H * W) // block)
+    dev = torch.device("cuda", 0)
+    row_ptr = torch.empty(nqb + 1, dtype=torch.int32, device=dev)
+    with pytest.raises(va.VAError) as e:
+        va.mask_build_static(kind, T, H, W, row_ptr,
+                             torch.empty(0, dtype=torch.int32, device=dev), **kw)
+    need = e.value.nnz
+    assert need > 0
+    col = torch.empty(need, dtype=torch.int32, device=dev)
+    assert va.mask_build_static(kind, T, H, W, row_ptr, col, **kw) == need
+    torch.cuda.synchronize()
+    m = va.mask_build(kind, T, H, W, **kw)
+    rp, cl = m.csr()
+    assert np.array_equal(row_ptr.cpu().numpy(), rp) and np.array_equal(col.cpu().numpy(), cl)
+    m.free()
+    with pytest.raises(va.VAError):  # a short row_ptr is refused on the host
+        va.mask_build_static(kind, T, H, W, row_ptr[:nqb], col, **kw)
+    assert va.device_error() == va.OK
